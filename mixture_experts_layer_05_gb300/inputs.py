@@ -1,0 +1,135 @@
+"""Seeded synthetic inputs for the FusedMoE layer forward.
+
+This module serves both the CUDA path and the oracle. It draws random numbers and
+shapes them (seeds, normal draws, an order-preserving spread of each logit row, Zipf
+popularity offsets, redraws of rows a caller rejects); it holds none of the layer's
+arithmetic (no scoring, no top-k, no expert math). Rows whose routing decision is too
+close to call are rejected by a caller-supplied ``margin_fn`` (the tests pass the
+oracle's), so this module never needs to know how routing works.
+
+Layouts follow the FusedMoE weight layout on the vLLM ``fused_moe/layer`` page
+(``FusedMoE._load_w13`` / ``_load_w2``): ``w13 [E, 2I, H]`` with the gate (w1) rows
+first and the up (w3) rows second, ``w2 [E, H, I]``; router logits ``[T, E]`` fp32 and
+``e_score_correction_bias [E]`` fp32 as in ``MoEGate`` on the sglang
+``models/deepseek_v2.py`` page.
+"""
+from __future__ import annotations
+
+import zlib
+
+import torch
+
+from .configs import MoEWorkload
+
+LOGIT_GAP = 1e-3
+
+
+def tensor_seed(workload: str, tensor: str, seed: int = 0) -> int:
+    """Stable per-tensor seed: crc32 of "workload/tensor" xor the run seed."""
+    return (zlib.crc32(f"{workload}/{tensor}".encode()) ^ int(seed)) & 0x7FFFFFFF
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def normal(shape, std: float, seed: int, dtype=torch.float32, device="cpu") -> torch.Tensor:
+    """N(0, std) draws in fp32, rounded once to ``dtype``; drawn in slices of the first dim."""
+    device = torch.device(device)
+    out = torch.empty(shape, dtype=dtype, device=device)
+    g = _gen(seed, device)
+    if len(shape) == 0 or shape[0] == 0:
+        return out
+    per = 1
+    for s in shape[1:]:
+        per *= s
+    rows = max(1, (1 << 26) // max(per, 1))          # <= 256 MB of fp32 per slice
+    for r0 in range(0, shape[0], rows):
+        r1 = min(shape[0], r0 + rows)
+        tmp = torch.randn((r1 - r0,) + tuple(shape[1:]), generator=g, device=device,
+                          dtype=torch.float32)
+        if std != 1.0:
+            tmp.mul_(std)
+        out[r0:r1].copy_(tmp)
+    return out
+
+
+def make_weights(w: MoEWorkload, seed: int = 0, device="cpu") -> dict:
+    """Expert weights (bf16), correction bias (fp32) and shared-expert weights."""
+    E, H, I = w.num_experts, w.hidden_size, w.intermediate_size
+    out = {
+        "w13": normal((E, 2 * I, H), w.w_std, tensor_seed(w.name, "w13", seed),
+                      torch.bfloat16, device),
+        "w2": normal((E, H, I), w.w_std, tensor_seed(w.name, "w2", seed),
+                     torch.bfloat16, device),
+        "bias": None, "shared_w13": None, "shared_w2": None,
+    }
+    if w.has_bias:
+        out["bias"] = normal((E,), w.bias_std, tensor_seed(w.name, "bias", seed),
+                             torch.float32, device)
+    Is = w.shared_intermediate_size
+    if Is:
+        out["shared_w13"] = normal((2 * Is, H), w.w_std,
+                                   tensor_seed(w.name, "shared_w13", seed),
+                                   torch.bfloat16, device)
+        out["shared_w2"] = normal((H, Is), w.w_std, tensor_seed(w.name, "shared_w2", seed),
+                                  torch.bfloat16, device)
+    return out
+
+
+def spread_rows(logits: torch.Tensor, gap: float = LOGIT_GAP) -> torch.Tensor:
+    """Move values apart, order preserved, so that within each row any two differ by >= gap.
+
+    Sort each row, then raise each value to at least its predecessor + gap (a running
+    maximum of v_i - i*gap, plus i*gap), and put the values back in place.
+    """
+    if logits.numel() == 0:
+        return logits
+    v, order = torch.sort(logits.double(), dim=-1, stable=True)
+    ramp = torch.arange(v.shape[-1], dtype=torch.float64) * gap
+    v = torch.cummax(v - ramp, dim=-1).values + ramp
+    out = torch.empty_like(v)
+    out.scatter_(-1, order, v)
+    return out.to(logits.dtype)
+
+
+def zipf_offsets(w: MoEWorkload, seed: int = 0) -> torch.Tensor:
+    """Per-expert logit offsets beta * log(rank^-s) over a seeded rank permutation."""
+    E = w.num_experts
+    if w.zipf_s <= 0:
+        return torch.zeros(E, dtype=torch.float32)
+    g = _gen(tensor_seed(w.name, "zipf_rank", seed), "cpu")
+    rank = torch.randperm(E, generator=g) + 1                    # rank of expert e
+    off = -w.zipf_s * w.zipf_beta * torch.log(rank.double())
+    return off.float()
+
+
+def _draw_logits(w: MoEWorkload, n: int, tag: str, seed: int) -> torch.Tensor:
+    lg = normal((n, w.num_experts), w.logit_std, tensor_seed(w.name, tag, seed))
+    if w.zipf_s > 0:
+        lg += zipf_offsets(w, seed)
+    return spread_rows(lg)
+
+
+def make_tokens(w: MoEWorkload, T: int, seed: int = 0, margin_fn=None,
+                min_margin: float = LOGIT_GAP, max_redraws: int = 64):
+    """Hidden states ``x [T, H]`` bf16 and router logits ``[T, E]`` fp32 (on the CPU).
+
+    Logit rows are spread so that any two entries differ by >= ``LOGIT_GAP``. If
+    ``margin_fn(logits) -> [T] margins`` is given, rows whose margin is below
+    ``min_margin`` are redrawn (deterministically, from derived seeds).
+    """
+    x = normal((T, w.hidden_size), w.x_std, tensor_seed(w.name, f"x/T{T}", seed),
+               torch.bfloat16)
+    logits = _draw_logits(w, T, f"logits/T{T}", seed)
+    if margin_fn is not None and T > 0:
+        for r in range(max_redraws):
+            bad = torch.nonzero(torch.as_tensor(margin_fn(logits)) < min_margin).flatten()
+            if bad.numel() == 0:
+                break
+            logits[bad] = _draw_logits(w, int(bad.numel()), f"logits/T{T}/redraw{r}", seed)
+        else:
+            raise RuntimeError("could not draw router logits with the requested margin")
+    return x, logits
