@@ -1,0 +1,384 @@
+"""Benchmark of the FusedMoE layer forward on GB300 (one JSON line on stdout).
+
+Default workload: the Mixtral-8x7B-shaped MoE layer (H=4096, I=14336, E=8, top_k=2,
+softmax + renormalize) at T=4096 tokens, bf16 weights ~N(0, 0.02) (2.8 GB, larger
+than L2, so no flush is needed between steps), activations ~N(0, 1), fp32 router
+logits ~N(0, 1), seed = rank.
+
+A step is one full forward through the C ABI (routing, align, gather, w13 GEMM +
+SiLU*mul, w2 GEMM, combine) on inputs resident in HBM. W warm-up steps, then K
+timed steps between a barrier + synchronize on both sides, CUDA events on the
+launching stream, max over ranks; ``value`` = tokens of all ranks / that time.
+``e2e`` is the same metric with pinned host inputs copied in and the output copied
+out inside each timed step. ``--impl reference`` times the CPU oracle instead, on a
+bounded token sample per step.
+
+Multi-GPU (torchrun): independent data-parallel replicas, each rank its own batch
+and a full copy of the weights; no collective on the data path (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused-MoE layer tokens/s; TFLOP/s & HBM GB/s as % of GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------- host-side logic
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(rank: int) -> int:
+    """Each replica draws its own batch (weights are the same on every rank)."""
+    return int(rank)
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tokens_per_s(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    return tokens_per_rank * world / (ms_max / 1e3)
+
+
+def layer_work(w, T: int, n_active: int) -> dict:
+    """Algorithmic flops and bytes of one forward (no padding rows)."""
+    H, I, k, E, Is = w.hidden_size, w.intermediate_size, w.top_k, w.num_experts, \
+        w.shared_intermediate_size
+    flops_w13 = 4.0 * T * k * H * I + 4.0 * T * H * Is
+    flops_w2 = 2.0 * T * k * H * I + 2.0 * T * H * Is
+    w13_bytes = n_active * 2 * I * H * 2 + 2 * Is * H * 2
+    w2_bytes = n_active * H * I * 2 + H * Is * 2
+    act_bytes = T * k * I * 2 + T * Is * 2
+    bytes_total = (w13_bytes + w2_bytes + T * H * 2 * 2 + T * E * 4 + T * k * 8
+                   + 2 * act_bytes)
+    return {"flops": flops_w13 + flops_w2, "flops_w13": flops_w13, "flops_w2": flops_w2,
+            "bytes": float(bytes_total),
+            "bytes_w13": float(w13_bytes + T * k * H * 2 + act_bytes),
+            "bytes_w2": float(w2_bytes + act_bytes + T * k * H * 2)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms in the background."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    p = [x.strip() for x in line.split(",")]
+                    if len(p) < 10:
+                        continue
+                    try:
+                        ts = time.mktime(time.strptime(p[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                        ts += float("0." + p[0].split(".")[1]) if "." in p[0] else 0.0
+                        rows.append((ts, float(p[2]), float(p[3]), p[6:10]))
+                    except (ValueError, IndexError):
+                        continue
+        except OSError:
+            pass
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        used = inside or rows[-20:]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in used for i, v in enumerate(r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in used),
+                "sm_max_mhz": max(r[2] for r in used), "reasons": reasons,
+                "samples": len(used), "in_timed_region": bool(inside)}
+
+
+# ---------------------------------------------------------------- arms
+def run_ours(args, w, T):
+    import torch
+    import torch.distributed as dist
+
+    from mixture_experts_layer_05_gb300 import binding, inputs
+    from mixture_experts_layer_05_gb300 import build as build_mod
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=dev)
+    build_mod.build()
+    binding.load()
+
+    wts = inputs.make_weights(w, 0, device=dev)
+    x_cpu, logits_cpu = inputs.make_tokens(w, T, seed=rank_seed(rank))
+    x, logits = x_cpu.to(dev), logits_cpu.to(dev)
+    cfg = binding.config_from_workload(w)
+    layer = binding.FusedMoE(cfg, wts["w13"], wts["w2"], wts["bias"], wts["shared_w13"],
+                             wts["shared_w2"], max_tokens=T)
+    out = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    K, W = args.steps, args.warmup
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(binding.NUM_STAGE_EVENTS)]
+           for _ in range(K)]
+    for _ in range(W):
+        layer(x, logits, out=out)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    for _ in range(W):
+        layer(x, logits, out=out)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(K):
+        layer(x, logits, out=out, events=evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_end) / K
+    ms_max = reduce_max(ms, dev)
+    status = layer.device_status()
+    if status != binding.OK:
+        raise RuntimeError(f"device status {binding.STATUS.get(status, status)} after the run")
+    stage = {n: statistics.mean(e[a].elapsed_time(e[b]) for e in evs)
+             for n, a, b in (("route_align_gather", 0, 1), ("w13_gemm", 1, 2),
+                             ("w2_gemm", 2, 3), ("combine", 3, 4))}
+    clocks = sampler.summary(wall0, wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    # end to end: pinned host inputs in, output out, inside each timed step
+    x_h = x_cpu.pin_memory()
+    l_h = logits_cpu.pin_memory()
+    y_h = torch.empty(x_cpu.shape, dtype=x_cpu.dtype).pin_memory()
+    x_d, l_d = torch.empty_like(x), torch.empty_like(logits)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        l_d.copy_(l_h, non_blocking=True)
+        layer(x_d, l_d, out=out)
+        y_h.copy_(out, non_blocking=True)
+
+    for _ in range(W):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / K, dev)
+
+    # routing facts for the algorithmic work
+    lay = binding.moe_forward_workspace_layout(cfg, T)
+    ids = layer.workspace[lay.topk_ids:lay.topk_ids + T * w.top_k * 4].view(torch.int32)
+    n_active = int(torch.unique(ids).numel())
+    npp = int(layer.workspace[lay.num_tokens_post_padded:lay.num_tokens_post_padded + 4]
+              .view(torch.int32).item())
+    work = layer_work(w, T, n_active)
+    peaks, peak_src = load_peaks()
+    value = aggregate_tokens_per_s(T, world, ms_max)
+
+    res = None
+    if rank == 0:
+        # dominant kernel: the w13 grouped GEMM (two thirds of the flops and weight bytes)
+        t_w13 = stage["w13_gemm"] / 1e3
+        tensor_bound = work["flops_w13"] / (peaks["bf16_tflops"] * 1e12) >= \
+            work["bytes_w13"] / (peaks["hbm_gbs"] * 1e9)
+        if tensor_bound:
+            ach = work["flops_w13"] / t_w13 / 1e12
+            roof = {"kernel": "gemm_kernel<w13> (grouped w13 GEMM + SiLU*mul)", "bound": "tensor",
+                    "achieved": round(ach, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": round(ach / peaks["bf16_tflops"], 4)}
+        else:
+            ach = work["bytes_w13"] / t_w13 / 1e9
+            roof = {"kernel": "gemm_kernel<w13> (grouped w13 GEMM + SiLU*mul)", "bound": "hbm",
+                    "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(ach / peaks["hbm_gbs"], 4)}
+        roof["peak_source"] = f"{peak_src} (burst)"
+        roof["traffic"] = args.traffic
+        step_s = ms_max / 1e3
+        res = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{w.name}: FusedMoE layer H={w.hidden_size} "
+                                   f"I={w.intermediate_size} E={w.num_experts} k={w.top_k}",
+                       "tokens_per_gpu": T, "global_batch": T * world,
+                       "parallelism": f"dp{world} replicas",
+                       "l2": "inputs larger than L2 (expert weights streamed every step)",
+                       "seed": "weights 0, tokens = rank"},
+            "layer": {"tflops": round(work["flops"] / step_s / 1e12, 1),
+                      "tflops_frac": round(work["flops"] / step_s / 1e12 / peaks["bf16_tflops"], 4),
+                      "hbm_gbs": round(work["bytes"] / step_s / 1e9, 1),
+                      "hbm_frac": round(work["bytes"] / step_s / 1e9 / peaks["hbm_gbs"], 4),
+                      "active_experts": n_active, "rows_post_padded": npp,
+                      "stages_ms": {k: round(v, 4) for k, v in stage.items()}},
+            "roofline": roof,
+            "e2e": {"value": round(aggregate_tokens_per_s(T, world, e2e_ms), 1),
+                    "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
+                    "d2h_bytes_per_step": out.numel() * 2},
+            "gpu_launches": K * (8 + (2 if w.shared_intermediate_size else 0)),
+            "clocks": clocks,
+        }
+        if args.cpu_baseline and world == 1:
+            res["cpu_baseline"] = cpu_baseline(w, wts, x_cpu, logits_cpu, args.cpu_sample)
+    return res
+
+
+def _host_weights(w, wts):
+    import torch
+    return {k: (None if v is None else v.to("cpu")) for k, v in wts.items()}
+
+
+def oracle_cfg(w):
+    return dict(num_experts=w.num_experts, top_k=w.top_k, renormalize=w.renormalize,
+                use_grouped_topk=w.use_grouped_topk, num_expert_group=w.num_expert_group,
+                topk_group=w.topk_group, scoring_func=w.scoring_func,
+                routed_scaling_factor=w.routed_scaling_factor)
+
+
+def cpu_baseline(w, wts, x_cpu, logits_cpu, n_tokens: int) -> dict:
+    """The CPU oracle, as it stands, on the first n_tokens of the batch."""
+    import oracle
+    hw = _host_weights(w, wts)
+    t0 = time.perf_counter()
+    oracle.fused_moe_rows(x_cpu[:n_tokens], logits_cpu[:n_tokens], hw["bias"], hw["w13"],
+                          hw["w2"], hw["shared_w13"], hw["shared_w2"], **oracle_cfg(w))
+    dt = time.perf_counter() - t0
+    return {"value": round(n_tokens / dt, 4), "unit": "tokens/s",
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"first {n_tokens} tokens of the step's batch, full weights, fp64 numpy "
+                      f"(BLAS default threading), {dt:.1f} s"}
+
+
+def run_reference(args, w, T):
+    """The CPU oracle as the reference arm: each step routes and computes a bounded sample."""
+    import torch
+
+    from mixture_experts_layer_05_gb300 import inputs
+    import oracle
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    n = args.ref_sample
+    hw = inputs.make_weights(w, 0)           # CPU-generated: the oracle arm needs no GPU
+    x_cpu, logits_cpu = inputs.make_tokens(w, T, seed=0)
+
+    def step(i):
+        r0 = (i * n) % max(T - n + 1, 1)
+        oracle.fused_moe_rows(x_cpu[r0:r0 + n], logits_cpu[r0:r0 + n], hw["bias"], hw["w13"],
+                              hw["w2"], hw["shared_w13"], hw["shared_w2"], **oracle_cfg(w))
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = n / dt
+    cores = len(os.sched_getaffinity(0))
+    sample = f"{n} token(s) of the {T}-token batch per step, full weights, fp64 numpy"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.name}: FusedMoE layer H={w.hidden_size} "
+                                   f"I={w.intermediate_size} E={w.num_experts} k={w.top_k}",
+                       "tokens_per_gpu": T, "sample_tokens_per_step": n},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixtral")
+    ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--cpu-sample", type=int, default=4)
+    ap.add_argument("--ref-sample", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+    from mixture_experts_layer_05_gb300 import configs
+    w = configs.get(args.workload)
+    res = run_reference(args, w, args.tokens) if args.impl == "reference" \
+        else run_ours(args, w, args.tokens)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    try:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+    except Exception:
+        pass
+
+
+if __name__ == "__main__":
+    main()

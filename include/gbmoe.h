@@ -1,0 +1,217 @@
+/*
+ * gbmoe.h: C ABI of the GB300 (sm_103a) FusedMoE layer forward.
+ *
+ * The forward is the one the vLLM `fused_moe/layer` page builds around
+ * `FusedMoE` (constructor arguments, `select_experts`, `forward_impl`) and the
+ * sglang `fused_moe_triton/layer.py` page runs in one call
+ * (`FlashInferFusedMoE.forward_impl`: router logits, correction bias, hidden
+ * states and both expert weight stacks in, the combined output out), with the
+ * DeepSeek shared expert of the sglang `models/deepseek_v2.py` page
+ * (`DeepseekV2MoE.forward_normal`) added on top.
+ *
+ * Conventions for every entry point
+ *  - All array pointers are DEVICE pointers owned by the caller. The library
+ *    never allocates, frees or keeps them; scratch lives in a caller-provided
+ *    workspace whose size the matching *_workspace_size() call returns.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and the call returns without synchronising. Outputs are valid once
+ *    the stream reaches that point.
+ *  - Arguments are validated on the host before anything is enqueued; a
+ *    negative status means nothing was enqueued (except GBMOE_ERR_CUDA, which
+ *    reports a failed launch). Kernels never trap: a failed device-side check or a
+ *    bounded wait that ran out is recorded in the int32 status word at the start
+ *    of the workspace, read (and reset) with moe_get_device_status(). The word
+ *    keeps the first error since its last reset, so a new workspace must start
+ *    with its first 256 bytes zeroed.
+ *  - bf16 tensors are passed as `const void*` (IEEE bfloat16, row-major).
+ *  - num_tokens == 0 is a successful no-op (the empty-batch early return of
+ *    `DeepseekV2MoE.forward_normal`).
+ */
+#ifndef GBMOE_H
+#define GBMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* gbmoe_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  GBMOE_OK = 0,
+  GBMOE_ERR_INVALID_ARG = -1,   /* null pointer, bad size, inconsistent flags */
+  GBMOE_ERR_UNSUPPORTED = -2,   /* valid for the method, not built here (see each call) */
+  GBMOE_ERR_WORKSPACE = -3,     /* workspace null or smaller than *_workspace_size() */
+  GBMOE_ERR_CUDA = -4,          /* a CUDA runtime call or launch failed */
+  GBMOE_ERR_DEVICE_CHECK = -5,  /* a device-side bounds check failed */
+  GBMOE_ERR_TIMEOUT = -6        /* a device-side bounded wait ran out */
+} gbmoe_status_t;
+
+typedef enum { GBMOE_SCORE_SOFTMAX = 0, GBMOE_SCORE_SIGMOID = 1 } gbmoe_scoring_t;
+typedef enum { GBMOE_ACT_SILU = 0 } gbmoe_act_t;
+
+/*
+ * Layer configuration; field names follow the FusedMoE constructor (vLLM
+ * `fused_moe/layer` page, `FusedMoE.__init__`) and `DeepseekV2MoE.__init__`
+ * (sglang `models/deepseek_v2.py` page) for the shared expert.
+ *
+ *  num_experts            E, routed experts (1..1024)
+ *  top_k                  k, experts per token (1..min(E, 32))
+ *  hidden_size            H, a multiple of 128
+ *  intermediate_size      I, a multiple of 128
+ *  renormalize            !=0: divide the chosen weights by their sum
+ *  use_grouped_topk       !=0: group-limited routing (num_expert_group,
+ *                         topk_group required; E % num_expert_group == 0,
+ *                         num_expert_group <= 32, topk_group <= num_expert_group,
+ *                         top_k <= topk_group * E / num_expert_group)
+ *  scoring_func           gbmoe_scoring_t; SIGMOID requires use_grouped_topk
+ *                         (the constructor rejects non-softmax ungrouped routing)
+ *  routed_scaling_factor  multiplies every routed weight (not the shared expert)
+ *  activation             must be GBMOE_ACT_SILU (else UNSUPPORTED)
+ *  is_act_and_mul         must be 1: act = silu(gate) * up (else UNSUPPORTED)
+ *  shared_intermediate_size  I_s of the dense shared SwiGLU expert; 0 = none;
+ *                         else a multiple of 128
+ */
+typedef struct {
+  int32_t num_experts;
+  int32_t top_k;
+  int32_t hidden_size;
+  int32_t intermediate_size;
+  int32_t renormalize;
+  int32_t use_grouped_topk;
+  int32_t num_expert_group;
+  int32_t topk_group;
+  int32_t scoring_func;
+  float routed_scaling_factor;
+  int32_t activation;
+  int32_t is_act_and_mul;
+  int32_t shared_intermediate_size;
+} gbmoe_config_t;
+
+/*
+ * moe_topk: router scoring and (grouped) top-k.
+ * Defined by `FusedMoE.select_experts` (vLLM `fused_moe/layer` page): the
+ * grouped_topk branch (num_expert_group, topk_group, scoring_func,
+ * routed_scaling_factor, e_score_correction_bias), the biased fused_topk_bias
+ * branch and the plain fused_topk branch.
+ *  - score s = softmax(logits row) or sigmoid(logits); key q = s + bias when
+ *    `e_score_correction_bias` is non-NULL, else q = s.
+ *  - grouped: the topk_group groups (contiguous runs of E/num_expert_group
+ *    experts) with the largest group score survive; the group score is the
+ *    largest s in the group without a bias and the sum of the two largest q in
+ *    the group with one.
+ *  - the top_k largest q among surviving experts (ties to the lower index), in
+ *    descending q order; weight = s of that expert, divided by the sum of the
+ *    chosen s if renormalize, then times routed_scaling_factor.
+ * router_logits [T, E] fp32; e_score_correction_bias [E] fp32 or NULL;
+ * topk_weights [T, top_k] fp32 (out); topk_ids [T, top_k] int32 (out).
+ * Errors: INVALID_ARG (nulls, sizes, group arguments), UNSUPPORTED (sigmoid
+ * without grouping).
+ */
+gbmoe_status_t moe_topk(const gbmoe_config_t* cfg, int32_t num_tokens,
+                        const float* router_logits, const float* e_score_correction_bias,
+                        float* topk_weights, int32_t* topk_ids, gbmoe_stream_t stream);
+
+/*
+ * moe_align_block_size: group the (token, slot) pairs by expert, padded to
+ * block_size, for the grouped expert GEMMs of the FusedMoE forward (the
+ * Triton fused_moe path behind `UnquantizedFusedMoEMethod` on the vLLM
+ * `fused_moe/layer` page).
+ *  - flat index f = t*top_k + j of topk_ids [T, top_k] (int32, values in [0, E));
+ *  - experts in ascending order, each expert's flat indices ascending (stable),
+ *    each run padded with the sentinel T*top_k to a multiple of block_size;
+ *  - sorted_token_ids [T*top_k + E*(block_size-1)] int32 (out; entries past
+ *    num_tokens_post_padded are unspecified);
+ *  - expert_ids [(T*top_k + E*(block_size-1)) / block_size + 1] int32 (out;
+ *    one per block; entries past num_tokens_post_padded/block_size are -1);
+ *  - num_tokens_post_padded [1] int32 (out) = sum over experts of the padded runs.
+ * block_size: 1..1024. Workspace: moe_align_block_size_workspace_size().
+ * A topk_id outside [0, E) sets GBMOE_ERR_DEVICE_CHECK in the device status and
+ * is counted as expert 0.
+ */
+size_t moe_align_block_size_workspace_size(int32_t num_tokens, int32_t top_k, int32_t num_experts);
+gbmoe_status_t moe_align_block_size(const int32_t* topk_ids, int32_t num_tokens, int32_t top_k,
+                                    int32_t num_experts, int32_t block_size,
+                                    int32_t* sorted_token_ids, int32_t* expert_ids,
+                                    int32_t* num_tokens_post_padded, void* workspace,
+                                    size_t workspace_bytes, gbmoe_stream_t stream);
+
+/*
+ * moe_forward: the whole layer, from router logits to the combined output.
+ *  1. moe_topk (above);
+ *  2. align by expert (above) with the block size moe_forward_block_size(),
+ *     and gather the hidden rows into expert order;
+ *  3. per block: [gate | up] = x_rows @ w13[e]^T, act = silu(gate) * up
+ *     (`SiluAndMul` of `DeepseekV2MLP`; w13 rows [0, I) gate, [I, 2I) up as
+ *     `FusedMoE._load_w13` lays them out), rounded to bf16;
+ *  4. o = act @ w2[e]^T, times the token's routing weight;
+ *  5. y[t] = sum over j ascending of the weighted o[t, j], plus the shared expert
+ *     silu(x W1s^T) * (x W3s^T) W2s^T unscaled (`DeepseekV2MoE.forward_normal`),
+ *     accumulated in fp32 and rounded once to bf16.
+ * hidden_states [T, H] bf16; router_logits [T, E] fp32; bias [E] fp32 or NULL;
+ * w13_weight [E, 2I, H] bf16; w2_weight [E, H, I] bf16; shared_w13 [2I_s, H] and
+ * shared_w2 [H, I_s] bf16 (both NULL iff cfg->shared_intermediate_size == 0);
+ * output [T, H] bf16 (out). All bf16 pointers 16-byte aligned.
+ * Workspace: moe_forward_workspace_size(cfg, max_tokens) bytes, 256-byte
+ * aligned, for any num_tokens <= max_tokens; its layout is reported by
+ * moe_forward_workspace_layout().
+ */
+size_t moe_forward_workspace_size(const gbmoe_config_t* cfg, int32_t max_num_tokens);
+int32_t moe_forward_block_size(const gbmoe_config_t* cfg, int32_t num_tokens);
+gbmoe_status_t moe_forward(const gbmoe_config_t* cfg, int32_t num_tokens,
+                           const void* hidden_states, const float* router_logits,
+                           const float* e_score_correction_bias, const void* w13_weight,
+                           const void* w2_weight, const void* shared_w13, const void* shared_w2,
+                           void* output, void* workspace, size_t workspace_bytes,
+                           gbmoe_stream_t stream);
+
+/*
+ * moe_forward_events: moe_forward that also records caller-created CUDA events
+ * (cudaEvent_t, passed as void*) on `stream` at the stage boundaries:
+ * events[0] before routing, [1] after routing + align + gather, [2] after the
+ * w13 GEMMs, [3] after the w2 GEMMs, [4] after the combine. `events` may be
+ * NULL (then identical to moe_forward); num_events must then be 0, else 5.
+ */
+#define GBMOE_NUM_STAGE_EVENTS 5
+gbmoe_status_t moe_forward_events(const gbmoe_config_t* cfg, int32_t num_tokens,
+                                  const void* hidden_states, const float* router_logits,
+                                  const float* e_score_correction_bias, const void* w13_weight,
+                                  const void* w2_weight, const void* shared_w13,
+                                  const void* shared_w2, void* output, void* workspace,
+                                  size_t workspace_bytes, void* const* events, int32_t num_events,
+                                  gbmoe_stream_t stream);
+
+/*
+ * Byte offsets of the intermediate results inside a moe_forward workspace
+ * (for inspection and tests). Each is valid after the call completes.
+ */
+typedef struct {
+  size_t status;                 /* int32 device status word (see moe_get_device_status) */
+  size_t topk_weights;           /* fp32 [T, top_k] */
+  size_t topk_ids;               /* int32 [T, top_k] */
+  size_t sorted_token_ids;       /* int32 [T*top_k + E*(bs-1)] */
+  size_t expert_ids;             /* int32 [that / bs + 1] */
+  size_t num_tokens_post_padded; /* int32 [1] */
+  size_t act;                    /* bf16 [rows, I]: silu(gate)*up in expert order */
+  size_t total;                  /* == moe_forward_workspace_size() */
+} gbmoe_workspace_layout_t;
+gbmoe_status_t moe_forward_workspace_layout(const gbmoe_config_t* cfg, int32_t max_num_tokens,
+                                            gbmoe_workspace_layout_t* layout);
+
+/*
+ * moe_get_device_status: wait for `stream`, copy the int32 status word at the
+ * start of `workspace` (a moe_forward or moe_align_block_size workspace) to
+ * *status (GBMOE_OK or a negative gbmoe_status_t) and reset it to GBMOE_OK.
+ * Returns GBMOE_ERR_CUDA if the copy fails.
+ */
+gbmoe_status_t moe_get_device_status(void* workspace, int32_t* status, gbmoe_stream_t stream);
+
+/* Library version, (major << 16) | minor. */
+int32_t gbmoe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GBMOE_H */

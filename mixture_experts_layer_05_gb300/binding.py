@@ -1,0 +1,239 @@
+"""Python binding of libgbmoe.so: the C ABI of ``include/gbmoe.h`` with the same names.
+
+Argument marshalling only: torch tensors become device pointers, the current torch
+CUDA stream becomes the ``stream`` argument, and a negative status raises
+``GbmoeError``. Every step of the layer runs in the library's kernels; there is no
+fallback of any kind, and loading fails loudly when the library is not built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgbmoe.so")
+
+STATUS = {0: "GBMOE_OK", -1: "GBMOE_ERR_INVALID_ARG", -2: "GBMOE_ERR_UNSUPPORTED",
+          -3: "GBMOE_ERR_WORKSPACE", -4: "GBMOE_ERR_CUDA", -5: "GBMOE_ERR_DEVICE_CHECK",
+          -6: "GBMOE_ERR_TIMEOUT"}
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_CHECK, ERR_TIMEOUT = \
+    0, -1, -2, -3, -4, -5, -6
+SCORE = {"softmax": 0, "sigmoid": 1}
+NUM_STAGE_EVENTS = 5
+
+# every entry point declared in include/gbmoe.h
+EXPORTS = ("moe_topk", "moe_align_block_size_workspace_size", "moe_align_block_size",
+           "moe_forward_workspace_size", "moe_forward_block_size", "moe_forward",
+           "moe_forward_events", "moe_forward_workspace_layout", "moe_get_device_status",
+           "gbmoe_version")
+
+
+class GbmoeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {STATUS.get(code, code)}")
+        self.code = code
+
+
+class Config(ctypes.Structure):
+    """gbmoe_config_t."""
+    _fields_ = [("num_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("hidden_size", ctypes.c_int32), ("intermediate_size", ctypes.c_int32),
+                ("renormalize", ctypes.c_int32), ("use_grouped_topk", ctypes.c_int32),
+                ("num_expert_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
+                ("scoring_func", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
+                ("activation", ctypes.c_int32), ("is_act_and_mul", ctypes.c_int32),
+                ("shared_intermediate_size", ctypes.c_int32)]
+
+
+class WorkspaceLayout(ctypes.Structure):
+    """gbmoe_workspace_layout_t."""
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "status", "topk_weights", "topk_ids", "sorted_token_ids", "expert_ids",
+        "num_tokens_post_padded", "act", "total")]
+
+
+def make_config(num_experts, top_k, hidden_size, intermediate_size, renormalize=True,
+                use_grouped_topk=False, num_expert_group=0, topk_group=0,
+                scoring_func="softmax", routed_scaling_factor=1.0, activation=0,
+                is_act_and_mul=1, shared_intermediate_size=0) -> Config:
+    return Config(int(num_experts), int(top_k), int(hidden_size), int(intermediate_size),
+                  int(bool(renormalize)), int(bool(use_grouped_topk)), int(num_expert_group or 0),
+                  int(topk_group or 0), SCORE.get(scoring_func, scoring_func),
+                  float(routed_scaling_factor), int(activation), int(is_act_and_mul),
+                  int(shared_intermediate_size or 0))
+
+
+def config_from_workload(w) -> Config:
+    return make_config(w.num_experts, w.top_k, w.hidden_size, w.intermediate_size,
+                       w.renormalize, w.use_grouped_topk, w.num_expert_group, w.topk_group,
+                       w.scoring_func, w.routed_scaling_factor,
+                       shared_intermediate_size=w.shared_intermediate_size)
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libgbmoe.so (built by ``build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built: run mixture_experts_layer_05_gb300.build"
+                           ".build() (nvcc, sm_103a)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    CP = ctypes.POINTER(Config)
+    sig = {
+        "moe_topk": (I32, [CP, I32, P, P, P, P, P]),
+        "moe_align_block_size_workspace_size": (SZ, [I32, I32, I32]),
+        "moe_align_block_size": (I32, [P, I32, I32, I32, I32, P, P, P, P, SZ, P]),
+        "moe_forward_workspace_size": (SZ, [CP, I32]),
+        "moe_forward_block_size": (I32, [CP, I32]),
+        "moe_forward": (I32, [CP, I32, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "moe_forward_events": (I32, [CP, I32, P, P, P, P, P, P, P, P, P, SZ, P, I32, P]),
+        "moe_forward_workspace_layout": (I32, [CP, I32, ctypes.POINTER(WorkspaceLayout)]),
+        "moe_get_device_status": (I32, [P, ctypes.POINTER(I32), P]),
+        "gbmoe_version": (I32, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn: str, code: int):
+    if code != OK:
+        raise GbmoeError(fn, code)
+
+
+def _need(t, dtype, name):
+    if t is None:
+        return
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def moe_topk(cfg: Config, router_logits, e_score_correction_bias, topk_weights, topk_ids,
+             stream=None):
+    _need(router_logits, torch.float32, "router_logits")
+    _need(e_score_correction_bias, torch.float32, "e_score_correction_bias")
+    _need(topk_weights, torch.float32, "topk_weights")
+    _need(topk_ids, torch.int32, "topk_ids")
+    _check("moe_topk", load().moe_topk(ctypes.byref(cfg), router_logits.shape[0],
+                                       _p(router_logits), _p(e_score_correction_bias),
+                                       _p(topk_weights), _p(topk_ids), _stream(stream)))
+
+
+def moe_align_block_size_workspace_size(num_tokens, top_k, num_experts) -> int:
+    return load().moe_align_block_size_workspace_size(num_tokens, top_k, num_experts)
+
+
+def moe_align_block_size(topk_ids, num_experts, block_size, sorted_token_ids, expert_ids,
+                         num_tokens_post_padded, workspace, stream=None):
+    _need(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    _check("moe_align_block_size", load().moe_align_block_size(
+        _p(topk_ids), T, k, num_experts, block_size, _p(sorted_token_ids), _p(expert_ids),
+        _p(num_tokens_post_padded), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def moe_forward_workspace_size(cfg: Config, max_num_tokens: int) -> int:
+    n = load().moe_forward_workspace_size(ctypes.byref(cfg), max_num_tokens)
+    if n == 0:
+        raise GbmoeError("moe_forward_workspace_size", ERR_INVALID_ARG)
+    return n
+
+
+def moe_forward_block_size(cfg: Config, num_tokens: int) -> int:
+    return load().moe_forward_block_size(ctypes.byref(cfg), num_tokens)
+
+
+def moe_forward_workspace_layout(cfg: Config, num_tokens: int) -> WorkspaceLayout:
+    out = WorkspaceLayout()
+    _check("moe_forward_workspace_layout",
+           load().moe_forward_workspace_layout(ctypes.byref(cfg), num_tokens, ctypes.byref(out)))
+    return out
+
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A uint8 workspace; its status word (first 256 bytes) starts at zero."""
+    ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    ws[:256].zero_()
+    return ws
+
+
+def moe_forward(cfg: Config, hidden_states, router_logits, e_score_correction_bias, w13_weight,
+                w2_weight, shared_w13, shared_w2, output, workspace, events=None, stream=None):
+    _need(hidden_states, torch.bfloat16, "hidden_states")
+    _need(router_logits, torch.float32, "router_logits")
+    _need(e_score_correction_bias, torch.float32, "e_score_correction_bias")
+    for t, n in ((w13_weight, "w13_weight"), (w2_weight, "w2_weight"), (shared_w13, "shared_w13"),
+                 (shared_w2, "shared_w2"), (output, "output")):
+        _need(t, torch.bfloat16, n)
+    lib = load()
+    args = [ctypes.byref(cfg), hidden_states.shape[0], _p(hidden_states), _p(router_logits),
+            _p(e_score_correction_bias), _p(w13_weight), _p(w2_weight), _p(shared_w13),
+            _p(shared_w2), _p(output), _p(workspace),
+            workspace.numel() * workspace.element_size()]
+    if events is None:
+        _check("moe_forward", lib.moe_forward(*args, _stream(stream)))
+    else:
+        for ev in events:                  # torch creates the CUDA event on first record
+            if not ev.cuda_event:
+                ev.record()
+        arr = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+        _check("moe_forward_events",
+               lib.moe_forward_events(*args, arr, len(events), _stream(stream)))
+
+
+def moe_get_device_status(workspace, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    _check("moe_get_device_status",
+           load().moe_get_device_status(_p(workspace), ctypes.byref(v), _stream(stream)))
+    return v.value
+
+
+class FusedMoE:
+    """The layer with its weights resident on the GPU and a workspace sized for max_tokens."""
+
+    def __init__(self, cfg: Config, w13_weight, w2_weight, e_score_correction_bias=None,
+                 shared_w13=None, shared_w2=None, max_tokens: int = 1):
+        self.cfg = cfg
+        self.w13, self.w2 = w13_weight, w2_weight
+        self.bias, self.shared_w13, self.shared_w2 = e_score_correction_bias, shared_w13, shared_w2
+        self.max_tokens = 0
+        self.workspace = None
+        self.reserve(max_tokens)
+
+    def reserve(self, max_tokens: int):
+        if max_tokens > self.max_tokens:
+            dev = self.w13.device
+            self.workspace = alloc_workspace(moe_forward_workspace_size(self.cfg, max_tokens), dev)
+            self.max_tokens = max_tokens
+
+    def __call__(self, hidden_states, router_logits, out=None, events=None):
+        T = hidden_states.shape[0]
+        self.reserve(T)
+        if out is None:
+            out = torch.empty_like(hidden_states)
+        moe_forward(self.cfg, hidden_states, router_logits, self.bias, self.w13, self.w2,
+                    self.shared_w13, self.shared_w2, out, self.workspace, events=events)
+        return out
+
+    def device_status(self) -> int:
+        return moe_get_device_status(self.workspace)

@@ -1,0 +1,200 @@
+// Expert align (stable counting sort of the flat (token, slot) indices by expert,
+// runs padded to the block size) and the gather of hidden rows into that order.
+//
+// The FusedMoE forward (vLLM `fused_moe/layer` page, the Triton fused_moe path
+// behind `UnquantizedFusedMoEMethod`) runs its expert GEMMs over tokens grouped by
+// expert; sorted_token_ids / expert_ids / num_tokens_post_padded are the outputs of
+// that grouping step.
+//
+// Three launches, no grid-wide waits:
+//   count   per chunk of kAlignChunk flat indices, per-expert counts (shared atomics,
+//           order-free);
+//   scan    one CTA: per-expert totals, padded runs, exclusive scan over experts,
+//           per-(chunk, expert) start offsets, sentinel padding, expert_ids;
+//   scatter one CTA per chunk; its warps own consecutive slices, count them, take
+//           start offsets in slice order, and walk their slices in order, ranking
+//           equal experts in each 32-wide step with __match_any_sync: stable order.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gbmoe {
+
+__global__ void __launch_bounds__(256) align_count_kernel(const int* __restrict__ ids, int n,
+                                                          int E, int* __restrict__ counts,
+                                                          int* status) {
+  extern __shared__ int sc[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sc[e] = 0;
+  __syncthreads();
+  const int f0 = blockIdx.x * kAlignChunk;
+  const int f1 = min(n, f0 + kAlignChunk);
+  for (int f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
+    int e = __ldg(ids + f);
+    if ((unsigned)e >= (unsigned)E) {
+      record_status(status, GBMOE_ERR_DEVICE_CHECK);
+      e = 0;
+    }
+    atomicAdd(&sc[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[(size_t)blockIdx.x * E + e] = sc[e];
+}
+
+// One CTA of 1024 threads; thread e owns expert e (E <= 1024).
+__global__ void __launch_bounds__(1024) align_scan_kernel(const int* __restrict__ counts, int C,
+                                                          int E, int bs, int n,
+                                                          int* __restrict__ offs,
+                                                          int* __restrict__ sorted,
+                                                          int* __restrict__ expert_ids,
+                                                          int max_blocks, int* __restrict__ npp) {
+  __shared__ int warp_tot[32];
+  __shared__ int s_total;
+  const int e = threadIdx.x;
+  const int lane = e & 31, wid = e >> 5;
+  int tot = 0;
+  if (e < E)
+    for (int c = 0; c < C; ++c) tot += counts[(size_t)c * E + e];
+  const int pad = (tot + bs - 1) / bs * bs;
+  // exclusive scan of pad over threads
+  int incl = pad;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int w = warp_tot[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
+    if (lane == 31) s_total = wi;
+  }
+  __syncthreads();
+  const int start = warp_tot[wid] + incl - pad;
+  if (e < E) {
+    int run = start;
+    for (int c = 0; c < C; ++c) {
+      offs[(size_t)c * E + e] = run;
+      run += counts[(size_t)c * E + e];
+    }
+    for (int p = start + tot; p < start + pad; ++p) sorted[p] = n;
+    for (int b = start / bs; b < (start + pad) / bs; ++b) expert_ids[b] = e;
+  }
+  const int total = s_total;
+  if (e == 0) *npp = total;
+  for (int b = total / bs + e; b < max_blocks; b += blockDim.x) expert_ids[b] = -1;
+}
+
+// One CTA per chunk, kScatterWarps warps, each owning a contiguous slice of the chunk.
+// Each warp counts its slice per expert (match_any groups, no atomics), the CTA turns
+// the per-warp counts into per-warp start offsets (warps in slice order), then each
+// warp walks its slice in order: the order within an expert stays stable.
+constexpr int kScatterWarps = 8;
+constexpr int kSliceLen = kAlignChunk / kScatterWarps;
+
+__global__ void __launch_bounds__(kScatterWarps * 32)
+    align_scatter_kernel(const int* __restrict__ ids, int n, int E, const int* __restrict__ offs,
+                         int* __restrict__ sorted) {
+  extern __shared__ int wcnt[];  // [kScatterWarps][E]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int* cnt = wcnt + warp * E;
+  for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  const int s0 = blockIdx.x * kAlignChunk + warp * kSliceLen;
+  const int s1 = min(n, s0 + kSliceLen);
+  for (int base = s0; base < s1; base += 32) {
+    const int f = base + lane;
+    const bool v = f < s1;
+    int e = v ? __ldg(ids + f) : -1;
+    if (v && (unsigned)e >= (unsigned)E) e = 0;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (v && (peers & lt) == 0u) cnt[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = offs[(size_t)blockIdx.x * E + e];
+    for (int w = 0; w < kScatterWarps; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int base = s0; base < s1; base += 32) {
+    const int f = base + lane;
+    const bool v = f < s1;
+    int e = v ? __ldg(ids + f) : -1;
+    if (v && (unsigned)e >= (unsigned)E) e = 0;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    int slot = 0;
+    if (v) slot = cnt[e] + __popc(peers & lt);
+    __syncwarp();
+    if (v) {
+      sorted[slot] = f;
+      if ((peers & lt) == 0u) cnt[e] += __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+// x_perm[p] = x[sorted[p] / k] for real entries, zeros for the padding sentinel.
+__global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restrict__ x, int H8,
+                                                          const int* __restrict__ sorted,
+                                                          const int* __restrict__ npp, int n,
+                                                          int k, int max_rows,
+                                                          uint4* __restrict__ xp) {
+  int rows = *npp;
+  if (rows > max_rows) rows = max_rows;
+  for (int p = blockIdx.x; p < rows; p += gridDim.x) {
+    const int f = sorted[p];
+    uint4* dst = xp + (size_t)p * H8;
+    if (f >= 0 && f < n) {
+      const uint4* src = x + (size_t)(f / k) * H8;
+      for (int i = threadIdx.x; i < H8; i += blockDim.x) dst[i] = __ldg(src + i);
+    } else {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int i = threadIdx.x; i < H8; i += blockDim.x) dst[i] = z;
+    }
+  }
+}
+
+size_t align_scratch_bytes(int n, int E) {
+  const size_t C = (size_t)((n + kAlignChunk - 1) / kAlignChunk);
+  return 2 * C * (size_t)E * sizeof(int);
+}
+
+cudaError_t launch_align(const int* ids, int n, int E, int bs, int* sorted, int* expert_ids,
+                         int max_blocks, int* npp, void* scratch, int* status,
+                         cudaStream_t stream) {
+  const int C = (n + kAlignChunk - 1) / kAlignChunk;
+  int* counts = static_cast<int*>(scratch);
+  int* offs = counts + (size_t)C * E;
+  const size_t shm = (size_t)E * sizeof(int);
+  if (C > 0) align_count_kernel<<<C, 256, shm, stream>>>(ids, n, E, counts, status);
+  align_scan_kernel<<<1, 1024, 0, stream>>>(counts, C, E, bs, n, offs, sorted, expert_ids,
+                                            max_blocks, npp);
+  if (C > 0)
+    align_scatter_kernel<<<C, kScatterWarps * 32, shm * kScatterWarps, stream>>>(ids, n, E, offs,
+                                                                              sorted);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const void* x, int H, const int* sorted, const int* npp, int n, int k,
+                          int max_rows, void* x_perm, cudaStream_t stream) {
+  int blocks = num_sms() * 8;
+  if (blocks > max_rows) blocks = max_rows;
+  if (blocks < 1) blocks = 1;
+  gather_rows_kernel<<<blocks, 128, 0, stream>>>(static_cast<const uint4*>(x), H / 8, sorted,
+                                                  npp, n, k, max_rows,
+                                                  static_cast<uint4*>(x_perm));
+  return cudaGetLastError();
+}
+
+}  // namespace gbmoe

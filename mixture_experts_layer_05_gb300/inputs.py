@@ -125,11 +125,13 @@ def make_tokens(w: MoEWorkload, T: int, seed: int = 0, margin_fn=None,
                torch.bfloat16)
     logits = _draw_logits(w, T, f"logits/T{T}", seed)
     if margin_fn is not None and T > 0:
+        rows = torch.arange(T)
         for r in range(max_redraws):
-            bad = torch.nonzero(torch.as_tensor(margin_fn(logits)) < min_margin).flatten()
+            bad = rows[torch.as_tensor(margin_fn(logits[rows])) < min_margin]
             if bad.numel() == 0:
                 break
             logits[bad] = _draw_logits(w, int(bad.numel()), f"logits/T{T}/redraw{r}", seed)
+            rows = bad
         else:
             raise RuntimeError("could not draw router logits with the requested margin")
     return x, logits

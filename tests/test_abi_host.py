@@ -1,0 +1,135 @@
+"""The C ABI on the host: every declared symbol is exported, argument validation
+returns the documented status before anything touches a GPU, workspace sizing.
+
+No compute call runs here (these tests need no GPU)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from mixture_experts_layer_05_gb300 import binding, configs
+from mixture_experts_layer_05_gb300 import build as build_mod
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "gbmoe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return binding.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\w[\w ]*?\b(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declarations_match_binding():
+    assert sorted(binding.EXPORTS) == _declared()
+
+
+def test_every_declared_symbol_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    for name in _declared():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def _cfg(**kw):
+    d = dict(num_experts=8, top_k=2, hidden_size=128, intermediate_size=256)
+    d.update(kw)
+    return binding.make_config(**d)
+
+
+def _topk(lib, cfg, T=4, logits=1, w=1, ids=1):
+    P = ctypes.c_void_p
+    return lib.moe_topk(ctypes.byref(cfg), T, P(logits), None, P(w), P(ids), None)
+
+
+def test_topk_validation(lib):
+    ok = _cfg()
+    # T = 0 is a no-op, before any pointer is looked at
+    assert lib.moe_topk(ctypes.byref(ok), 0, None, None, None, None, None) == binding.OK
+    assert lib.moe_topk(None, 4, None, None, None, None, None) == binding.ERR_INVALID_ARG
+    assert lib.moe_topk(ctypes.byref(ok), 4, None, None, None, None, None) == binding.ERR_INVALID_ARG
+    assert _topk(lib, ok, T=-1) == binding.ERR_INVALID_ARG
+    # sigmoid scoring needs grouped routing (FusedMoE constructor)
+    assert _topk(lib, _cfg(scoring_func="sigmoid")) == binding.ERR_UNSUPPORTED
+    # grouped routing needs both group arguments
+    assert _topk(lib, _cfg(use_grouped_topk=True, num_expert_group=4)) == binding.ERR_INVALID_ARG
+    assert _topk(lib, _cfg(use_grouped_topk=True, topk_group=2)) == binding.ERR_INVALID_ARG
+    assert _topk(lib, _cfg(use_grouped_topk=True, num_expert_group=3, topk_group=1)) == \
+        binding.ERR_INVALID_ARG                                   # E % G != 0
+    assert _topk(lib, _cfg(use_grouped_topk=True, num_expert_group=4, topk_group=5)) == \
+        binding.ERR_INVALID_ARG                                   # g > G
+    assert _topk(lib, _cfg(top_k=3, use_grouped_topk=True, num_expert_group=8, topk_group=2)) == \
+        binding.ERR_INVALID_ARG                                   # k > g * E/G
+    assert _topk(lib, _cfg(top_k=9)) == binding.ERR_INVALID_ARG   # k > E
+    assert _topk(lib, _cfg(top_k=0)) == binding.ERR_INVALID_ARG
+    assert _topk(lib, _cfg(num_experts=2000, top_k=2)) == binding.ERR_INVALID_ARG
+    assert _topk(lib, _cfg(routed_scaling_factor=float("nan"))) == binding.ERR_INVALID_ARG
+
+
+def _fwd(lib, cfg, T=4, ws_bytes=1 << 40, ptr=256, shared=False, events=None, nev=0):
+    P = ctypes.c_void_p
+    sw = P(ptr) if shared else None
+    return lib.moe_forward_events(ctypes.byref(cfg), T, P(ptr), P(ptr), None, P(ptr), P(ptr), sw,
+                                  sw, P(ptr), P(ptr), ws_bytes, events, nev, None)
+
+
+def test_forward_validation(lib):
+    ok = _cfg()
+    assert _fwd(lib, _cfg(activation=1)) == binding.ERR_UNSUPPORTED     # only silu
+    assert _fwd(lib, _cfg(is_act_and_mul=0)) == binding.ERR_UNSUPPORTED
+    assert _fwd(lib, _cfg(hidden_size=96)) == binding.ERR_UNSUPPORTED    # H % 128
+    assert _fwd(lib, _cfg(intermediate_size=200)) == binding.ERR_UNSUPPORTED
+    assert _fwd(lib, _cfg(hidden_size=0)) == binding.ERR_INVALID_ARG
+    assert _fwd(lib, ok, T=-3) == binding.ERR_INVALID_ARG
+    assert _fwd(lib, ok, ptr=258) == binding.ERR_INVALID_ARG             # bf16 not 16-B aligned
+    assert _fwd(lib, ok, shared=True) == binding.ERR_INVALID_ARG         # shared weights, I_s = 0
+    assert _fwd(lib, _cfg(shared_intermediate_size=128)) == binding.ERR_INVALID_ARG
+    assert _fwd(lib, ok, nev=5) == binding.ERR_INVALID_ARG               # events NULL, count 5
+    need = lib.moe_forward_workspace_size(ctypes.byref(ok), 4)
+    assert need > 0
+    assert _fwd(lib, ok, ws_bytes=need - 1) == binding.ERR_WORKSPACE
+    assert _fwd(lib, ok, T=0) == binding.OK                               # empty batch: no-op
+
+
+def test_align_validation(lib):
+    P = ctypes.c_void_p
+    f = lib.moe_align_block_size
+    assert f(P(256), 0, 2, 8, 16, None, None, None, None, 0, None) == binding.OK
+    assert f(None, 4, 2, 8, 16, P(256), P(256), P(256), P(256), 1 << 30, None) == \
+        binding.ERR_INVALID_ARG
+    assert f(P(256), 4, 2, 8, 0, P(256), P(256), P(256), P(256), 1 << 30, None) == \
+        binding.ERR_INVALID_ARG                                   # block size 0
+    assert f(P(256), 4, 9, 8, 16, P(256), P(256), P(256), P(256), 1 << 30, None) == \
+        binding.ERR_INVALID_ARG                                   # k > E
+    need = lib.moe_align_block_size_workspace_size(4, 2, 8)
+    assert f(P(256), 4, 2, 8, 16, P(256), P(256), P(256), P(256), need - 1, None) == \
+        binding.ERR_WORKSPACE
+    assert f(P(256), 4, 2, 8, 16, P(256), P(256), P(256), P(257), need, None) == \
+        binding.ERR_WORKSPACE                                     # misaligned workspace
+
+
+def test_workspace_sizes_monotone(lib):
+    for w in configs.WORKLOADS.values():
+        cfg = binding.config_from_workload(w)
+        sizes = [lib.moe_forward_workspace_size(ctypes.byref(cfg), T) for T in (0, 1, 16, 4096)]
+        assert all(s > 0 for s in sizes) and sizes == sorted(sizes), (w.name, sizes)
+        lay = binding.moe_forward_workspace_layout(cfg, 16)
+        assert lay.total == sizes[2]
+        offs = [lay.status, lay.topk_weights, lay.topk_ids, lay.sorted_token_ids, lay.expert_ids,
+                lay.num_tokens_post_padded, lay.act]
+        assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert lib.moe_forward_block_size(ctypes.byref(binding.config_from_workload(configs.TINY)),
+                                      16) in (16, 32, 64, 128)
+
+
+def test_device_status_validation(lib):
+    v = ctypes.c_int32(0)
+    assert lib.moe_get_device_status(None, ctypes.byref(v), None) == binding.ERR_INVALID_ARG

@@ -1,0 +1,232 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on the GPU.
+
+Routing (topk_ids) and align (sorted_token_ids, expert_ids, num_tokens_post_padded)
+must match bit for bit; topk_weights within the fp32 rounding bound of a softmax over
+E terms; the layer output within |y - y_ref| <= 2e-2 |y_ref| + 1e-2 rms(y_ref).
+Inputs are seeded; every routing decision is at least 1e-3 from a tie.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_layer_05_gb300 import binding, configs, inputs
+from tests.moe_cases import check_close, oracle_cfg, tokens
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def weight_rtol(w) -> float:
+    """fp32 softmax/sigmoid + renormalize vs fp64: (E + 2k + 16) units of 2^-24."""
+    return (w.num_experts + 2 * w.top_k + 16) * 2.0 ** -24
+
+
+def _small(w, **kw):
+    return configs.shrink(w, **kw)
+
+
+SMALL = {
+    "tiny": configs.TINY,
+    "mixtral": _small(configs.MIXTRAL, hidden_size=256, intermediate_size=384),
+    "dsv2": _small(configs.DSV2, hidden_size=384, intermediate_size=128,
+                   shared_intermediate_size=256),
+    "dsv3": _small(configs.DSV3, hidden_size=256, intermediate_size=256,
+                   shared_intermediate_size=256),
+    "skew": _small(configs.SKEW, hidden_size=512, intermediate_size=128,
+                   shared_intermediate_size=128),
+}
+
+
+def _routing(w, T, seed=0):
+    wts = inputs.make_weights(_small(w, hidden_size=128, intermediate_size=128,
+                                     shared_intermediate_size=0), seed)
+    bias = wts["bias"]
+    _, logits = tokens(w, T, bias, seed)
+    return logits, bias
+
+
+# ------------------------------------------------------------------ moe_topk
+@pytest.mark.parametrize("name", list(configs.WORKLOADS))
+@pytest.mark.parametrize("T", [1, 37, 1000])
+def test_topk_bitexact(cuda_lib, name, T):
+    w = configs.WORKLOADS[name]
+    logits, bias = _routing(w, T)
+    cfg = binding.config_from_workload(w)
+    tw = torch.empty(T, w.top_k, dtype=torch.float32, device=DEV)
+    ti = torch.empty(T, w.top_k, dtype=torch.int32, device=DEV)
+    binding.moe_topk(cfg, logits.to(DEV), None if bias is None else bias.to(DEV), tw, ti)
+    torch.cuda.synchronize()
+    W, ids = oracle.select_experts(logits, bias, **oracle_cfg(w))
+    assert np.array_equal(ti.cpu().numpy(), ids), "topk_ids differ"
+    np.testing.assert_allclose(tw.cpu().numpy(), W, rtol=weight_rtol(w), atol=0)
+
+
+@pytest.mark.parametrize("variant", ["softmax_bias_ungrouped", "sigmoid_grouped_nobias",
+                                     "softmax_grouped_bias_renorm"])
+def test_topk_other_branches(cuda_lib, variant):
+    """The fused_topk_bias branch and the two other bias/scoring combinations."""
+    base = dict(num_experts=64, top_k=4, renormalize=True)
+    if variant == "softmax_bias_ungrouped":
+        w = _small(configs.DSV3, scoring_func="softmax", use_grouped_topk=False, **base)
+    elif variant == "sigmoid_grouped_nobias":
+        w = _small(configs.DSV3, has_bias=False, num_expert_group=8, topk_group=2, **base)
+    else:
+        w = _small(configs.DSV2, has_bias=True, bias_std=0.01, num_expert_group=4, topk_group=2,
+                   routed_scaling_factor=1.5, **base)
+    logits, bias = _routing(w, 300)
+    cfg = binding.config_from_workload(w)
+    tw = torch.empty(300, 4, dtype=torch.float32, device=DEV)
+    ti = torch.empty(300, 4, dtype=torch.int32, device=DEV)
+    binding.moe_topk(cfg, logits.to(DEV), None if bias is None else bias.to(DEV), tw, ti)
+    W, ids = oracle.select_experts(logits, bias, **oracle_cfg(w))
+    assert np.array_equal(ti.cpu().numpy(), ids)
+    np.testing.assert_allclose(tw.cpu().numpy(), W, rtol=weight_rtol(w), atol=0)
+
+
+# ------------------------------------------------------------------ moe_align_block_size
+def _align_gpu(ids_np, E, bs):
+    T, k = ids_np.shape
+    n = T * k
+    max_sorted = n + E * (bs - 1)
+    ids = torch.from_numpy(ids_np.astype(np.int32)).to(DEV)
+    srt = torch.full((max_sorted,), -7, dtype=torch.int32, device=DEV)
+    eid = torch.full((max_sorted // bs + 1,), -7, dtype=torch.int32, device=DEV)
+    npp = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = binding.alloc_workspace(binding.moe_align_block_size_workspace_size(T, k, E))
+    binding.moe_align_block_size(ids, E, bs, srt, eid, npp, ws)
+    assert binding.moe_get_device_status(ws) == binding.OK
+    return srt.cpu().numpy(), eid.cpu().numpy(), int(npp.item())
+
+
+@pytest.mark.parametrize("T,k,E,bs,skew", [
+    (1, 1, 1, 1, False), (1, 2, 8, 128, False), (5, 3, 7, 16, False), (16, 2, 8, 128, False),
+    (1000, 8, 256, 64, False), (3000, 6, 160, 128, False), (4097, 2, 8, 32, True),
+    (20000, 8, 256, 128, True), (700, 4, 1024, 16, False)])
+def test_align_bitexact(cuda_lib, T, k, E, bs, skew):
+    rng = np.random.default_rng(T * 31 + E)
+    if skew:
+        p = 1.0 / np.arange(1, E + 1) ** 1.2
+        p /= p.sum()
+        ids = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)])
+    else:
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    srt, eid, npp = _align_gpu(ids, E, bs)
+    s_ref, e_ref, n_ref = oracle.moe_align_block_size(ids, E, bs)
+    assert npp == n_ref
+    assert np.array_equal(srt[:npp], s_ref)
+    assert np.array_equal(eid[:npp // bs], e_ref)
+    assert (eid[npp // bs:] == -1).all()
+
+
+# ------------------------------------------------------------------ the layer, small shapes
+def _layer(w, wts, T):
+    cfg = binding.config_from_workload(w)
+    d = {k: (None if v is None else v.to(DEV)) for k, v in wts.items()}
+    return binding.FusedMoE(cfg, d["w13"], d["w2"], d["bias"], d["shared_w13"], d["shared_w2"],
+                            max_tokens=max(T, 1)), d
+
+
+def _routing_from_ws(layer, T, k):
+    lay = binding.moe_forward_workspace_layout(layer.cfg, T)
+    ws = layer.workspace
+    ids = ws[lay.topk_ids:lay.topk_ids + T * k * 4].view(torch.int32).cpu().numpy()
+    tw = ws[lay.topk_weights:lay.topk_weights + T * k * 4].view(torch.float32).cpu().numpy()
+    return ids.reshape(T, k), tw.reshape(T, k)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("T", [1, 16, 203])
+def test_forward_small(cuda_lib, name, T):
+    w = SMALL[name]
+    wts = inputs.make_weights(w, 0)
+    x, logits = tokens(w, T, wts["bias"])
+    layer, d = _layer(w, wts, T)
+    y = layer(x.to(DEV), logits.to(DEV))
+    torch.cuda.synchronize()
+    assert layer.device_status() == binding.OK
+    y_ref, parts = oracle.fused_moe(x, logits, wts["bias"], wts["w13"], wts["w2"],
+                                    wts["shared_w13"], wts["shared_w2"], return_parts=True,
+                                    **oracle_cfg(w))
+    ids, tw = _routing_from_ws(layer, T, w.top_k)
+    assert np.array_equal(ids, parts["topk_ids"])
+    np.testing.assert_allclose(tw, parts["topk_weights"], rtol=weight_rtol(w), atol=0)
+    check_close(y, y_ref, f"{name} T={T}")
+
+
+def test_forward_deterministic(cuda_lib):
+    w = SMALL["dsv3"]
+    wts = inputs.make_weights(w, 0)
+    x, logits = tokens(w, 300, wts["bias"])
+    layer, _ = _layer(w, wts, 300)
+    y1 = layer(x.to(DEV), logits.to(DEV)).clone()
+    y2 = layer(x.to(DEV), logits.to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    assert layer.device_status() == binding.OK
+
+
+def test_forward_empty_and_single_expert(cuda_lib):
+    # empty batch: a no-op that leaves the output untouched
+    w = SMALL["mixtral"]
+    wts = inputs.make_weights(w, 0)
+    layer, _ = _layer(w, wts, 4)
+    out = torch.full((0, w.hidden_size), 1.0, dtype=torch.bfloat16, device=DEV)
+    layer(torch.empty(0, w.hidden_size, dtype=torch.bfloat16, device=DEV),
+          torch.empty(0, w.num_experts, device=DEV), out=out)
+    # E = 1, k = 1: a dense SwiGLU MLP
+    w1 = _small(configs.MIXTRAL, num_experts=1, top_k=1, hidden_size=256, intermediate_size=256)
+    wts1 = inputs.make_weights(w1, 0)
+    x, logits = tokens(w1, 130, None)
+    layer1, _ = _layer(w1, wts1, 130)
+    y = layer1(x.to(DEV), logits.to(DEV))
+    y_ref = oracle.fused_moe(x, logits, None, wts1["w13"], wts1["w2"], **oracle_cfg(w1))
+    check_close(y, y_ref, "E=1 k=1")
+    assert layer1.device_status() == binding.OK
+
+
+# ------------------------------------------------------------------ full sizes, sampled
+class _Experts:
+    """Expert slices copied to the host on demand (the oracle indexes w[e])."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, e):
+        return self.t[e].cpu()
+
+
+FULL = [("mixtral", 4096, 8), ("dsv2", 4096, 6), ("dsv3", 8192, 4), ("skew", 16384, 4)]
+
+
+@pytest.mark.parametrize("name,T,n_sample", FULL)
+def test_forward_full_size_sampled(cuda_lib, name, T, n_sample):
+    """Full shapes at the largest token count: routing over all tokens bit-exact, the
+    output of sampled tokens (first, last, random) against the oracle row by row."""
+    w = configs.WORKLOADS[name]
+    torch.cuda.empty_cache()
+    wts = inputs.make_weights(w, 0, device=DEV)
+    bias_cpu = None if wts["bias"] is None else wts["bias"].cpu()
+    x, logits = tokens(w, T, bias_cpu)
+    layer = binding.FusedMoE(binding.config_from_workload(w), wts["w13"], wts["w2"], wts["bias"],
+                             wts["shared_w13"], wts["shared_w2"], max_tokens=T)
+    y = layer(x.to(DEV), logits.to(DEV))
+    torch.cuda.synchronize()
+    assert layer.device_status() == binding.OK
+    W, ids_ref = oracle.select_experts(logits, bias_cpu, **oracle_cfg(w))
+    ids, tw = _routing_from_ws(layer, T, w.top_k)
+    assert np.array_equal(ids, ids_ref)
+    np.testing.assert_allclose(tw, W, rtol=weight_rtol(w), atol=0)
+    rng = np.random.default_rng(T)
+    rows = sorted({0, T - 1, *rng.choice(T, size=n_sample - 2, replace=False).tolist()})
+    y_ref = oracle.fused_moe_rows(x[rows], logits[rows], bias_cpu, _Experts(wts["w13"]),
+                                  _Experts(wts["w2"]),
+                                  None if wts["shared_w13"] is None else wts["shared_w13"].cpu(),
+                                  None if wts["shared_w2"] is None else wts["shared_w2"].cpu(),
+                                  **oracle_cfg(w))
+    check_close(y[rows], y_ref, f"{name} T={T} rows {rows}")
+    del layer, wts
+    torch.cuda.empty_cache()
