@@ -139,6 +139,31 @@ gbmoe_status_t moe_align_block_size(const int32_t* topk_ids, int32_t num_tokens,
                                     size_t workspace_bytes, gbmoe_stream_t stream);
 
 /*
+ * moe_align_block_size_no_workspace: moe_align_block_size for callers that cannot
+ * allocate device memory. The pages have no counterpart; this entry point exists for
+ * the deployment, not the method. Plugins hosted by a framework that owns and
+ * pre-plans every device allocation (an inference server with a fixed memory pool, a
+ * runtime whose extensions may not call cudaMalloc) have no workspace to pass, so
+ * this variant keeps its scratch in a fixed 1 MiB device array inside the library and
+ * allocates nothing. Same arguments and outputs as moe_align_block_size, minus the
+ * workspace.
+ *  - Limit: requests needing more than 1 MiB of scratch
+ *    (2 * ceil(T*top_k / 2048) * num_experts * 4 bytes) return GBMOE_ERR_WORKSPACE.
+ *  - The array is shared by every call on a device and keeps the last call's
+ *    contents; each call overwrites what it reads, so nothing must start at zero.
+ *    Calls that overlap on the GPU (unordered streams) race on it: do not issue them.
+ *  - The first call on a device looks up the array's device address with that device
+ *    current; make that first call before any stream capture.
+ *  - No status word: a topk_id outside [0, E) is counted as expert 0, unreported.
+ */
+gbmoe_status_t moe_align_block_size_no_workspace(const int32_t* topk_ids, int32_t num_tokens,
+                                                 int32_t top_k, int32_t num_experts,
+                                                 int32_t block_size, int32_t* sorted_token_ids,
+                                                 int32_t* expert_ids,
+                                                 int32_t* num_tokens_post_padded,
+                                                 gbmoe_stream_t stream);
+
+/*
  * moe_forward: the whole layer, from router logits to the combined output.
  *  1. moe_topk (above);
  *  2. align by expert (above) with the block size moe_forward_block_size(),

@@ -24,6 +24,7 @@ NUM_STAGE_EVENTS = 5
 
 # every entry point declared in include/gbmoe.h
 EXPORTS = ("moe_topk", "moe_align_block_size_workspace_size", "moe_align_block_size",
+           "moe_align_block_size_no_workspace",
            "moe_forward_workspace_size", "moe_forward_block_size", "moe_forward",
            "moe_forward_events", "moe_forward_workspace_layout", "moe_get_device_status",
            "gbmoe_version")
@@ -89,6 +90,7 @@ def load() -> ctypes.CDLL:
         "moe_topk": (I32, [CP, I32, P, P, P, P, P]),
         "moe_align_block_size_workspace_size": (SZ, [I32, I32, I32]),
         "moe_align_block_size": (I32, [P, I32, I32, I32, I32, P, P, P, P, SZ, P]),
+        "moe_align_block_size_no_workspace": (I32, [P, I32, I32, I32, I32, P, P, P, P]),
         "moe_forward_workspace_size": (SZ, [CP, I32]),
         "moe_forward_block_size": (I32, [CP, I32]),
         "moe_forward": (I32, [CP, I32, P, P, P, P, P, P, P, P, P, SZ, P]),
@@ -150,6 +152,20 @@ def moe_align_block_size(topk_ids, num_experts, block_size, sorted_token_ids, ex
         _p(topk_ids), T, k, num_experts, block_size, _p(sorted_token_ids), _p(expert_ids),
         _p(num_tokens_post_padded), _p(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def moe_align_block_size_no_workspace(topk_ids, num_experts, block_size, sorted_token_ids,
+                                      expert_ids, num_tokens_post_padded, stream=None):
+    """moe_align_block_size with the library's built-in 1 MiB scratch (no workspace).
+
+    For callers that may not allocate device memory (a host framework owns every
+    allocation); calls that overlap on the GPU share that scratch and must not be issued.
+    """
+    _need(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    _check("moe_align_block_size_no_workspace", load().moe_align_block_size_no_workspace(
+        _p(topk_ids), T, k, num_experts, block_size, _p(sorted_token_ids), _p(expert_ids),
+        _p(num_tokens_post_padded), _stream(stream)))
 
 
 def moe_forward_workspace_size(cfg: Config, max_num_tokens: int) -> int:
