@@ -1,5 +1,6 @@
 // Expert align (stable counting sort of the flat (token, slot) indices by expert,
-// runs padded to the block size) and the gather of hidden rows into that order.
+// runs padded to the block size) and the gather of the real hidden rows into that
+// order (padding rows are left unwritten).
 //
 // The FusedMoE forward (vLLM `fused_moe/layer` page, the Triton fused_moe path
 // behind `UnquantizedFusedMoEMethod`) runs its expert GEMMs over tokens grouped by
@@ -10,12 +11,14 @@
 //   count   per chunk of kAlignChunk flat indices, per-expert counts (shared atomics,
 //           order-free);
 //   scan    one CTA: per-expert totals, padded runs, exclusive scan over experts,
-//           per-(chunk, expert) start offsets, sentinel padding, expert_ids;
+//           per-(chunk, expert) start offsets, sentinel padding, expert_ids, and
+//           (for the GEMMs) each block's expert segment (first block, block count);
 //   scatter one CTA per chunk; its warps own consecutive slices, count them, take
 //           start offsets in slice order, and walk their slices in order, ranking
 //           equal experts in each 32-wide step with __match_any_sync: stable order.
 #include "common.cuh"
 #include "kernels.h"
+#include "route.cuh"
 
 namespace gbmoe {
 
@@ -45,7 +48,8 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(const int* __restrict_
                                                           int* __restrict__ offs,
                                                           int* __restrict__ sorted,
                                                           int* __restrict__ expert_ids,
-                                                          int max_blocks, int* __restrict__ npp) {
+                                                          int max_blocks, int* __restrict__ npp,
+                                                          int2* __restrict__ block_seg) {
   __shared__ int warp_tot[32];
   __shared__ int s_total;
   const int e = threadIdx.x;
@@ -83,7 +87,10 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(const int* __restrict_
       run += counts[(size_t)c * E + e];
     }
     for (int p = start + tot; p < start + pad; ++p) sorted[p] = n;
-    for (int b = start / bs; b < (start + pad) / bs; ++b) expert_ids[b] = e;
+    for (int b = start / bs; b < (start + pad) / bs; ++b) {
+      expert_ids[b] = e;
+      if (block_seg) block_seg[b] = make_int2(start / bs, pad / bs);
+    }
   }
   const int total = s_total;
   if (e == 0) *npp = total;
@@ -99,7 +106,7 @@ constexpr int kSliceLen = kAlignChunk / kScatterWarps;
 
 __global__ void __launch_bounds__(kScatterWarps * 32)
     align_scatter_kernel(const int* __restrict__ ids, int n, int E, const int* __restrict__ offs,
-                         int* __restrict__ sorted) {
+                         int* __restrict__ sorted, int* __restrict__ inv) {
   extern __shared__ int wcnt[];  // [kScatterWarps][E]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int* cnt = wcnt + warp * E;
@@ -138,31 +145,191 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
     __syncwarp();
     if (v) {
       sorted[slot] = f;
+      if (inv) inv[f] = slot;
       if ((peers & lt) == 0u) cnt[e] += __popc(peers);
     }
     __syncwarp();
   }
 }
 
-// x_perm[p] = x[sorted[p] / k] for real entries, zeros for the padding sentinel.
+// x_perm[inv[f]] = x[f / k] for every flat index f: only the T*k real rows are written.
+// Padding rows of x_perm are never written: a GEMM output row depends on its own A row
+// only, and padding rows are never stored or read back.
 __global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restrict__ x, int H8,
-                                                          const int* __restrict__ sorted,
-                                                          const int* __restrict__ npp, int n,
+                                                          const int* __restrict__ inv, int n,
                                                           int k, int max_rows,
                                                           uint4* __restrict__ xp) {
-  int rows = *npp;
-  if (rows > max_rows) rows = max_rows;
-  for (int p = blockIdx.x; p < rows; p += gridDim.x) {
-    const int f = sorted[p];
+  for (int f = blockIdx.x; f < n; f += gridDim.x) {
+    const int p = inv[f];
+    if (p < 0 || p >= max_rows) continue;
+    const uint4* src = x + (size_t)(f / k) * H8;
     uint4* dst = xp + (size_t)p * H8;
-    if (f >= 0 && f < n) {
-      const uint4* src = x + (size_t)(f / k) * H8;
-      for (int i = threadIdx.x; i < H8; i += blockDim.x) dst[i] = __ldg(src + i);
-    } else {
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      for (int i = threadIdx.x; i < H8; i += blockDim.x) dst[i] = z;
+    for (int i = threadIdx.x; i < H8; i += blockDim.x) dst[i] = __ldg(src + i);
+  }
+}
+
+// Small batches (T*k <= kAlignChunk): routing and the whole align in one CTA of
+// kSmallWarps warps, no global scratch. Warps route tokens (route.cuh) into shared
+// memory, count their slices of the flat indices per expert, the CTA scans the padded
+// runs (four experts per thread, E <= 1024) and turns the per-warp counts into start
+// offsets in slice order, and each warp scatters its slice in order (stable).
+constexpr int kSmallWarps = 8;
+constexpr int kSmallThreads = kSmallWarps * 32;
+
+template <int EPT>
+__global__ void __launch_bounds__(kSmallThreads)
+    route_align_small_kernel(TopkArgs a, int bs, int* __restrict__ sorted,
+                             int* __restrict__ expert_ids, int max_blocks, int* __restrict__ npp,
+                             int2* __restrict__ block_seg, int* __restrict__ inv,
+                             const uint4* __restrict__ x, int H8, uint4* __restrict__ xp) {
+  extern __shared__ int sm[];
+  const int n = a.T * a.k, E = a.E;
+  int* s_ids = sm;                                   // [n]
+  int* wcnt = sm + ((n + 31) & ~31);                 // [kSmallWarps][E]
+  __shared__ int warp_tot[kSmallWarps];
+  __shared__ int s_total;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) wcnt[i] = 0;
+  // 1. routing
+  for (int t = warp; t < a.T; t += kSmallWarps) {
+    const int id = route_token_warp<EPT>(a, t, lane);
+    if (lane < a.k) s_ids[t * a.k + lane] = id;
+  }
+  __syncthreads();
+  // 2. per-warp slice counts
+  const unsigned lt = (1u << lane) - 1u;
+  const int slice = (n + kSmallWarps - 1) / kSmallWarps;
+  const int s0 = warp * slice, s1 = min(n, s0 + slice);
+  int* cnt = wcnt + warp * E;
+  for (int base = s0; base < s1; base += 32) {
+    const int f = base + lane;
+    const bool v = f < s1;
+    int e = v ? s_ids[f] : -1;
+    if (v && (unsigned)e >= (unsigned)E) e = 0;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (v && (peers & lt) == 0u) cnt[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // 3. padded runs, exclusive scan over experts (thread j owns experts 4j .. 4j+3)
+  int tot[4], pad[4], sum = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = 4 * threadIdx.x + i;
+    tot[i] = 0;
+    if (e < E)
+      for (int w = 0; w < kSmallWarps; ++w) tot[i] += wcnt[w * E + e];
+    pad[i] = (tot[i] + bs - 1) / bs * bs;
+    sum += pad[i];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int w = 0; w < kSmallWarps; ++w) {
+      const int v = warp_tot[w];
+      warp_tot[w] = run;
+      run += v;
+    }
+    s_total = run;
+  }
+  __syncthreads();
+  int start = warp_tot[warp] + incl - sum;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = 4 * threadIdx.x + i;
+    if (e < E) {
+      int run = start;
+      for (int w = 0; w < kSmallWarps; ++w) {
+        const int c = wcnt[w * E + e];
+        wcnt[w * E + e] = run;
+        run += c;
+      }
+      for (int p = start + tot[i]; p < start + pad[i]; ++p) sorted[p] = n;
+      for (int b = start / bs; b < (start + pad[i]) / bs; ++b) {
+        expert_ids[b] = e;
+        if (block_seg) block_seg[b] = make_int2(start / bs, pad[i] / bs);
+      }
+    }
+    start += pad[i];
+  }
+  const int total = s_total;
+  if (threadIdx.x == 0) *npp = total;
+  for (int b = total / bs + threadIdx.x; b < max_blocks; b += blockDim.x) expert_ids[b] = -1;
+  __syncthreads();
+  // 4. stable scatter of each warp's slice
+  for (int base = s0; base < s1; base += 32) {
+    const int f = base + lane;
+    const bool v = f < s1;
+    int e = v ? s_ids[f] : -1;
+    if (v && (unsigned)e >= (unsigned)E) e = 0;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    int slot = 0;
+    if (v) slot = cnt[e] + __popc(peers & lt);
+    __syncwarp();
+    if (v) {
+      sorted[slot] = f;
+      if (inv) inv[f] = slot;
+      if ((peers & lt) == 0u) cnt[e] += __popc(peers);
+    }
+    __syncwarp();
+    // 5. tiny batches: the warp also copies its rows into expert order
+    if (xp) {
+      for (int i = 0; i < 32; ++i) {
+        const int fi = base + i;
+        if (fi >= s1) break;
+        const int pi = __shfl_sync(0xffffffffu, slot, i);
+        const uint4* src = x + (size_t)(fi / a.k) * H8;
+        uint4* dst = xp + (size_t)pi * H8;
+        for (int j = lane; j < H8; j += 32) dst[j] = __ldg(src + j);
+      }
     }
   }
+}
+
+struct RouteAlignSmall {
+  TopkArgs a;
+  int bs;
+  int* sorted;
+  int* expert_ids;
+  int max_blocks;
+  int* npp;
+  int2* block_seg;
+  int* inv;
+  const uint4* x;
+  int H8;
+  uint4* xp;
+  cudaStream_t stream;
+  template <int EPT>
+  void operator()() {
+    const int n = a.T * a.k;
+    const size_t shm = (size_t)(((n + 31) & ~31) + kSmallWarps * a.E) * sizeof(int);
+    route_align_small_kernel<EPT><<<1, kSmallThreads, shm, stream>>>(
+        a, bs, sorted, expert_ids, max_blocks, npp, block_seg, inv, x, H8, xp);
+  }
+};
+
+bool route_align_small_ok(int T, int k, int E) {
+  return T * k <= kAlignChunk && E <= 1024;
+}
+
+cudaError_t launch_route_align_small(const gbmoe_config_t& c, int T, const float* logits,
+                                     const float* bias, float* weights, int* ids, int bs,
+                                     int* sorted, int* expert_ids, int max_blocks, int* npp,
+                                     int2* block_seg, int* inv, const void* x, void* x_perm,
+                                     int* status, cudaStream_t stream) {
+  RouteAlignSmall L{make_topk_args(c, T, logits, bias, weights, ids, status), bs, sorted,
+                    expert_ids, max_blocks, npp, block_seg, inv,
+                    static_cast<const uint4*>(x), c.hidden_size / 8,
+                    static_cast<uint4*>(x_perm), stream};
+  dispatch_ept(c.num_experts, L);
+  return cudaGetLastError();
 }
 
 size_t align_scratch_bytes(int n, int E) {
@@ -172,28 +339,27 @@ size_t align_scratch_bytes(int n, int E) {
 
 cudaError_t launch_align(const int* ids, int n, int E, int bs, int* sorted, int* expert_ids,
                          int max_blocks, int* npp, void* scratch, int* status,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, int2* block_seg, int* inv) {
   const int C = (n + kAlignChunk - 1) / kAlignChunk;
   int* counts = static_cast<int*>(scratch);
   int* offs = counts + (size_t)C * E;
   const size_t shm = (size_t)E * sizeof(int);
   if (C > 0) align_count_kernel<<<C, 256, shm, stream>>>(ids, n, E, counts, status);
   align_scan_kernel<<<1, 1024, 0, stream>>>(counts, C, E, bs, n, offs, sorted, expert_ids,
-                                            max_blocks, npp);
+                                            max_blocks, npp, block_seg);
   if (C > 0)
     align_scatter_kernel<<<C, kScatterWarps * 32, shm * kScatterWarps, stream>>>(ids, n, E, offs,
-                                                                              sorted);
+                                                                              sorted, inv);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const void* x, int H, const int* sorted, const int* npp, int n, int k,
-                          int max_rows, void* x_perm, cudaStream_t stream) {
+cudaError_t launch_gather(const void* x, int H, const int* inv, int n, int k, int max_rows,
+                          void* x_perm, cudaStream_t stream) {
   int blocks = num_sms() * 8;
-  if (blocks > max_rows) blocks = max_rows;
-  if (blocks < 1) blocks = 1;
-  gather_rows_kernel<<<blocks, 128, 0, stream>>>(static_cast<const uint4*>(x), H / 8, sorted,
-                                                  npp, n, k, max_rows,
-                                                  static_cast<uint4*>(x_perm));
+  if (blocks > n) blocks = n;
+  if (blocks < 1) return cudaSuccess;
+  gather_rows_kernel<<<blocks, 128, 0, stream>>>(static_cast<const uint4*>(x), H / 8, inv, n, k,
+                                                  max_rows, static_cast<uint4*>(x_perm));
   return cudaGetLastError();
 }
 

@@ -30,6 +30,8 @@ int num_sms() {
 namespace {
 
 constexpr int kMaxTokens = 1 << 22;
+constexpr int kSplitMaxTokens = 64;  // split-K only at decode-sized batches
+constexpr size_t kMaxSplits = 8;
 constexpr size_t kAlign = 256;
 
 size_t up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
@@ -70,8 +72,8 @@ gbmoe_status_t check_layer(const gbmoe_config_t* c) {
 
 struct Layout {
   int bs, n, max_sorted, max_blocks, slots;
-  size_t status, topk_weights, topk_ids, sorted, expert_ids, npp, scratch, x_perm, act, ytok,
-      act_s, total;
+  size_t status, topk_weights, topk_ids, sorted, expert_ids, npp, block_seg, inv, scratch,
+      x_perm, act, ytok, act_s, part_r, part_s, total;
 };
 
 Layout layout_for(const gbmoe_config_t& c, int T) {
@@ -96,16 +98,27 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   o = up(o + (size_t)L.max_blocks * 4);
   L.npp = o;
   o = up(o + 4);
+  L.block_seg = o;
+  o = up(o + (size_t)L.max_blocks * 8);
+  L.inv = o;
+  o = up(o + (size_t)L.n * 4);
   L.scratch = o;
   o = up(o + align_scratch_bytes(L.n, E));
   L.x_perm = o;
   o = up(o + (size_t)L.max_sorted * H * 2);
   L.act = o;
   o = up(o + (size_t)L.max_sorted * I * 2);
+  // split-K copies exist only for T <= kSplitMaxTokens; every region grows with T
+  const size_t ts = (size_t)(T < kSplitMaxTokens ? T : kSplitMaxTokens);
+  const size_t ytok_rows = (size_t)T > kMaxSplits * ts ? (size_t)T : kMaxSplits * ts;
   L.ytok = o;
-  o = up(o + (size_t)T * L.slots * H * 4);
+  o = up(o + ytok_rows * L.slots * H * 4);
   L.act_s = o;
   o = up(o + (size_t)T * Is * 2);
+  L.part_r = o;
+  o = up(o + kMaxSplits * ts * k * 2 * I * 4);
+  L.part_s = o;
+  o = up(o + kMaxSplits * ts * 2 * Is * 4);
   L.total = o;
   return L;
 }
@@ -116,6 +129,34 @@ T* at(void* ws, size_t off) {
 }
 
 gbmoe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA; }
+
+// Split-K factor: the persistent grid runs ceil(units / SMs) rounds of units whose
+// length is 1/s of a tile's K range, so pick s minimising ceil(tiles*s / SMs) / s
+// (a split must keep >= 4 K blocks, and must beat the smaller s by 3 %).
+int choose_splits(long tiles, int k_blocks, int T) {
+  if (T > kSplitMaxTokens || tiles <= 0) return 1;
+  const long sms = num_sms();
+  int best = 1;
+  double best_t = (double)((tiles + sms - 1) / sms);
+  for (int s = 2; s <= (int)kMaxSplits && k_blocks / s >= 4; ++s) {
+    const long u = tiles * s;
+    const double t = (double)((u + sms - 1) / sms) / s;
+    if (t < best_t * 0.97) {
+      best = s;
+      best_t = t;
+    }
+  }
+  return best;
+}
+
+// Row blocks walked together: keep a group's A rows (128 x K bf16 each) near 24 MB.
+int group_m_for(int K) {
+  const long per_block = (long)kGemmBM * K * 2;
+  long g = (24l << 20) / per_block;
+  if (g < 1) g = 1;
+  if (g > 16) g = 16;
+  return (int)g;
+}
 
 }  // namespace
 }  // namespace gbmoe
@@ -248,81 +289,146 @@ GBMOE_API gbmoe_status_t moe_forward_events(
   } while (0)
 
   GBMOE_TRY(rec(0));
-  GBMOE_TRY(launch_topk(c, T, router_logits, e_score_correction_bias, tw, tids, status, stream));
-  GBMOE_TRY(launch_align(tids, L.n, E, L.bs, sorted, eids, L.max_blocks, npp,
-                         at<char>(workspace, L.scratch), status, stream));
-  GBMOE_TRY(launch_gather(hidden_states, H, sorted, npp, L.n, k, L.max_sorted, x_perm, stream));
+  int2* bseg = at<int2>(workspace, L.block_seg);
+  int* inv = at<int>(workspace, L.inv);
+  if (route_align_small_ok(T, k, E)) {
+    const bool fused_copy = L.n <= kFusedCopyMaxRows;
+    GBMOE_TRY(launch_route_align_small(c, T, router_logits, e_score_correction_bias, tw, tids,
+                                       L.bs, sorted, eids, L.max_blocks, npp, bseg, inv,
+                                       hidden_states, fused_copy ? x_perm : nullptr, status,
+                                       stream));
+    if (!fused_copy)
+      GBMOE_TRY(launch_gather(hidden_states, H, inv, L.n, k, L.max_sorted, x_perm, stream));
+  } else {
+    GBMOE_TRY(launch_topk(c, T, router_logits, e_score_correction_bias, tw, tids, status, stream));
+    GBMOE_TRY(launch_align(tids, L.n, E, L.bs, sorted, eids, L.max_blocks, npp,
+                           at<char>(workspace, L.scratch), status, stream, bseg, inv));
+    GBMOE_TRY(launch_gather(hidden_states, H, inv, L.n, k, L.max_sorted, x_perm, stream));
+  }
   GBMOE_TRY(rec(1));
 
-  GemmArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.status = status;
-  // routed w13 + SiLU*mul
-  a.n_tiles = I / kGemmBM;
-  a.k_blocks = H / kGemmBK;
-  a.m_rows_dev = npp;
-  a.max_m_blocks = L.max_sorted / kGemmBM;
-  a.expert_ids = eids;
-  a.num_experts = E;
-  a.b_rows_per_expert = 2 * I;
-  a.up_offset = I;
-  a.out = act;
-  a.ldo = I;
-  a.store_rows = L.max_sorted;
-  GBMOE_TRY(launch_gemm(kGemmW13, kGemmBM, x_perm, L.max_sorted, H, w13_weight, E * 2 * I, a,
-                        stream));
-  if (Is) {
-    GemmArgs b = a;
-    b.n_tiles = Is / kGemmBM;
-    b.m_rows_dev = nullptr;
-    b.m_rows_host = t_pad;
-    b.max_m_blocks = t_pad / kGemmBM;
-    b.expert_ids = nullptr;
-    b.num_experts = 1;
-    b.b_rows_per_expert = 2 * Is;
-    b.up_offset = Is;
-    b.out = act_s;
-    b.ldo = Is;
-    b.store_rows = T;
-    GBMOE_TRY(launch_gemm(kGemmW13, kGemmBM, hidden_states, T, H, shared_w13, 2 * Is, b, stream));
+  // routed blocks: at most one partial block per active expert plus the full ones
+  const long est_blocks = (long)(L.n < E ? L.n : E) + L.n / kGemmBM;
+  const long t_blocks = t_pad / kGemmBM;
+
+  // ---- w13 + SiLU*mul: routed experts and the shared expert in one launch
+  GemmLaunch g1;
+  std::memset(&g1, 0, sizeof(g1));
+  g1.status = status;
+  g1.num_problems = Is ? 2 : 1;
+  {
+    GemmProblem& P = g1.p[0];
+    P.A = x_perm;
+    P.a_rows = L.max_sorted;
+    P.B = w13_weight;
+    P.b_rows = E * 2 * I;
+    P.K = H;
+    P.n_tiles = I / kGemmBM;
+    P.k_blocks = H / kGemmBK;
+    P.m_rows_dev = npp;
+    P.max_m_blocks = L.max_sorted / kGemmBM;
+    P.expert_ids = eids;
+    P.block_seg = bseg;
+    P.group_m = group_m_for(H);
+    P.num_experts = E;
+    P.b_rows_per_expert = 2 * I;
+    P.up_offset = I;
+    P.out = act;
+    P.ldo = I;
+    P.store_rows = L.max_sorted;
+    P.sorted_ids = sorted;
+    P.num_flat = L.n;
+    P.part = at<float>(workspace, L.part_r);
+    P.part_split_stride = (long long)L.n * 2 * I;
   }
+  if (Is) {
+    GemmProblem& P = g1.p[1];
+    P.A = hidden_states;
+    P.a_rows = T;
+    P.B = shared_w13;
+    P.b_rows = 2 * Is;
+    P.K = H;
+    P.n_tiles = Is / kGemmBM;
+    P.k_blocks = H / kGemmBK;
+    P.m_rows_host = t_pad;
+    P.max_m_blocks = t_pad / kGemmBM;
+    P.group_m = group_m_for(H);
+    P.num_experts = 1;
+    P.b_rows_per_expert = 2 * Is;
+    P.up_offset = Is;
+    P.out = act_s;
+    P.ldo = Is;
+    P.store_rows = T;
+    P.num_flat = L.n;
+    P.part = at<float>(workspace, L.part_s);
+    P.part_split_stride = (long long)T * 2 * Is;
+  }
+  g1.splits = choose_splits(est_blocks * (I / kGemmBM) + t_blocks * (Is / kGemmBM) * (Is ? 1 : 0),
+                            H / kGemmBK, T);
+  GBMOE_TRY(launch_gemm(kGemmW13, kGemmBM, g1, stream));
+  if (g1.splits > 1) GBMOE_TRY(launch_silu_reduce(g1, npp, L.max_sorted, stream));
   GBMOE_TRY(rec(2));
 
-  // routed w2, weighted, scattered to the token's slot
-  GemmArgs d;
-  std::memset(&d, 0, sizeof(d));
-  d.status = status;
-  d.n_tiles = H / w2_bn;
-  d.k_blocks = I / kGemmBK;
-  d.m_rows_dev = npp;
-  d.max_m_blocks = L.max_sorted / kGemmBM;
-  d.expert_ids = eids;
-  d.num_experts = E;
-  d.b_rows_per_expert = H;
-  d.out = ytok;
-  d.ldo = H;
-  d.sorted_ids = sorted;
-  d.row_weight = tw;
-  d.num_flat = L.n;
-  d.top_k = k;
-  d.slots = L.slots;
-  GBMOE_TRY(launch_gemm(kGemmW2, w2_bn, act, L.max_sorted, I, w2_weight, E * H, d, stream));
-  if (Is) {
-    GemmArgs f = d;
-    f.k_blocks = Is / kGemmBK;
-    f.m_rows_dev = nullptr;
-    f.m_rows_host = t_pad;
-    f.max_m_blocks = t_pad / kGemmBM;
-    f.expert_ids = nullptr;
-    f.num_experts = 1;
-    f.sorted_ids = nullptr;
-    f.row_weight = nullptr;
-    f.store_rows = T;
-    f.slot_offset = k;
-    GBMOE_TRY(launch_gemm(kGemmW2, w2_bn, act_s, T, Is, shared_w2, H, f, stream));
+  // ---- w2: weighted, scattered to the token's slot; shared expert to slot k
+  GemmLaunch g2;
+  std::memset(&g2, 0, sizeof(g2));
+  g2.status = status;
+  g2.num_problems = Is ? 2 : 1;
+  const long long slot_copy = (long long)T * L.slots * H;
+  {
+    GemmProblem& P = g2.p[0];
+    P.A = act;
+    P.a_rows = L.max_sorted;
+    P.B = w2_weight;
+    P.b_rows = E * H;
+    P.K = I;
+    P.n_tiles = H / w2_bn;
+    P.k_blocks = I / kGemmBK;
+    P.m_rows_dev = npp;
+    P.max_m_blocks = L.max_sorted / kGemmBM;
+    P.expert_ids = eids;
+    P.block_seg = bseg;
+    P.group_m = group_m_for(I);
+    P.num_experts = E;
+    P.b_rows_per_expert = H;
+    P.out = ytok;
+    P.ldo = H;
+    P.store_rows = L.max_sorted;
+    P.sorted_ids = sorted;
+    P.row_weight = tw;
+    P.num_flat = L.n;
+    P.top_k = k;
+    P.slots = L.slots;
+    P.out_split_stride = slot_copy;
   }
+  if (Is) {
+    GemmProblem& P = g2.p[1];
+    P.A = act_s;
+    P.a_rows = T;
+    P.B = shared_w2;
+    P.b_rows = H;
+    P.K = Is;
+    P.n_tiles = H / w2_bn;
+    P.k_blocks = Is / kGemmBK;
+    P.m_rows_host = t_pad;
+    P.max_m_blocks = t_pad / kGemmBM;
+    P.group_m = group_m_for(Is);
+    P.num_experts = 1;
+    P.b_rows_per_expert = H;
+    P.out = ytok;
+    P.ldo = H;
+    P.store_rows = T;
+    P.num_flat = L.n;
+    P.top_k = k;
+    P.slots = L.slots;
+    P.slot_offset = k;
+    P.out_split_stride = slot_copy;
+  }
+  const int kb2 = Is ? ((I < Is ? I : Is) / kGemmBK) : I / kGemmBK;
+  g2.splits = choose_splits((est_blocks + (Is ? t_blocks : 0)) * (H / w2_bn), kb2, T);
+  GBMOE_TRY(launch_gemm(kGemmW2, w2_bn, g2, stream));
   GBMOE_TRY(rec(3));
-  GBMOE_TRY(launch_combine(ytok, L.slots, H, T, output, stream));
+  GBMOE_TRY(launch_combine(ytok, L.slots, H, T, g2.splits, slot_copy, output, stream));
   GBMOE_TRY(rec(4));
 #undef GBMOE_TRY
   return GBMOE_OK;

@@ -1,6 +1,7 @@
-// Combine: y[t] = sum over the token's slots (routed j ascending, then the shared
-// expert) of the already-weighted fp32 expert outputs, accumulated in fp32 and
-// rounded once to bf16. The routed outputs arrive weighted by topk_weights (scaled by
+// Combine: y[t] = sum over the split-K partial copies and, inside each, over the
+// token's slots (routed j ascending, then the shared expert) of the already-weighted
+// fp32 expert outputs, accumulated in fp32 in that fixed order and rounded once to
+// bf16. The routed outputs arrive weighted by topk_weights (scaled by
 // routed_scaling_factor) from the w2 epilogue; the shared-expert slot is unscaled,
 // as `DeepseekV2MoE.forward_normal` adds it (sglang `models/deepseek_v2.py` page).
 // HBM-bound: 16-byte vector loads and stores, grid-stride over (token, 8 columns).
@@ -10,18 +11,22 @@
 namespace gbmoe {
 
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ ytok, int slots,
-                                                      int H8, int T, uint4* __restrict__ y) {
+                                                      int H8, int T, int splits,
+                                                      long long split_stride4,
+                                                      uint4* __restrict__ y) {
   const size_t total = (size_t)T * H8;
   for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (size_t)gridDim.x * blockDim.x) {
     const size_t t = idx / H8, h = idx % H8;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-    const float4* src = ytok + (t * slots * H8 + h) * 2;
-    for (int s = 0; s < slots; ++s) {
-      const float4 u = __ldg(src + (size_t)s * H8 * 2);
-      const float4 v = __ldg(src + (size_t)s * H8 * 2 + 1);
-      a.x += u.x; a.y += u.y; a.z += u.z; a.w += u.w;
-      b.x += v.x; b.y += v.y; b.z += v.z; b.w += v.w;
+    for (int sp = 0; sp < splits; ++sp) {
+      const float4* src = ytok + (size_t)sp * split_stride4 + (t * slots * H8 + h) * 2;
+      for (int s = 0; s < slots; ++s) {
+        const float4 u = __ldg(src + (size_t)s * H8 * 2);
+        const float4 v = __ldg(src + (size_t)s * H8 * 2 + 1);
+        a.x += u.x; a.y += u.y; a.z += u.z; a.w += u.w;
+        b.x += v.x; b.y += v.y; b.z += v.z; b.w += v.w;
+      }
     }
     uint4 o;
     o.x = pack_bf16x2(a.x, a.y);
@@ -32,15 +37,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
   }
 }
 
-cudaError_t launch_combine(const void* ytok, int slots, int H, int T, void* y,
-                           cudaStream_t stream) {
+cudaError_t launch_combine(const void* ytok, int slots, int H, int T, int splits,
+                           long long split_stride, void* y, cudaStream_t stream) {
   const size_t total = (size_t)T * (H / 8);
   size_t blocks = (total + 255) / 256;
   const size_t cap = (size_t)num_sms() * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   combine_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const float4*>(ytok), slots,
-                                                        H / 8, T, static_cast<uint4*>(y));
+                                                        H / 8, T, splits, split_stride / 4,
+                                                        static_cast<uint4*>(y));
   return cudaGetLastError();
 }
 

@@ -19,8 +19,9 @@
 //   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes, SiLU*mul (bf16 stores) or
 //               weighting (fp32 stores); then release the accumulator, so the epilogue of tile i
 //               overlaps the MMAs of tile i+1.
-// Tiles (row block, N tile) are walked row-block-fastest, so CTAs running at the
-// same time share the weight tile of one expert through L2. Every wait is bounded:
+// Tiles (row block, N tile) are walked in expert-aligned groups of row blocks, row
+// block fastest (tile_coords), so concurrent CTAs share one expert's weight tile and
+// the group's A rows stay resident in L2. Every wait is bounded:
 // after kWaitTimeoutNs the CTA records GBMOE_ERR_TIMEOUT, stops, and frees its TMEM.
 #include <cudaTypedefs.h>
 
@@ -168,6 +169,75 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + __expf(-g)) * u; }
 
+// Tile t -> (row block, N tile). Row blocks are taken in groups of at most group_m
+// consecutive blocks of one expert; a group's tiles run over all N tiles with the
+// row block fastest, so the group's A rows stay in L2 while its expert's weight
+// tiles stream past, and each weight tile is shared by the group's CTAs.
+// The tiles of a group starting at block gs with gn blocks are [gs*NT, (gs+gn)*NT),
+// so block t / NT always lies inside the group that owns tile t.
+__device__ __forceinline__ void tile_coords(const GemmProblem& a, int m_blocks, int tile,
+                                            int* status, int& mb, int& nt) {
+  const int b = tile / a.n_tiles;
+  int s0 = 0, sn = m_blocks;
+  if (a.block_seg) {
+    const int2 sg = a.block_seg[b];
+    s0 = sg.x;
+    sn = sg.y;
+    if (sn < 1 || b < s0 || b >= s0 + sn) {
+      record_status(status, GBMOE_ERR_DEVICE_CHECK);
+      s0 = b;
+      sn = 1;
+    }
+  }
+  const int gm = a.group_m > 0 ? a.group_m : 1;
+  const int g0 = ((b - s0) / gm) * gm;
+  const int gs = s0 + g0;
+  const int gn = min(gm, sn - g0);
+  const int local = tile - gs * a.n_tiles;
+  nt = local / gn;
+  mb = gs + local % gn;
+}
+
+// Work unit u -> (problem, split, row block, N tile, K-block range).
+struct Unit {
+  int p, split, mb, nt, kb0, kb1;
+};
+
+struct Schedule {
+  int mblk[2], tiles[2], total_tiles, units;
+
+  __device__ void init(const GemmLaunch& L) {
+    total_tiles = 0;
+    for (int p = 0; p < 2; ++p) {
+      mblk[p] = tiles[p] = 0;
+      if (p >= L.num_problems) continue;
+      const GemmProblem& P = L.p[p];
+      int rows = P.m_rows_dev ? *P.m_rows_dev : P.m_rows_host;
+      if (rows < 0 || rows % kGemmBM != 0 || rows > P.max_m_blocks * kGemmBM) {
+        if (threadIdx.x == 0) record_status(L.status, GBMOE_ERR_DEVICE_CHECK);
+        rows = 0;
+      }
+      mblk[p] = rows / kGemmBM;
+      tiles[p] = mblk[p] * P.n_tiles;
+      total_tiles += tiles[p];
+    }
+    units = total_tiles * L.splits;
+  }
+
+  __device__ Unit unit(const GemmLaunch& L, int u) const {
+    Unit r;
+    r.split = u / total_tiles;
+    int t = u - r.split * total_tiles;
+    r.p = t < tiles[0] ? 0 : 1;
+    if (r.p) t -= tiles[0];
+    const GemmProblem& P = L.p[r.p];
+    tile_coords(P, mblk[r.p], t, L.status, r.mb, r.nt);
+    r.kb0 = (r.split * P.k_blocks) / L.splits;
+    r.kb1 = ((r.split + 1) * P.k_blocks) / L.splits;
+    return r;
+  }
+};
+
 template <int KIND, int BN>
 struct Shape {
   static constexpr int kBRows = KIND == kGemmW13 ? 2 * BN : BN;  // B rows per stage = MMA N
@@ -177,10 +247,19 @@ struct Shape {
   static_assert(kBRows % 16 == 0 && kBRows <= 256, "MMA N out of range for M=128");
 };
 
+__device__ __forceinline__ void store_f32x32(float* dst, const uint32_t (&r)[32], float w) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int v = 0; v < 8; ++v)
+    d[v] = make_float4(w * __uint_as_float(r[4 * v]), w * __uint_as_float(r[4 * v + 1]),
+                       w * __uint_as_float(r[4 * v + 2]), w * __uint_as_float(r[4 * v + 3]));
+}
+
 template <int KIND, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmArgs args) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+                const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                const GemmLaunch args) {
   using S = Shape<KIND, BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -210,8 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch(&tmA);
-    tma_prefetch(&tmB);
+    tma_prefetch(&tmA0);
+    tma_prefetch(&tmB0);
+    if (args.num_problems > 1) {
+      tma_prefetch(&tmA1);
+      tma_prefetch(&tmB1);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -222,29 +305,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  int m_rows = args.m_rows_dev ? *args.m_rows_dev : args.m_rows_host;
-  if (m_rows < 0 || m_rows % kGemmBM != 0 || m_rows > args.max_m_blocks * kGemmBM) {
-    if (threadIdx.x == 0) record_status(args.status, GBMOE_ERR_DEVICE_CHECK);
-    m_rows = 0;
-  }
-  const int m_blocks = m_rows / kGemmBM;
-  const int num_tiles = m_blocks * args.n_tiles;
+  Schedule sched;
+  sched.init(args);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0;
-      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-        const int mb = tile % m_blocks, nt = tile / m_blocks;
-        int e = args.expert_ids ? args.expert_ids[mb] : 0;
-        if ((unsigned)e >= (unsigned)args.num_experts) {
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+        const Unit w = sched.unit(args, u);
+        const GemmProblem& P = args.p[w.p];
+        const CUtensorMap* ta = w.p ? &tmA1 : &tmA0;
+        const CUtensorMap* tb = w.p ? &tmB1 : &tmB0;
+        int e = P.expert_ids ? P.expert_ids[w.mb] : 0;
+        if ((unsigned)e >= (unsigned)P.num_experts) {
           record_status(args.status, GBMOE_ERR_DEVICE_CHECK);
           e = 0;
         }
-        const int a_row = mb * kGemmBM;
-        const int b_row = e * args.b_rows_per_expert + nt * BN;
-        bool ok = true;
-        for (int kb = 0; kb < args.k_blocks; ++kb, ++it) {
+        const int a_row = w.mb * kGemmBM;
+        const int b_row = e * P.b_rows_per_expert + w.nt * BN;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
           if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
@@ -254,12 +335,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = base + s * S::kStageBytes;
           const uint32_t sb = sa + kABytes;
           mbar_expect_tx(full_bar(s), S::kStageBytes);
-          tma_load_2d(sa, &tmA, full_bar(s), kb * kGemmBK, a_row);
-          tma_load_2d(sb, &tmB, full_bar(s), kb * kGemmBK, b_row);
+          tma_load_2d(sa, ta, full_bar(s), kb * kGemmBK, a_row);
+          tma_load_2d(sb, tb, full_bar(s), kb * kGemmBK, b_row);
           if (KIND == kGemmW13)
-            tma_load_2d(sb + BN * 128, &tmB, full_bar(s), kb * kGemmBK, b_row + args.up_offset);
+            tma_load_2d(sb + BN * 128, tb, full_bar(s), kb * kGemmBK, b_row + P.up_offset);
         }
-        if (!ok) break;
       }
     }
     __syncwarp();
@@ -269,14 +349,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16(kGemmBM, S::kBRows);
       uint32_t it = 0;
       int local = 0;
-      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x, ++local) {
+        const Unit w = sched.unit(args, u);
         const int acc = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
         if (!wait_bounded(tempty_bar(acc), (use & 1u) ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + acc * kAccStride;
-        bool ok = true;
-        for (int kb = 0; kb < args.k_blocks; ++kb, ++it) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
           if (!wait_bounded(full_bar(s), ph, abort_flag, args.status)) {
@@ -289,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk)
             mma_bf16(d, sdesc_sw128(sa + kk * 32), sdesc_sw128(sb + kk * 32), idesc,
-                     (kb | kk) != 0 ? 1u : 0u);
+                     (kb > w.kb0 || kk != 0) ? 1u : 0u);
           mma_commit(empty_bar(s));
         }
         if (!ok) break;
@@ -301,66 +382,84 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;            // TMEM lanes [32*quarter, 32*quarter + 32)
     const int row = quarter * 32 + lane;
+    const bool split = args.splits > 1;
     int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+    for (int u = blockIdx.x; u < sched.units; u += gridDim.x, ++local) {
+      const Unit w = sched.unit(args, u);
+      const GemmProblem& P = args.p[w.p];
       const int acc = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
       if (!wait_bounded(tfull_bar(acc), use & 1u, abort_flag, args.status)) break;
       tc_fence_after();
-      const int mb = tile % m_blocks, nt = tile / m_blocks;
-      const int m = mb * kGemmBM + row;
+      const int m = w.mb * kGemmBM + row;
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kAccStride;
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
+      // valid row: its flat index (routed) or token (identity rows), else -1
+      int f = -1;
+      if (P.sorted_ids) {
+        const int v = P.sorted_ids[m];
+        if (v >= 0 && v < P.num_flat) f = v;
+      } else if (m < P.store_rows) {
+        f = m;
+      }
       if (KIND == kGemmW13) {
-        const bool store = m < args.store_rows;
-        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)m * args.ldo + (size_t)nt * BN);
+        if (!split) {
+          const bool store = P.sorted_ids ? true : (m < P.store_rows);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.out) +
+                                                (size_t)m * P.ldo + (size_t)w.nt * BN);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t g[32], u[32];
-          tmem_ld32(tbase + c * 32, g);
-          tmem_ld32(tbase + BN + c * 32, u);
-          tmem_wait_ld(g);
-          reg_fence(u);
-          uint32_t p[16];
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t g[32], up[32];
+            tmem_ld32(tbase + c * 32, g);
+            tmem_ld32(tbase + BN + c * 32, up);
+            tmem_wait_ld(g);
+            reg_fence(up);
+            uint32_t p[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            p[i] = pack_bf16x2(silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
-                               silu_mul(__uint_as_float(g[2 * i + 1]),
-                                        __uint_as_float(u[2 * i + 1])));
-          if (store) {
+            for (int i = 0; i < 16; ++i)
+              p[i] = pack_bf16x2(silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(up[2 * i])),
+                                 silu_mul(__uint_as_float(g[2 * i + 1]),
+                                          __uint_as_float(up[2 * i + 1])));
+            if (store) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[c * 4 + v] = make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+              for (int v = 0; v < 4; ++v)
+                dst[c * 4 + v] = make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+            }
+          }
+        } else {
+          float* dst = P.part + (size_t)w.split * P.part_split_stride +
+                       (size_t)(f < 0 ? 0 : f) * (2 * P.ldo) + (size_t)w.nt * BN;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t g[32], up[32];
+            tmem_ld32(tbase + c * 32, g);
+            tmem_ld32(tbase + BN + c * 32, up);
+            tmem_wait_ld(g);
+            reg_fence(up);
+            if (f >= 0) {
+              store_f32x32(dst + c * 32, g, 1.f);
+              store_f32x32(dst + P.ldo + c * 32, up, 1.f);
+            }
           }
         }
       } else {
         int dest = -1;
-        float w = 1.f;
-        if (args.sorted_ids) {
-          const int f = args.sorted_ids[m];
-          if (f >= 0 && f < args.num_flat) {
-            dest = (f / args.top_k) * args.slots + (f % args.top_k);
-            w = args.row_weight ? args.row_weight[f] : 1.f;
+        float wt = 1.f;
+        if (f >= 0) {
+          if (P.sorted_ids) {
+            dest = (f / P.top_k) * P.slots + (f % P.top_k);
+            wt = P.row_weight ? P.row_weight[f] : 1.f;
+          } else {
+            dest = f * P.slots + P.slot_offset;
           }
-        } else if (m < args.store_rows) {
-          dest = m * args.slots + args.slot_offset;
         }
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.out) +
-                                                (size_t)(dest < 0 ? 0 : dest) * args.ldo +
-                                                (size_t)nt * BN);
+        float* dst = static_cast<float*>(P.out) + (size_t)w.split * P.out_split_stride +
+                     (size_t)(dest < 0 ? 0 : dest) * P.ldo + (size_t)w.nt * BN;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(tbase + c * 32, r);
           tmem_wait_ld(r);
-          if (dest >= 0) {
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[c * 8 + v] = make_float4(w * __uint_as_float(r[4 * v]),
-                                           w * __uint_as_float(r[4 * v + 1]),
-                                           w * __uint_as_float(r[4 * v + 2]),
-                                           w * __uint_as_float(r[4 * v + 3]));
-          }
+          if (dest >= 0) store_f32x32(dst + c * 32, r, wt);
         }
       }
       tc_fence_before();
@@ -374,6 +473,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// act = silu(sum_s gate_s) * sum_s up_s, one CTA per output row, 8 columns per step.
+__global__ void __launch_bounds__(128) silu_reduce_kernel(const GemmLaunch L, const int* npp,
+                                                          int max_routed_rows) {
+  const GemmProblem& R = L.p[0];
+  int routed_rows = npp ? *npp : R.m_rows_host;
+  if (routed_rows > max_routed_rows) routed_rows = max_routed_rows;
+  const int shared_rows = L.num_problems > 1 ? L.p[1].store_rows : 0;
+  for (int r = blockIdx.x; r < max_routed_rows + shared_rows; r += gridDim.x) {
+    const GemmProblem* P;
+    int src, dst_row;
+    if (r < max_routed_rows) {
+      if (r >= routed_rows) continue;
+      P = &L.p[0];
+      const int f = P->sorted_ids ? P->sorted_ids[r] : r;
+      if (f < 0 || f >= P->num_flat) continue;          // padding rows are never read back
+      src = f;
+      dst_row = r;
+    } else {
+      P = &L.p[1];
+      src = dst_row = r - max_routed_rows;
+    }
+    const int N = P->ldo;
+    const float* base = P->part + (size_t)src * 2 * N;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(P->out) + (size_t)dst_row * N;
+    for (int j = threadIdx.x * 8; j < N; j += blockDim.x * 8) {
+      float g[8], u[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) g[i] = u[i] = 0.f;
+      for (int s = 0; s < L.splits; ++s) {
+        const float* q = base + (size_t)s * P->part_split_stride + j;
+        const float4 g0 = *reinterpret_cast<const float4*>(q);
+        const float4 g1 = *reinterpret_cast<const float4*>(q + 4);
+        const float4 u0 = *reinterpret_cast<const float4*>(q + N);
+        const float4 u1 = *reinterpret_cast<const float4*>(q + N + 4);
+        g[0] += g0.x; g[1] += g0.y; g[2] += g0.z; g[3] += g0.w;
+        g[4] += g1.x; g[5] += g1.y; g[6] += g1.z; g[7] += g1.w;
+        u[0] += u0.x; u[1] += u0.y; u[2] += u0.z; u[3] += u0.w;
+        u[4] += u1.x; u[5] += u1.y; u[6] += u1.z; u[7] += u1.w;
+      }
+      uint4 o;
+      o.x = pack_bf16x2(silu_mul(g[0], u[0]), silu_mul(g[1], u[1]));
+      o.y = pack_bf16x2(silu_mul(g[2], u[2]), silu_mul(g[3], u[3]));
+      o.z = pack_bf16x2(silu_mul(g[4], u[4]), silu_mul(g[5], u[5]));
+      o.w = pack_bf16x2(silu_mul(g[6], u[6]), silu_mul(g[7], u[7]));
+      *reinterpret_cast<uint4*>(out + j) = o;
+    }
   }
 }
 
@@ -405,8 +553,8 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, ui
 }
 
 template <int KIND, int BN>
-cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args,
-                         int grid, cudaStream_t stream) {
+cudaError_t launch_typed(const CUtensorMap* tm, const GemmLaunch& args, int grid,
+                         cudaStream_t stream) {
   using S = Shape<KIND, BN>;
   static int configured_device = -1;
   int dev = 0;
@@ -418,26 +566,43 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const Gem
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  gemm_kernel<KIND, BN><<<grid, kThreads, S::kSmem, stream>>>(ta, tb, args);
+  gemm_kernel<KIND, BN><<<grid, kThreads, S::kSmem, stream>>>(tm[0], tm[1], tm[2], tm[3], args);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(int kind, int bn, const void* A, int a_rows_alloc, int K, const void* B,
-                        int b_rows_total, const GemmArgs& args, cudaStream_t stream) {
-  CUtensorMap ta, tb;
-  if (!make_map(&ta, A, (uint64_t)K, (uint64_t)a_rows_alloc, kGemmBM)) return cudaErrorInvalidValue;
-  if (!make_map(&tb, B, (uint64_t)K, (uint64_t)b_rows_total, (uint32_t)bn))
-    return cudaErrorInvalidValue;
-  long tiles = (long)args.max_m_blocks * args.n_tiles;
+cudaError_t launch_gemm(int kind, int bn, const GemmLaunch& L, cudaStream_t stream) {
+  if (L.num_problems < 1 || L.num_problems > 2 || L.splits < 1) return cudaErrorInvalidValue;
+  CUtensorMap tm[4];
+  long units = 0;
+  for (int p = 0; p < 2; ++p) {
+    const GemmProblem& P = L.p[L.num_problems > p ? p : 0];
+    if (!make_map(&tm[2 * p], P.A, (uint64_t)P.K, (uint64_t)P.a_rows, kGemmBM) ||
+        !make_map(&tm[2 * p + 1], P.B, (uint64_t)P.K, (uint64_t)P.b_rows, (uint32_t)bn))
+      return cudaErrorInvalidValue;
+    if (p < L.num_problems) {
+      if (P.k_blocks < L.splits) return cudaErrorInvalidValue;
+      units += (long)P.max_m_blocks * P.n_tiles * L.splits;
+    }
+  }
   int grid = num_sms();
-  if (tiles < grid) grid = (int)tiles;
+  if (units < grid) grid = (int)units;
   if (grid < 1) grid = 1;
-  if (kind == kGemmW13 && bn == 128) return launch_typed<kGemmW13, 128>(ta, tb, args, grid, stream);
-  if (kind == kGemmW2 && bn == 256) return launch_typed<kGemmW2, 256>(ta, tb, args, grid, stream);
-  if (kind == kGemmW2 && bn == 128) return launch_typed<kGemmW2, 128>(ta, tb, args, grid, stream);
+  if (kind == kGemmW13 && bn == 128) return launch_typed<kGemmW13, 128>(tm, L, grid, stream);
+  if (kind == kGemmW2 && bn == 256) return launch_typed<kGemmW2, 256>(tm, L, grid, stream);
+  if (kind == kGemmW2 && bn == 128) return launch_typed<kGemmW2, 128>(tm, L, grid, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_silu_reduce(const GemmLaunch& L, const int* npp, int max_routed_rows,
+                               cudaStream_t stream) {
+  const int rows = max_routed_rows + (L.num_problems > 1 ? L.p[1].store_rows : 0);
+  int grid = num_sms() * 4;
+  if (rows < grid) grid = rows;
+  if (grid < 1) return cudaSuccess;
+  silu_reduce_kernel<<<grid, 128, 0, stream>>>(L, npp, max_routed_rows);
+  return cudaGetLastError();
 }
 
 }  // namespace gbmoe

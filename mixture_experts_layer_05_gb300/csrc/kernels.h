@@ -20,45 +20,79 @@ cudaError_t launch_topk(const gbmoe_config_t& c, int T, const float* logits, con
                         float* weights, int* ids, int* status, cudaStream_t stream);
 
 size_t align_scratch_bytes(int n, int E);
+// block_seg (optional): per block, (first block, block count) of its expert's run.
+// inv (optional): per flat index, its position in sorted order.
 cudaError_t launch_align(const int* ids, int n, int E, int bs, int* sorted, int* expert_ids,
                          int max_blocks, int* npp, void* scratch, int* status,
-                         cudaStream_t stream);
-cudaError_t launch_gather(const void* x, int H, const int* sorted, const int* npp, int n, int k,
-                          int max_rows, void* x_perm, cudaStream_t stream);
+                         cudaStream_t stream, int2* block_seg = nullptr, int* inv = nullptr);
+// Routing + align of a small batch in one launch (when route_align_small_ok).
+bool route_align_small_ok(int T, int k, int E);
+cudaError_t launch_route_align_small(const gbmoe_config_t& c, int T, const float* logits,
+                                     const float* bias, float* weights, int* ids, int bs,
+                                     int* sorted, int* expert_ids, int max_blocks, int* npp,
+                                     int2* block_seg, int* inv, const void* x, void* x_perm,
+                                     int* status, cudaStream_t stream);
+// x_perm[inv[f]] = x[f / k] for f < n (x_perm == NULL in the small launch: no copy there).
+cudaError_t launch_gather(const void* x, int H, const int* inv, int n, int k, int max_rows,
+                          void* x_perm, cudaStream_t stream);
+constexpr int kFusedCopyMaxRows = 16;  // the small route+align launch copies rows itself
 
-cudaError_t launch_combine(const void* ytok, int slots, int H, int T, void* y,
-                           cudaStream_t stream);
+// y[t] = sum over splits s and slots of ytok[s * split_stride + (t * slots + slot) * H + :]
+cudaError_t launch_combine(const void* ytok, int slots, int H, int T, int splits,
+                           long long split_stride, void* y, cudaStream_t stream);
 
 enum GemmKind { kGemmW13 = 0, kGemmW2 = 1 };
 
-// One grouped GEMM launch. A rows are grouped in blocks of kGemmBM that each belong
+// One grouped GEMM problem. A rows are grouped in blocks of kGemmBM that each belong
 // to one expert (expert_ids[block]); B is the expert weight stack flattened to
 // [num_experts * b_rows_per_expert, K].
-struct GemmArgs {
+struct GemmProblem {
+  const void* A;           // bf16 [a_rows, K] (host side: for the tensor map)
+  int a_rows;
+  const void* B;           // bf16 [b_rows, K]
+  int b_rows;
+  int K;
   int n_tiles;             // output tiles along N
   int k_blocks;            // K / kGemmBK
   const int* m_rows_dev;   // device count of A rows (multiple of kGemmBM), or NULL
   int m_rows_host;         // A rows when m_rows_dev is NULL (multiple of kGemmBM)
   int max_m_blocks;        // upper bound on A row blocks
   const int* expert_ids;   // expert per row block, or NULL (all expert 0)
+  const int2* block_seg;   // per row block: (first block, block count) of its expert run,
+                           // or NULL (one run over all blocks)
+  int group_m;             // row blocks walked together across all N tiles (L2 reuse)
   int num_experts;
   int b_rows_per_expert;   // rows of B per expert
   int up_offset;           // w13: row offset of the up half inside an expert
-  void* out;               // w13: bf16 act; w2: fp32 per-slot outputs
+  void* out;               // w13: bf16 act [rows, ldo]; w2: fp32 slot outputs [T*slots, ldo]
   int ldo;                 // output row stride (elements)
-  int store_rows;          // w13: rows >= store_rows are not stored; w2 identity rows: valid rows
-  const int* sorted_ids;   // w2: row -> flat index, or NULL (row = token, identity)
+  int store_rows;          // identity-row problems: rows >= store_rows are padding
+  const int* sorted_ids;   // routed problems: row -> flat index (>= num_flat: padding)
   const float* row_weight; // w2: weight per flat index, or NULL (weight 1)
-  int num_flat;            // w2: T * top_k (the sentinel)
+  int num_flat;            // T * top_k (the sentinel)
   int top_k;               // w2: slots of routed experts per token
   int slots;               // w2: output slots per token
   int slot_offset;         // w2: slot of identity rows
+  float* part;             // w13 with splits > 1: fp32 [splits][row][2 * ldo] (gate | up),
+                           // row = flat index (routed) or token (identity rows)
+  long long part_split_stride;
+  long long out_split_stride;  // w2: elements between the per-split copies of out
+};
+
+// Up to two problems (the routed experts and the shared expert) in one persistent
+// launch; every (problem, tile) is cut into `splits` equal K ranges (split-K).
+struct GemmLaunch {
+  GemmProblem p[2];
+  int num_problems;
+  int splits;
   int* status;
 };
 
-// w13: A [rows, H] (x_perm or x), B = w13 [E*2I, H]; out act [rows, I] bf16
-// w2:  A [rows, I] (act),           B = w2  [E*H, I]; out scattered to [T*slots, H] fp32
-cudaError_t launch_gemm(int kind, int bn, const void* A, int a_rows_alloc, int K, const void* B,
-                        int b_rows_total, const GemmArgs& args, cudaStream_t stream);
+cudaError_t launch_gemm(int kind, int bn, const GemmLaunch& L, cudaStream_t stream);
+
+// act = silu(sum_s gate_s) * sum_s up_s for the valid rows of each problem of a split
+// w13 launch (routed rows in expert order; identity rows for the shared expert).
+cudaError_t launch_silu_reduce(const GemmLaunch& L, const int* npp, int max_routed_rows,
+                               cudaStream_t stream);
 
 }  // namespace gbmoe

@@ -230,3 +230,49 @@ def test_forward_full_size_sampled(cuda_lib, name, T, n_sample):
     check_close(y[rows], y_ref, f"{name} T={T} rows {rows}")
     del layer, wts
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ decode sizes (split-K)
+SPLIT = _small(configs.MIXTRAL, num_experts=4, hidden_size=1024, intermediate_size=1024)
+SPLIT_SHARED = _small(configs.DSV3, num_experts=16, num_expert_group=4, topk_group=2, top_k=4,
+                      hidden_size=1024, intermediate_size=512, shared_intermediate_size=1024)
+
+
+@pytest.mark.parametrize("w", [SPLIT, SPLIT_SHARED], ids=["routed", "routed+shared"])
+@pytest.mark.parametrize("T", [1, 3, 17, 64])
+def test_forward_split_k(cuda_lib, w, T):
+    """Shapes whose few tiles make moe_forward cut K into several splits."""
+    wts = inputs.make_weights(w, 0)
+    x, logits = tokens(w, T, wts["bias"])
+    layer, _ = _layer(w, wts, T)
+    y = layer(x.to(DEV), logits.to(DEV))
+    torch.cuda.synchronize()
+    assert layer.device_status() == binding.OK
+    y_ref = oracle.fused_moe(x, logits, wts["bias"], wts["w13"], wts["w2"], wts["shared_w13"],
+                             wts["shared_w2"], **oracle_cfg(w))
+    check_close(y, y_ref, f"split-K T={T}")
+    y2 = layer(x.to(DEV), logits.to(DEV))
+    assert torch.equal(y, y2)                       # fixed reduction order: deterministic
+
+
+@pytest.mark.parametrize("name,T", [("mixtral", 1), ("mixtral", 16), ("dsv2", 1), ("dsv3", 1),
+                                    ("dsv3", 8)])
+def test_forward_decode_full_shapes(cuda_lib, name, T):
+    """Full shapes at decode token counts, every token against the oracle."""
+    w = configs.WORKLOADS[name]
+    torch.cuda.empty_cache()
+    wts = inputs.make_weights(w, 0, device=DEV)
+    bias_cpu = None if wts["bias"] is None else wts["bias"].cpu()
+    x, logits = tokens(w, T, bias_cpu)
+    layer = binding.FusedMoE(binding.config_from_workload(w), wts["w13"], wts["w2"], wts["bias"],
+                             wts["shared_w13"], wts["shared_w2"], max_tokens=T)
+    y = layer(x.to(DEV), logits.to(DEV))
+    torch.cuda.synchronize()
+    assert layer.device_status() == binding.OK
+    y_ref = oracle.fused_moe(x, logits, bias_cpu, _Experts(wts["w13"]), _Experts(wts["w2"]),
+                             None if wts["shared_w13"] is None else wts["shared_w13"].cpu(),
+                             None if wts["shared_w2"] is None else wts["shared_w2"].cpu(),
+                             **oracle_cfg(w))
+    check_close(y, y_ref, f"{name} T={T}")
+    del layer, wts
+    torch.cuda.empty_cache()
