@@ -233,6 +233,24 @@ gbmoe_status_t moe_forward_workspace_layout(const gbmoe_config_t* cfg, int32_t m
  */
 gbmoe_status_t moe_get_device_status(void* workspace, int32_t* status, gbmoe_stream_t stream);
 
+/*
+ * moe_forward_num_launches: number of kernels one moe_forward(cfg, num_tokens, ...)
+ * enqueues (it depends on num_tokens: the small-batch routing path, split-K reduces).
+ * Returns -1 for an invalid configuration.
+ */
+int32_t moe_forward_num_launches(const gbmoe_config_t* cfg, int32_t num_tokens);
+
+/*
+ * moe_selftest_bounded_wait: failure-detection self test. Enqueues one kernel whose
+ * single thread waits on a shared-memory mbarrier that nothing completes, with the
+ * same bounded wait the GEMM pipelines use, but giving up after timeout_us
+ * (0..10^7) instead of one second; it then records GBMOE_ERR_TIMEOUT in the status
+ * word of `workspace` (read it with moe_get_device_status) and exits, leaving the
+ * context usable. Has no counterpart on the pages.
+ */
+gbmoe_status_t moe_selftest_bounded_wait(void* workspace, int32_t timeout_us,
+                                         gbmoe_stream_t stream);
+
 /* Library version, (major << 16) | minor. */
 int32_t gbmoe_version(void);
 

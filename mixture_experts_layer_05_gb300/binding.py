@@ -27,7 +27,7 @@ EXPORTS = ("moe_topk", "moe_align_block_size_workspace_size", "moe_align_block_s
            "moe_align_block_size_no_workspace",
            "moe_forward_workspace_size", "moe_forward_block_size", "moe_forward",
            "moe_forward_events", "moe_forward_workspace_layout", "moe_get_device_status",
-           "gbmoe_version")
+           "moe_forward_num_launches", "moe_selftest_bounded_wait", "gbmoe_version")
 
 
 class GbmoeError(RuntimeError):
@@ -97,6 +97,8 @@ def load() -> ctypes.CDLL:
         "moe_forward_events": (I32, [CP, I32, P, P, P, P, P, P, P, P, P, SZ, P, I32, P]),
         "moe_forward_workspace_layout": (I32, [CP, I32, ctypes.POINTER(WorkspaceLayout)]),
         "moe_get_device_status": (I32, [P, ctypes.POINTER(I32), P]),
+        "moe_forward_num_launches": (I32, [CP, I32]),
+        "moe_selftest_bounded_wait": (I32, [P, I32, P]),
         "gbmoe_version": (I32, []),
     }
     for name, (res, args) in sig.items():
@@ -217,6 +219,15 @@ def moe_forward(cfg: Config, hidden_states, router_logits, e_score_correction_bi
                lib.moe_forward_events(*args, arr, len(events), _stream(stream)))
 
 
+def moe_forward_num_launches(cfg: Config, num_tokens: int) -> int:
+    return load().moe_forward_num_launches(ctypes.byref(cfg), num_tokens)
+
+
+def moe_selftest_bounded_wait(workspace, timeout_us: int, stream=None):
+    _check("moe_selftest_bounded_wait",
+           load().moe_selftest_bounded_wait(_p(workspace), timeout_us, _stream(stream)))
+
+
 def moe_get_device_status(workspace, stream=None) -> int:
     v = ctypes.c_int32(0)
     _check("moe_get_device_status",
@@ -242,14 +253,59 @@ class FusedMoE:
             self.workspace = alloc_workspace(moe_forward_workspace_size(self.cfg, max_tokens), dev)
             self.max_tokens = max_tokens
 
-    def __call__(self, hidden_states, router_logits, out=None, events=None):
+    def __call__(self, hidden_states, router_logits, out=None, events=None, stream=None):
         T = hidden_states.shape[0]
         self.reserve(T)
         if out is None:
             out = torch.empty_like(hidden_states)
         moe_forward(self.cfg, hidden_states, router_logits, self.bias, self.w13, self.w2,
-                    self.shared_w13, self.shared_w2, out, self.workspace, events=events)
+                    self.shared_w13, self.shared_w2, out, self.workspace, events=events,
+                    stream=stream)
         return out
 
     def device_status(self) -> int:
         return moe_get_device_status(self.workspace)
+
+
+class HostPipeline:
+    """Runs a FusedMoE layer over batches held in pinned host memory.
+
+    Three CUDA streams and double-buffered device tensors: batch i's host-to-device copy
+    runs while batch i-1 computes, and batch i-1's device-to-host copy while batch i
+    computes. Every batch still pays its own copies; they are only overlapped.
+    """
+
+    def __init__(self, layer: FusedMoE, max_tokens: int):
+        dev = layer.w13.device
+        H = layer.cfg.hidden_size
+        E = layer.cfg.num_experts
+        layer.reserve(max_tokens)
+        self.layer = layer
+        self.h2d, self.comp, self.d2h = (torch.cuda.Stream(dev) for _ in range(3))
+        self.x = [torch.empty(max_tokens, H, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.l = [torch.empty(max_tokens, E, dtype=torch.float32, device=dev) for _ in range(2)]
+        self.y = [torch.empty(max_tokens, H, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.in_ready = [torch.cuda.Event() for _ in range(2)]
+        self.comp_done = [torch.cuda.Event() for _ in range(2)]
+        self.d2h_done = [torch.cuda.Event() for _ in range(2)]
+
+    def run(self, xs, logits, ys):
+        """Forward of every (xs[i], logits[i]) host batch into the host tensor ys[i]."""
+        for i in range(len(xs)):
+            b = i & 1
+            T = xs[i].shape[0]
+            x, lg, y = self.x[b][:T], self.l[b][:T], self.y[b][:T]
+            self.h2d.wait_event(self.comp_done[b])         # batch i-2 no longer reads x[b]
+            with torch.cuda.stream(self.h2d):
+                x.copy_(xs[i], non_blocking=True)
+                lg.copy_(logits[i], non_blocking=True)
+                self.in_ready[b].record(self.h2d)
+            self.comp.wait_event(self.in_ready[b])
+            self.comp.wait_event(self.d2h_done[b])         # batch i-2 has left y[b]
+            self.layer(x, lg, out=y, stream=self.comp)
+            self.comp_done[b].record(self.comp)
+            self.d2h.wait_event(self.comp_done[b])
+            with torch.cuda.stream(self.d2h):
+                ys[i].copy_(y, non_blocking=True)
+                self.d2h_done[b].record(self.d2h)
+        return ys

@@ -36,9 +36,10 @@ def flags(verbose_ptxas: bool = False) -> list:
     return f
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc()] + flags(verbose_ptxas) + ["-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(src: str, verbose_ptxas: bool, defines=(), build_dir: str = BUILD) -> str:
+    obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
+    cmd = ([nvcc()] + flags(verbose_ptxas) + [f"-D{d}" for d in defines]
+           + ["-c", os.path.join(CSRC, src), "-o", obj])
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -47,24 +48,29 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile every CUDA source and link libgbmoe.so; returns the library path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, defines=(), lib: str = LIB,
+          build_dir: str = BUILD) -> str:
+    """Compile every CUDA source and link libgbmoe.so; returns the library path.
+
+    ``defines`` (NAME=VALUE strings) override compile-time tunables of csrc/kernels.h;
+    with ``lib`` / ``build_dir`` such a variant builds next to the default library.
+    """
+    os.makedirs(build_dir, exist_ok=True)
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     hdrs = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))]
     hdrs.append(os.path.join(ROOT, "include", "gbmoe.h"))
-    if (not force and os.path.exists(LIB)
-            and os.path.getmtime(LIB) > max(os.path.getmtime(p) for p in srcs + hdrs)):
-        return LIB
+    if (not force and os.path.exists(lib)
+            and os.path.getmtime(lib) > max(os.path.getmtime(p) for p in srcs + hdrs)):
+        return lib
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, defines, build_dir), SOURCES))
+    tmp = lib + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

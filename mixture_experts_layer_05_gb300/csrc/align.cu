@@ -164,7 +164,16 @@ __global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restric
     if (p < 0 || p >= max_rows) continue;
     const uint4* src = x + (size_t)(f / k) * H8;
     uint4* dst = xp + (size_t)p * H8;
-    for (int i = threadIdx.x; i < H8; i += blockDim.x) dst[i] = __ldg(src + i);
+    int i = threadIdx.x;
+    for (; i + 3 * 128 < H8; i += 4 * 128) {       // four 16-byte loads in flight per thread
+      const uint4 v0 = __ldg(src + i), v1 = __ldg(src + i + 128);
+      const uint4 v2 = __ldg(src + i + 256), v3 = __ldg(src + i + 384);
+      dst[i] = v0;
+      dst[i + 128] = v1;
+      dst[i + 256] = v2;
+      dst[i + 384] = v3;
+    }
+    for (; i < H8; i += 128) dst[i] = __ldg(src + i);
   }
 }
 
@@ -287,7 +296,16 @@ __global__ void __launch_bounds__(kSmallThreads)
         const int pi = __shfl_sync(0xffffffffu, slot, i);
         const uint4* src = x + (size_t)(fi / a.k) * H8;
         uint4* dst = xp + (size_t)pi * H8;
-        for (int j = lane; j < H8; j += 32) dst[j] = __ldg(src + j);
+        int j = lane;
+        for (; j + 96 < H8; j += 128) {             // four 16-byte loads in flight per lane
+          const uint4 v0 = __ldg(src + j), v1 = __ldg(src + j + 32);
+          const uint4 v2 = __ldg(src + j + 64), v3 = __ldg(src + j + 96);
+          dst[j] = v0;
+          dst[j + 32] = v1;
+          dst[j + 64] = v2;
+          dst[j + 96] = v3;
+        }
+        for (; j < H8; j += 32) dst[j] = __ldg(src + j);
       }
     }
   }
@@ -315,8 +333,9 @@ struct RouteAlignSmall {
   }
 };
 
+// One CTA routes all tokens here (8 warps), so only batches of a few tokens qualify.
 bool route_align_small_ok(int T, int k, int E) {
-  return T * k <= kAlignChunk && E <= 1024;
+  return T <= 16 && T * k <= kAlignChunk && E <= 1024;
 }
 
 cudaError_t launch_route_align_small(const gbmoe_config_t& c, int T, const float* logits,

@@ -70,8 +70,38 @@ gbmoe_status_t check_layer(const gbmoe_config_t* c) {
   return GBMOE_OK;
 }
 
+// CTA-pair GEMMs (row blocks of 256) when the experts average >= kPairMinRowsPerExpert
+// rows and the w2 output tiles are 256 wide.
+bool use_pair(const gbmoe_config_t& c, int T) {
+  return (long)T * c.top_k >= (long)kPairMinRowsPerExpert * c.num_experts &&
+         c.hidden_size % 256 == 0;
+}
+
+// Split-K factor: the persistent grid runs ceil(units / SMs) rounds of units whose
+// length is 1/s of a tile's K range, so pick s minimising ceil(tiles*s / SMs) / s
+// (a split must keep >= 4 K blocks, and must beat the smaller s by 3 %).
+int choose_splits(long tiles, int k_blocks, int T) {
+  if (T > kSplitMaxTokens || tiles <= 0) return 1;
+  const long sms = num_sms();
+  int best = 1;
+  double best_t = (double)((tiles + sms - 1) / sms);
+  for (int s = 2; s <= (int)kMaxSplits && k_blocks / s >= 4; ++s) {
+    const long u = tiles * s;
+    const double t = (double)((u + sms - 1) / sms) / s;
+    if (t < best_t * 0.97) {
+      best = s;
+      best_t = t;
+    }
+  }
+  return best;
+}
+
 struct Layout {
   int bs, n, max_sorted, max_blocks, slots;
+  bool pair;
+  // launch plan of one forward: small-batch routing, fused row copy, split factors
+  bool small, fused_copy;
+  int w2_bn, splits13, splits2, launches;
   size_t status, topk_weights, topk_ids, sorted, expert_ids, npp, block_seg, inv, scratch,
       x_perm, act, ytok, act_s, part_r, part_s, total;
 };
@@ -80,7 +110,8 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   Layout L;
   const int E = c.num_experts, k = c.top_k, H = c.hidden_size, I = c.intermediate_size;
   const int Is = c.shared_intermediate_size;
-  L.bs = kGemmBM;
+  L.pair = use_pair(c, T);
+  L.bs = L.pair ? 2 * kGemmBM : kGemmBM;
   L.n = T * k;
   L.max_sorted = L.n + E * (L.bs - 1);
   L.max_blocks = L.max_sorted / L.bs + 1;
@@ -120,6 +151,19 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   L.part_s = o;
   o = up(o + kMaxSplits * ts * 2 * Is * 4);
   L.total = o;
+
+  // launch plan
+  L.small = route_align_small_ok(T, k, E);
+  L.fused_copy = L.small && L.n <= kFusedCopyMaxRows;
+  L.w2_bn = (H % 256 == 0) ? 256 : 128;
+  const long est_blocks = (long)(L.n < E ? L.n : E) + L.n / kGemmBM;  // >= 1 partial per expert
+  const long t_blocks = ((long)T + L.bs - 1) / L.bs;
+  L.splits13 = L.pair ? 1
+                      : choose_splits(est_blocks * (I / kGemmBM) + (Is ? t_blocks * (Is / kGemmBM) : 0),
+                                      H / kGemmBK, T);
+  const int kb2 = (Is && Is < I ? Is : I) / kGemmBK;
+  L.splits2 = L.pair ? 1 : choose_splits((est_blocks + (Is ? t_blocks : 0)) * (H / L.w2_bn), kb2, T);
+  L.launches = (L.small ? (L.fused_copy ? 1 : 2) : 5) + 1 + (L.splits13 > 1 ? 1 : 0) + 1 + 1;
   return L;
 }
 
@@ -130,29 +174,10 @@ T* at(void* ws, size_t off) {
 
 gbmoe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA; }
 
-// Split-K factor: the persistent grid runs ceil(units / SMs) rounds of units whose
-// length is 1/s of a tile's K range, so pick s minimising ceil(tiles*s / SMs) / s
-// (a split must keep >= 4 K blocks, and must beat the smaller s by 3 %).
-int choose_splits(long tiles, int k_blocks, int T) {
-  if (T > kSplitMaxTokens || tiles <= 0) return 1;
-  const long sms = num_sms();
-  int best = 1;
-  double best_t = (double)((tiles + sms - 1) / sms);
-  for (int s = 2; s <= (int)kMaxSplits && k_blocks / s >= 4; ++s) {
-    const long u = tiles * s;
-    const double t = (double)((u + sms - 1) / sms) / s;
-    if (t < best_t * 0.97) {
-      best = s;
-      best_t = t;
-    }
-  }
-  return best;
-}
-
-// Row blocks walked together: keep a group's A rows (128 x K bf16 each) near 24 MB.
-int group_m_for(int K) {
-  const long per_block = (long)kGemmBM * K * 2;
-  long g = (24l << 20) / per_block;
+// Row blocks walked together: keep a group's A rows (bm x K bf16 each) near 40 MB.
+int group_m_for(int K, int bm = kGemmBM) {
+  const long per_block = (long)bm * K * 2;
+  long g = (40l << 20) / per_block;
   if (g < 1) g = 1;
   if (g > 16) g = 16;
   return (int)g;
@@ -214,9 +239,8 @@ GBMOE_API size_t moe_forward_workspace_size(const gbmoe_config_t* cfg, int32_t m
 }
 
 GBMOE_API int32_t moe_forward_block_size(const gbmoe_config_t* cfg, int32_t num_tokens) {
-  (void)cfg;
-  (void)num_tokens;
-  return kGemmBM;
+  if (check_layer(cfg) != GBMOE_OK || num_tokens < 0) return kGemmBM;
+  return use_pair(*cfg, num_tokens) ? 2 * kGemmBM : kGemmBM;
 }
 
 GBMOE_API gbmoe_status_t moe_forward_workspace_layout(const gbmoe_config_t* cfg,
@@ -278,8 +302,8 @@ GBMOE_API gbmoe_status_t moe_forward_events(
   auto rec = [&](int i) -> cudaError_t {
     return events ? cudaEventRecord((cudaEvent_t)events[i], stream) : cudaSuccess;
   };
-  const int w2_bn = (H % 256 == 0) ? 256 : 128;
-  const int t_pad = (T + kGemmBM - 1) / kGemmBM * kGemmBM;
+  const int w2_bn = L.w2_bn;
+  const int t_pad = (T + L.bs - 1) / L.bs * L.bs;
   cudaError_t e;
 
 #define GBMOE_TRY(x)                   \
@@ -291,8 +315,8 @@ GBMOE_API gbmoe_status_t moe_forward_events(
   GBMOE_TRY(rec(0));
   int2* bseg = at<int2>(workspace, L.block_seg);
   int* inv = at<int>(workspace, L.inv);
-  if (route_align_small_ok(T, k, E)) {
-    const bool fused_copy = L.n <= kFusedCopyMaxRows;
+  if (L.small) {
+    const bool fused_copy = L.fused_copy;
     GBMOE_TRY(launch_route_align_small(c, T, router_logits, e_score_correction_bias, tw, tids,
                                        L.bs, sorted, eids, L.max_blocks, npp, bseg, inv,
                                        hidden_states, fused_copy ? x_perm : nullptr, status,
@@ -307,9 +331,6 @@ GBMOE_API gbmoe_status_t moe_forward_events(
   }
   GBMOE_TRY(rec(1));
 
-  // routed blocks: at most one partial block per active expert plus the full ones
-  const long est_blocks = (long)(L.n < E ? L.n : E) + L.n / kGemmBM;
-  const long t_blocks = t_pad / kGemmBM;
 
   // ---- w13 + SiLU*mul: routed experts and the shared expert in one launch
   GemmLaunch g1;
@@ -326,10 +347,10 @@ GBMOE_API gbmoe_status_t moe_forward_events(
     P.n_tiles = I / kGemmBM;
     P.k_blocks = H / kGemmBK;
     P.m_rows_dev = npp;
-    P.max_m_blocks = L.max_sorted / kGemmBM;
+    P.max_m_blocks = L.max_sorted / L.bs;
     P.expert_ids = eids;
     P.block_seg = bseg;
-    P.group_m = group_m_for(H);
+    P.group_m = group_m_for(H, L.bs);
     P.num_experts = E;
     P.b_rows_per_expert = 2 * I;
     P.up_offset = I;
@@ -351,8 +372,8 @@ GBMOE_API gbmoe_status_t moe_forward_events(
     P.n_tiles = Is / kGemmBM;
     P.k_blocks = H / kGemmBK;
     P.m_rows_host = t_pad;
-    P.max_m_blocks = t_pad / kGemmBM;
-    P.group_m = group_m_for(H);
+    P.max_m_blocks = t_pad / L.bs;
+    P.group_m = group_m_for(H, L.bs);
     P.num_experts = 1;
     P.b_rows_per_expert = 2 * Is;
     P.up_offset = Is;
@@ -363,9 +384,9 @@ GBMOE_API gbmoe_status_t moe_forward_events(
     P.part = at<float>(workspace, L.part_s);
     P.part_split_stride = (long long)T * 2 * Is;
   }
-  g1.splits = choose_splits(est_blocks * (I / kGemmBM) + t_blocks * (Is / kGemmBM) * (Is ? 1 : 0),
-                            H / kGemmBK, T);
-  GBMOE_TRY(launch_gemm(kGemmW13, kGemmBM, g1, stream));
+  g1.splits = L.splits13;
+  // a row block holds at most T real rows (a token meets an expert once)
+  GBMOE_TRY(launch_gemm(kGemmW13, kGemmBM, g1, stream, L.pair, T));
   if (g1.splits > 1) GBMOE_TRY(launch_silu_reduce(g1, npp, L.max_sorted, stream));
   GBMOE_TRY(rec(2));
 
@@ -385,10 +406,10 @@ GBMOE_API gbmoe_status_t moe_forward_events(
     P.n_tiles = H / w2_bn;
     P.k_blocks = I / kGemmBK;
     P.m_rows_dev = npp;
-    P.max_m_blocks = L.max_sorted / kGemmBM;
+    P.max_m_blocks = L.max_sorted / L.bs;
     P.expert_ids = eids;
     P.block_seg = bseg;
-    P.group_m = group_m_for(I);
+    P.group_m = group_m_for(I, L.bs);
     P.num_experts = E;
     P.b_rows_per_expert = H;
     P.out = ytok;
@@ -411,8 +432,8 @@ GBMOE_API gbmoe_status_t moe_forward_events(
     P.n_tiles = H / w2_bn;
     P.k_blocks = Is / kGemmBK;
     P.m_rows_host = t_pad;
-    P.max_m_blocks = t_pad / kGemmBM;
-    P.group_m = group_m_for(Is);
+    P.max_m_blocks = t_pad / L.bs;
+    P.group_m = group_m_for(Is, L.bs);
     P.num_experts = 1;
     P.b_rows_per_expert = H;
     P.out = ytok;
@@ -424,9 +445,8 @@ GBMOE_API gbmoe_status_t moe_forward_events(
     P.slot_offset = k;
     P.out_split_stride = slot_copy;
   }
-  const int kb2 = Is ? ((I < Is ? I : Is) / kGemmBK) : I / kGemmBK;
-  g2.splits = choose_splits((est_blocks + (Is ? t_blocks : 0)) * (H / w2_bn), kb2, T);
-  GBMOE_TRY(launch_gemm(kGemmW2, w2_bn, g2, stream));
+  g2.splits = L.splits2;
+  GBMOE_TRY(launch_gemm(kGemmW2, w2_bn, g2, stream, L.pair, T));
   GBMOE_TRY(rec(3));
   GBMOE_TRY(launch_combine(ytok, L.slots, H, T, g2.splits, slot_copy, output, stream));
   GBMOE_TRY(rec(4));
@@ -443,6 +463,21 @@ GBMOE_API gbmoe_status_t moe_forward(const gbmoe_config_t* cfg, int32_t num_toke
   return moe_forward_events(cfg, num_tokens, hidden_states, router_logits,
                             e_score_correction_bias, w13_weight, w2_weight, shared_w13, shared_w2,
                             output, workspace, workspace_bytes, nullptr, 0, stream);
+}
+
+GBMOE_API int32_t moe_forward_num_launches(const gbmoe_config_t* cfg, int32_t num_tokens) {
+  if (check_layer(cfg) != GBMOE_OK || num_tokens < 0 || num_tokens > kMaxTokens) return -1;
+  if (num_tokens == 0) return 0;
+  return layout_for(*cfg, num_tokens).launches;
+}
+
+GBMOE_API gbmoe_status_t moe_selftest_bounded_wait(void* workspace, int32_t timeout_us,
+                                                   gbmoe_stream_t stream) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) || timeout_us < 0 ||
+      timeout_us > 10000000)
+    return GBMOE_ERR_INVALID_ARG;
+  return cuda_status(launch_wait_selftest(at<int>(workspace, 0), timeout_us,
+                                          (cudaStream_t)stream));
 }
 
 GBMOE_API gbmoe_status_t moe_get_device_status(void* workspace, int32_t* status,

@@ -71,14 +71,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase of `bar` with parity `parity`; false if the CTA is aborting or
 // the wait ran past kWaitTimeoutNs (then the CTA is marked aborting).
 __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
+                                          int* status,
+                                          unsigned long long timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      if (globaltimer_ns() - t0 > timeout_ns) {
         *abort_flag = 1;
         record_status(status, GBMOE_ERR_TIMEOUT);
         return false;
@@ -167,6 +168,95 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
          ((uint32_t)(M >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- CTA pair (cluster of 2)
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __noinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, int* status) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 63u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        *abort_flag = 1;
+        record_status(status, GBMOE_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+// TMA load into this CTA's shared memory whose completion is counted on an mbarrier
+// that may live in the peer CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".cta_group::2 [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// D[tmem of both CTAs] (+)= A[smem of both CTAs] * B[halves in both CTAs]^T, M = 256.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the mbarrier at this offset in both CTAs of the pair once the issued
+// MMAs have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + __expf(-g)) * u; }
 
 // Tile t -> (row block, N tile). Row blocks are taken in groups of at most group_m
@@ -206,18 +296,18 @@ struct Unit {
 struct Schedule {
   int mblk[2], tiles[2], total_tiles, units;
 
-  __device__ void init(const GemmLaunch& L) {
+  __device__ void init(const GemmLaunch& L, int bm = kGemmBM) {
     total_tiles = 0;
     for (int p = 0; p < 2; ++p) {
       mblk[p] = tiles[p] = 0;
       if (p >= L.num_problems) continue;
       const GemmProblem& P = L.p[p];
       int rows = P.m_rows_dev ? *P.m_rows_dev : P.m_rows_host;
-      if (rows < 0 || rows % kGemmBM != 0 || rows > P.max_m_blocks * kGemmBM) {
+      if (rows < 0 || rows % bm != 0 || rows > P.max_m_blocks * bm) {
         if (threadIdx.x == 0) record_status(L.status, GBMOE_ERR_DEVICE_CHECK);
         rows = 0;
       }
-      mblk[p] = rows / kGemmBM;
+      mblk[p] = rows / bm;
       tiles[p] = mblk[p] * P.n_tiles;
       total_tiles += tiles[p];
     }
@@ -238,13 +328,23 @@ struct Schedule {
   }
 };
 
-template <int KIND, int BN>
+// AROWS: A rows actually loaded per stage (128, or 32 when every row block holds at most
+// 32 real rows, T <= 32); the MMA still reads a 128-row A tile, and the rows not loaded
+// only feed output rows that are never stored. Smaller stages buy a deeper pipeline.
+template <int KIND, int BN, int AROWS = kGemmBM>
 struct Shape {
   static constexpr int kBRows = KIND == kGemmW13 ? 2 * BN : BN;  // B rows per stage = MMA N
   static constexpr uint32_t kBBytes = kBRows * kGemmBK * 2;
-  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 1024 + 256;
+  // A region of a stage = the rows actually loaded; the MMA's 128-row read of a 32-row
+  // region runs on into the stage's own B bytes (inside this CTA's shared memory), which
+  // only feeds discarded output rows.
+  static constexpr uint32_t kARegion = AROWS * kGemmBK * 2;
+  static constexpr uint32_t kStageBytes = kARegion + kBBytes;    // smem footprint per stage
+  static constexpr uint32_t kTxBytes = kARegion + kBBytes;       // bytes TMA delivers per stage
+  static constexpr int kNumStages = AROWS == kGemmBM ? kStages : 6;
+  static constexpr size_t kSmem = (size_t)kNumStages * kStageBytes + 1024 + 256;
   static_assert(kBRows % 16 == 0 && kBRows <= 256, "MMA N out of range for M=128");
+  static_assert(kSmem <= 232448, "shared memory per CTA exceeded");
 };
 
 __device__ __forceinline__ void store_f32x32(float* dst, const uint32_t (&r)[32], float w) {
@@ -255,12 +355,13 @@ __device__ __forceinline__ void store_f32x32(float* dst, const uint32_t (&r)[32]
                        w * __uint_as_float(r[4 * v + 2]), w * __uint_as_float(r[4 * v + 3]));
 }
 
-template <int KIND, int BN>
+template <int KIND, int BN, int AROWS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                 const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                 const GemmLaunch args) {
-  using S = Shape<KIND, BN>;
+  using S = Shape<KIND, BN, AROWS>;
+  constexpr int kStages = S::kNumStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;            // 1024-aligned tiles
@@ -333,8 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t sa = base + s * S::kStageBytes;
-          const uint32_t sb = sa + kABytes;
-          mbar_expect_tx(full_bar(s), S::kStageBytes);
+          const uint32_t sb = sa + S::kARegion;
+          mbar_expect_tx(full_bar(s), S::kTxBytes);
           tma_load_2d(sa, ta, full_bar(s), kb * kGemmBK, a_row);
           tma_load_2d(sb, tb, full_bar(s), kb * kGemmBK, b_row);
           if (KIND == kGemmW13)
@@ -366,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t sa = base + s * S::kStageBytes;
-          const uint32_t sb = sa + kABytes;
+          const uint32_t sb = sa + S::kARegion;
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk)
             mma_bf16(d, sdesc_sw128(sa + kk * 32), sdesc_sw128(sb + kk * 32), idesc,
@@ -476,6 +577,264 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- the CTA-pair GEMM
+// One work unit = 256 rows (a 256-row block of one expert) x one N tile of 256 MMA
+// columns, computed by a cluster of two CTAs with tcgen05.mma.cta_group::2 (M = 256):
+// CTA r loads A rows [256 b + 128 r, +128) and half r of the B tile, so each SM stages
+// 32 KB per K step instead of 48 KB and half of each weight tile. w13: half 0 = the
+// gate rows, half 1 = the up rows (D columns [0,128) gate, [128,256) up); w2: the
+// two 128-row halves of a 256-row weight tile. The leader CTA (rank 0) issues the
+// MMAs; both CTAs' loads complete on the leader's full barrier; commits arrive on the
+// barriers of both CTAs. Each CTA has two 256-column accumulators; its 8 epilogue
+// warps copy one to registers, release it, and only then apply SiLU*mul or the
+// routing weight and store, while the MMAs of the next units run.
+constexpr int kPairStages = 6;
+constexpr int kPairEpiWarps = 8;
+constexpr int kPairThreads = 64 + 32 * kPairEpiWarps;
+constexpr uint32_t kPairTmemCols = 512;  // two 256-column accumulators
+constexpr uint32_t kPairStageBytes = kABytes + 128 * kGemmBK * 2;
+constexpr size_t kPairSmem = (size_t)kPairStages * kPairStageBytes + 1024 + 256;
+constexpr int kPairBM = 2 * kGemmBM;
+
+template <int KIND>
+__global__ void __launch_bounds__(kPairThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0,
+                     const __grid_constant__ CUtensorMap tmB0,
+                     const __grid_constant__ CUtensorMap tmA1,
+                     const __grid_constant__ CUtensorMap tmB1, const GemmLaunch args) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStageBytes);
+  // bars: full[kPairStages] empty[kPairStages] tfull[2] tempty[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_addr(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kPairStages + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kPairStages + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kPairStages + 2 + a); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 2 * kPairEpiWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tmA0);
+    tma_prefetch(&tmB0);
+    if (args.num_problems > 1) {
+      tma_prefetch(&tmA1);
+      tma_prefetch(&tmB1);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_addr(tmem_slot), kPairTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();             // barriers of both CTAs initialised, TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t leader_full0 = mapa_shared(full_bar(0), 0);
+  const uint32_t leader_tempty0 = mapa_shared(tempty_bar(0), 0);
+
+  Schedule sched;
+  sched.init(args, kPairBM);
+  const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = cluster_id; ok && u < sched.units; u += num_clusters) {
+        const Unit w = sched.unit(args, u);
+        const GemmProblem& P = args.p[w.p];
+        const CUtensorMap* ta = w.p ? &tmA1 : &tmA0;
+        const CUtensorMap* tb = w.p ? &tmB1 : &tmB0;
+        int e = P.expert_ids ? P.expert_ids[w.mb] : 0;
+        if ((unsigned)e >= (unsigned)P.num_experts) {
+          record_status(args.status, GBMOE_ERR_DEVICE_CHECK);
+          e = 0;
+        }
+        const int a_row = w.mb * kPairBM + (int)rank * kGemmBM;
+        const int b_row = KIND == kGemmW13
+                              ? e * P.b_rows_per_expert + w.nt * 128 + (rank ? P.up_offset : 0)
+                              : e * P.b_rows_per_expert + w.nt * 256 + (int)rank * 128;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+          const int s = it % kPairStages;
+          const uint32_t ph = (it / kPairStages) & 1u;
+          if (!wait_bounded_cluster(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = base + s * kPairStageBytes;
+          if (leader) mbar_expect_tx(full_bar(s), 2 * kPairStageBytes);
+          const uint32_t fb = leader_full0 + 8u * s;
+          tma_load_2d_pair(sa, ta, fb, kb * kGemmBK, a_row);
+          tma_load_2d_pair(sa + kABytes, tb, fb, kb * kGemmBK, b_row);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    if (leader && lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kPairBM, 256);
+      uint32_t it = 0;
+      int local = 0;
+      bool ok = true;
+      for (int u = cluster_id; ok && u < sched.units; u += num_clusters, ++local) {
+        const Unit w = sched.unit(args, u);
+        const int acc = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!wait_bounded_cluster(tempty_bar(acc), (use & 1u) ^ 1u, abort_flag, args.status))
+          break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * kAccStride;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+          const int s = it % kPairStages;
+          const uint32_t ph = (it / kPairStages) & 1u;
+          if (!wait_bounded_cluster(full_bar(s), ph, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + s * kPairStageBytes;
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kGemmBK / 16; ++kk)
+            mma_bf16_pair(d, sdesc_sw128(sa + kk * 32), sdesc_sw128(sb + kk * 32), idesc,
+                          (kb > w.kb0 || kk != 0) ? 1u : 0u);
+          mma_commit_pair(empty_bar(s));
+        }
+        if (!ok) break;
+        mma_commit_pair(tfull_bar(acc));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int ew = warp - 2;
+    const int quarter = warp & 3;             // TMEM lanes [32*quarter, 32*quarter + 32)
+    const int half = ew >> 2;                 // which half of this thread's columns
+    const int row = quarter * 32 + lane;
+    int local = 0;
+    for (int u = cluster_id; u < sched.units; u += num_clusters, ++local) {
+      const Unit w = sched.unit(args, u);
+      const GemmProblem& P = args.p[w.p];
+      const int acc = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      if (!wait_bounded_cluster(tfull_bar(acc), use & 1u, abort_flag, args.status)) break;
+      tc_fence_after();
+      const int m = w.mb * kPairBM + (int)rank * kGemmBM + row;
+      const uint32_t tl = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kAccStride;
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      if (KIND == kGemmW13) {         // gate cols [64 h, +64), up cols [128 + 64 h, +64)
+        tmem_ld32(tl + half * 64, r0);
+        tmem_ld32(tl + half * 64 + 32, r1);
+        tmem_ld32(tl + 128 + half * 64, r2);
+        tmem_ld32(tl + 128 + half * 64 + 32, r3);
+      } else {                        // output cols [128 h, +128)
+        tmem_ld32(tl + half * 128, r0);
+        tmem_ld32(tl + half * 128 + 32, r1);
+        tmem_ld32(tl + half * 128 + 64, r2);
+        tmem_ld32(tl + half * 128 + 96, r3);
+      }
+      tmem_wait_ld(r0);
+      reg_fence(r1);
+      reg_fence(r2);
+      reg_fence(r3);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8u * acc);  // accumulator free again
+      int f = -1;
+      if (P.sorted_ids) {
+        const int v = P.sorted_ids[m];
+        if (v >= 0 && v < P.num_flat) f = v;
+      } else if (m < P.store_rows) {
+        f = m;
+      }
+      if (KIND == kGemmW13) {
+        const bool store = P.sorted_ids ? true : (m < P.store_rows);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.out) +
+                                                (size_t)m * P.ldo + (size_t)w.nt * 128 + half * 64);
+          // 64 consecutive activations -> 8 x 16-byte stores
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t* g = c ? r1 : r0;
+            const uint32_t* up = c ? r3 : r2;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t q[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                q[i] = pack_bf16x2(silu_mul(__uint_as_float(g[8 * v + 2 * i]),
+                                            __uint_as_float(up[8 * v + 2 * i])),
+                                   silu_mul(__uint_as_float(g[8 * v + 2 * i + 1]),
+                                            __uint_as_float(up[8 * v + 2 * i + 1])));
+              dst[c * 4 + v] = make_uint4(q[0], q[1], q[2], q[3]);
+            }
+          }
+        }
+      } else {
+        int dest = -1;
+        float wt = 1.f;
+        if (f >= 0) {
+          if (P.sorted_ids) {
+            dest = (f / P.top_k) * P.slots + (f % P.top_k);
+            wt = P.row_weight ? P.row_weight[f] : 1.f;
+          } else {
+            dest = f * P.slots + P.slot_offset;
+          }
+        }
+        if (dest >= 0) {
+          float* dst = static_cast<float*>(P.out) + (size_t)dest * P.ldo + (size_t)w.nt * 256 +
+                       half * 128;
+          store_f32x32(dst, r0, wt);
+          store_f32x32(dst + 32, r1, wt);
+          store_f32x32(dst + 64, r2, wt);
+          store_f32x32(dst + 96, r3, wt);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();             // no CTA leaves while its peer may still signal or read it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kPairTmemCols);
+  }
+}
+
+// Self test of the bounded wait: one thread waits on an mbarrier nobody arrives on; the
+// wait gives up after timeout_ns and records GBMOE_ERR_TIMEOUT in the status word.
+__global__ void wait_selftest_kernel(int* status, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_bounded(smem_addr(&bar), 0u, &abort_flag, status, timeout_ns);
+}
+
 // act = silu(sum_s gate_s) * sum_s up_s, one CTA per output row, 8 columns per step.
 __global__ void __launch_bounds__(128) silu_reduce_kernel(const GemmLaunch L, const int* npp,
                                                           int max_routed_rows) {
@@ -504,12 +863,13 @@ __global__ void __launch_bounds__(128) silu_reduce_kernel(const GemmLaunch L, co
       float g[8], u[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) g[i] = u[i] = 0.f;
+#pragma unroll 4
       for (int s = 0; s < L.splits; ++s) {
         const float* q = base + (size_t)s * P->part_split_stride + j;
-        const float4 g0 = *reinterpret_cast<const float4*>(q);
-        const float4 g1 = *reinterpret_cast<const float4*>(q + 4);
-        const float4 u0 = *reinterpret_cast<const float4*>(q + N);
-        const float4 u1 = *reinterpret_cast<const float4*>(q + N + 4);
+        const float4 g0 = __ldg(reinterpret_cast<const float4*>(q));
+        const float4 g1 = __ldg(reinterpret_cast<const float4*>(q + 4));
+        const float4 u0 = __ldg(reinterpret_cast<const float4*>(q + N));
+        const float4 u1 = __ldg(reinterpret_cast<const float4*>(q + N + 4));
         g[0] += g0.x; g[1] += g0.y; g[2] += g0.z; g[3] += g0.w;
         g[4] += g1.x; g[5] += g1.y; g[6] += g1.z; g[7] += g1.w;
         u[0] += u0.x; u[1] += u0.y; u[2] += u0.z; u[3] += u0.w;
@@ -552,47 +912,100 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, ui
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int KIND, int BN>
+template <int KIND, int BN, int AROWS>
 cudaError_t launch_typed(const CUtensorMap* tm, const GemmLaunch& args, int grid,
                          cudaStream_t stream) {
-  using S = Shape<KIND, BN>;
+  using S = Shape<KIND, BN, AROWS>;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND, BN>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<KIND, BN, AROWS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)S::kSmem);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  gemm_kernel<KIND, BN><<<grid, kThreads, S::kSmem, stream>>>(tm[0], tm[1], tm[2], tm[3], args);
+  gemm_kernel<KIND, BN, AROWS>
+      <<<grid, kThreads, S::kSmem, stream>>>(tm[0], tm[1], tm[2], tm[3], args);
   return cudaGetLastError();
+}
+
+template <int AROWS>
+cudaError_t launch_rows(int kind, int bn, const CUtensorMap* tm, const GemmLaunch& L, int grid,
+                        cudaStream_t stream) {
+  if (kind == kGemmW13 && bn == 128) return launch_typed<kGemmW13, 128, AROWS>(tm, L, grid, stream);
+  if (kind == kGemmW2 && bn == 256) return launch_typed<kGemmW2, 256, AROWS>(tm, L, grid, stream);
+  if (kind == kGemmW2 && bn == 128) return launch_typed<kGemmW2, 128, AROWS>(tm, L, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+template <int KIND>
+cudaError_t launch_pair_typed(const CUtensorMap* tm, const GemmLaunch& args, int clusters,
+                              cudaStream_t stream) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<KIND>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kPairSmem);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(kPairThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<KIND>, tm[0], tm[1], tm[2], tm[3], args);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(int kind, int bn, const GemmLaunch& L, cudaStream_t stream) {
+cudaError_t launch_gemm(int kind, int bn, const GemmLaunch& L, cudaStream_t stream, bool pair,
+                        int max_rows_per_block) {
+  const int arows = (!pair && max_rows_per_block <= 32) ? 32 : kGemmBM;
   if (L.num_problems < 1 || L.num_problems > 2 || L.splits < 1) return cudaErrorInvalidValue;
+  if (pair && (L.splits != 1 || (kind == kGemmW2 && bn != 256) || (kind == kGemmW13 && bn != 128)))
+    return cudaErrorInvalidValue;
   CUtensorMap tm[4];
   long units = 0;
+  const uint32_t b_box = pair ? 128u : (uint32_t)bn;
   for (int p = 0; p < 2; ++p) {
     const GemmProblem& P = L.p[L.num_problems > p ? p : 0];
-    if (!make_map(&tm[2 * p], P.A, (uint64_t)P.K, (uint64_t)P.a_rows, kGemmBM) ||
-        !make_map(&tm[2 * p + 1], P.B, (uint64_t)P.K, (uint64_t)P.b_rows, (uint32_t)bn))
+    if (!make_map(&tm[2 * p], P.A, (uint64_t)P.K, (uint64_t)P.a_rows, (uint32_t)arows) ||
+        !make_map(&tm[2 * p + 1], P.B, (uint64_t)P.K, (uint64_t)P.b_rows, b_box))
       return cudaErrorInvalidValue;
     if (p < L.num_problems) {
       if (P.k_blocks < L.splits) return cudaErrorInvalidValue;
       units += (long)P.max_m_blocks * P.n_tiles * L.splits;
     }
   }
+  if (pair) {
+    int clusters = num_sms() / 2;
+    if (units < clusters) clusters = (int)units;
+    if (clusters < 1) clusters = 1;
+    return kind == kGemmW13 ? launch_pair_typed<kGemmW13>(tm, L, clusters, stream)
+                            : launch_pair_typed<kGemmW2>(tm, L, clusters, stream);
+  }
   int grid = num_sms();
   if (units < grid) grid = (int)units;
   if (grid < 1) grid = 1;
-  if (kind == kGemmW13 && bn == 128) return launch_typed<kGemmW13, 128>(tm, L, grid, stream);
-  if (kind == kGemmW2 && bn == 256) return launch_typed<kGemmW2, 256>(tm, L, grid, stream);
-  if (kind == kGemmW2 && bn == 128) return launch_typed<kGemmW2, 128>(tm, L, grid, stream);
-  return cudaErrorInvalidValue;
+  return arows == 32 ? launch_rows<32>(kind, bn, tm, L, grid, stream)
+                     : launch_rows<kGemmBM>(kind, bn, tm, L, grid, stream);
+}
+
+cudaError_t launch_wait_selftest(int* status, int timeout_us, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, (unsigned long long)timeout_us * 1000ull);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_silu_reduce(const GemmLaunch& L, const int* npp, int max_routed_rows,

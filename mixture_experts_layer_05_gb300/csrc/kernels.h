@@ -12,6 +12,11 @@ namespace gbmoe {
 
 constexpr int kAlignChunk = 2048;  // flat indices per align chunk (one scatter warp each)
 constexpr int kGemmBM = 128;       // token rows per GEMM tile (= align block size)
+#ifndef GBMOE_PAIR_MIN_ROWS
+#define GBMOE_PAIR_MIN_ROWS 2048
+#endif
+// CTA-pair GEMMs when the experts average at least this many rows.
+constexpr int kPairMinRowsPerExpert = GBMOE_PAIR_MIN_ROWS;
 constexpr int kGemmBK = 64;        // K elements per pipeline stage (one 128-byte swizzle row)
 
 int num_sms();
@@ -88,7 +93,16 @@ struct GemmLaunch {
   int* status;
 };
 
-cudaError_t launch_gemm(int kind, int bn, const GemmLaunch& L, cudaStream_t stream);
+// pair: the CTA-pair kernel (clusters of 2, M = 256 per unit, row blocks of 256; w13 with
+// bn = 128, w2 with bn = 256; no split-K).
+// max_rows_per_block: an upper bound on the real rows of any row block (<= 32 lets the
+// kernel load 32-row A boxes and run a deeper pipeline).
+cudaError_t launch_gemm(int kind, int bn, const GemmLaunch& L, cudaStream_t stream,
+                        bool pair = false, int max_rows_per_block = kGemmBM);
+
+// One mbarrier wait that nothing completes; gives up after timeout_us and records
+// GBMOE_ERR_TIMEOUT in *status.
+cudaError_t launch_wait_selftest(int* status, int timeout_us, cudaStream_t stream);
 
 // act = silu(sum_s gate_s) * sum_s up_s for the valid rows of each problem of a split
 // w13 launch (routed rows in expert order; identity rows for the shared expert).

@@ -187,20 +187,52 @@ def silu(z: np.ndarray) -> np.ndarray:
 
 def swiglu_mlp(h: np.ndarray, w13_e, w2_e) -> np.ndarray:
     """o = w2 @ (silu(w1 @ h) * (w3 @ h)) for rows h [n, H]; w13_e [2I, H], w2_e [H, I]."""
+    return expert_mlp(h, w13_e, w2_e)
+
+
+def expert_mlp(h, w13_e, w2_e, *, b13_e=None, b2_e=None, gated=True, swiglu_limit=None,
+               gemm1_alpha=1.0) -> np.ndarray:
+    """One expert's MLP with the layer's optional variants (sglang ``fused_moe_triton/layer``
+    page, ``FusedMoE.__init__``: ``with_bias``, ``is_gated``, ``gemm1_alpha``,
+    ``gemm1_clamp_limit``; ``DeepseekV2MLP.forward``: ``swiglu_limit``).
+
+    z = h @ w13^T (+ b13). Gated: gate = z[:, :I], up = z[:, I:]; with a limit L,
+    gate = min(gate, L) and up = clip(up, -L, L); act = gate * sigmoid(alpha * gate) * up.
+    Not gated (w13_e is [I, H]): act = silu(z). o = act @ w2^T (+ b2).
+    The pages name these parameters without their arithmetic; this is the reading the
+    NPU clipped-SwiGLU call's arguments (alpha, limit, bias) point to.
+    """
     W13 = _f64(w13_e)
     W2 = _f64(w2_e)
-    I = W13.shape[0] // 2
     h = np.atleast_2d(_f64(h))
-    gate = h @ W13[:I].T
-    up = h @ W13[I:].T
-    act = silu(gate) * up
-    return act @ W2.T
+    z = h @ W13.T
+    if b13_e is not None:
+        z = z + _f64(b13_e)
+    if gated:
+        I = W13.shape[0] // 2
+        gate, up = z[:, :I], z[:, I:]
+        if swiglu_limit is not None:
+            gate = np.minimum(gate, swiglu_limit)
+            up = np.clip(up, -swiglu_limit, swiglu_limit)
+        act = gate / (1.0 + np.exp(-gemm1_alpha * gate)) * up
+    else:
+        act = silu(z)
+    o = act @ W2.T
+    if b2_e is not None:
+        o = o + _f64(b2_e)
+    return o
 
 
 # ---------------------------------------------------------------- 8. the layer
 def fused_moe(x, logits, bias, w13, w2, shared_w13=None, shared_w2=None, *,
-              return_parts=False, **cfg):
-    """y [T, H] fp64 = routed experts (weighted, combined) + shared expert."""
+              return_parts=False, w13_bias=None, w2_bias=None, gated=True, swiglu_limit=None,
+              gemm1_alpha=1.0, apply_router_weight_on_input=False, **cfg):
+    """y [T, H] fp64 = routed experts (weighted, combined) + shared expert.
+
+    With ``apply_router_weight_on_input`` (FusedMoE constructor argument) the routing
+    weight scales the expert's input instead of its output. The shared expert
+    (``DeepseekV2MLP``: no bias, alpha 1) shares the SwiGLU limit.
+    """
     X = _f64(x)
     T, H = X.shape
     W, ids = select_experts(logits, bias, **cfg)
@@ -208,16 +240,23 @@ def fused_moe(x, logits, bias, w13, w2, shared_w13=None, shared_w2=None, *,
     o = np.zeros((T, k, H), dtype=np.float64)
     for e in sorted(set(ids.reshape(-1).tolist())):           # each expert's weights once
         rows = [(t, j) for t in range(T) for j in range(k) if ids[t, j] == e]
-        out = swiglu_mlp(X[[t for t, _ in rows]], w13[e], w2[e])
+        h = X[[t for t, _ in rows]]
+        if apply_router_weight_on_input:
+            h = h * np.array([W[t, j] for t, j in rows])[:, None]
+        out = expert_mlp(h, w13[e], w2[e],
+                         b13_e=None if w13_bias is None else w13_bias[e],
+                         b2_e=None if w2_bias is None else w2_bias[e], gated=gated,
+                         swiglu_limit=swiglu_limit, gemm1_alpha=gemm1_alpha)
         for (t, j), r in zip(rows, out):
             o[t, j] = r
     y = np.zeros((T, H), dtype=np.float64)
     for t in range(T):
         for j in range(k):
-            y[t] += W[t, j] * o[t, j]
+            y[t] += o[t, j] if apply_router_weight_on_input else W[t, j] * o[t, j]
     shared = None
     if shared_w13 is not None:
-        shared = swiglu_mlp(X, shared_w13, shared_w2) if T else np.zeros((0, H))
+        shared = (expert_mlp(X, shared_w13, shared_w2, swiglu_limit=swiglu_limit) if T
+                  else np.zeros((0, H)))
         y = y + shared
     if return_parts:
         return y, {"topk_weights": W, "topk_ids": ids, "expert_out": o, "shared": shared}

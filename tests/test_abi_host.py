@@ -133,3 +133,16 @@ def test_workspace_sizes_monotone(lib):
 def test_device_status_validation(lib):
     v = ctypes.c_int32(0)
     assert lib.moe_get_device_status(None, ctypes.byref(v), None) == binding.ERR_INVALID_ARG
+    P = ctypes.c_void_p
+    assert lib.moe_selftest_bounded_wait(None, 1000, None) == binding.ERR_INVALID_ARG
+    assert lib.moe_selftest_bounded_wait(P(257), 1000, None) == binding.ERR_INVALID_ARG
+    assert lib.moe_selftest_bounded_wait(P(256), -1, None) == binding.ERR_INVALID_ARG
+
+
+def test_launch_count_host(lib):
+    bad = binding.make_config(num_experts=8, top_k=2, hidden_size=100, intermediate_size=256)
+    assert lib.moe_forward_num_launches(ctypes.byref(bad), 4) == -1
+    for w in configs.WORKLOADS.values():
+        cfg = binding.config_from_workload(w)
+        counts = [lib.moe_forward_num_launches(ctypes.byref(cfg), T) for T in (1, 16, 64, 4096)]
+        assert all(4 <= c <= 9 for c in counts), (w.name, counts)

@@ -276,3 +276,79 @@ def test_forward_decode_full_shapes(cuda_lib, name, T):
     check_close(y, y_ref, f"{name} T={T}")
     del layer, wts
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ CTA-pair GEMMs (large T)
+PAIR_ROUTED = _small(configs.MIXTRAL, num_experts=4, hidden_size=512, intermediate_size=384)
+PAIR_SHARED = _small(configs.DSV3, num_experts=8, top_k=4, num_expert_group=4, topk_group=2,
+                     hidden_size=256, intermediate_size=256, shared_intermediate_size=384)
+
+
+@pytest.mark.parametrize("w,T", [(PAIR_ROUTED, 4096), (PAIR_ROUTED, 4501), (PAIR_SHARED, 4100)],
+                         ids=["routed-4096", "routed-4501", "shared-4100"])
+def test_forward_pair_mode(cuda_lib, w, T):
+    """Experts averaging >= 2048 rows: row blocks of 256 on CTA pairs (cta_group::2)."""
+    cfg = binding.config_from_workload(w)
+    assert binding.moe_forward_block_size(cfg, T) == 256
+    wts = inputs.make_weights(w, 0)
+    x, logits = tokens(w, T, wts["bias"])
+    layer, _ = _layer(w, wts, T)
+    y = layer(x.to(DEV), logits.to(DEV))
+    torch.cuda.synchronize()
+    assert layer.device_status() == binding.OK
+    y_ref, parts = oracle.fused_moe(x, logits, wts["bias"], wts["w13"], wts["w2"],
+                                    wts["shared_w13"], wts["shared_w2"], return_parts=True,
+                                    **oracle_cfg(w))
+    lay = binding.moe_forward_workspace_layout(cfg, T)
+    ws = layer.workspace
+    npp = int(ws[lay.num_tokens_post_padded:lay.num_tokens_post_padded + 4].view(torch.int32))
+    s_ref, e_ref, n_ref = oracle.moe_align_block_size(parts["topk_ids"], w.num_experts, 256)
+    assert npp == n_ref
+    srt = ws[lay.sorted_token_ids:lay.sorted_token_ids + npp * 4].view(torch.int32).cpu().numpy()
+    assert np.array_equal(srt, s_ref)
+    check_close(y, y_ref, f"pair T={T}")
+    y2 = layer(x.to(DEV), logits.to(DEV))
+    assert torch.equal(y, y2)
+
+
+# ------------------------------------------------------------------ failure detection
+def test_bounded_wait_times_out_and_context_survives(cuda_lib):
+    """A wait that nothing completes gives up, reports GBMOE_ERR_TIMEOUT, and the
+    context stays usable for the next forward."""
+    ws = binding.alloc_workspace(256)
+    binding.moe_selftest_bounded_wait(ws, 2000)          # 2 ms limit
+    assert binding.moe_get_device_status(ws) == binding.ERR_TIMEOUT
+    assert binding.moe_get_device_status(ws) == binding.OK   # the read resets the word
+    w = SMALL["tiny"]
+    wts = inputs.make_weights(w, 0)
+    x, logits = tokens(w, 16, wts["bias"])
+    layer, _ = _layer(w, wts, 16)
+    y = layer(x.to(DEV), logits.to(DEV))
+    y_ref = oracle.fused_moe(x, logits, None, wts["w13"], wts["w2"], **oracle_cfg(w))
+    check_close(y, y_ref, "after timeout")
+    assert layer.device_status() == binding.OK
+
+
+def test_launch_count_matches_path(cuda_lib):
+    """moe_forward_num_launches: fused small-batch path, gather, split-K reduce."""
+    cfg = binding.config_from_workload(configs.MIXTRAL)
+    n1 = binding.moe_forward_num_launches(cfg, 1)      # fused route+align+copy, w13, reduce, w2, combine
+    n4096 = binding.moe_forward_num_launches(cfg, 4096)  # topk, 3 align, gather, w13, w2, combine
+    assert n4096 == 8
+    assert 4 <= n1 <= 6
+    assert binding.moe_forward_num_launches(cfg, 0) == 0
+
+
+def test_host_pipeline_matches_direct_calls(cuda_lib):
+    """Overlapped host batches give exactly the outputs of one-at-a-time forwards."""
+    w = SMALL["dsv3"]
+    wts = inputs.make_weights(w, 0)
+    layer, _ = _layer(w, wts, 300)
+    batches = [tokens(w, T, wts["bias"], seed=s) for s, T in ((1, 300), (2, 17), (3, 255))]
+    ys = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x, _ in batches]
+    pipe = binding.HostPipeline(layer, 300)
+    pipe.run([x.pin_memory() for x, _ in batches], [lg.pin_memory() for _, lg in batches], ys)
+    torch.cuda.synchronize()
+    for (x, lg), y in zip(batches, ys):
+        assert torch.equal(y, layer(x.to(DEV), lg.to(DEV)).cpu())
+    assert layer.device_status() == binding.OK
