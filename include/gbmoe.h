@@ -70,9 +70,19 @@ typedef enum { GBMOE_ACT_SILU = 0 } gbmoe_act_t;
  *                         (the constructor rejects non-softmax ungrouped routing)
  *  routed_scaling_factor  multiplies every routed weight (not the shared expert)
  *  activation             must be GBMOE_ACT_SILU (else UNSUPPORTED)
- *  is_act_and_mul         must be 1: act = silu(gate) * up (else UNSUPPORTED)
+ *  is_act_and_mul         1: gated, w13 [E, 2I, H], act = silu-gate * up;
+ *                         0: not gated (`is_gated=False`), w13 [E, I, H], act = silu(z)
  *  shared_intermediate_size  I_s of the dense shared SwiGLU expert; 0 = none;
- *                         else a multiple of 128
+ *                         else a multiple of 128 (gated routed experts only)
+ *  swiglu_limit           > 0: clamp the gate to <= L and the up half to [-L, L]
+ *                         before the activation (`swiglu_limit`, `gemm1_clamp_limit`;
+ *                         also applied to the shared expert); 0 = no clamp
+ *  gemm1_alpha            gated act = g * sigmoid(alpha * g) * u for the routed experts
+ *                         (`gemm1_alpha`); 0 means 1
+ *  apply_router_weight_on_input  != 0: the routing weight scales the expert's input
+ *                         rows instead of its output (FusedMoE constructor argument)
+ * The pages name the last three options without their arithmetic; the reading used is
+ * the one the NPU clipped-SwiGLU call's arguments (alpha, limit, bias) point to.
  */
 typedef struct {
   int32_t num_experts;
@@ -88,6 +98,9 @@ typedef struct {
   int32_t activation;
   int32_t is_act_and_mul;
   int32_t shared_intermediate_size;
+  float swiglu_limit;
+  float gemm1_alpha;
+  int32_t apply_router_weight_on_input;
 } gbmoe_config_t;
 
 /*
@@ -196,7 +209,9 @@ gbmoe_status_t moe_forward(const gbmoe_config_t* cfg, int32_t num_tokens,
  * moe_forward_events: moe_forward that also records caller-created CUDA events
  * (cudaEvent_t, passed as void*) on `stream` at the stage boundaries:
  * events[0] before routing, [1] after routing + align + gather, [2] after the
- * w13 GEMMs, [3] after the w2 GEMMs, [4] after the combine. `events` may be
+ * w13 GEMMs, [3] after the w2 GEMMs, [4] after the combine; a NULL entry is
+ * skipped. The records are external (cudaEventRecordExternal): inside a stream
+ * capture they become event-record nodes that time each replay. `events` may be
  * NULL (then identical to moe_forward); num_events must then be 0, else 5.
  */
 #define GBMOE_NUM_STAGE_EVENTS 5
@@ -207,6 +222,47 @@ gbmoe_status_t moe_forward_events(const gbmoe_config_t* cfg, int32_t num_tokens,
                                   const void* shared_w2, void* output, void* workspace,
                                   size_t workspace_bytes, void* const* events, int32_t num_events,
                                   gbmoe_stream_t stream);
+
+/*
+ * moe_forward_ex: moe_forward with every tensor in one struct, plus the per-expert
+ * biases of the FusedMoE `with_bias` / `has_bias` option (sglang
+ * `fused_moe_triton/layer.py` page: `w13_weight_bias`, `w2_weight_bias`):
+ *   [gate | up] = x @ w13[e]^T + w13_bias[e]   (w13_bias [E, 2I] bf16; [E, I] not gated)
+ *   o = act @ w2[e]^T + w2_bias[e]              (w2_bias [E, H] bf16)
+ * Either bias may be NULL; the shared expert has none. events / num_events as in
+ * moe_forward_events (NULL / 0 for none).
+ */
+typedef struct {
+  const void* hidden_states;
+  const float* router_logits;
+  const float* e_score_correction_bias;
+  const void* w13_weight;
+  const void* w2_weight;
+  const void* shared_w13;
+  const void* shared_w2;
+  const void* w13_bias;
+  const void* w2_bias;
+  void* output;
+  void* workspace;
+  size_t workspace_bytes;
+  void* const* events;
+  int32_t num_events;
+  const void* gate_weight;   /* [E, H] bf16: when router_logits is NULL, the logits are
+                                computed first as hidden_states @ gate_weight^T in fp32
+                                (moe_router_logits); exactly one of the two is given */
+} gbmoe_forward_args_t;
+gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_tokens,
+                              const gbmoe_forward_args_t* args, gbmoe_stream_t stream);
+
+/*
+ * moe_router_logits: the router GEMM in front of the layer, `MoEGate.forward` on the
+ * sglang `models/deepseek_v2.py` page: router_logits [T, E] fp32 = hidden_states
+ * [T, H] bf16 @ gate_weight [E, H]^T bf16, fp32 accumulation on the tensor cores.
+ * H a multiple of 64, 1 <= E <= 1024, pointers 16-byte aligned, T = 0 a no-op.
+ */
+gbmoe_status_t moe_router_logits(int32_t num_tokens, int32_t hidden_size, int32_t num_experts,
+                                 const void* hidden_states, const void* gate_weight,
+                                 float* router_logits, gbmoe_stream_t stream);
 
 /*
  * Byte offsets of the intermediate results inside a moe_forward workspace

@@ -27,7 +27,8 @@ EXPORTS = ("moe_topk", "moe_align_block_size_workspace_size", "moe_align_block_s
            "moe_align_block_size_no_workspace",
            "moe_forward_workspace_size", "moe_forward_block_size", "moe_forward",
            "moe_forward_events", "moe_forward_workspace_layout", "moe_get_device_status",
-           "moe_forward_num_launches", "moe_selftest_bounded_wait", "gbmoe_version")
+           "moe_forward_num_launches", "moe_selftest_bounded_wait", "moe_forward_ex",
+           "moe_router_logits", "gbmoe_version")
 
 
 class GbmoeError(RuntimeError):
@@ -44,7 +45,21 @@ class Config(ctypes.Structure):
                 ("num_expert_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
                 ("scoring_func", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
                 ("activation", ctypes.c_int32), ("is_act_and_mul", ctypes.c_int32),
-                ("shared_intermediate_size", ctypes.c_int32)]
+                ("shared_intermediate_size", ctypes.c_int32), ("swiglu_limit", ctypes.c_float),
+                ("gemm1_alpha", ctypes.c_float),
+                ("apply_router_weight_on_input", ctypes.c_int32)]
+
+
+class ForwardArgs(ctypes.Structure):
+    """gbmoe_forward_args_t."""
+    _fields_ = [("hidden_states", ctypes.c_void_p), ("router_logits", ctypes.c_void_p),
+                ("e_score_correction_bias", ctypes.c_void_p), ("w13_weight", ctypes.c_void_p),
+                ("w2_weight", ctypes.c_void_p), ("shared_w13", ctypes.c_void_p),
+                ("shared_w2", ctypes.c_void_p), ("w13_bias", ctypes.c_void_p),
+                ("w2_bias", ctypes.c_void_p), ("output", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("events", ctypes.c_void_p), ("num_events", ctypes.c_int32),
+                ("gate_weight", ctypes.c_void_p)]
 
 
 class WorkspaceLayout(ctypes.Structure):
@@ -57,19 +72,21 @@ class WorkspaceLayout(ctypes.Structure):
 def make_config(num_experts, top_k, hidden_size, intermediate_size, renormalize=True,
                 use_grouped_topk=False, num_expert_group=0, topk_group=0,
                 scoring_func="softmax", routed_scaling_factor=1.0, activation=0,
-                is_act_and_mul=1, shared_intermediate_size=0) -> Config:
+                is_act_and_mul=1, shared_intermediate_size=0, swiglu_limit=None,
+                gemm1_alpha=1.0, apply_router_weight_on_input=False) -> Config:
     return Config(int(num_experts), int(top_k), int(hidden_size), int(intermediate_size),
                   int(bool(renormalize)), int(bool(use_grouped_topk)), int(num_expert_group or 0),
                   int(topk_group or 0), SCORE.get(scoring_func, scoring_func),
                   float(routed_scaling_factor), int(activation), int(is_act_and_mul),
-                  int(shared_intermediate_size or 0))
+                  int(shared_intermediate_size or 0), float(swiglu_limit or 0.0),
+                  float(gemm1_alpha), int(bool(apply_router_weight_on_input)))
 
 
-def config_from_workload(w) -> Config:
+def config_from_workload(w, **variants) -> Config:
     return make_config(w.num_experts, w.top_k, w.hidden_size, w.intermediate_size,
                        w.renormalize, w.use_grouped_topk, w.num_expert_group, w.topk_group,
                        w.scoring_func, w.routed_scaling_factor,
-                       shared_intermediate_size=w.shared_intermediate_size)
+                       shared_intermediate_size=w.shared_intermediate_size, **variants)
 
 
 _lib = None
@@ -98,6 +115,8 @@ def load() -> ctypes.CDLL:
         "moe_forward_workspace_layout": (I32, [CP, I32, ctypes.POINTER(WorkspaceLayout)]),
         "moe_get_device_status": (I32, [P, ctypes.POINTER(I32), P]),
         "moe_forward_num_launches": (I32, [CP, I32]),
+        "moe_forward_ex": (I32, [CP, I32, ctypes.POINTER(ForwardArgs), P]),
+        "moe_router_logits": (I32, [I32, I32, I32, P, P, P, P]),
         "moe_selftest_bounded_wait": (I32, [P, I32, P]),
         "gbmoe_version": (I32, []),
     }
@@ -212,9 +231,10 @@ def moe_forward(cfg: Config, hidden_states, router_logits, e_score_correction_bi
         _check("moe_forward", lib.moe_forward(*args, _stream(stream)))
     else:
         for ev in events:                  # torch creates the CUDA event on first record
-            if not ev.cuda_event:
+            if ev is not None and not ev.cuda_event:
                 ev.record()
-        arr = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
+        arr = (ctypes.c_void_p * len(events))(
+            *[None if ev is None else ev.cuda_event for ev in events])
         _check("moe_forward_events",
                lib.moe_forward_events(*args, arr, len(events), _stream(stream)))
 
@@ -228,6 +248,47 @@ def moe_selftest_bounded_wait(workspace, timeout_us: int, stream=None):
            load().moe_selftest_bounded_wait(_p(workspace), timeout_us, _stream(stream)))
 
 
+def moe_router_logits(hidden_states, gate_weight, router_logits, stream=None):
+    """router_logits [T, E] fp32 = hidden_states [T, H] @ gate_weight [E, H]^T (tensor cores)."""
+    _need(hidden_states, torch.bfloat16, "hidden_states")
+    _need(gate_weight, torch.bfloat16, "gate_weight")
+    _need(router_logits, torch.float32, "router_logits")
+    T, H = hidden_states.shape
+    _check("moe_router_logits", load().moe_router_logits(
+        T, H, gate_weight.shape[0], _p(hidden_states), _p(gate_weight), _p(router_logits),
+        _stream(stream)))
+
+
+def moe_forward_ex(cfg: Config, hidden_states, router_logits, e_score_correction_bias,
+                   w13_weight, w2_weight, shared_w13, shared_w2, output, workspace,
+                   w13_bias=None, w2_bias=None, events=None, stream=None, gate_weight=None):
+    """moe_forward with the optional per-expert biases, stage events, or (router_logits
+    None) the gate weight whose router GEMM runs first."""
+    _need(hidden_states, torch.bfloat16, "hidden_states")
+    _need(router_logits, torch.float32, "router_logits")
+    _need(e_score_correction_bias, torch.float32, "e_score_correction_bias")
+    for t, n in ((w13_weight, "w13_weight"), (w2_weight, "w2_weight"), (shared_w13, "shared_w13"),
+                 (shared_w2, "shared_w2"), (w13_bias, "w13_bias"), (w2_bias, "w2_bias"),
+                 (output, "output"), (gate_weight, "gate_weight")):
+        _need(t, torch.bfloat16, n)
+    arr = None
+    if events is not None:
+        for ev in events:
+            if ev is not None and not ev.cuda_event:
+                ev.record()
+        arr = (ctypes.c_void_p * len(events))(
+            *[None if ev is None else ev.cuda_event for ev in events])
+    ptr = lambda t: None if t is None else t.data_ptr()
+    a = ForwardArgs(ptr(hidden_states), ptr(router_logits), ptr(e_score_correction_bias),
+                    ptr(w13_weight), ptr(w2_weight), ptr(shared_w13), ptr(shared_w2),
+                    ptr(w13_bias), ptr(w2_bias), ptr(output), ptr(workspace),
+                    workspace.numel() * workspace.element_size(),
+                    ctypes.cast(arr, ctypes.c_void_p) if arr is not None else None,
+                    0 if events is None else len(events), ptr(gate_weight))
+    _check("moe_forward_ex", load().moe_forward_ex(ctypes.byref(cfg), hidden_states.shape[0],
+                                                   ctypes.byref(a), _stream(stream)))
+
+
 def moe_get_device_status(workspace, stream=None) -> int:
     v = ctypes.c_int32(0)
     _check("moe_get_device_status",
@@ -239,10 +300,12 @@ class FusedMoE:
     """The layer with its weights resident on the GPU and a workspace sized for max_tokens."""
 
     def __init__(self, cfg: Config, w13_weight, w2_weight, e_score_correction_bias=None,
-                 shared_w13=None, shared_w2=None, max_tokens: int = 1):
+                 shared_w13=None, shared_w2=None, max_tokens: int = 1, w13_bias=None,
+                 w2_bias=None):
         self.cfg = cfg
         self.w13, self.w2 = w13_weight, w2_weight
         self.bias, self.shared_w13, self.shared_w2 = e_score_correction_bias, shared_w13, shared_w2
+        self.w13_bias, self.w2_bias = w13_bias, w2_bias
         self.max_tokens = 0
         self.workspace = None
         self.reserve(max_tokens)
@@ -253,14 +316,27 @@ class FusedMoE:
             self.workspace = alloc_workspace(moe_forward_workspace_size(self.cfg, max_tokens), dev)
             self.max_tokens = max_tokens
 
-    def __call__(self, hidden_states, router_logits, out=None, events=None, stream=None):
+    def __call__(self, hidden_states, router_logits=None, out=None, events=None, stream=None,
+                 gate_weight=None):
+        """Forward from router logits, or (router_logits None) from the gate weight."""
         T = hidden_states.shape[0]
         self.reserve(T)
         if out is None:
             out = torch.empty_like(hidden_states)
-        moe_forward(self.cfg, hidden_states, router_logits, self.bias, self.w13, self.w2,
-                    self.shared_w13, self.shared_w2, out, self.workspace, events=events,
-                    stream=stream)
+        if gate_weight is not None or router_logits is None:
+            moe_forward_ex(self.cfg, hidden_states, None, self.bias, self.w13, self.w2,
+                           self.shared_w13, self.shared_w2, out, self.workspace,
+                           w13_bias=self.w13_bias, w2_bias=self.w2_bias, events=events,
+                           stream=stream, gate_weight=gate_weight)
+        elif self.w13_bias is None and self.w2_bias is None:
+            moe_forward(self.cfg, hidden_states, router_logits, self.bias, self.w13, self.w2,
+                        self.shared_w13, self.shared_w2, out, self.workspace, events=events,
+                        stream=stream)
+        else:
+            moe_forward_ex(self.cfg, hidden_states, router_logits, self.bias, self.w13, self.w2,
+                           self.shared_w13, self.shared_w2, out, self.workspace,
+                           w13_bias=self.w13_bias, w2_bias=self.w2_bias, events=events,
+                           stream=stream)
         return out
 
     def device_status(self) -> int:

@@ -152,18 +152,37 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
   }
 }
 
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = unpack_bf16x2(w[i]);
+    o[i] = pack_bf16x2(f.x * s, f.y * s);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // x_perm[inv[f]] = x[f / k] for every flat index f: only the T*k real rows are written.
+// With row_scale (apply_router_weight_on_input) the row is multiplied by row_scale[f]
+// in fp32 and rounded once to bf16.
 // Padding rows of x_perm are never written: a GEMM output row depends on its own A row
 // only, and padding rows are never stored or read back.
 __global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restrict__ x, int H8,
                                                           const int* __restrict__ inv, int n,
                                                           int k, int max_rows,
+                                                          const float* __restrict__ row_scale,
                                                           uint4* __restrict__ xp) {
   for (int f = blockIdx.x; f < n; f += gridDim.x) {
     const int p = inv[f];
     if (p < 0 || p >= max_rows) continue;
     const uint4* src = x + (size_t)(f / k) * H8;
     uint4* dst = xp + (size_t)p * H8;
+    if (row_scale) {
+      const float sc = row_scale[f];
+      for (int i = threadIdx.x; i < H8; i += blockDim.x) dst[i] = scale_bf16x8(__ldg(src + i), sc);
+      continue;
+    }
     int i = threadIdx.x;
     for (; i + 3 * 128 < H8; i += 4 * 128) {       // four 16-byte loads in flight per thread
       const uint4 v0 = __ldg(src + i), v1 = __ldg(src + i + 128);
@@ -190,7 +209,8 @@ __global__ void __launch_bounds__(kSmallThreads)
     route_align_small_kernel(TopkArgs a, int bs, int* __restrict__ sorted,
                              int* __restrict__ expert_ids, int max_blocks, int* __restrict__ npp,
                              int2* __restrict__ block_seg, int* __restrict__ inv,
-                             const uint4* __restrict__ x, int H8, uint4* __restrict__ xp) {
+                             const uint4* __restrict__ x, int H8, uint4* __restrict__ xp,
+                             const float* __restrict__ row_scale) {
   extern __shared__ int sm[];
   const int n = a.T * a.k, E = a.E;
   int* s_ids = sm;                                   // [n]
@@ -296,6 +316,11 @@ __global__ void __launch_bounds__(kSmallThreads)
         const int pi = __shfl_sync(0xffffffffu, slot, i);
         const uint4* src = x + (size_t)(fi / a.k) * H8;
         uint4* dst = xp + (size_t)pi * H8;
+        if (row_scale) {                 // the weights were written by this CTA's routing
+          const float sc = a.weights[fi];
+          for (int jj = lane; jj < H8; jj += 32) dst[jj] = scale_bf16x8(__ldg(src + jj), sc);
+          continue;
+        }
         int j = lane;
         for (; j + 96 < H8; j += 128) {             // four 16-byte loads in flight per lane
           const uint4 v0 = __ldg(src + j), v1 = __ldg(src + j + 32);
@@ -323,13 +348,14 @@ struct RouteAlignSmall {
   const uint4* x;
   int H8;
   uint4* xp;
+  const float* row_scale;
   cudaStream_t stream;
   template <int EPT>
   void operator()() {
     const int n = a.T * a.k;
     const size_t shm = (size_t)(((n + 31) & ~31) + kSmallWarps * a.E) * sizeof(int);
     route_align_small_kernel<EPT><<<1, kSmallThreads, shm, stream>>>(
-        a, bs, sorted, expert_ids, max_blocks, npp, block_seg, inv, x, H8, xp);
+        a, bs, sorted, expert_ids, max_blocks, npp, block_seg, inv, x, H8, xp, row_scale);
   }
 };
 
@@ -342,11 +368,15 @@ cudaError_t launch_route_align_small(const gbmoe_config_t& c, int T, const float
                                      const float* bias, float* weights, int* ids, int bs,
                                      int* sorted, int* expert_ids, int max_blocks, int* npp,
                                      int2* block_seg, int* inv, const void* x, void* x_perm,
-                                     int* status, cudaStream_t stream) {
-  RouteAlignSmall L{make_topk_args(c, T, logits, bias, weights, ids, status), bs, sorted,
+                                     const float* row_scale, int* status, cudaStream_t stream,
+                                     int logit_splits, long long logit_split_stride) {
+  TopkArgs ta = make_topk_args(c, T, logits, bias, weights, ids, status);
+  ta.logit_splits = logit_splits;
+  ta.logit_split_stride = logit_split_stride;
+  RouteAlignSmall L{ta, bs, sorted,
                     expert_ids, max_blocks, npp, block_seg, inv,
                     static_cast<const uint4*>(x), c.hidden_size / 8,
-                    static_cast<uint4*>(x_perm), stream};
+                    static_cast<uint4*>(x_perm), row_scale, stream};
   dispatch_ept(c.num_experts, L);
   return cudaGetLastError();
 }
@@ -373,12 +403,13 @@ cudaError_t launch_align(const int* ids, int n, int E, int bs, int* sorted, int*
 }
 
 cudaError_t launch_gather(const void* x, int H, const int* inv, int n, int k, int max_rows,
-                          void* x_perm, cudaStream_t stream) {
+                          void* x_perm, const float* row_scale, cudaStream_t stream) {
   int blocks = num_sms() * 8;
   if (blocks > n) blocks = n;
   if (blocks < 1) return cudaSuccess;
   gather_rows_kernel<<<blocks, 128, 0, stream>>>(static_cast<const uint4*>(x), H / 8, inv, n, k,
-                                                  max_rows, static_cast<uint4*>(x_perm));
+                                                  max_rows, row_scale,
+                                                  static_cast<uint4*>(x_perm));
   return cudaGetLastError();
 }
 

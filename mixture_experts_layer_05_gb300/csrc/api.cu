@@ -61,7 +61,15 @@ gbmoe_status_t check_layer(const gbmoe_config_t* c) {
   if (s != GBMOE_OK) return s;
   if (c->hidden_size <= 0 || c->intermediate_size <= 0 || c->shared_intermediate_size < 0)
     return GBMOE_ERR_INVALID_ARG;
-  if (c->activation != GBMOE_ACT_SILU || c->is_act_and_mul != 1) return GBMOE_ERR_UNSUPPORTED;
+  if (c->activation != GBMOE_ACT_SILU) return GBMOE_ERR_UNSUPPORTED;
+  if (c->is_act_and_mul != 0 && c->is_act_and_mul != 1) return GBMOE_ERR_INVALID_ARG;
+  if (!std::isfinite(c->swiglu_limit) || c->swiglu_limit < 0.f ||
+      !std::isfinite(c->gemm1_alpha) || c->gemm1_alpha < 0.f)
+    return GBMOE_ERR_INVALID_ARG;
+  if (!c->is_act_and_mul &&
+      (c->swiglu_limit > 0.f || (c->gemm1_alpha != 0.f && c->gemm1_alpha != 1.f) ||
+       c->shared_intermediate_size > 0))
+    return GBMOE_ERR_UNSUPPORTED;                  // clamp / alpha / shared need the gated form
   if (c->hidden_size % 128 || c->intermediate_size % 128 || c->shared_intermediate_size % 128)
     return GBMOE_ERR_UNSUPPORTED;
   if ((long long)c->num_experts * 2 * c->intermediate_size > INT_MAX / 2 ||
@@ -73,7 +81,9 @@ gbmoe_status_t check_layer(const gbmoe_config_t* c) {
 // CTA-pair GEMMs (row blocks of 256) when the experts average >= kPairMinRowsPerExpert
 // rows and the w2 output tiles are 256 wide.
 bool use_pair(const gbmoe_config_t& c, int T) {
-  return (long)T * c.top_k >= (long)kPairMinRowsPerExpert * c.num_experts &&
+  const bool plain = c.is_act_and_mul && c.swiglu_limit == 0.f &&
+                     (c.gemm1_alpha == 0.f || c.gemm1_alpha == 1.f);
+  return plain && (long)T * c.top_k >= (long)kPairMinRowsPerExpert * c.num_experts &&
          c.hidden_size % 256 == 0;
 }
 
@@ -96,14 +106,16 @@ int choose_splits(long tiles, int k_blocks, int T) {
   return best;
 }
 
+long t_blocks_128(int T) { return ((long)T + kGemmBM - 1) / kGemmBM; }
+
 struct Layout {
   int bs, n, max_sorted, max_blocks, slots;
   bool pair;
   // launch plan of one forward: small-batch routing, fused row copy, split factors
   bool small, fused_copy;
-  int w2_bn, splits13, splits2, launches;
+  int w2_bn, splits13, splits2, splits_router, launches;
   size_t status, topk_weights, topk_ids, sorted, expert_ids, npp, block_seg, inv, scratch,
-      x_perm, act, ytok, act_s, part_r, part_s, total;
+      x_perm, act, ytok, act_s, part_r, part_s, logits, total;
 };
 
 Layout layout_for(const gbmoe_config_t& c, int T) {
@@ -147,9 +159,11 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   L.act_s = o;
   o = up(o + (size_t)T * Is * 2);
   L.part_r = o;
-  o = up(o + kMaxSplits * ts * k * 2 * I * 4);
+  o = up(o + kMaxSplits * ts * k * (c.is_act_and_mul ? 2 : 1) * I * 4);
   L.part_s = o;
   o = up(o + kMaxSplits * ts * 2 * Is * 4);
+  L.logits = o;                       // router GEMM output (per-split copies at decode)
+  o = up(o + ((size_t)T > kMaxSplits * ts ? (size_t)T : kMaxSplits * ts) * E * 4);
   L.total = o;
 
   // launch plan
@@ -164,6 +178,7 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   const int kb2 = (Is && Is < I ? Is : I) / kGemmBK;
   L.splits2 = L.pair ? 1 : choose_splits((est_blocks + (Is ? t_blocks : 0)) * (H / L.w2_bn), kb2, T);
   L.launches = (L.small ? (L.fused_copy ? 1 : 2) : 5) + 1 + (L.splits13 > 1 ? 1 : 0) + 1 + 1;
+  L.splits_router = choose_splits(t_blocks_128(T) * ((E + kGemmBM - 1) / kGemmBM), H / kGemmBK, T);
   return L;
 }
 
@@ -261,12 +276,25 @@ GBMOE_API gbmoe_status_t moe_forward_workspace_layout(const gbmoe_config_t* cfg,
   return GBMOE_OK;
 }
 
-GBMOE_API gbmoe_status_t moe_forward_events(
-    const gbmoe_config_t* cfg, int32_t num_tokens, const void* hidden_states,
-    const float* router_logits, const float* e_score_correction_bias, const void* w13_weight,
-    const void* w2_weight, const void* shared_w13, const void* shared_w2, void* output,
-    void* workspace, size_t workspace_bytes, void* const* events, int32_t num_events,
-    gbmoe_stream_t stream_) {
+GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_tokens,
+                                        const gbmoe_forward_args_t* args,
+                                        gbmoe_stream_t stream_) {
+  if (!args) return GBMOE_ERR_INVALID_ARG;
+  const void* hidden_states = args->hidden_states;
+  const float* router_logits = args->router_logits;
+  const void* gate_weight = args->gate_weight;
+  const float* e_score_correction_bias = args->e_score_correction_bias;
+  const void* w13_weight = args->w13_weight;
+  const void* w2_weight = args->w2_weight;
+  const void* shared_w13 = args->shared_w13;
+  const void* shared_w2 = args->shared_w2;
+  const __nv_bfloat16* w13_bias = static_cast<const __nv_bfloat16*>(args->w13_bias);
+  const __nv_bfloat16* w2_bias = static_cast<const __nv_bfloat16*>(args->w2_bias);
+  void* output = args->output;
+  void* workspace = args->workspace;
+  const size_t workspace_bytes = args->workspace_bytes;
+  void* const* events = args->events;
+  const int32_t num_events = args->num_events;
   gbmoe_status_t s = check_layer(cfg);
   if (s != GBMOE_OK) return s;
   if (num_tokens < 0 || num_tokens > kMaxTokens) return GBMOE_ERR_INVALID_ARG;
@@ -277,10 +305,12 @@ GBMOE_API gbmoe_status_t moe_forward_events(
   if ((shared_w13 != nullptr) != (Is > 0) || (shared_w2 != nullptr) != (Is > 0))
     return GBMOE_ERR_INVALID_ARG;
   if (num_tokens == 0) return GBMOE_OK;
-  if (!hidden_states || !router_logits || !w13_weight || !w2_weight || !output)
+  if (!hidden_states || (!router_logits == !gate_weight) || !w13_weight || !w2_weight ||
+      !output || !aligned16(gate_weight))
     return GBMOE_ERR_INVALID_ARG;
   if (!aligned16(hidden_states) || !aligned16(w13_weight) || !aligned16(w2_weight) ||
-      !aligned16(output) || (Is && (!aligned16(shared_w13) || !aligned16(shared_w2))))
+      !aligned16(output) || (Is && (!aligned16(shared_w13) || !aligned16(shared_w2))) ||
+      !aligned16(w13_bias) || !aligned16(w2_bias))
     return GBMOE_ERR_INVALID_ARG;
   const Layout L = layout_for(c, num_tokens);
   if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) % kAlign))
@@ -299,8 +329,15 @@ GBMOE_API gbmoe_status_t moe_forward_events(
   void* act = at<char>(workspace, L.act);
   void* ytok = at<char>(workspace, L.ytok);
   void* act_s = at<char>(workspace, L.act_s);
+  // inside a stream capture the records are external, so they become event-record nodes
+  // of the graph (a plain record there only marks a capture dependency)
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (events && cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return GBMOE_ERR_CUDA;
   auto rec = [&](int i) -> cudaError_t {
-    return events ? cudaEventRecord((cudaEvent_t)events[i], stream) : cudaSuccess;
+    if (!events || !events[i]) return cudaSuccess;
+    return cap == cudaStreamCaptureStatusActive
+               ? cudaEventRecordWithFlags((cudaEvent_t)events[i], stream, cudaEventRecordExternal)
+               : cudaEventRecord((cudaEvent_t)events[i], stream);
   };
   const int w2_bn = L.w2_bn;
   const int t_pad = (T + L.bs - 1) / L.bs * L.bs;
@@ -313,21 +350,59 @@ GBMOE_API gbmoe_status_t moe_forward_events(
   } while (0)
 
   GBMOE_TRY(rec(0));
+  // router GEMM when the caller passes the gate weight instead of logits
+  int logit_splits = 1;
+  long long logit_stride = 0;
+  if (!router_logits) {
+    GemmLaunch gr;
+    std::memset(&gr, 0, sizeof(gr));
+    gr.status = status;
+    gr.num_problems = 1;
+    gr.splits = L.splits_router;
+    GemmProblem& P = gr.p[0];
+    const int tp = (T + kGemmBM - 1) / kGemmBM * kGemmBM;
+    P.A = hidden_states;
+    P.a_rows = T;
+    P.B = gate_weight;
+    P.b_rows = E;
+    P.K = H;
+    P.n_tiles = (E + kGemmBM - 1) / kGemmBM;
+    P.k_blocks = H / kGemmBK;
+    P.m_rows_host = tp;
+    P.max_m_blocks = tp / kGemmBM;
+    P.group_m = 16;
+    P.num_experts = 1;
+    P.out = at<float>(workspace, L.logits);
+    P.ldo = E;
+    P.store_rows = T;
+    P.out_split_stride = (long long)T * E;
+    GBMOE_TRY(launch_gemm(kGemmRouter, kGemmBM, gr, stream, false, T));
+    router_logits = at<float>(workspace, L.logits);
+    logit_splits = gr.splits;
+    logit_stride = (long long)T * E;
+  }
   int2* bseg = at<int2>(workspace, L.block_seg);
   int* inv = at<int>(workspace, L.inv);
+  // apply_router_weight_on_input: the gathered rows carry the routing weight instead
+  const float* row_scale = c.apply_router_weight_on_input ? tw : nullptr;
+  const bool gated = c.is_act_and_mul != 0;
+  const float alpha = c.gemm1_alpha == 0.f ? 1.f : c.gemm1_alpha;
   if (L.small) {
     const bool fused_copy = L.fused_copy;
     GBMOE_TRY(launch_route_align_small(c, T, router_logits, e_score_correction_bias, tw, tids,
                                        L.bs, sorted, eids, L.max_blocks, npp, bseg, inv,
-                                       hidden_states, fused_copy ? x_perm : nullptr, status,
-                                       stream));
+                                       hidden_states, fused_copy ? x_perm : nullptr, row_scale,
+                                       status, stream, logit_splits, logit_stride));
     if (!fused_copy)
-      GBMOE_TRY(launch_gather(hidden_states, H, inv, L.n, k, L.max_sorted, x_perm, stream));
+      GBMOE_TRY(launch_gather(hidden_states, H, inv, L.n, k, L.max_sorted, x_perm, row_scale,
+                              stream));
   } else {
-    GBMOE_TRY(launch_topk(c, T, router_logits, e_score_correction_bias, tw, tids, status, stream));
+    GBMOE_TRY(launch_topk(c, T, router_logits, e_score_correction_bias, tw, tids, status, stream,
+                          logit_splits, logit_stride));
     GBMOE_TRY(launch_align(tids, L.n, E, L.bs, sorted, eids, L.max_blocks, npp,
                            at<char>(workspace, L.scratch), status, stream, bseg, inv));
-    GBMOE_TRY(launch_gather(hidden_states, H, inv, L.n, k, L.max_sorted, x_perm, stream));
+    GBMOE_TRY(launch_gather(hidden_states, H, inv, L.n, k, L.max_sorted, x_perm, row_scale,
+                            stream));
   }
   GBMOE_TRY(rec(1));
 
@@ -342,9 +417,13 @@ GBMOE_API gbmoe_status_t moe_forward_events(
     P.A = x_perm;
     P.a_rows = L.max_sorted;
     P.B = w13_weight;
-    P.b_rows = E * 2 * I;
+    P.b_rows = E * (gated ? 2 : 1) * I;
     P.K = H;
     P.n_tiles = I / kGemmBM;
+    P.bias = w13_bias;
+    P.clamp_limit = c.swiglu_limit;
+    P.alpha = alpha;
+    P.expert_of_flat = tids;
     P.k_blocks = H / kGemmBK;
     P.m_rows_dev = npp;
     P.max_m_blocks = L.max_sorted / L.bs;
@@ -352,15 +431,15 @@ GBMOE_API gbmoe_status_t moe_forward_events(
     P.block_seg = bseg;
     P.group_m = group_m_for(H, L.bs);
     P.num_experts = E;
-    P.b_rows_per_expert = 2 * I;
-    P.up_offset = I;
+    P.b_rows_per_expert = (gated ? 2 : 1) * I;
+    P.up_offset = gated ? I : 0;
     P.out = act;
     P.ldo = I;
     P.store_rows = L.max_sorted;
     P.sorted_ids = sorted;
     P.num_flat = L.n;
     P.part = at<float>(workspace, L.part_r);
-    P.part_split_stride = (long long)L.n * 2 * I;
+    P.part_split_stride = (long long)L.n * (gated ? 2 : 1) * I;
   }
   if (Is) {
     GemmProblem& P = g1.p[1];
@@ -381,13 +460,15 @@ GBMOE_API gbmoe_status_t moe_forward_events(
     P.ldo = Is;
     P.store_rows = T;
     P.num_flat = L.n;
+    P.clamp_limit = c.swiglu_limit;              // the shared SwiGLU shares the limit,
+    P.alpha = 1.f;                               // not alpha
     P.part = at<float>(workspace, L.part_s);
     P.part_split_stride = (long long)T * 2 * Is;
   }
   g1.splits = L.splits13;
   // a row block holds at most T real rows (a token meets an expert once)
-  GBMOE_TRY(launch_gemm(kGemmW13, kGemmBM, g1, stream, L.pair, T));
-  if (g1.splits > 1) GBMOE_TRY(launch_silu_reduce(g1, npp, L.max_sorted, stream));
+  GBMOE_TRY(launch_gemm(gated ? kGemmW13 : kGemmW1, kGemmBM, g1, stream, L.pair, T));
+  if (g1.splits > 1) GBMOE_TRY(launch_silu_reduce(g1, npp, L.max_sorted, gated, stream));
   GBMOE_TRY(rec(2));
 
   // ---- w2: weighted, scattered to the token's slot; shared expert to slot k
@@ -416,7 +497,8 @@ GBMOE_API gbmoe_status_t moe_forward_events(
     P.ldo = H;
     P.store_rows = L.max_sorted;
     P.sorted_ids = sorted;
-    P.row_weight = tw;
+    P.row_weight = c.apply_router_weight_on_input ? nullptr : tw;
+    P.bias = w2_bias;
     P.num_flat = L.n;
     P.top_k = k;
     P.slots = L.slots;
@@ -454,6 +536,29 @@ GBMOE_API gbmoe_status_t moe_forward_events(
   return GBMOE_OK;
 }
 
+GBMOE_API gbmoe_status_t moe_forward_events(
+    const gbmoe_config_t* cfg, int32_t num_tokens, const void* hidden_states,
+    const float* router_logits, const float* e_score_correction_bias, const void* w13_weight,
+    const void* w2_weight, const void* shared_w13, const void* shared_w2, void* output,
+    void* workspace, size_t workspace_bytes, void* const* events, int32_t num_events,
+    gbmoe_stream_t stream) {
+  gbmoe_forward_args_t a;
+  std::memset(&a, 0, sizeof(a));
+  a.hidden_states = hidden_states;
+  a.router_logits = router_logits;
+  a.e_score_correction_bias = e_score_correction_bias;
+  a.w13_weight = w13_weight;
+  a.w2_weight = w2_weight;
+  a.shared_w13 = shared_w13;
+  a.shared_w2 = shared_w2;
+  a.output = output;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.events = events;
+  a.num_events = num_events;
+  return moe_forward_ex(cfg, num_tokens, &a, stream);
+}
+
 GBMOE_API gbmoe_status_t moe_forward(const gbmoe_config_t* cfg, int32_t num_tokens,
                                      const void* hidden_states, const float* router_logits,
                                      const float* e_score_correction_bias, const void* w13_weight,
@@ -463,6 +568,41 @@ GBMOE_API gbmoe_status_t moe_forward(const gbmoe_config_t* cfg, int32_t num_toke
   return moe_forward_events(cfg, num_tokens, hidden_states, router_logits,
                             e_score_correction_bias, w13_weight, w2_weight, shared_w13, shared_w2,
                             output, workspace, workspace_bytes, nullptr, 0, stream);
+}
+
+GBMOE_API gbmoe_status_t moe_router_logits(int32_t num_tokens, int32_t hidden_size,
+                                           int32_t num_experts, const void* hidden_states,
+                                           const void* gate_weight, float* router_logits,
+                                           gbmoe_stream_t stream) {
+  if (num_tokens < 0 || num_tokens > kMaxTokens || hidden_size <= 0 || hidden_size % kGemmBK ||
+      num_experts < 1 || num_experts > 1024)
+    return GBMOE_ERR_INVALID_ARG;
+  if (num_tokens == 0) return GBMOE_OK;
+  if (!hidden_states || !gate_weight || !router_logits || !aligned16(hidden_states) ||
+      !aligned16(gate_weight) || !aligned16(router_logits))
+    return GBMOE_ERR_INVALID_ARG;
+  const int T = num_tokens, E = num_experts;
+  const int tp = (T + kGemmBM - 1) / kGemmBM * kGemmBM;
+  GemmLaunch gr;
+  std::memset(&gr, 0, sizeof(gr));
+  gr.num_problems = 1;
+  gr.splits = 1;
+  GemmProblem& P = gr.p[0];
+  P.A = hidden_states;
+  P.a_rows = T;
+  P.B = gate_weight;
+  P.b_rows = E;
+  P.K = hidden_size;
+  P.n_tiles = (E + kGemmBM - 1) / kGemmBM;
+  P.k_blocks = hidden_size / kGemmBK;
+  P.m_rows_host = tp;
+  P.max_m_blocks = tp / kGemmBM;
+  P.group_m = 16;
+  P.num_experts = 1;
+  P.out = router_logits;
+  P.ldo = E;
+  P.store_rows = T;
+  return cuda_status(launch_gemm(kGemmRouter, kGemmBM, gr, (cudaStream_t)stream, false, T));
 }
 
 GBMOE_API int32_t moe_forward_num_launches(const gbmoe_config_t* cfg, int32_t num_tokens) {

@@ -258,6 +258,36 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + __expf(-g)) * u; }
+__device__ __forceinline__ float silu_f(float g) { return g / (1.f + __expf(-g)); }
+// Gated activation with the layer's options: gate' = min(gate, L), up' = clip(up, -L, L)
+// when L > 0, act = gate' * sigmoid(alpha * gate') * up'.
+__device__ __forceinline__ float act_gated(float g, float u, float alpha, float limit) {
+  if (limit > 0.f) {
+    g = fminf(g, limit);
+    u = fminf(fmaxf(u, -limit), limit);
+  }
+  return g / (1.f + __expf(-alpha * g)) * u;
+}
+// 32 consecutive bf16 biases as fp32 (zeros when b is NULL).
+__device__ __forceinline__ void load_bias32(const __nv_bfloat16* b, float (&out)[32]) {
+  if (!b) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) out[i] = 0.f;
+    return;
+  }
+  const uint4* q = reinterpret_cast<const uint4*>(b);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint4 x = __ldg(q + v);
+    const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = unpack_bf16x2(wv[i]);
+      out[8 * v + 2 * i] = f.x;
+      out[8 * v + 2 * i + 1] = f.y;
+    }
+  }
+}
 
 // Tile t -> (row block, N tile). Row blocks are taken in groups of at most group_m
 // consecutive blocks of one expert; a group's tiles run over all N tiles with the
@@ -334,6 +364,7 @@ struct Schedule {
 template <int KIND, int BN, int AROWS = kGemmBM>
 struct Shape {
   static constexpr int kBRows = KIND == kGemmW13 ? 2 * BN : BN;  // B rows per stage = MMA N
+  // (kGemmW1: the non-gated first GEMM, BN rows of w1 per tile, like kGemmW2)
   static constexpr uint32_t kBBytes = kBRows * kGemmBK * 2;
   // A region of a stage = the rows actually loaded; the MMA's 128-row read of a 32-row
   // region runs on into the stage's own B bytes (inside this CTA's shared memory), which
@@ -502,7 +533,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (m < P.store_rows) {
         f = m;
       }
-      if (KIND == kGemmW13) {
+      // expert of this tile's rows (its bias), the routed problem only
+      int e_tile = 0;
+      if (P.bias && P.expert_ids) {
+        e_tile = P.expert_ids[w.mb];
+        if ((unsigned)e_tile >= (unsigned)P.num_experts) e_tile = 0;
+      }
+      if (KIND == kGemmW13 || KIND == kGemmW1) {
+        constexpr bool kGated = KIND == kGemmW13;
+        const int brow = kGated ? 2 * P.ldo : P.ldo;              // bias entries per expert
+        const __nv_bfloat16* bg =
+            P.bias ? P.bias + (size_t)e_tile * brow + (size_t)w.nt * BN : nullptr;
         if (!split) {
           const bool store = P.sorted_ids ? true : (m < P.store_rows);
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.out) +
@@ -511,15 +552,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < BN / 32; ++c) {
             uint32_t g[32], up[32];
             tmem_ld32(tbase + c * 32, g);
-            tmem_ld32(tbase + BN + c * 32, up);
+            if (kGated) tmem_ld32(tbase + BN + c * 32, up);
             tmem_wait_ld(g);
-            reg_fence(up);
+            if (kGated) reg_fence(up);
+            float gb[32], ub[32];
+            load_bias32(bg ? bg + c * 32 : nullptr, gb);
+            if (kGated) load_bias32(bg ? bg + P.ldo + c * 32 : nullptr, ub);
             uint32_t p[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              p[i] = pack_bf16x2(silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(up[2 * i])),
-                                 silu_mul(__uint_as_float(g[2 * i + 1]),
-                                          __uint_as_float(up[2 * i + 1])));
+            for (int i = 0; i < 16; ++i) {
+              float a0, a1;
+              if (kGated) {
+                a0 = act_gated(__uint_as_float(g[2 * i]) + gb[2 * i],
+                               __uint_as_float(up[2 * i]) + ub[2 * i], P.alpha, P.clamp_limit);
+                a1 = act_gated(__uint_as_float(g[2 * i + 1]) + gb[2 * i + 1],
+                               __uint_as_float(up[2 * i + 1]) + ub[2 * i + 1], P.alpha,
+                               P.clamp_limit);
+              } else {
+                a0 = silu_f(__uint_as_float(g[2 * i]) + gb[2 * i]);
+                a1 = silu_f(__uint_as_float(g[2 * i + 1]) + gb[2 * i + 1]);
+              }
+              p[i] = pack_bf16x2(a0, a1);
+            }
             if (store) {
 #pragma unroll
               for (int v = 0; v < 4; ++v)
@@ -527,18 +581,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
+          // raw K-slice sums; bias and activation are applied by the split reduce
           float* dst = P.part + (size_t)w.split * P.part_split_stride +
-                       (size_t)(f < 0 ? 0 : f) * (2 * P.ldo) + (size_t)w.nt * BN;
+                       (size_t)(f < 0 ? 0 : f) * (kGated ? 2 * P.ldo : P.ldo) +
+                       (size_t)w.nt * BN;
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
             uint32_t g[32], up[32];
             tmem_ld32(tbase + c * 32, g);
-            tmem_ld32(tbase + BN + c * 32, up);
+            if (kGated) tmem_ld32(tbase + BN + c * 32, up);
             tmem_wait_ld(g);
-            reg_fence(up);
+            if (kGated) reg_fence(up);
             if (f >= 0) {
               store_f32x32(dst + c * 32, g, 1.f);
-              store_f32x32(dst + P.ldo + c * 32, up, 1.f);
+              if (kGated) store_f32x32(dst + P.ldo + c * 32, up, 1.f);
+            }
+          }
+        }
+      } else if (KIND == kGemmRouter) {
+        // logits[split][m][n] for m < T, n < E (ldo = E); rows/columns past them are the
+        // zero fill of out-of-range TMA boxes and are not stored
+        float* dst = static_cast<float*>(P.out) + (size_t)w.split * P.out_split_stride +
+                     (size_t)m * P.ldo;
+        const int col0 = w.nt * BN;
+        const bool vec = (P.ldo & 3) == 0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          tmem_wait_ld(r);
+          const int cc = col0 + c * 32;
+          if (m < P.store_rows && cc < P.ldo) {
+            if (vec && cc + 32 <= P.ldo) {
+              store_f32x32(dst + cc, r, 1.f);
+            } else {
+              for (int i = 0; i < 32 && cc + i < P.ldo; ++i) dst[cc + i] = __uint_as_float(r[i]);
             }
           }
         }
@@ -553,6 +630,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             dest = f * P.slots + P.slot_offset;
           }
         }
+        // the expert's output bias enters once (split 0), inside the routing weight
+        const __nv_bfloat16* b2 = (P.bias && w.split == 0)
+                                      ? P.bias + (size_t)e_tile * P.ldo + (size_t)w.nt * BN
+                                      : nullptr;
         float* dst = static_cast<float*>(P.out) + (size_t)w.split * P.out_split_stride +
                      (size_t)(dest < 0 ? 0 : dest) * P.ldo + (size_t)w.nt * BN;
 #pragma unroll 1
@@ -560,6 +641,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t r[32];
           tmem_ld32(tbase + c * 32, r);
           tmem_wait_ld(r);
+          if (b2) {
+            float bb[32];
+            load_bias32(b2 + c * 32, bb);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + bb[i]);
+          }
           if (dest >= 0) store_f32x32(dst + c * 32, r, wt);
         }
       }
@@ -837,14 +924,15 @@ __global__ void wait_selftest_kernel(int* status, unsigned long long timeout_ns)
 
 // act = silu(sum_s gate_s) * sum_s up_s, one CTA per output row, 8 columns per step.
 __global__ void __launch_bounds__(128) silu_reduce_kernel(const GemmLaunch L, const int* npp,
-                                                          int max_routed_rows) {
+                                                          int max_routed_rows, int gated) {
   const GemmProblem& R = L.p[0];
   int routed_rows = npp ? *npp : R.m_rows_host;
   if (routed_rows > max_routed_rows) routed_rows = max_routed_rows;
   const int shared_rows = L.num_problems > 1 ? L.p[1].store_rows : 0;
   for (int r = blockIdx.x; r < max_routed_rows + shared_rows; r += gridDim.x) {
     const GemmProblem* P;
-    int src, dst_row;
+    int src, dst_row, row_gated = gated;
+    const __nv_bfloat16* bias = nullptr;
     if (r < max_routed_rows) {
       if (r >= routed_rows) continue;
       P = &L.p[0];
@@ -852,12 +940,18 @@ __global__ void __launch_bounds__(128) silu_reduce_kernel(const GemmLaunch L, co
       if (f < 0 || f >= P->num_flat) continue;          // padding rows are never read back
       src = f;
       dst_row = r;
+      if (P->bias && P->expert_of_flat) {
+        int e = P->expert_of_flat[f];
+        if ((unsigned)e >= (unsigned)P->num_experts) e = 0;
+        bias = P->bias + (size_t)e * (row_gated ? 2 * P->ldo : P->ldo);
+      }
     } else {
-      P = &L.p[1];
+      P = &L.p[1];                                      // the shared expert: always gated
       src = dst_row = r - max_routed_rows;
+      row_gated = 1;
     }
     const int N = P->ldo;
-    const float* base = P->part + (size_t)src * 2 * N;
+    const float* base = P->part + (size_t)src * (row_gated ? 2 * N : N);
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(P->out) + (size_t)dst_row * N;
     for (int j = threadIdx.x * 8; j < N; j += blockDim.x * 8) {
       float g[8], u[8];
@@ -868,18 +962,44 @@ __global__ void __launch_bounds__(128) silu_reduce_kernel(const GemmLaunch L, co
         const float* q = base + (size_t)s * P->part_split_stride + j;
         const float4 g0 = __ldg(reinterpret_cast<const float4*>(q));
         const float4 g1 = __ldg(reinterpret_cast<const float4*>(q + 4));
-        const float4 u0 = __ldg(reinterpret_cast<const float4*>(q + N));
-        const float4 u1 = __ldg(reinterpret_cast<const float4*>(q + N + 4));
         g[0] += g0.x; g[1] += g0.y; g[2] += g0.z; g[3] += g0.w;
         g[4] += g1.x; g[5] += g1.y; g[6] += g1.z; g[7] += g1.w;
-        u[0] += u0.x; u[1] += u0.y; u[2] += u0.z; u[3] += u0.w;
-        u[4] += u1.x; u[5] += u1.y; u[6] += u1.z; u[7] += u1.w;
+        if (row_gated) {
+          const float4 u0 = __ldg(reinterpret_cast<const float4*>(q + N));
+          const float4 u1 = __ldg(reinterpret_cast<const float4*>(q + N + 4));
+          u[0] += u0.x; u[1] += u0.y; u[2] += u0.z; u[3] += u0.w;
+          u[4] += u1.x; u[5] += u1.y; u[6] += u1.z; u[7] += u1.w;
+        }
       }
+      if (bias) {
+        const uint4 bg = __ldg(reinterpret_cast<const uint4*>(bias + j));
+        const uint32_t wg[4] = {bg.x, bg.y, bg.z, bg.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 fb = unpack_bf16x2(wg[i]);
+          g[2 * i] += fb.x;
+          g[2 * i + 1] += fb.y;
+        }
+        if (row_gated) {
+          const uint4 bu = __ldg(reinterpret_cast<const uint4*>(bias + N + j));
+          const uint32_t wu[4] = {bu.x, bu.y, bu.z, bu.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 fb = unpack_bf16x2(wu[i]);
+            u[2 * i] += fb.x;
+            u[2 * i + 1] += fb.y;
+          }
+        }
+      }
+      float a[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        a[i] = row_gated ? act_gated(g[i], u[i], P->alpha, P->clamp_limit) : silu_f(g[i]);
       uint4 o;
-      o.x = pack_bf16x2(silu_mul(g[0], u[0]), silu_mul(g[1], u[1]));
-      o.y = pack_bf16x2(silu_mul(g[2], u[2]), silu_mul(g[3], u[3]));
-      o.z = pack_bf16x2(silu_mul(g[4], u[4]), silu_mul(g[5], u[5]));
-      o.w = pack_bf16x2(silu_mul(g[6], u[6]), silu_mul(g[7], u[7]));
+      o.x = pack_bf16x2(a[0], a[1]);
+      o.y = pack_bf16x2(a[2], a[3]);
+      o.z = pack_bf16x2(a[4], a[5]);
+      o.w = pack_bf16x2(a[6], a[7]);
       *reinterpret_cast<uint4*>(out + j) = o;
     }
   }
@@ -935,6 +1055,9 @@ template <int AROWS>
 cudaError_t launch_rows(int kind, int bn, const CUtensorMap* tm, const GemmLaunch& L, int grid,
                         cudaStream_t stream) {
   if (kind == kGemmW13 && bn == 128) return launch_typed<kGemmW13, 128, AROWS>(tm, L, grid, stream);
+  if (kind == kGemmW1 && bn == 128) return launch_typed<kGemmW1, 128, AROWS>(tm, L, grid, stream);
+  if (kind == kGemmRouter && bn == 128)
+    return launch_typed<kGemmRouter, 128, AROWS>(tm, L, grid, stream);
   if (kind == kGemmW2 && bn == 256) return launch_typed<kGemmW2, 256, AROWS>(tm, L, grid, stream);
   if (kind == kGemmW2 && bn == 128) return launch_typed<kGemmW2, 128, AROWS>(tm, L, grid, stream);
   return cudaErrorInvalidValue;
@@ -974,7 +1097,8 @@ cudaError_t launch_gemm(int kind, int bn, const GemmLaunch& L, cudaStream_t stre
                         int max_rows_per_block) {
   const int arows = (!pair && max_rows_per_block <= 32) ? 32 : kGemmBM;
   if (L.num_problems < 1 || L.num_problems > 2 || L.splits < 1) return cudaErrorInvalidValue;
-  if (pair && (L.splits != 1 || (kind == kGemmW2 && bn != 256) || (kind == kGemmW13 && bn != 128)))
+  if (pair && (L.splits != 1 || (kind == kGemmW2 && bn != 256) || (kind == kGemmW13 && bn != 128) ||
+               kind == kGemmW1 || kind == kGemmRouter))
     return cudaErrorInvalidValue;
   CUtensorMap tm[4];
   long units = 0;
@@ -1009,12 +1133,12 @@ cudaError_t launch_wait_selftest(int* status, int timeout_us, cudaStream_t strea
 }
 
 cudaError_t launch_silu_reduce(const GemmLaunch& L, const int* npp, int max_routed_rows,
-                               cudaStream_t stream) {
+                               bool gated, cudaStream_t stream) {
   const int rows = max_routed_rows + (L.num_problems > 1 ? L.p[1].store_rows : 0);
   int grid = num_sms() * 4;
   if (rows < grid) grid = rows;
   if (grid < 1) return cudaSuccess;
-  silu_reduce_kernel<<<grid, 128, 0, stream>>>(L, npp, max_routed_rows);
+  silu_reduce_kernel<<<grid, 128, 0, stream>>>(L, npp, max_routed_rows, gated ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -21,8 +22,11 @@ constexpr int kGemmBK = 64;        // K elements per pipeline stage (one 128-byt
 
 int num_sms();
 
+// logits may arrive as logit_splits fp32 copies, logit_split_stride floats apart, whose sum
+// is the logit (the split-K router GEMM); 1 = plain logits.
 cudaError_t launch_topk(const gbmoe_config_t& c, int T, const float* logits, const float* bias,
-                        float* weights, int* ids, int* status, cudaStream_t stream);
+                        float* weights, int* ids, int* status, cudaStream_t stream,
+                        int logit_splits = 1, long long logit_split_stride = 0);
 
 size_t align_scratch_bytes(int n, int E);
 // block_seg (optional): per block, (first block, block count) of its expert's run.
@@ -36,17 +40,20 @@ cudaError_t launch_route_align_small(const gbmoe_config_t& c, int T, const float
                                      const float* bias, float* weights, int* ids, int bs,
                                      int* sorted, int* expert_ids, int max_blocks, int* npp,
                                      int2* block_seg, int* inv, const void* x, void* x_perm,
-                                     int* status, cudaStream_t stream);
-// x_perm[inv[f]] = x[f / k] for f < n (x_perm == NULL in the small launch: no copy there).
+                                     const float* row_scale, int* status, cudaStream_t stream,
+                                     int logit_splits = 1, long long logit_split_stride = 0);
+// x_perm[inv[f]] = x[f / k] (times row_scale[f] when row_scale is not NULL) for f < n
+// (x_perm == NULL in the small launch: no copy there).
 cudaError_t launch_gather(const void* x, int H, const int* inv, int n, int k, int max_rows,
-                          void* x_perm, cudaStream_t stream);
+                          void* x_perm, const float* row_scale, cudaStream_t stream);
 constexpr int kFusedCopyMaxRows = 16;  // the small route+align launch copies rows itself
 
 // y[t] = sum over splits s and slots of ytok[s * split_stride + (t * slots + slot) * H + :]
 cudaError_t launch_combine(const void* ytok, int slots, int H, int T, int splits,
                            long long split_stride, void* y, cudaStream_t stream);
 
-enum GemmKind { kGemmW13 = 0, kGemmW2 = 1 };
+// W1: the non-gated first GEMM; Router: logits = x @ gate^T, fp32 per-split copies
+enum GemmKind { kGemmW13 = 0, kGemmW2 = 1, kGemmW1 = 2, kGemmRouter = 3 };
 
 // One grouped GEMM problem. A rows are grouped in blocks of kGemmBM that each belong
 // to one expert (expert_ids[block]); B is the expert weight stack flattened to
@@ -78,8 +85,13 @@ struct GemmProblem {
   int top_k;               // w2: slots of routed experts per token
   int slots;               // w2: output slots per token
   int slot_offset;         // w2: slot of identity rows
-  float* part;             // w13 with splits > 1: fp32 [splits][row][2 * ldo] (gate | up),
-                           // row = flat index (routed) or token (identity rows)
+  const __nv_bfloat16* bias;  // per-expert bias (w13: [E][2 ldo] gate | up; w1, w2: [E][ldo]),
+                             // routed problem only, or NULL
+  float clamp_limit;         // gated first GEMM: > 0 clamps gate <= L and up to [-L, L]
+  float alpha;               // gated first GEMM: act = g * sigmoid(alpha g) * u
+  const int* expert_of_flat; // split reduce: expert of each flat index (for the bias)
+  float* part;             // first GEMM with splits > 1: fp32 [splits][row][2 ldo] (gate | up;
+                           // [row][ldo] non-gated), row = flat index (routed) or token
   long long part_split_stride;
   long long out_split_stride;  // w2: elements between the per-split copies of out
 };
@@ -104,9 +116,10 @@ cudaError_t launch_gemm(int kind, int bn, const GemmLaunch& L, cudaStream_t stre
 // GBMOE_ERR_TIMEOUT in *status.
 cudaError_t launch_wait_selftest(int* status, int timeout_us, cudaStream_t stream);
 
-// act = silu(sum_s gate_s) * sum_s up_s for the valid rows of each problem of a split
-// w13 launch (routed rows in expert order; identity rows for the shared expert).
+// act = f(sum_s gate_s + bias, sum_s up_s + bias) for the valid rows of each problem of a
+// split first-GEMM launch (routed rows in expert order; identity rows for the shared
+// expert, always gated); f = the gated activation with clamp / alpha, or silu (non-gated).
 cudaError_t launch_silu_reduce(const GemmLaunch& L, const int* npp, int max_routed_rows,
-                               cudaStream_t stream);
+                               bool gated, cudaStream_t stream);
 
 }  // namespace gbmoe

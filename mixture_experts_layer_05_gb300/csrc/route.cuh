@@ -26,6 +26,8 @@ struct TopkArgs {
   int* status;
   int T, E, k, renorm, grouped, G, g, sigmoid;
   float rsf;
+  int logit_splits;              // logits arrive as this many fp32 partial copies (>= 1),
+  long long logit_split_stride;  // summed in copy order on load (split-K router GEMM)
 };
 
 // (key, index) pair maximum: larger key wins, equal keys go to the lower index.
@@ -55,7 +57,12 @@ __device__ __forceinline__ int route_token_warp(const TopkArgs& a, int t, int la
 #pragma unroll
   for (int i = 0; i < EPT; ++i) {
     const int e = lane + 32 * i;
-    s[i] = e < a.E ? __ldg(row + e) : -INFINITY;
+    float l = -INFINITY;
+    if (e < a.E) {
+      l = __ldg(row + e);
+      for (int sp = 1; sp < a.logit_splits; ++sp) l += __ldg(row + sp * a.logit_split_stride + e);
+    }
+    s[i] = l;
     mx = fmaxf(mx, s[i]);
   }
   // 1. scores
@@ -206,6 +213,8 @@ inline TopkArgs make_topk_args(const gbmoe_config_t& c, int T, const float* logi
   a.g = a.grouped ? c.topk_group : 1;
   a.sigmoid = c.scoring_func == GBMOE_SCORE_SIGMOID;
   a.rsf = c.routed_scaling_factor;
+  a.logit_splits = 1;
+  a.logit_split_stride = 0;
   return a;
 }
 

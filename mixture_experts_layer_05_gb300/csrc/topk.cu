@@ -23,12 +23,15 @@ struct TopkLaunch {
 };
 
 cudaError_t launch_topk(const gbmoe_config_t& c, int T, const float* logits, const float* bias,
-                        float* weights, int* ids, int* status, cudaStream_t stream) {
+                        float* weights, int* ids, int* status, cudaStream_t stream,
+                        int logit_splits, long long logit_split_stride) {
   const int warps = 256 / 32;
   int blocks = (T + warps - 1) / warps;
   const int cap = num_sms() * 8;
   if (blocks > cap) blocks = cap;
   TopkLaunch L{make_topk_args(c, T, logits, bias, weights, ids, status), blocks, stream};
+  L.a.logit_splits = logit_splits;
+  L.a.logit_split_stride = logit_split_stride;
   dispatch_ept(c.num_experts, L);
   return cudaGetLastError();
 }

@@ -79,6 +79,23 @@ def make_weights(w: MoEWorkload, seed: int = 0, device="cpu") -> dict:
     return out
 
 
+def make_expert_extras(w: MoEWorkload, seed: int = 0, gated: bool = True, bias_std: float = 0.1,
+                       device="cpu") -> dict:
+    """Per-expert biases (bf16 ~N(0, bias_std)) and, when not gated, a w1-only weight
+    stack ``w1 [E, I, H]`` (bf16 ~N(0, w_std)) for the layer's optional variants."""
+    E, H, I = w.num_experts, w.hidden_size, w.intermediate_size
+    out = {
+        "w13_bias": normal((E, (2 if gated else 1) * I), bias_std,
+                           tensor_seed(w.name, "w13_bias", seed), torch.bfloat16, device),
+        "w2_bias": normal((E, H), bias_std, tensor_seed(w.name, "w2_bias", seed),
+                          torch.bfloat16, device),
+    }
+    if not gated:
+        out["w1"] = normal((E, I, H), w.w_std, tensor_seed(w.name, "w1", seed), torch.bfloat16,
+                           device)
+    return out
+
+
 def spread_rows(logits: torch.Tensor, gap: float = LOGIT_GAP) -> torch.Tensor:
     """Move values apart, order preserved, so that within each row any two differ by >= gap.
 

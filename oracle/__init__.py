@@ -1,5 +1,5 @@
 """CPU oracle of the FusedMoE layer forward (test infrastructure only; see moe_oracle)."""
 from .moe_oracle import (  # noqa: F401
-    score, group_score, route_token, select_experts, decision_margins,
+    router_logits, score, group_score, route_token, select_experts, decision_margins,
     moe_align_block_size, silu, swiglu_mlp, expert_mlp, fused_moe, fused_moe_rows,
 )

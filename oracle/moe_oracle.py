@@ -81,6 +81,13 @@ def _rank_desc(values: np.ndarray, candidates) -> list:
     return sorted(candidates, key=lambda i: (-values[i], i))
 
 
+# ---------------------------------------------------------------- 0. router GEMM
+def router_logits(x, gate_weight) -> np.ndarray:
+    """logits [T, E] = x [T, H] @ gate_weight [E, H]^T in fp64 (``MoEGate.forward`` on the
+    sglang ``models/deepseek_v2.py`` page: bf16 operands, fp32 logits)."""
+    return _f64(x) @ _f64(gate_weight).T
+
+
 # ---------------------------------------------------------------- 2-5. routing of one token
 def route_token(logits_row, bias, *, num_experts, top_k, renormalize,
                 use_grouped_topk=False, num_expert_group=0, topk_group=0,

@@ -84,7 +84,14 @@ def _fwd(lib, cfg, T=4, ws_bytes=1 << 40, ptr=256, shared=False, events=None, ne
 def test_forward_validation(lib):
     ok = _cfg()
     assert _fwd(lib, _cfg(activation=1)) == binding.ERR_UNSUPPORTED     # only silu
-    assert _fwd(lib, _cfg(is_act_and_mul=0)) == binding.ERR_UNSUPPORTED
+    assert _fwd(lib, _cfg(is_act_and_mul=2)) == binding.ERR_INVALID_ARG
+    # the clamp, alpha and a shared expert need the gated form
+    assert _fwd(lib, _cfg(is_act_and_mul=0, swiglu_limit=7.0)) == binding.ERR_UNSUPPORTED
+    assert _fwd(lib, _cfg(is_act_and_mul=0, gemm1_alpha=1.7)) == binding.ERR_UNSUPPORTED
+    assert _fwd(lib, _cfg(is_act_and_mul=0, shared_intermediate_size=128),
+                shared=True) == binding.ERR_UNSUPPORTED
+    assert _fwd(lib, _cfg(swiglu_limit=-1.0)) == binding.ERR_INVALID_ARG
+    assert _fwd(lib, _cfg(gemm1_alpha=float("nan"))) == binding.ERR_INVALID_ARG
     assert _fwd(lib, _cfg(hidden_size=96)) == binding.ERR_UNSUPPORTED    # H % 128
     assert _fwd(lib, _cfg(intermediate_size=200)) == binding.ERR_UNSUPPORTED
     assert _fwd(lib, _cfg(hidden_size=0)) == binding.ERR_INVALID_ARG

@@ -352,3 +352,148 @@ def test_host_pipeline_matches_direct_calls(cuda_lib):
     for (x, lg), y in zip(batches, ys):
         assert torch.equal(y, layer(x.to(DEV), lg.to(DEV)).cpu())
     assert layer.device_status() == binding.OK
+
+
+@pytest.mark.parametrize("name,T", [("dsv3", 1), ("dsv3", 300), ("mixtral", 16)])
+def test_forward_cuda_graph_replay(cuda_lib, name, T):
+    """moe_forward enqueues no host synchronisation or allocation: captured into a CUDA
+    graph and replayed it gives the eager result bit for bit."""
+    w = SMALL[name]
+    wts = inputs.make_weights(w, 0)
+    x, logits = tokens(w, T, wts["bias"])
+    layer, _ = _layer(w, wts, T)
+    xd, ld = x.to(DEV), logits.to(DEV)
+    eager = layer(xd, ld).clone()
+    out = torch.empty_like(xd)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        layer(xd, ld, out=out)
+    out.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    assert layer.device_status() == binding.OK
+
+
+# ------------------------------------------------------------------ layer variants
+VARIANTS = {
+    "bias": dict(bias=True),
+    "clamp_alpha": dict(swiglu_limit=0.25, gemm1_alpha=1.7),
+    "bias_clamp": dict(bias=True, swiglu_limit=0.25),
+    "non_gated": dict(gated=False),
+    "non_gated_bias": dict(gated=False, bias=True),
+    "weight_on_input": dict(apply_router_weight_on_input=True),
+}
+VARIANT_SHAPES = {
+    "dsv3": SMALL["dsv3"],        # grouped sigmoid routing + shared expert
+    "split": SPLIT,               # decode shapes: split-K and the split reduce
+}
+
+
+@pytest.mark.parametrize("vname", list(VARIANTS))
+@pytest.mark.parametrize("sname,T", [("dsv3", 203), ("split", 1), ("split", 17)])
+def test_forward_variants(cuda_lib, vname, sname, T):
+    v = dict(VARIANTS[vname])
+    w = VARIANT_SHAPES[sname]
+    gated = v.pop("gated", True)
+    use_bias = v.pop("bias", False)
+    if not gated:
+        w = configs.shrink(w, shared_intermediate_size=0)  # a shared expert needs gating
+    wts = inputs.make_weights(w, 0)
+    extra = inputs.make_expert_extras(w, 0, gated=gated)
+    w13 = wts["w13"] if gated else extra["w1"]
+    b13 = extra["w13_bias"] if use_bias else None
+    b2 = extra["w2_bias"] if use_bias else None
+    x, logits = tokens(w, T, wts["bias"])
+    cfg = binding.config_from_workload(w, is_act_and_mul=int(gated), **v)
+    dv = lambda t: None if t is None else t.to(DEV)
+    layer = binding.FusedMoE(cfg, w13.to(DEV), wts["w2"].to(DEV), dv(wts["bias"]),
+                             dv(wts["shared_w13"]), dv(wts["shared_w2"]), max_tokens=T,
+                             w13_bias=dv(b13), w2_bias=dv(b2))
+    y = layer(x.to(DEV), logits.to(DEV))
+    torch.cuda.synchronize()
+    assert layer.device_status() == binding.OK
+    y_ref = oracle.fused_moe(x, logits, wts["bias"], w13, wts["w2"], wts["shared_w13"],
+                             wts["shared_w2"], w13_bias=b13, w2_bias=b2, gated=gated,
+                             **v, **oracle_cfg(w))
+    check_close(y, y_ref, f"{vname} {sname} T={T}")
+
+
+def test_stage_events_eager_and_captured(cuda_lib):
+    """moe_forward_events times stages eagerly and inside a CUDA graph replay."""
+    w = SMALL["mixtral"]
+    wts = inputs.make_weights(w, 0)
+    x, logits = tokens(w, 64, None)
+    layer, _ = _layer(w, wts, 64)
+    xd, ld = x.to(DEV), logits.to(DEV)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(binding.NUM_STAGE_EVENTS)]
+    layer(xd, ld, events=ev)
+    torch.cuda.synchronize()
+    assert all(ev[i].elapsed_time(ev[i + 1]) >= 0.0 for i in range(4))
+    out = torch.empty_like(xd)
+    gev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for e in gev:
+        e.record()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        layer(xd, ld, out=out, events=[None, gev[0], gev[1], None, None])
+    g.replay()
+    torch.cuda.synchronize()
+    assert gev[0].elapsed_time(gev[1]) > 0.0
+    assert layer.device_status() == binding.OK
+
+
+# ------------------------------------------------------------------ router GEMM
+def _gate(w, seed=0):
+    """Gate weight ~N(0, 1/sqrt(H)) so that the logits of N(0, 1) hidden states are ~N(0, 1)."""
+    return inputs.normal((w.num_experts, w.hidden_size), w.hidden_size ** -0.5,
+                         inputs.tensor_seed(w.name, "gate", seed), torch.bfloat16)
+
+
+@pytest.mark.parametrize("E,H,T", [(8, 4096, 1), (8, 4096, 300), (160, 5120, 64),
+                                   (256, 7168, 129), (256, 7168, 1)])
+def test_router_logits(cuda_lib, E, H, T):
+    x = inputs.normal((T, H), 1.0, 1, torch.bfloat16)
+    wg = inputs.normal((E, H), H ** -0.5, 2, torch.bfloat16)
+    out = torch.full((T, E), float("nan"), device=DEV)
+    binding.moe_router_logits(x.to(DEV), wg.to(DEV), out)
+    torch.cuda.synchronize()
+    ref = oracle.router_logits(x, wg)
+    # fp32 accumulation over H products: |error| <= H * 2^-24 * sum |x| |w| (rounded up)
+    bound = (x.double().abs() @ wg.double().abs().T).numpy() * (H * 2.0 ** -24) + 1e-30
+    err = np.abs(out.cpu().numpy().astype(np.float64) - ref)
+    assert (err <= bound).all(), float((err / bound).max())
+
+
+@pytest.mark.parametrize("name,T", [("dsv3", 1), ("dsv3", 77), ("mixtral", 16)])
+def test_forward_from_gate_weight(cuda_lib, name, T):
+    """moe_forward_ex with the gate weight: router GEMM (split-K at decode), routing,
+    experts. Ids must match wherever the oracle's decision margin exceeds 1e-4 (far above
+    the fp32 logit error); closer rows are only checked for a valid choice."""
+    w = SMALL[name]
+    wts = inputs.make_weights(w, 0)
+    wg = _gate(w)
+    x = inputs.normal((T, w.hidden_size), 1.0, 5, torch.bfloat16)
+    layer, d = _layer(w, wts, T)
+    y = layer(x.to(DEV), gate_weight=wg.to(DEV))
+    torch.cuda.synchronize()
+    assert layer.device_status() == binding.OK
+    logits = oracle.router_logits(x, wg)
+    margins = oracle.decision_margins(logits, wts["bias"], **oracle_cfg(w))
+    safe = margins >= 1e-4
+    y_ref, parts = oracle.fused_moe(x, logits, wts["bias"], wts["w13"], wts["w2"],
+                                    wts["shared_w13"], wts["shared_w2"], return_parts=True,
+                                    **oracle_cfg(w))
+    ids, _ = _routing_from_ws(layer, T, w.top_k)
+    assert np.array_equal(ids[safe], parts["topk_ids"][safe])
+    for t in np.flatnonzero(~safe):
+        assert len(set(ids[t].tolist())) == w.top_k
+    check_close(y.cpu()[torch.from_numpy(safe)], y_ref[safe], f"{name} T={T} gate")
+    assert safe.mean() > 0.9

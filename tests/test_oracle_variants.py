@@ -190,3 +190,18 @@ def test_planted_weight_on_both_sides_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "fused_moe", both)
     with pytest.raises(AssertionError):
         pin_router_weight_on_input()
+
+
+def test_router_logits_is_a_matmul():
+    """The router GEMM reduces to torch's matmul of the bf16 operands widened to fp64."""
+    g = torch.Generator().manual_seed(30)
+    x = torch.randn(9, 64, generator=g).to(torch.bfloat16)
+    wg = torch.randn(12, 64, generator=g).to(torch.bfloat16)
+    ref = (x.double() @ wg.double().T).numpy()
+    np.testing.assert_allclose(oracle.router_logits(x, wg), ref, rtol=1e-15, atol=0)
+    # a transposed operand would not even have the right shape
+    assert oracle.router_logits(x, wg).shape == (9, 12)
+    # hand-worked: x = (1, 2), gate rows (3, 4) and (5, 6) -> logits 11, 17
+    np.testing.assert_array_equal(oracle.router_logits(np.array([[1.0, 2.0]]),
+                                                       np.array([[3.0, 4.0], [5.0, 6.0]])),
+                                  [[11.0, 17.0]])
