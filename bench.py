@@ -78,6 +78,30 @@ def layer_work(w, T: int, n_active: int) -> dict:
             "bytes_w2": float(w2_bytes + act_bytes + T * k * H * 2)}
 
 
+def kernel_traffic(kernel: str, workload: str, tokens: int):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary, if it was captured on
+    this workload with the current kernel source (sha1 of csrc/gemm.cu); else None.
+
+    A summary states it on a line `traffic: <kernel> <workload> <tokens> <bytes> <sha1>`.
+    """
+    import glob
+    import hashlib
+    src = os.path.join(ROOT, "mixture_experts_layer_05_gb300", "csrc", "gemm.cu")
+    try:
+        with open(src, "rb") as f:
+            sha = hashlib.sha1(f.read()).hexdigest()
+    except OSError:
+        return None
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        with open(path) as f:
+            for line in f:
+                p = line.split()
+                if len(p) == 6 and p[0] == "traffic:" and p[1] == kernel and p[2] == workload \
+                        and p[3] == str(tokens) and p[5] == sha:
+                    return float(p[4])
+    return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -294,7 +318,8 @@ def run_ours(args, w, T):
                     "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": round(ach / peaks["hbm_gbs"], 4)}
         roof["peak_source"] = f"{peak_src} (burst)"
-        roof["traffic"] = args.traffic
+        roof["traffic"] = args.traffic if args.traffic is not None else \
+            kernel_traffic("gemm_w13", w.name, T)
         step_s = ms_max / 1e3
         res = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -341,17 +366,26 @@ def oracle_cfg(w):
                 routed_scaling_factor=w.routed_scaling_factor)
 
 
-def cpu_baseline(w, wts, x_cpu, logits_cpu, n_tokens: int) -> dict:
-    """The CPU oracle, as it stands, on the first n_tokens of the batch."""
+def _oracle_rows(w, hw, x_cpu, logits_cpu, r0, n):
     import oracle
-    hw = _host_weights(w, wts)
     t0 = time.perf_counter()
-    oracle.fused_moe_rows(x_cpu[:n_tokens], logits_cpu[:n_tokens], hw["bias"], hw["w13"],
+    oracle.fused_moe_rows(x_cpu[r0:r0 + n], logits_cpu[r0:r0 + n], hw["bias"], hw["w13"],
                           hw["w2"], hw["shared_w13"], hw["shared_w2"], **oracle_cfg(w))
-    dt = time.perf_counter() - t0
-    return {"value": round(n_tokens / dt, 4), "unit": "tokens/s",
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, wts, x_cpu, logits_cpu, n_tokens: int, target_s: float = 12.0) -> dict:
+    """The CPU oracle, as it stands, on a leading sample of the batch sized to ~target_s."""
+    hw = _host_weights(w, wts)
+    T = x_cpu.shape[0]
+    n = min(n_tokens, T)
+    dt = _oracle_rows(w, hw, x_cpu, logits_cpu, 0, n)
+    if dt < target_s / 4 and n < T:                 # grow the sample to ~target_s of work
+        n = int(min(T, max(n + 1, n * target_s / max(dt, 1e-3))))
+        dt = _oracle_rows(w, hw, x_cpu, logits_cpu, 0, n)
+    return {"value": round(n / dt, 4), "unit": "tokens/s",
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"first {n_tokens} tokens of the step's batch, full weights, fp64 numpy "
+            "sample": f"first {n} of the step's {T} tokens, full weights, fp64 numpy "
                       f"(BLAS default threading), {dt:.1f} s"}
 
 
@@ -365,7 +399,7 @@ def run_reference(args, w, T):
     rank, world, _ = dist_env()
     if rank != 0:
         return None
-    n = args.ref_sample
+    n = args.ref_sample if args.ref_sample > 0 else 1
     hw = inputs.make_weights(w, 0)           # CPU-generated: the oracle arm needs no GPU
     x_cpu, logits_cpu = inputs.make_tokens(w, T, seed=0)
 
@@ -374,6 +408,13 @@ def run_reference(args, w, T):
         oracle.fused_moe_rows(x_cpu[r0:r0 + n], logits_cpu[r0:r0 + n], hw["bias"], hw["w13"],
                               hw["w2"], hw["shared_w13"], hw["shared_w2"], **oracle_cfg(w))
 
+    # size each step's sample so one step is ~1.5 s of oracle work (the whole run then
+    # stays within a few minutes for the usual K, W)
+    t0 = time.perf_counter()
+    step(0)
+    dt0 = time.perf_counter() - t0
+    if args.ref_sample <= 0:
+        n = max(1, min(T, int(n * 1.5 / max(dt0, 1e-3))))
     for i in range(args.warmup):
         step(i)
     t0 = time.perf_counter()
@@ -404,8 +445,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral")
     ap.add_argument("--tokens", type=int, default=4096)
-    ap.add_argument("--cpu-sample", type=int, default=4)
-    ap.add_argument("--ref-sample", type=int, default=1)
+    ap.add_argument("--cpu-sample", type=int, default=4,
+                    help="initial oracle sample (tokens); grown to ~12 s of CPU work")
+    ap.add_argument("--ref-sample", type=int, default=0,
+                    help="tokens per reference step (0: sized to ~1.5 s per step)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture")

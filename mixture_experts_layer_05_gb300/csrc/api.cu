@@ -87,24 +87,36 @@ bool use_pair(const gbmoe_config_t& c, int T) {
          c.hidden_size % 256 == 0;
 }
 
-// Split-K factor: the persistent grid runs ceil(units / SMs) rounds of units whose
-// length is 1/s of a tile's K range, so pick s minimising ceil(tiles*s / SMs) / s
-// (a split must keep >= 4 K blocks, and must beat the smaller s by 3 %).
-int choose_splits(long tiles, int k_blocks, int T) {
-  if (T > kSplitMaxTokens || tiles <= 0) return 1;
+// Split-K factors of a launch with a routed problem (tiles_r tiles of kb_r K blocks) and
+// an optional shared problem (tiles_s of kb_s): the persistent grid runs
+// ceil(units / SMs) rounds, each as long as the longest unit, so pick (s_r, s_s)
+// minimising rounds * max(kb_r / s_r, kb_s / s_s); a split keeps >= 4 K blocks and must
+// beat the best so far by 3 %. Only at decode-sized batches.
+struct Splits {
+  int r, s;
+};
+Splits choose_splits2(long tiles_r, int kb_r, long tiles_s, int kb_s, int T) {
+  Splits best{1, 1};
+  if (T > kSplitMaxTokens || tiles_r + tiles_s <= 0) return best;
   const long sms = num_sms();
-  int best = 1;
-  double best_t = (double)((tiles + sms - 1) / sms);
-  for (int s = 2; s <= (int)kMaxSplits && k_blocks / s >= 4; ++s) {
-    const long u = tiles * s;
-    const double t = (double)((u + sms - 1) / sms) / s;
-    if (t < best_t * 0.97) {
-      best = s;
-      best_t = t;
+  auto cost = [&](int sr, int ss) {
+    const long units = tiles_r * sr + tiles_s * ss;
+    double len = tiles_r ? (double)kb_r / sr : 0.0;
+    if (tiles_s && (double)kb_s / ss > len) len = (double)kb_s / ss;
+    return (double)((units + sms - 1) / sms) * len;
+  };
+  double best_t = cost(1, 1);
+  for (int sr = 1; sr <= (int)kMaxSplits && kb_r / sr >= 4; ++sr)
+    for (int ss = 1; ss <= (int)kMaxSplits && (tiles_s == 0 ? ss == 1 : kb_s / ss >= 4); ++ss) {
+      const double t = cost(sr, ss);
+      if (t < best_t * 0.97) {
+        best = {sr, ss};
+        best_t = t;
+      }
     }
-  }
   return best;
 }
+int choose_splits(long tiles, int k_blocks, int T) { return choose_splits2(tiles, k_blocks, 0, 0, T).r; }
 
 long t_blocks_128(int T) { return ((long)T + kGemmBM - 1) / kGemmBM; }
 
@@ -113,7 +125,7 @@ struct Layout {
   bool pair;
   // launch plan of one forward: small-batch routing, fused row copy, split factors
   bool small, fused_copy;
-  int w2_bn, splits13, splits2, splits_router, launches;
+  int w2_bn, splits13, splits13_shared, splits2, splits2_shared, splits_router, launches;
   size_t status, topk_weights, topk_ids, sorted, expert_ids, npp, block_seg, inv, scratch,
       x_perm, act, ytok, act_s, part_r, part_s, logits, total;
 };
@@ -172,12 +184,20 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   L.w2_bn = (H % 256 == 0) ? 256 : 128;
   const long est_blocks = (long)(L.n < E ? L.n : E) + L.n / kGemmBM;  // >= 1 partial per expert
   const long t_blocks = ((long)T + L.bs - 1) / L.bs;
-  L.splits13 = L.pair ? 1
-                      : choose_splits(est_blocks * (I / kGemmBM) + (Is ? t_blocks * (Is / kGemmBM) : 0),
-                                      H / kGemmBK, T);
-  const int kb2 = (Is && Is < I ? Is : I) / kGemmBK;
-  L.splits2 = L.pair ? 1 : choose_splits((est_blocks + (Is ? t_blocks : 0)) * (H / L.w2_bn), kb2, T);
-  L.launches = (L.small ? (L.fused_copy ? 1 : 2) : 5) + 1 + (L.splits13 > 1 ? 1 : 0) + 1 + 1;
+  if (L.pair) {
+    L.splits13 = L.splits13_shared = L.splits2 = L.splits2_shared = 1;
+  } else {
+    const Splits a = choose_splits2(est_blocks * (I / kGemmBM), H / kGemmBK,
+                                    Is ? t_blocks * (Is / kGemmBM) : 0, H / kGemmBK, T);
+    L.splits13 = a.r;
+    L.splits13_shared = a.s;
+    const Splits b = choose_splits2(est_blocks * (H / L.w2_bn), I / kGemmBK,
+                                    Is ? t_blocks * (H / L.w2_bn) : 0, Is / kGemmBK, T);
+    L.splits2 = b.r;
+    L.splits2_shared = b.s;
+  }
+  L.launches = (L.small ? (L.fused_copy ? 1 : 2) : 5) + 1 +
+               (L.splits13 > 1 || (Is && L.splits13_shared > 1) ? 1 : 0) + 1 + 1;
   L.splits_router = choose_splits(t_blocks_128(T) * ((E + kGemmBM - 1) / kGemmBM), H / kGemmBK, T);
   return L;
 }
@@ -466,9 +486,11 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
     P.part_split_stride = (long long)T * 2 * Is;
   }
   g1.splits = L.splits13;
+  g1.splits_p1 = L.splits13_shared;
   // a row block holds at most T real rows (a token meets an expert once)
   GBMOE_TRY(launch_gemm(gated ? kGemmW13 : kGemmW1, kGemmBM, g1, stream, L.pair, T));
-  if (g1.splits > 1) GBMOE_TRY(launch_silu_reduce(g1, npp, L.max_sorted, gated, stream));
+  if (g1.splits > 1 || (Is && g1.splits_p1 > 1))
+    GBMOE_TRY(launch_silu_reduce(g1, npp, L.max_sorted, gated, stream));
   GBMOE_TRY(rec(2));
 
   // ---- w2: weighted, scattered to the token's slot; shared expert to slot k
@@ -528,9 +550,11 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
     P.out_split_stride = slot_copy;
   }
   g2.splits = L.splits2;
+  g2.splits_p1 = L.splits2_shared;
   GBMOE_TRY(launch_gemm(kGemmW2, w2_bn, g2, stream, L.pair, T));
   GBMOE_TRY(rec(3));
-  GBMOE_TRY(launch_combine(ytok, L.slots, H, T, g2.splits, slot_copy, output, stream));
+  GBMOE_TRY(launch_combine(ytok, L.slots, k, H, T, g2.splits, Is ? g2.splits_p1 : g2.splits,
+                           slot_copy, output, stream));
   GBMOE_TRY(rec(4));
 #undef GBMOE_TRY
   return GBMOE_OK;

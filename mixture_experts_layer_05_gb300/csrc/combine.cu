@@ -11,40 +11,38 @@
 namespace gbmoe {
 
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ ytok, int slots,
-                                                      int H8, int T, int splits,
+                                                      int routed_slots, int H8, int T, int splits,
+                                                      int splits_last,
                                                       long long split_stride4,
                                                       uint4* __restrict__ y) {
   const size_t total = (size_t)T * H8;
-  const int terms = splits * slots;
+  const int copies = splits > splits_last ? splits : splits_last;
+  const int terms = copies * slots;
   for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (size_t)gridDim.x * blockDim.x) {
     const size_t t = idx / H8, h = idx % H8;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
     const float4* row = ytok + (t * slots * H8 + h) * 2;
-    // term i = (split i / slots, slot i % slots), summed in that order; loads of four
-    // terms are issued before their adds so they are in flight together
-    int i = 0;
-    for (; i + 4 <= terms; i += 4) {
+    // term i = (copy i / slots, slot i % slots), summed in that order; a slot only has the
+    // copies of its own problem. Loads of four terms are issued before their adds.
+    for (int i = 0; i < terms; i += 4) {
       float4 u[4], v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int sp = (i + j) / slots, sl = (i + j) % slots;
-        const float4* src = row + (size_t)sp * split_stride4 + (size_t)sl * H8 * 2;
-        u[j] = __ldg(src);
-        v[j] = __ldg(src + 1);
+        const int c = (i + j) / slots, sl = (i + j) % slots;
+        const bool live = i + j < terms && c < (sl < routed_slots ? splits : splits_last);
+        u[j] = v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live) {
+          const float4* src = row + (size_t)c * split_stride4 + (size_t)sl * H8 * 2;
+          u[j] = __ldg(src);
+          v[j] = __ldg(src + 1);
+        }
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         a.x += u[j].x; a.y += u[j].y; a.z += u[j].z; a.w += u[j].w;
         b.x += v[j].x; b.y += v[j].y; b.z += v[j].z; b.w += v[j].w;
       }
-    }
-    for (; i < terms; ++i) {
-      const int sp = i / slots, sl = i % slots;
-      const float4* src = row + (size_t)sp * split_stride4 + (size_t)sl * H8 * 2;
-      const float4 u = __ldg(src), v = __ldg(src + 1);
-      a.x += u.x; a.y += u.y; a.z += u.z; a.w += u.w;
-      b.x += v.x; b.y += v.y; b.z += v.z; b.w += v.w;
     }
     uint4 o;
     o.x = pack_bf16x2(a.x, a.y);
@@ -55,18 +53,18 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
   }
 }
 
-cudaError_t launch_combine(const void* ytok, int slots, int H, int T, int splits,
-                           long long split_stride, void* y, cudaStream_t stream) {
+cudaError_t launch_combine(const void* ytok, int slots, int routed_slots, int H, int T,
+                           int splits, int splits_last, long long split_stride, void* y,
+                           cudaStream_t stream) {
   const size_t total = (size_t)T * (H / 8);
   const int threads = total < (size_t)num_sms() * 256 ? 64 : 256;  // spread small T over SMs
   size_t blocks = (total + threads - 1) / threads;
   const size_t cap = (size_t)num_sms() * (2048 / threads);
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  combine_kernel<<<(unsigned)blocks, threads, 0, stream>>>(static_cast<const float4*>(ytok),
-                                                            slots, H / 8, T, splits,
-                                                            split_stride / 4,
-                                                            static_cast<uint4*>(y));
+  combine_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+      static_cast<const float4*>(ytok), slots, routed_slots, H / 8, T, splits, splits_last,
+      split_stride / 4, static_cast<uint4*>(y));
   return cudaGetLastError();
 }
 

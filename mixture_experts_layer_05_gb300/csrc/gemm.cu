@@ -324,7 +324,7 @@ struct Unit {
 };
 
 struct Schedule {
-  int mblk[2], tiles[2], total_tiles, units;
+  int mblk[2], tiles[2], total_tiles, units, units0;
 
   __device__ void init(const GemmLaunch& L, int bm = kGemmBM) {
     total_tiles = 0;
@@ -341,19 +341,22 @@ struct Schedule {
       tiles[p] = mblk[p] * P.n_tiles;
       total_tiles += tiles[p];
     }
-    units = total_tiles * L.splits;
+    units0 = tiles[0] * splits_of(L, 0);
+    units = units0 + tiles[1] * splits_of(L, 1);
   }
 
+  // units: problem 0 first, then problem 1; within a problem split-major
   __device__ Unit unit(const GemmLaunch& L, int u) const {
     Unit r;
-    r.split = u / total_tiles;
-    int t = u - r.split * total_tiles;
-    r.p = t < tiles[0] ? 0 : 1;
-    if (r.p) t -= tiles[0];
+    r.p = u < units0 ? 0 : 1;
+    const int local = r.p ? u - units0 : u;
+    const int sp = splits_of(L, r.p);
+    r.split = local / tiles[r.p];
+    const int t = local - r.split * tiles[r.p];
     const GemmProblem& P = L.p[r.p];
     tile_coords(P, mblk[r.p], t, L.status, r.mb, r.nt);
-    r.kb0 = (r.split * P.k_blocks) / L.splits;
-    r.kb1 = ((r.split + 1) * P.k_blocks) / L.splits;
+    r.kb0 = (r.split * P.k_blocks) / sp;
+    r.kb1 = ((r.split + 1) * P.k_blocks) / sp;
     return r;
   }
 };
@@ -514,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;            // TMEM lanes [32*quarter, 32*quarter + 32)
     const int row = quarter * 32 + lane;
-    const bool split = args.splits > 1;
+
     int local = 0;
     for (int u = blockIdx.x; u < sched.units; u += gridDim.x, ++local) {
       const Unit w = sched.unit(args, u);
@@ -523,6 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t use = (uint32_t)(local >> 1);
       if (!wait_bounded(tfull_bar(acc), use & 1u, abort_flag, args.status)) break;
       tc_fence_after();
+      const bool split = splits_of(args, w.p) > 1;
       const int m = w.mb * kGemmBM + row;
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kAccStride;
       // valid row: its flat index (routed) or token (identity rows), else -1
@@ -957,8 +961,9 @@ __global__ void __launch_bounds__(128) silu_reduce_kernel(const GemmLaunch L, co
       float g[8], u[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) g[i] = u[i] = 0.f;
+      const int nsp = splits_of(L, P == &L.p[0] ? 0 : 1);
 #pragma unroll 4
-      for (int s = 0; s < L.splits; ++s) {
+      for (int s = 0; s < nsp; ++s) {
         const float* q = base + (size_t)s * P->part_split_stride + j;
         const float4 g0 = __ldg(reinterpret_cast<const float4*>(q));
         const float4 g1 = __ldg(reinterpret_cast<const float4*>(q + 4));
@@ -1097,7 +1102,8 @@ cudaError_t launch_gemm(int kind, int bn, const GemmLaunch& L, cudaStream_t stre
                         int max_rows_per_block) {
   const int arows = (!pair && max_rows_per_block <= 32) ? 32 : kGemmBM;
   if (L.num_problems < 1 || L.num_problems > 2 || L.splits < 1) return cudaErrorInvalidValue;
-  if (pair && (L.splits != 1 || (kind == kGemmW2 && bn != 256) || (kind == kGemmW13 && bn != 128) ||
+  if (pair && (L.splits != 1 || splits_of(L, 1) != 1 || (kind == kGemmW2 && bn != 256) ||
+               (kind == kGemmW13 && bn != 128) ||
                kind == kGemmW1 || kind == kGemmRouter))
     return cudaErrorInvalidValue;
   CUtensorMap tm[4];
@@ -1109,8 +1115,8 @@ cudaError_t launch_gemm(int kind, int bn, const GemmLaunch& L, cudaStream_t stre
         !make_map(&tm[2 * p + 1], P.B, (uint64_t)P.K, (uint64_t)P.b_rows, b_box))
       return cudaErrorInvalidValue;
     if (p < L.num_problems) {
-      if (P.k_blocks < L.splits) return cudaErrorInvalidValue;
-      units += (long)P.max_m_blocks * P.n_tiles * L.splits;
+      if (splits_of(L, p) < 1 || P.k_blocks < splits_of(L, p)) return cudaErrorInvalidValue;
+      units += (long)P.max_m_blocks * P.n_tiles * splits_of(L, p);
     }
   }
   if (pair) {

@@ -48,9 +48,12 @@ cudaError_t launch_gather(const void* x, int H, const int* inv, int n, int k, in
                           void* x_perm, const float* row_scale, cudaStream_t stream);
 constexpr int kFusedCopyMaxRows = 16;  // the small route+align launch copies rows itself
 
-// y[t] = sum over splits s and slots of ytok[s * split_stride + (t * slots + slot) * H + :]
-cudaError_t launch_combine(const void* ytok, int slots, int H, int T, int splits,
-                           long long split_stride, void* y, cudaStream_t stream);
+// y[t] = sum over copies c and slots of ytok[c * split_stride + (t * slots + slot) * H + :],
+// where the routed slots (< routed_slots) have `splits` copies and the others
+// `splits_last` copies (the split-K factors of the two w2 problems).
+cudaError_t launch_combine(const void* ytok, int slots, int routed_slots, int H, int T,
+                           int splits, int splits_last, long long split_stride, void* y,
+                           cudaStream_t stream);
 
 // W1: the non-gated first GEMM; Router: logits = x @ gate^T, fp32 per-split copies
 enum GemmKind { kGemmW13 = 0, kGemmW2 = 1, kGemmW1 = 2, kGemmRouter = 3 };
@@ -101,9 +104,14 @@ struct GemmProblem {
 struct GemmLaunch {
   GemmProblem p[2];
   int num_problems;
-  int splits;
+  int splits;       // split-K factor of problem 0
+  int splits_p1;    // split-K factor of problem 1 (0 = same as problem 0)
   int* status;
 };
+
+__host__ __device__ inline int splits_of(const GemmLaunch& L, int p) {
+  return (p == 0 || L.splits_p1 <= 0) ? L.splits : L.splits_p1;
+}
 
 // pair: the CTA-pair kernel (clusters of 2, M = 256 per unit, row blocks of 256; w13 with
 // bn = 128, w2 with bn = 256; no split-K).
