@@ -280,7 +280,6 @@ __global__ void __launch_bounds__(kSmallThreads)
         wcnt[w * E + e] = run;
         run += c;
       }
-      for (int p = start + tot[i]; p < start + pad[i]; ++p) sorted[p] = n;
       for (int b = start / bs; b < (start + pad[i]) / bs; ++b) {
         expert_ids[b] = e;
         if (block_seg) block_seg[b] = make_int2(start / bs, pad[i] / bs);
@@ -291,6 +290,9 @@ __global__ void __launch_bounds__(kSmallThreads)
   const int total = s_total;
   if (threadIdx.x == 0) *npp = total;
   for (int b = total / bs + threadIdx.x; b < max_blocks; b += blockDim.x) expert_ids[b] = -1;
+  // every slot starts as padding (the sentinel n); the scatter below overwrites the real ones
+  // after the barrier, which orders the CTA's writes to the same address
+  for (int p = threadIdx.x; p < total; p += blockDim.x) sorted[p] = n;
   __syncthreads();
   // 4. stable scatter of each warp's slice
   for (int base = s0; base < s1; base += 32) {

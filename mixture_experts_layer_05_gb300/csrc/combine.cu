@@ -53,10 +53,74 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
   }
 }
 
+// Small batches: the terms of each (token, 8 columns) are spread over 8 lanes (lane l takes
+// terms l, l+8, ...), and the 8 partial sums are added by a fixed xor-butterfly, so the
+// result is the same on every run; many more loads are in flight than with one thread.
+constexpr int kTermLanes = 8;
+
+__global__ void __launch_bounds__(256) combine_small_kernel(const float4* __restrict__ ytok,
+                                                            int slots, int routed_slots, int H8,
+                                                            int T, int splits, int splits_last,
+                                                            long long split_stride4,
+                                                            uint4* __restrict__ y) {
+  const size_t groups = (size_t)T * H8;
+  const int lane8 = threadIdx.x & (kTermLanes - 1);
+  const int copies = splits > splits_last ? splits : splits_last;
+  const int terms = copies * slots;
+  // The loop runs over each warp's first group, so every lane of a warp takes the same number
+  // of trips and reaches the shuffles; lanes past the last group add zeros and store nothing.
+  const size_t warp_first = ((size_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31u)) / kTermLanes;
+  const size_t stride = (size_t)gridDim.x * blockDim.x / kTermLanes;
+  for (size_t g0 = warp_first; g0 < groups; g0 += stride) {
+    const size_t g = g0 + (threadIdx.x & 31) / kTermLanes;
+    const bool valid = g < groups;
+    const size_t t = g / H8, h = g % H8;
+    const float4* row = ytok + (t * slots * H8 + h) * 2;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    for (int i = lane8; valid && i < terms; i += kTermLanes) {
+      const int c = i / slots, sl = i % slots;
+      if (c < (sl < routed_slots ? splits : splits_last)) {
+        const float4* src = row + (size_t)c * split_stride4 + (size_t)sl * H8 * 2;
+        const float4 u = __ldg(src), v = __ldg(src + 1);
+        a.x += u.x; a.y += u.y; a.z += u.z; a.w += u.w;
+        b.x += v.x; b.y += v.y; b.z += v.z; b.w += v.w;
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < kTermLanes; o <<= 1) {
+      a.x += __shfl_xor_sync(0xffffffffu, a.x, o);
+      a.y += __shfl_xor_sync(0xffffffffu, a.y, o);
+      a.z += __shfl_xor_sync(0xffffffffu, a.z, o);
+      a.w += __shfl_xor_sync(0xffffffffu, a.w, o);
+      b.x += __shfl_xor_sync(0xffffffffu, b.x, o);
+      b.y += __shfl_xor_sync(0xffffffffu, b.y, o);
+      b.z += __shfl_xor_sync(0xffffffffu, b.z, o);
+      b.w += __shfl_xor_sync(0xffffffffu, b.w, o);
+    }
+    if (valid && lane8 == 0) {
+      uint4 o;
+      o.x = pack_bf16x2(a.x, a.y);
+      o.y = pack_bf16x2(a.z, a.w);
+      o.z = pack_bf16x2(b.x, b.y);
+      o.w = pack_bf16x2(b.z, b.w);
+      y[g] = o;
+    }
+  }
+}
+
 cudaError_t launch_combine(const void* ytok, int slots, int routed_slots, int H, int T,
                            int splits, int splits_last, long long split_stride, void* y,
                            cudaStream_t stream) {
   const size_t total = (size_t)T * (H / 8);
+  if (total * kTermLanes <= (size_t)num_sms() * 1024) {
+    const size_t threads_needed = total * kTermLanes;
+    size_t blocks = (threads_needed + 255) / 256;
+    if (blocks < 1) blocks = 1;
+    combine_small_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        static_cast<const float4*>(ytok), slots, routed_slots, H / 8, T, splits, splits_last,
+        split_stride / 4, static_cast<uint4*>(y));
+    return cudaGetLastError();
+  }
   const int threads = total < (size_t)num_sms() * 256 ? 64 : 256;  // spread small T over SMs
   size_t blocks = (total + threads - 1) / threads;
   const size_t cap = (size_t)num_sms() * (2048 / threads);
