@@ -35,8 +35,10 @@ def _gen(seed: int, device) -> torch.Generator:
     return g
 
 
-def normal(shape, std: float, seed: int, dtype=torch.float32, device="cpu") -> torch.Tensor:
-    """N(0, std) draws in fp32, rounded once to ``dtype``; drawn in slices of the first dim."""
+def normal(shape, std: float, seed: int, dtype=torch.float32, device="cpu",
+           clamp: float | None = None) -> torch.Tensor:
+    """N(0, std) draws in fp32 (clamped to +-clamp if given), rounded once to ``dtype``;
+    drawn in slices of the first dim."""
     device = torch.device(device)
     out = torch.empty(shape, dtype=dtype, device=device)
     g = _gen(seed, device)
@@ -52,6 +54,8 @@ def normal(shape, std: float, seed: int, dtype=torch.float32, device="cpu") -> t
                           dtype=torch.float32)
         if std != 1.0:
             tmp.mul_(std)
+        if clamp is not None:
+            tmp.clamp_(-clamp, clamp)
         out[r0:r1].copy_(tmp)
     return out
 
@@ -152,3 +156,52 @@ def make_tokens(w: MoEWorkload, T: int, seed: int = 0, margin_fn=None,
         else:
             raise RuntimeError("could not draw router logits with the requested margin")
     return x, logits
+
+
+FP8_BLOCK = 128
+
+
+def fp8_codes(shape, seed: int, code_std: float = 112.0, device="cpu") -> torch.Tensor:
+    """Random e4m3fn numbers (torch.float8_e4m3fn): N(0, code_std) draws, clamped to the
+    format's finite range +-448 and converted to the nearest fp8 value."""
+    return normal(shape, code_std, seed, torch.float8_e4m3fn, device, clamp=448.0)
+
+
+def make_fp8_weights(w: MoEWorkload, seed: int = 0, device="cpu") -> dict:
+    """FP8 block-128 expert weights as a checkpoint stores them: e4m3fn codes
+    ``w13_q [E, 2I, H]``, ``w2_q [E, H, I]`` and one fp32 scale per 128 x 128 block
+    (``w13_s [E, 2I/128, H/128]``, ``w2_s [E, H/128, I/128]``), plus the shared expert's.
+
+    Codes ~ N(0, 112) and scales ~ U(0.8, 1.2) * w_std * 4 / 448, so the weights the
+    codes stand for are about N(0, w_std) like the bf16 workloads'. The bias is the bf16
+    workload's (fp32).
+    """
+    E, H, I = w.num_experts, w.hidden_size, w.intermediate_size
+    B = FP8_BLOCK
+    base = w.w_std * 4.0 / 448.0
+
+    def scales(shape, tag):
+        g = _gen(tensor_seed(w.name, tag, seed), "cpu")
+        s = (0.8 + 0.4 * torch.rand(shape, generator=g, dtype=torch.float32)) * base
+        return s.to(device)
+
+    out = {
+        "w13_q": fp8_codes((E, 2 * I, H), tensor_seed(w.name, "fp8/w13", seed), device=device),
+        "w13_s": scales((E, 2 * I // B, H // B), "fp8/w13_s"),
+        "w2_q": fp8_codes((E, H, I), tensor_seed(w.name, "fp8/w2", seed), device=device),
+        "w2_s": scales((E, H // B, I // B), "fp8/w2_s"),
+        "bias": None, "shared_w13_q": None, "shared_w13_s": None, "shared_w2_q": None,
+        "shared_w2_s": None,
+    }
+    if w.has_bias:
+        out["bias"] = normal((E,), w.bias_std, tensor_seed(w.name, "bias", seed),
+                             torch.float32, device)
+    Is = w.shared_intermediate_size
+    if Is:
+        out["shared_w13_q"] = fp8_codes((2 * Is, H), tensor_seed(w.name, "fp8/shared_w13", seed),
+                                        device=device)
+        out["shared_w13_s"] = scales((2 * Is // B, H // B), "fp8/shared_w13_s")
+        out["shared_w2_q"] = fp8_codes((H, Is), tensor_seed(w.name, "fp8/shared_w2", seed),
+                                       device=device)
+        out["shared_w2_s"] = scales((H // B, Is // B), "fp8/shared_w2_s")
+    return out
