@@ -51,6 +51,7 @@ typedef enum {
 
 typedef enum { GBMOE_SCORE_SOFTMAX = 0, GBMOE_SCORE_SIGMOID = 1 } gbmoe_scoring_t;
 typedef enum { GBMOE_ACT_SILU = 0 } gbmoe_act_t;
+typedef enum { GBMOE_QUANT_NONE = 0, GBMOE_QUANT_FP8_BLOCK128 = 1 } gbmoe_weight_quant_t;
 
 /*
  * Layer configuration; field names follow the FusedMoE constructor (vLLM
@@ -83,6 +84,17 @@ typedef enum { GBMOE_ACT_SILU = 0 } gbmoe_act_t;
  *                         rows instead of its output (FusedMoE constructor argument)
  * The pages name the last three options without their arithmetic; the reading used is
  * the one the NPU clipped-SwiGLU call's arguments (alpha, limit, bias) point to.
+ *  weight_quant           gbmoe_weight_quant_t. FP8_BLOCK128: the w8a8 fp8 layer of the
+ *                         sglang `models/deepseek_v2.py` page (`DeepseekV2MoE`'s
+ *                         quant-once path, `DeepseekV2MLP.forward`'s fp8 down GEMM):
+ *                         expert and shared weights are e4m3fn bytes with one fp32 scale
+ *                         per 128 x 128 block (w = q * scale[n / 128][k / 128]); the input
+ *                         is quantized once per token and group of 128 hidden columns
+ *                         (s = max(amax, 1e-10) / 448, q = e4m3(x / s), fp32), feeds the
+ *                         routed and the shared experts, and each act is quantized the
+ *                         same way before its w2 GEMM. Requires H % 256 == 0, gated SiLU
+ *                         without clamp or alpha, no expert biases, no
+ *                         apply_router_weight_on_input (else UNSUPPORTED).
  */
 typedef struct {
   int32_t num_experts;
@@ -101,6 +113,7 @@ typedef struct {
   float swiglu_limit;
   float gemm1_alpha;
   int32_t apply_router_weight_on_input;
+  int32_t weight_quant;
 } gbmoe_config_t;
 
 /*
@@ -250,6 +263,14 @@ typedef struct {
   const void* gate_weight;   /* [E, H] bf16: when router_logits is NULL, the logits are
                                 computed first as hidden_states @ gate_weight^T in fp32
                                 (moe_router_logits); exactly one of the two is given */
+  /* weight_quant == FP8_BLOCK128 only (else NULL): the weights above are e4m3fn bytes and
+     these their fp32 block scales, row-major per matrix:
+     w13_scale [E, 2I/128, H/128], w2_scale [E, H/128, I/128],
+     shared_w13_scale [2I_s/128, H/128], shared_w2_scale [H/128, I_s/128] */
+  const float* w13_scale;
+  const float* w2_scale;
+  const float* shared_w13_scale;
+  const float* shared_w2_scale;
 } gbmoe_forward_args_t;
 gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_tokens,
                               const gbmoe_forward_args_t* args, gbmoe_stream_t stream);
@@ -265,6 +286,23 @@ gbmoe_status_t moe_router_logits(int32_t num_tokens, int32_t hidden_size, int32_
                                  float* router_logits, gbmoe_stream_t stream);
 
 /*
+ * moe_quant_fp8_per_token_group: the per-token-group-128 fp8 quant of bf16 rows that the
+ * FP8_BLOCK128 layer applies to its input (sglang `models/deepseek_v2.py` page,
+ * `DeepseekV2MoE._maybe_quant_moe_input_once`): for each row r and group g of 128
+ * consecutive columns, s = max(max |x|, 1e-10) / 448 and q = e4m3fn(x / s), both one fp32
+ * division, the conversion round-to-nearest-even saturating at +-448.
+ *   x      [num_rows, hidden_size] bf16, device, 16-byte aligned
+ *   q      [num_rows, hidden_size] e4m3fn bytes, device (written)
+ *   scale  [hidden_size / 128, num_rows] fp32, device, group-major ("column-major
+ *          scales"): scale[g * num_rows + r] (written)
+ * hidden_size a positive multiple of 128; num_rows = 0 is a no-op. Asynchronous on
+ * `stream`; INVALID_ARG for bad sizes or pointers.
+ */
+gbmoe_status_t moe_quant_fp8_per_token_group(int32_t num_rows, int32_t hidden_size,
+                                             const void* x, uint8_t* q, float* scale,
+                                             gbmoe_stream_t stream);
+
+/*
  * Byte offsets of the intermediate results inside a moe_forward workspace
  * (for inspection and tests). Each is valid after the call completes.
  */
@@ -275,7 +313,10 @@ typedef struct {
   size_t sorted_token_ids;       /* int32 [T*top_k + E*(bs-1)] */
   size_t expert_ids;             /* int32 [that / bs + 1] */
   size_t num_tokens_post_padded; /* int32 [1] */
-  size_t act;                    /* bf16 [rows, I]: silu(gate)*up in expert order */
+  size_t act;                    /* bf16 [rows, I]: silu(gate)*up in expert order
+                                    (FP8_BLOCK128: e4m3fn [rows, I], then fp32 scales
+                                    [I/128][rows] at act_scale) */
+  size_t act_scale;              /* FP8_BLOCK128 only, else 0 */
   size_t total;                  /* == moe_forward_workspace_size() */
 } gbmoe_workspace_layout_t;
 gbmoe_status_t moe_forward_workspace_layout(const gbmoe_config_t* cfg, int32_t max_num_tokens,

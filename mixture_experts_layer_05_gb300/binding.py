@@ -20,6 +20,7 @@ STATUS = {0: "GBMOE_OK", -1: "GBMOE_ERR_INVALID_ARG", -2: "GBMOE_ERR_UNSUPPORTED
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_CHECK, ERR_TIMEOUT = \
     0, -1, -2, -3, -4, -5, -6
 SCORE = {"softmax": 0, "sigmoid": 1}
+QUANT = {None: 0, "none": 0, "fp8": 1, "fp8_block128": 1}
 NUM_STAGE_EVENTS = 5
 
 # every entry point declared in include/gbmoe.h
@@ -28,7 +29,7 @@ EXPORTS = ("moe_topk", "moe_align_block_size_workspace_size", "moe_align_block_s
            "moe_forward_workspace_size", "moe_forward_block_size", "moe_forward",
            "moe_forward_events", "moe_forward_workspace_layout", "moe_get_device_status",
            "moe_forward_num_launches", "moe_selftest_bounded_wait", "moe_forward_ex",
-           "moe_router_logits", "gbmoe_version")
+           "moe_router_logits", "moe_quant_fp8_per_token_group", "gbmoe_version")
 
 
 class GbmoeError(RuntimeError):
@@ -47,7 +48,8 @@ class Config(ctypes.Structure):
                 ("activation", ctypes.c_int32), ("is_act_and_mul", ctypes.c_int32),
                 ("shared_intermediate_size", ctypes.c_int32), ("swiglu_limit", ctypes.c_float),
                 ("gemm1_alpha", ctypes.c_float),
-                ("apply_router_weight_on_input", ctypes.c_int32)]
+                ("apply_router_weight_on_input", ctypes.c_int32),
+                ("weight_quant", ctypes.c_int32)]
 
 
 class ForwardArgs(ctypes.Structure):
@@ -59,27 +61,32 @@ class ForwardArgs(ctypes.Structure):
                 ("w2_bias", ctypes.c_void_p), ("output", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("events", ctypes.c_void_p), ("num_events", ctypes.c_int32),
-                ("gate_weight", ctypes.c_void_p)]
+                ("gate_weight", ctypes.c_void_p), ("w13_scale", ctypes.c_void_p),
+                ("w2_scale", ctypes.c_void_p), ("shared_w13_scale", ctypes.c_void_p),
+                ("shared_w2_scale", ctypes.c_void_p)]
 
 
 class WorkspaceLayout(ctypes.Structure):
     """gbmoe_workspace_layout_t."""
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "topk_weights", "topk_ids", "sorted_token_ids", "expert_ids",
-        "num_tokens_post_padded", "act", "total")]
+        "num_tokens_post_padded", "act", "act_scale", "total")]
 
 
 def make_config(num_experts, top_k, hidden_size, intermediate_size, renormalize=True,
                 use_grouped_topk=False, num_expert_group=0, topk_group=0,
                 scoring_func="softmax", routed_scaling_factor=1.0, activation=0,
                 is_act_and_mul=1, shared_intermediate_size=0, swiglu_limit=None,
-                gemm1_alpha=1.0, apply_router_weight_on_input=False) -> Config:
+                gemm1_alpha=1.0, apply_router_weight_on_input=False,
+                weight_quant=None) -> Config:
+    """weight_quant: None / "none", or "fp8" (e4m3 weights with 128 x 128 fp32 block scales)."""
     return Config(int(num_experts), int(top_k), int(hidden_size), int(intermediate_size),
                   int(bool(renormalize)), int(bool(use_grouped_topk)), int(num_expert_group or 0),
                   int(topk_group or 0), SCORE.get(scoring_func, scoring_func),
                   float(routed_scaling_factor), int(activation), int(is_act_and_mul),
                   int(shared_intermediate_size or 0), float(swiglu_limit or 0.0),
-                  float(gemm1_alpha), int(bool(apply_router_weight_on_input)))
+                  float(gemm1_alpha), int(bool(apply_router_weight_on_input)),
+                  QUANT.get(weight_quant, weight_quant))
 
 
 def config_from_workload(w, **variants) -> Config:
@@ -117,6 +124,7 @@ def load() -> ctypes.CDLL:
         "moe_forward_num_launches": (I32, [CP, I32]),
         "moe_forward_ex": (I32, [CP, I32, ctypes.POINTER(ForwardArgs), P]),
         "moe_router_logits": (I32, [I32, I32, I32, P, P, P, P]),
+        "moe_quant_fp8_per_token_group": (I32, [I32, I32, P, P, P, P]),
         "moe_selftest_bounded_wait": (I32, [P, I32, P]),
         "gbmoe_version": (I32, []),
     }
@@ -259,17 +267,36 @@ def moe_router_logits(hidden_states, gate_weight, router_logits, stream=None):
         _stream(stream)))
 
 
+def _fp8_bytes(t, name):
+    """e4m3 weights as passed to the library: float8_e4m3fn or uint8 storage."""
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous() or t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise ValueError(f"{name} must be a contiguous CUDA float8_e4m3fn (or uint8) tensor")
+    return t
+
+
 def moe_forward_ex(cfg: Config, hidden_states, router_logits, e_score_correction_bias,
                    w13_weight, w2_weight, shared_w13, shared_w2, output, workspace,
-                   w13_bias=None, w2_bias=None, events=None, stream=None, gate_weight=None):
-    """moe_forward with the optional per-expert biases, stage events, or (router_logits
-    None) the gate weight whose router GEMM runs first."""
+                   w13_bias=None, w2_bias=None, events=None, stream=None, gate_weight=None,
+                   w13_scale=None, w2_scale=None, shared_w13_scale=None, shared_w2_scale=None):
+    """moe_forward with the optional per-expert biases, stage events, (router_logits None)
+    the gate weight whose router GEMM runs first, or (cfg.weight_quant fp8) e4m3 weights
+    with their fp32 128 x 128 block scales."""
     _need(hidden_states, torch.bfloat16, "hidden_states")
     _need(router_logits, torch.float32, "router_logits")
     _need(e_score_correction_bias, torch.float32, "e_score_correction_bias")
-    for t, n in ((w13_weight, "w13_weight"), (w2_weight, "w2_weight"), (shared_w13, "shared_w13"),
-                 (shared_w2, "shared_w2"), (w13_bias, "w13_bias"), (w2_bias, "w2_bias"),
-                 (output, "output"), (gate_weight, "gate_weight")):
+    weights = ((w13_weight, "w13_weight"), (w2_weight, "w2_weight"), (shared_w13, "shared_w13"),
+               (shared_w2, "shared_w2"))
+    if cfg.weight_quant:
+        for t, n in weights:
+            _fp8_bytes(t, n)
+        for t, n in ((w13_scale, "w13_scale"), (w2_scale, "w2_scale"),
+                     (shared_w13_scale, "shared_w13_scale"), (shared_w2_scale, "shared_w2_scale")):
+            _need(t, torch.float32, n)
+        weights = ()
+    for t, n in weights + ((w13_bias, "w13_bias"), (w2_bias, "w2_bias"),
+                           (output, "output"), (gate_weight, "gate_weight")):
         _need(t, torch.bfloat16, n)
     arr = None
     if events is not None:
@@ -284,9 +311,26 @@ def moe_forward_ex(cfg: Config, hidden_states, router_logits, e_score_correction
                     ptr(w13_bias), ptr(w2_bias), ptr(output), ptr(workspace),
                     workspace.numel() * workspace.element_size(),
                     ctypes.cast(arr, ctypes.c_void_p) if arr is not None else None,
-                    0 if events is None else len(events), ptr(gate_weight))
+                    0 if events is None else len(events), ptr(gate_weight), ptr(w13_scale),
+                    ptr(w2_scale), ptr(shared_w13_scale), ptr(shared_w2_scale))
     _check("moe_forward_ex", load().moe_forward_ex(ctypes.byref(cfg), hidden_states.shape[0],
                                                    ctypes.byref(a), _stream(stream)))
+
+
+def moe_quant_fp8_per_token_group(x, q=None, scale=None, stream=None):
+    """Per-token-group-128 e4m3 quant of bf16 rows: q [R, H] float8_e4m3fn and the
+    group-major fp32 scales scale [H / 128, R]; returns (q, scale)."""
+    _need(x, torch.bfloat16, "x")
+    R, H = x.shape
+    if q is None:
+        q = torch.empty(R, H, dtype=torch.float8_e4m3fn, device=x.device)
+    if scale is None:
+        scale = torch.empty(H // 128, R, dtype=torch.float32, device=x.device)
+    _fp8_bytes(q, "q")
+    _need(scale, torch.float32, "scale")
+    _check("moe_quant_fp8_per_token_group", load().moe_quant_fp8_per_token_group(
+        R, H, _p(x), _p(q), _p(scale), _stream(stream)))
+    return q, scale
 
 
 def moe_get_device_status(workspace, stream=None) -> int:
@@ -301,11 +345,14 @@ class FusedMoE:
 
     def __init__(self, cfg: Config, w13_weight, w2_weight, e_score_correction_bias=None,
                  shared_w13=None, shared_w2=None, max_tokens: int = 1, w13_bias=None,
-                 w2_bias=None):
+                 w2_bias=None, w13_scale=None, w2_scale=None, shared_w13_scale=None,
+                 shared_w2_scale=None):
         self.cfg = cfg
         self.w13, self.w2 = w13_weight, w2_weight
         self.bias, self.shared_w13, self.shared_w2 = e_score_correction_bias, shared_w13, shared_w2
         self.w13_bias, self.w2_bias = w13_bias, w2_bias
+        self.scales = dict(w13_scale=w13_scale, w2_scale=w2_scale,
+                           shared_w13_scale=shared_w13_scale, shared_w2_scale=shared_w2_scale)
         self.max_tokens = 0
         self.workspace = None
         self.reserve(max_tokens)
@@ -323,11 +370,11 @@ class FusedMoE:
         self.reserve(T)
         if out is None:
             out = torch.empty_like(hidden_states)
-        if gate_weight is not None or router_logits is None:
-            moe_forward_ex(self.cfg, hidden_states, None, self.bias, self.w13, self.w2,
-                           self.shared_w13, self.shared_w2, out, self.workspace,
-                           w13_bias=self.w13_bias, w2_bias=self.w2_bias, events=events,
-                           stream=stream, gate_weight=gate_weight)
+        if gate_weight is not None or router_logits is None or self.cfg.weight_quant:
+            moe_forward_ex(self.cfg, hidden_states, router_logits if gate_weight is None else None,
+                           self.bias, self.w13, self.w2, self.shared_w13, self.shared_w2, out,
+                           self.workspace, w13_bias=self.w13_bias, w2_bias=self.w2_bias,
+                           events=events, stream=stream, gate_weight=gate_weight, **self.scales)
         elif self.w13_bias is None and self.w2_bias is None:
             moe_forward(self.cfg, hidden_states, router_logits, self.bias, self.w13, self.w2,
                         self.shared_w13, self.shared_w2, out, self.workspace, events=events,

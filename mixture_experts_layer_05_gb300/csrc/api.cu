@@ -72,6 +72,13 @@ gbmoe_status_t check_layer(const gbmoe_config_t* c) {
     return GBMOE_ERR_UNSUPPORTED;                  // clamp / alpha / shared need the gated form
   if (c->hidden_size % 128 || c->intermediate_size % 128 || c->shared_intermediate_size % 128)
     return GBMOE_ERR_UNSUPPORTED;
+  if (c->weight_quant != GBMOE_QUANT_NONE && c->weight_quant != GBMOE_QUANT_FP8_BLOCK128)
+    return GBMOE_ERR_INVALID_ARG;
+  if (c->weight_quant == GBMOE_QUANT_FP8_BLOCK128 &&
+      (!c->is_act_and_mul || c->swiglu_limit > 0.f ||
+       (c->gemm1_alpha != 0.f && c->gemm1_alpha != 1.f) || c->apply_router_weight_on_input ||
+       c->hidden_size % 256))
+    return GBMOE_ERR_UNSUPPORTED;                  // the fp8 layer is the plain gated one
   if ((long long)c->num_experts * 2 * c->intermediate_size > INT_MAX / 2 ||
       (long long)c->num_experts * c->hidden_size > INT_MAX / 2)
     return GBMOE_ERR_UNSUPPORTED;
@@ -82,7 +89,8 @@ gbmoe_status_t check_layer(const gbmoe_config_t* c) {
 // rows and the w2 output tiles are 256 wide.
 bool use_pair(const gbmoe_config_t& c, int T) {
   const bool plain = c.is_act_and_mul && c.swiglu_limit == 0.f &&
-                     (c.gemm1_alpha == 0.f || c.gemm1_alpha == 1.f);
+                     (c.gemm1_alpha == 0.f || c.gemm1_alpha == 1.f) &&
+                     c.weight_quant == GBMOE_QUANT_NONE;
   return plain && (long)T * c.top_k >= (long)kPairMinRowsPerExpert * c.num_experts &&
          c.hidden_size % 256 == 0;
 }
@@ -122,12 +130,14 @@ long t_blocks_128(int T) { return ((long)T + kGemmBM - 1) / kGemmBM; }
 
 struct Layout {
   int bs, n, max_sorted, max_blocks, slots;
-  bool pair;
+  bool pair, fp8;
   // launch plan of one forward: small-batch routing, fused row copy, split factors
   bool small, fused_copy;
   int w2_bn, splits13, splits13_shared, splits2, splits2_shared, splits_router, launches;
   size_t status, topk_weights, topk_ids, sorted, expert_ids, npp, block_seg, inv, scratch,
-      x_perm, act, ytok, act_s, part_r, part_s, logits, total;
+      x_perm, act, ytok, act_s, part_r, part_s, logits, xq, total;
+  // fp8: byte offsets of the scales inside x_perm / act / act_s / xq
+  size_t xs_perm, act_scale, act_s_scale, xs_tok;
 };
 
 Layout layout_for(const gbmoe_config_t& c, int T) {
@@ -135,6 +145,7 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   const int E = c.num_experts, k = c.top_k, H = c.hidden_size, I = c.intermediate_size;
   const int Is = c.shared_intermediate_size;
   L.pair = use_pair(c, T);
+  L.fp8 = c.weight_quant == GBMOE_QUANT_FP8_BLOCK128;
   L.bs = L.pair ? 2 * kGemmBM : kGemmBM;
   L.n = T * k;
   L.max_sorted = L.n + E * (L.bs - 1);
@@ -169,30 +180,43 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   L.ytok = o;
   o = up(o + ytok_rows * L.slots * H * 4);
   L.act_s = o;
-  o = up(o + (size_t)T * Is * 2);
+  {
+    const size_t bf16_bytes = (size_t)T * Is * 2;
+    const size_t fp8_bytes = Is ? up((size_t)T * Is) + (size_t)(Is / 128) * T * 4 : 0;
+    o = up(o + (bf16_bytes > fp8_bytes ? bf16_bytes : fp8_bytes));
+  }
   L.part_r = o;
   o = up(o + kMaxSplits * ts * k * (c.is_act_and_mul ? 2 : 1) * I * 4);
   L.part_s = o;
   o = up(o + kMaxSplits * ts * 2 * Is * 4);
   L.logits = o;                       // router GEMM output (per-split copies at decode)
   o = up(o + ((size_t)T > kMaxSplits * ts ? (size_t)T : kMaxSplits * ts) * E * 4);
+  // fp8: e4m3 rows then group-major fp32 scales, inside the bf16-sized regions above (a
+  // byte plus 4/128 bytes per element fits in 2 bytes); the token-order input has its own
+  L.xq = o;
+  if (L.fp8) o = up(o + up((size_t)T * H) + (size_t)(H / kFp8Block) * T * 4);
+  L.xs_perm = L.fp8 ? up((size_t)L.max_sorted * H) : 0;
+  L.act_scale = L.fp8 ? up((size_t)L.max_sorted * I) : 0;
+  L.act_s_scale = L.fp8 ? up((size_t)T * Is) : 0;
+  L.xs_tok = L.fp8 ? up((size_t)T * H) : 0;
   L.total = o;
 
   // launch plan
   L.small = route_align_small_ok(T, k, E);
-  L.fused_copy = L.small && L.n <= kFusedCopyMaxRows;
+  L.fused_copy = L.small && L.n <= kFusedCopyMaxRows && !L.fp8;
   L.w2_bn = (H % 256 == 0) ? 256 : 128;
+  const int kblk = L.fp8 ? kFp8Block : kGemmBK;  // K elements per GEMM pipeline stage
   const long est_blocks = (long)(L.n < E ? L.n : E) + L.n / kGemmBM;  // >= 1 partial per expert
   const long t_blocks = ((long)T + L.bs - 1) / L.bs;
   if (L.pair) {
     L.splits13 = L.splits13_shared = L.splits2 = L.splits2_shared = 1;
   } else {
-    const Splits a = choose_splits2(est_blocks * (I / kGemmBM), H / kGemmBK,
-                                    Is ? t_blocks * (Is / kGemmBM) : 0, H / kGemmBK, T);
+    const Splits a = choose_splits2(est_blocks * (I / kGemmBM), H / kblk,
+                                    Is ? t_blocks * (Is / kGemmBM) : 0, H / kblk, T);
     L.splits13 = a.r;
     L.splits13_shared = a.s;
-    const Splits b = choose_splits2(est_blocks * (H / L.w2_bn), I / kGemmBK,
-                                    Is ? t_blocks * (H / L.w2_bn) : 0, Is / kGemmBK, T);
+    const Splits b = choose_splits2(est_blocks * (H / L.w2_bn), I / kblk,
+                                    Is ? t_blocks * (H / L.w2_bn) : 0, Is / kblk, T);
     L.splits2 = b.r;
     L.splits2_shared = b.s;
   }
@@ -292,6 +316,7 @@ GBMOE_API gbmoe_status_t moe_forward_workspace_layout(const gbmoe_config_t* cfg,
   out->expert_ids = L.expert_ids;
   out->num_tokens_post_padded = L.npp;
   out->act = L.act;
+  out->act_scale = L.fp8 ? L.act + L.act_scale : 0;
   out->total = L.total;
   return GBMOE_OK;
 }
@@ -331,6 +356,12 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
   if (!aligned16(hidden_states) || !aligned16(w13_weight) || !aligned16(w2_weight) ||
       !aligned16(output) || (Is && (!aligned16(shared_w13) || !aligned16(shared_w2))) ||
       !aligned16(w13_bias) || !aligned16(w2_bias))
+    return GBMOE_ERR_INVALID_ARG;
+  const bool fp8 = c.weight_quant == GBMOE_QUANT_FP8_BLOCK128;
+  if (fp8 && (w13_bias || w2_bias)) return GBMOE_ERR_UNSUPPORTED;
+  if (fp8 ? (!args->w13_scale || !args->w2_scale ||
+             (Is && (!args->shared_w13_scale || !args->shared_w2_scale)))
+          : (args->w13_scale || args->w2_scale || args->shared_w13_scale || args->shared_w2_scale))
     return GBMOE_ERR_INVALID_ARG;
   const Layout L = layout_for(c, num_tokens);
   if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) % kAlign))
@@ -407,24 +438,174 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
   const float* row_scale = c.apply_router_weight_on_input ? tw : nullptr;
   const bool gated = c.is_act_and_mul != 0;
   const float alpha = c.gemm1_alpha == 0.f ? 1.f : c.gemm1_alpha;
+  // fp8: the input is quantized once per token while it is gathered (and kept in token
+  // order for the shared expert)
+  uint8_t* xq_tok = at<uint8_t>(workspace, L.xq);
+  float* xs_tok = at<float>(workspace, L.xq + L.xs_tok);
+  float* xs_perm = at<float>(workspace, L.x_perm + L.xs_perm);
+  auto gather = [&]() -> cudaError_t {
+    if (fp8)
+      return launch_quant_gather_fp8(hidden_states, H, inv, L.n, k, T,
+                                     static_cast<uint8_t*>(x_perm), xs_perm, L.max_sorted,
+                                     Is ? xq_tok : nullptr, xs_tok, stream);
+    return launch_gather(hidden_states, H, inv, L.n, k, L.max_sorted, x_perm, row_scale, stream);
+  };
   if (L.small) {
     const bool fused_copy = L.fused_copy;
     GBMOE_TRY(launch_route_align_small(c, T, router_logits, e_score_correction_bias, tw, tids,
                                        L.bs, sorted, eids, L.max_blocks, npp, bseg, inv,
                                        hidden_states, fused_copy ? x_perm : nullptr, row_scale,
                                        status, stream, logit_splits, logit_stride));
-    if (!fused_copy)
-      GBMOE_TRY(launch_gather(hidden_states, H, inv, L.n, k, L.max_sorted, x_perm, row_scale,
-                              stream));
+    if (!fused_copy) GBMOE_TRY(gather());
   } else {
     GBMOE_TRY(launch_topk(c, T, router_logits, e_score_correction_bias, tw, tids, status, stream,
                           logit_splits, logit_stride));
     GBMOE_TRY(launch_align(tids, L.n, E, L.bs, sorted, eids, L.max_blocks, npp,
                            at<char>(workspace, L.scratch), status, stream, bseg, inv));
-    GBMOE_TRY(launch_gather(hidden_states, H, inv, L.n, k, L.max_sorted, x_perm, row_scale,
-                            stream));
+    GBMOE_TRY(gather());
   }
   GBMOE_TRY(rec(1));
+  const long long slot_copy = (long long)T * L.slots * H;
+
+  if (fp8) {
+    // ---- w13 (fp8): e4m3 act + scales, routed and shared experts in one launch
+    GemmLaunch g1;
+    std::memset(&g1, 0, sizeof(g1));
+    g1.status = status;
+    g1.num_problems = Is ? 2 : 1;
+    {
+      GemmProblem& P = g1.p[0];
+      P.A = x_perm;
+      P.a_rows = L.max_sorted;
+      P.a_scale = xs_perm;
+      P.a_scale_ld = L.max_sorted;
+      P.B = w13_weight;
+      P.b_rows = E * 2 * I;
+      P.b_scale = args->w13_scale;
+      P.K = H;
+      P.n_tiles = I / kFp8Block;
+      P.k_blocks = H / kFp8Block;
+      P.m_rows_dev = npp;
+      P.max_m_blocks = L.max_sorted / L.bs;
+      P.expert_ids = eids;
+      P.block_seg = bseg;
+      P.group_m = group_m_for(H / 2, L.bs);
+      P.num_experts = E;
+      P.b_rows_per_expert = 2 * I;
+      P.up_offset = I;
+      P.out = act;
+      P.out_scale = at<float>(workspace, L.act + L.act_scale);
+      P.out_scale_ld = L.max_sorted;
+      P.ldo = I;
+      P.store_rows = L.max_sorted;
+      P.sorted_ids = sorted;
+      P.num_flat = L.n;
+      P.part = at<float>(workspace, L.part_r);
+      P.part_split_stride = (long long)L.n * 2 * I;
+    }
+    if (Is) {
+      GemmProblem& P = g1.p[1];
+      P.A = xq_tok;
+      P.a_rows = T;
+      P.a_scale = xs_tok;
+      P.a_scale_ld = T;
+      P.B = shared_w13;
+      P.b_rows = 2 * Is;
+      P.b_scale = args->shared_w13_scale;
+      P.K = H;
+      P.n_tiles = Is / kFp8Block;
+      P.k_blocks = H / kFp8Block;
+      P.m_rows_host = t_pad;
+      P.max_m_blocks = t_pad / L.bs;
+      P.group_m = group_m_for(H / 2, L.bs);
+      P.num_experts = 1;
+      P.b_rows_per_expert = 2 * Is;
+      P.up_offset = Is;
+      P.out = act_s;
+      P.out_scale = at<float>(workspace, L.act_s + L.act_s_scale);
+      P.out_scale_ld = T;
+      P.ldo = Is;
+      P.store_rows = T;
+      P.num_flat = L.n;
+      P.part = at<float>(workspace, L.part_s);
+      P.part_split_stride = (long long)T * 2 * Is;
+    }
+    g1.splits = L.splits13;
+    g1.splits_p1 = L.splits13_shared;
+    GBMOE_TRY(launch_gemm_fp8(kGemmW13, g1, stream, T));
+    if (g1.splits > 1 || (Is && g1.splits_p1 > 1))
+      GBMOE_TRY(launch_silu_reduce_fp8(g1, npp, L.max_sorted, stream));
+    GBMOE_TRY(rec(2));
+
+    // ---- w2 (fp8): weighted fp32 slot outputs; the shared expert to slot k
+    GemmLaunch g2;
+    std::memset(&g2, 0, sizeof(g2));
+    g2.status = status;
+    g2.num_problems = Is ? 2 : 1;
+    {
+      GemmProblem& P = g2.p[0];
+      P.A = act;
+      P.a_rows = L.max_sorted;
+      P.a_scale = at<float>(workspace, L.act + L.act_scale);
+      P.a_scale_ld = L.max_sorted;
+      P.B = w2_weight;
+      P.b_rows = E * H;
+      P.b_scale = args->w2_scale;
+      P.K = I;
+      P.n_tiles = H / 256;
+      P.k_blocks = I / kFp8Block;
+      P.m_rows_dev = npp;
+      P.max_m_blocks = L.max_sorted / L.bs;
+      P.expert_ids = eids;
+      P.block_seg = bseg;
+      P.group_m = group_m_for(I / 2, L.bs);
+      P.num_experts = E;
+      P.b_rows_per_expert = H;
+      P.out = ytok;
+      P.ldo = H;
+      P.store_rows = L.max_sorted;
+      P.sorted_ids = sorted;
+      P.row_weight = tw;
+      P.num_flat = L.n;
+      P.top_k = k;
+      P.slots = L.slots;
+      P.out_split_stride = slot_copy;
+    }
+    if (Is) {
+      GemmProblem& P = g2.p[1];
+      P.A = act_s;
+      P.a_rows = T;
+      P.a_scale = at<float>(workspace, L.act_s + L.act_s_scale);
+      P.a_scale_ld = T;
+      P.B = shared_w2;
+      P.b_rows = H;
+      P.b_scale = args->shared_w2_scale;
+      P.K = Is;
+      P.n_tiles = H / 256;
+      P.k_blocks = Is / kFp8Block;
+      P.m_rows_host = t_pad;
+      P.max_m_blocks = t_pad / L.bs;
+      P.group_m = group_m_for(Is / 2, L.bs);
+      P.num_experts = 1;
+      P.b_rows_per_expert = H;
+      P.out = ytok;
+      P.ldo = H;
+      P.store_rows = T;
+      P.num_flat = L.n;
+      P.top_k = k;
+      P.slots = L.slots;
+      P.slot_offset = k;
+      P.out_split_stride = slot_copy;
+    }
+    g2.splits = L.splits2;
+    g2.splits_p1 = L.splits2_shared;
+    GBMOE_TRY(launch_gemm_fp8(kGemmW2, g2, stream, T));
+    GBMOE_TRY(rec(3));
+    GBMOE_TRY(launch_combine(ytok, L.slots, k, H, T, g2.splits, Is ? g2.splits_p1 : g2.splits,
+                             slot_copy, output, stream));
+    GBMOE_TRY(rec(4));
+    return GBMOE_OK;
+  }
 
 
   // ---- w13 + SiLU*mul: routed experts and the shared expert in one launch
@@ -498,7 +679,6 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
   std::memset(&g2, 0, sizeof(g2));
   g2.status = status;
   g2.num_problems = Is ? 2 : 1;
-  const long long slot_copy = (long long)T * L.slots * H;
   {
     GemmProblem& P = g2.p[0];
     P.A = act;
@@ -627,6 +807,19 @@ GBMOE_API gbmoe_status_t moe_router_logits(int32_t num_tokens, int32_t hidden_si
   P.ldo = E;
   P.store_rows = T;
   return cuda_status(launch_gemm(kGemmRouter, kGemmBM, gr, (cudaStream_t)stream, false, T));
+}
+
+GBMOE_API gbmoe_status_t moe_quant_fp8_per_token_group(int32_t num_rows, int32_t hidden_size,
+                                                       const void* x, uint8_t* q, float* scale,
+                                                       gbmoe_stream_t stream) {
+  if (num_rows < 0 || num_rows > kMaxTokens || hidden_size <= 0 || hidden_size % kFp8Block)
+    return GBMOE_ERR_INVALID_ARG;
+  if (num_rows == 0) return GBMOE_OK;
+  if (!x || !q || !scale || !aligned16(x) || !aligned16(q) ||
+      (reinterpret_cast<uintptr_t>(scale) & 3u))
+    return GBMOE_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_quant_fp8(x, num_rows, hidden_size, q, scale, num_rows, (cudaStream_t)stream));
 }
 
 GBMOE_API int32_t moe_forward_num_launches(const gbmoe_config_t* cfg, int32_t num_tokens) {

@@ -97,6 +97,13 @@ struct GemmProblem {
                            // [row][ldo] non-gated), row = flat index (routed) or token
   long long part_split_stride;
   long long out_split_stride;  // w2: elements between the per-split copies of out
+  // FP8 (e4m3 w8a8, 128 x 128 weight blocks) problems only: A and B are e4m3 bytes,
+  // K blocks are 128 wide, and out (w13) is e4m3 act with fp32 scales.
+  const float* a_scale;    // A scales, K-block major: a_scale[kb * a_scale_ld + row]
+  int a_scale_ld;          // rows covered by a_scale (rows >= it have no scale)
+  const float* b_scale;    // B block scales [b_rows / 128][K / 128], row-major
+  float* out_scale;        // w13: act scales, [ldo / 128][out_scale_ld] (group-major)
+  int out_scale_ld;
 };
 
 // Up to two problems (the routed experts and the shared expert) in one persistent
@@ -129,5 +136,27 @@ cudaError_t launch_wait_selftest(int* status, int timeout_us, cudaStream_t strea
 // expert, always gated); f = the gated activation with clamp / alpha, or silu (non-gated).
 cudaError_t launch_silu_reduce(const GemmLaunch& L, const int* npp, int max_routed_rows,
                                bool gated, cudaStream_t stream);
+
+// ---------------------------------------------------------------- FP8 (w8a8, block 128)
+constexpr int kFp8Block = 128;  // quant group / weight block edge, = K elements per GEMM stage
+
+// Per-token-group-128 quant of bf16 rows: q[r][c] = e4m3(x[r][c] / s), s = max(amax, 1e-10)
+// / 448 over the row's 128-column group, stored group-major: s_out[g * s_ld + r].
+cudaError_t launch_quant_fp8(const void* x, int rows, int H, uint8_t* q, float* s_out, int s_ld,
+                             cudaStream_t stream);
+// The same quant fused with the gather into expert order: x_perm_q[inv[f]] = q(x[f / k]) and
+// its scales at xs_perm[g * perm_ld + inv[f]]; the slot-0 copy (f % k == 0) also writes the
+// token-order row to xq_tok / xs_tok[g * T + t] when xq_tok is not NULL.
+cudaError_t launch_quant_gather_fp8(const void* x, int H, const int* inv, int n, int k, int T,
+                                    uint8_t* x_perm_q, float* xs_perm, int perm_ld,
+                                    uint8_t* xq_tok, float* xs_tok, cudaStream_t stream);
+// FP8 grouped GEMMs: kind kGemmW13 (bn 128: e4m3 act + scales, or fp32 partials when split)
+// or kGemmW2 (bn 256: weighted fp32 slot outputs); K is promoted per 128-wide block.
+cudaError_t launch_gemm_fp8(int kind, const GemmLaunch& L, cudaStream_t stream,
+                            int max_rows_per_block = kGemmBM);
+// Split reduce of an FP8 w13 launch: act = silu(sum gate) * sum up, quantized per group of
+// 128 columns into e4m3 act + group-major scales.
+cudaError_t launch_silu_reduce_fp8(const GemmLaunch& L, const int* npp, int max_routed_rows,
+                                   cudaStream_t stream);
 
 }  // namespace gbmoe

@@ -135,7 +135,7 @@ def dequant_block(q_codes, scale, block: int = GROUP) -> np.ndarray:
         if t.dtype != torch.uint8:
             t = t.view(torch.uint8)
         q_codes = t.numpy()
-    V = e4m3_value(np.asarray(q_codes))
+    V = e4m3_value(np.arange(256))[np.asarray(q_codes, dtype=np.uint8)]  # value of each code
     S = _mo._f64(scale)
     N, K = V.shape
     if S.shape != ((N + block - 1) // block, (K + block - 1) // block):

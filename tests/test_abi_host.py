@@ -153,3 +153,61 @@ def test_launch_count_host(lib):
         cfg = binding.config_from_workload(w)
         counts = [lib.moe_forward_num_launches(ctypes.byref(cfg), T) for T in (1, 16, 64, 4096)]
         assert all(4 <= c <= 9 for c in counts), (w.name, counts)
+
+
+def _fwd_ex(lib, cfg, T=4, ptr=256, **fields):
+    P = ctypes.c_void_p
+    a = binding.ForwardArgs()
+    for n in ("hidden_states", "router_logits", "w13_weight", "w2_weight", "output", "workspace"):
+        setattr(a, n, ptr)
+    a.workspace_bytes = 1 << 40
+    for n, v in fields.items():
+        setattr(a, n, v)
+    return lib.moe_forward_ex(ctypes.byref(cfg), T, ctypes.byref(a), None)
+
+
+def test_fp8_validation(lib):
+    fp8 = dict(weight_quant="fp8", hidden_size=256)
+    scales = dict(w13_scale=256, w2_scale=256)
+    # the fp8 layer is the plain gated SiLU one, H a multiple of 256
+    assert _fwd_ex(lib, _cfg(weight_quant="fp8"), **scales) == binding.ERR_UNSUPPORTED  # H 128
+    assert _fwd_ex(lib, _cfg(swiglu_limit=7.0, **fp8), **scales) == binding.ERR_UNSUPPORTED
+    assert _fwd_ex(lib, _cfg(gemm1_alpha=1.5, **fp8), **scales) == binding.ERR_UNSUPPORTED
+    assert _fwd_ex(lib, _cfg(is_act_and_mul=0, **fp8), **scales) == binding.ERR_UNSUPPORTED
+    assert _fwd_ex(lib, _cfg(apply_router_weight_on_input=True, **fp8),
+                   **scales) == binding.ERR_UNSUPPORTED
+    assert _fwd_ex(lib, _cfg(**fp8), w13_bias=256, **scales) == binding.ERR_UNSUPPORTED
+    assert _fwd_ex(lib, _cfg(weight_quant=7)) == binding.ERR_INVALID_ARG
+    # scales: required with fp8 weights, rejected without
+    assert _fwd_ex(lib, _cfg(**fp8), w13_scale=256) == binding.ERR_INVALID_ARG
+    assert _fwd_ex(lib, _cfg(hidden_size=256), **scales) == binding.ERR_INVALID_ARG
+    ok = _cfg(**fp8)
+    need = lib.moe_forward_workspace_size(ctypes.byref(ok), 4)
+    assert need > 0 and _fwd_ex(lib, ok, workspace_bytes=need - 1, **scales) == \
+        binding.ERR_WORKSPACE
+    assert _fwd_ex(lib, ok, T=0, **scales) == binding.OK
+    lay = binding.moe_forward_workspace_layout(ok, 4)
+    assert lay.act_scale > lay.act and lay.act_scale % 256 == 0
+    assert binding.moe_forward_workspace_layout(_cfg(hidden_size=256), 4).act_scale == 0
+    # the standalone quant
+    q = lib.moe_quant_fp8_per_token_group
+    P = ctypes.c_void_p
+    assert q(4, 100, P(256), P(256), P(256), None) == binding.ERR_INVALID_ARG    # H % 128
+    assert q(4, 128, P(258), P(256), P(256), None) == binding.ERR_INVALID_ARG    # x alignment
+    assert q(-1, 128, P(256), P(256), P(256), None) == binding.ERR_INVALID_ARG
+    assert q(0, 128, None, None, None, None) == binding.OK
+
+
+def test_fp8_workspace_fits_regions(lib):
+    """The fp8 rows + scales fit the bf16-sized regions for every workload and batch size,
+    including the smallest shared expert (T = 1, I_s = 128)."""
+    for w in configs.WORKLOADS.values():
+        if w.hidden_size % 256:
+            continue
+        cfg = binding.config_from_workload(w, weight_quant="fp8")
+        for T in (1, 2, 16, 300, 4096):
+            lay = binding.moe_forward_workspace_layout(cfg, T)
+            bf16 = binding.moe_forward_workspace_layout(binding.config_from_workload(w), T)
+            assert lay.total >= bf16.total and lay.act_scale > lay.act
+    tiny = _cfg(weight_quant="fp8", hidden_size=256, shared_intermediate_size=128)
+    assert lib.moe_forward_workspace_size(ctypes.byref(tiny), 1) > 0
