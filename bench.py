@@ -61,32 +61,39 @@ def aggregate_tokens_per_s(tokens_per_rank: int, world: int, ms_max: float) -> f
     return tokens_per_rank * world / (ms_max / 1e3)
 
 
-def layer_work(w, T: int, n_active: int) -> dict:
-    """Algorithmic flops and bytes of one forward (no padding rows)."""
+def layer_work(w, T: int, n_active: int, fp8: bool = False) -> dict:
+    """Algorithmic flops and bytes of one forward (no padding rows).
+
+    bf16: weights, gathered rows and act 2 bytes per element. fp8 (w8a8, block 128):
+    weights, gathered rows and act 1 byte per element plus one fp32 scale per 128 x 128
+    weight block and per 128-element activation group.
+    """
     H, I, k, E, Is = w.hidden_size, w.intermediate_size, w.top_k, w.num_experts, \
         w.shared_intermediate_size
+    wb = 1.0 + 4.0 / (128 * 128) if fp8 else 2.0        # bytes per weight element
+    ab = 1.0 + 4.0 / 128 if fp8 else 2.0                # bytes per activation element
     flops_w13 = 4.0 * T * k * H * I + 4.0 * T * H * Is
     flops_w2 = 2.0 * T * k * H * I + 2.0 * T * H * Is
-    w13_bytes = n_active * 2 * I * H * 2 + 2 * Is * H * 2
-    w2_bytes = n_active * H * I * 2 + H * Is * 2
-    act_bytes = T * k * I * 2 + T * Is * 2
+    w13_bytes = (n_active * 2 * I * H + 2 * Is * H) * wb
+    w2_bytes = (n_active * H * I + H * Is) * wb
+    act_bytes = (T * k * I + T * Is) * ab
     bytes_total = (w13_bytes + w2_bytes + T * H * 2 * 2 + T * E * 4 + T * k * 8
                    + 2 * act_bytes)
     return {"flops": flops_w13 + flops_w2, "flops_w13": flops_w13, "flops_w2": flops_w2,
             "bytes": float(bytes_total),
-            "bytes_w13": float(w13_bytes + T * k * H * 2 + act_bytes),
-            "bytes_w2": float(w2_bytes + act_bytes + T * k * H * 2)}
+            "bytes_w13": float(w13_bytes + T * k * H * ab + act_bytes),
+            "bytes_w2": float(w2_bytes + act_bytes + T * k * H * 4)}
 
 
-def kernel_traffic(kernel: str, workload: str, tokens: int):
+def kernel_traffic(kernel: str, workload: str, tokens: int, source: str = "gemm.cu"):
     """DRAM bytes per launch of `kernel` from a committed ncu summary, if it was captured on
-    this workload with the current kernel source (sha1 of csrc/gemm.cu); else None.
+    this workload with the current kernel source (sha1 of csrc/<source>); else None.
 
     A summary states it on a line `traffic: <kernel> <workload> <tokens> <bytes> <sha1>`.
     """
     import glob
     import hashlib
-    src = os.path.join(ROOT, "mixture_experts_layer_05_gb300", "csrc", "gemm.cu")
+    src = os.path.join(ROOT, "mixture_experts_layer_05_gb300", "csrc", source)
     try:
         with open(src, "rb") as f:
             sha = hashlib.sha1(f.read()).hexdigest()
@@ -181,12 +188,21 @@ def run_ours(args, w, T):
     build_mod.build()
     binding.load()
 
-    wts = inputs.make_weights(w, 0, device=dev)
+    fp8 = args.quant == "fp8"
     x_cpu, logits_cpu = inputs.make_tokens(w, T, seed=rank_seed(rank))
     x, logits = x_cpu.to(dev), logits_cpu.to(dev)
-    cfg = binding.config_from_workload(w)
-    layer = binding.FusedMoE(cfg, wts["w13"], wts["w2"], wts["bias"], wts["shared_w13"],
-                             wts["shared_w2"], max_tokens=T)
+    if fp8:
+        wts = inputs.make_fp8_weights(w, 0, device=dev)
+        cfg = binding.config_from_workload(w, weight_quant="fp8")
+        layer = binding.FusedMoE(cfg, wts["w13_q"], wts["w2_q"], wts["bias"], wts["shared_w13_q"],
+                                 wts["shared_w2_q"], max_tokens=T, w13_scale=wts["w13_s"],
+                                 w2_scale=wts["w2_s"], shared_w13_scale=wts["shared_w13_s"],
+                                 shared_w2_scale=wts["shared_w2_s"])
+    else:
+        wts = inputs.make_weights(w, 0, device=dev)
+        cfg = binding.config_from_workload(w)
+        layer = binding.FusedMoE(cfg, wts["w13"], wts["w2"], wts["bias"], wts["shared_w13"],
+                                 wts["shared_w2"], max_tokens=T)
     out = torch.empty_like(x)
     stream = torch.cuda.current_stream()
     K, W = args.steps, args.warmup
@@ -297,42 +313,50 @@ def run_ours(args, w, T):
     n_active = int(torch.unique(ids).numel())
     npp = int(layer.workspace[lay.num_tokens_post_padded:lay.num_tokens_post_padded + 4]
               .view(torch.int32).item())
-    work = layer_work(w, T, n_active)
+    work = layer_work(w, T, n_active, fp8)
     peaks, peak_src = load_peaks()
+    # the e4m3 tensor peak: the measured bf16 peak times the nominal dense ratio 4.5 / 2.25
+    tc_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    tc_src = f"{peak_src} bf16 (burst) x 2, the nominal e4m3/bf16 ratio" if fp8 else \
+        f"{peak_src} (burst)"
+    kname = ("gemm_fp8_kernel<w13> (grouped e4m3 w13 GEMM + SiLU*mul + act quant)" if fp8
+             else "gemm_kernel<w13> (grouped w13 GEMM + SiLU*mul)")
     value = aggregate_tokens_per_s(T, world, ms_max)
 
     res = None
     if rank == 0:
         # dominant kernel: the w13 grouped GEMM (two thirds of the flops and weight bytes)
         t_w13 = w13_ms / 1e3
-        tensor_bound = work["flops_w13"] / (peaks["bf16_tflops"] * 1e12) >= \
+        tensor_bound = work["flops_w13"] / (tc_peak * 1e12) >= \
             work["bytes_w13"] / (peaks["hbm_gbs"] * 1e9)
         if tensor_bound:
             ach = work["flops_w13"] / t_w13 / 1e12
-            roof = {"kernel": "gemm_kernel<w13> (grouped w13 GEMM + SiLU*mul)", "bound": "tensor",
-                    "achieved": round(ach, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": round(ach / peaks["bf16_tflops"], 4)}
+            roof = {"kernel": kname, "bound": "tensor", "achieved": round(ach, 1),
+                    "peak": round(tc_peak, 1), "unit": "TFLOP/s", "frac": round(ach / tc_peak, 4),
+                    "peak_source": tc_src}
         else:
             ach = work["bytes_w13"] / t_w13 / 1e9
-            roof = {"kernel": "gemm_kernel<w13> (grouped w13 GEMM + SiLU*mul)", "bound": "hbm",
-                    "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(ach / peaks["hbm_gbs"], 4)}
-        roof["peak_source"] = f"{peak_src} (burst)"
-        roof["traffic"] = args.traffic if args.traffic is not None else \
-            kernel_traffic("gemm_w13", w.name, T)
+            roof = {"kernel": kname, "bound": "hbm", "achieved": round(ach, 1),
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src}"}
+        roof["traffic"] = args.traffic if args.traffic is not None else (
+            kernel_traffic("gemm_fp8_w13", w.name, T, "gemm_fp8.cu") if fp8
+            else kernel_traffic("gemm_w13", w.name, T))
         step_s = ms_max / 1e3
         res = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+            "data": "synthetic",
             "config": {"workload": f"{w.name}: FusedMoE layer H={w.hidden_size} "
-                                   f"I={w.intermediate_size} E={w.num_experts} k={w.top_k}",
+                                   f"I={w.intermediate_size} E={w.num_experts} k={w.top_k}"
+                                   + (" w8a8 fp8 block-128" if fp8 else ""),
                        "tokens_per_gpu": T, "global_batch": T * world,
                        "parallelism": f"dp{world} replicas",
                        "l2": "inputs larger than L2 (expert weights streamed every step)",
                        "seed": "weights 0, tokens = rank"},
             "layer": {"tflops": round(work["flops"] / step_s / 1e12, 1),
-                      "tflops_frac": round(work["flops"] / step_s / 1e12 / peaks["bf16_tflops"], 4),
+                      "tflops_frac": round(work["flops"] / step_s / 1e12 / tc_peak, 4),
                       "hbm_gbs": round(work["bytes"] / step_s / 1e9, 1),
                       "hbm_frac": round(work["bytes"] / step_s / 1e9 / peaks["hbm_gbs"], 4),
                       "active_experts": n_active, "rows_post_padded": npp,
@@ -350,7 +374,7 @@ def run_ours(args, w, T):
             "clocks": clocks,
         }
         if args.cpu_baseline and world == 1:
-            res["cpu_baseline"] = cpu_baseline(w, wts, x_cpu, logits_cpu, args.cpu_sample)
+            res["cpu_baseline"] = cpu_baseline(w, wts, x_cpu, logits_cpu, args.cpu_sample, fp8=fp8)
     return res
 
 
@@ -366,23 +390,33 @@ def oracle_cfg(w):
                 routed_scaling_factor=w.routed_scaling_factor)
 
 
-def _oracle_rows(w, hw, x_cpu, logits_cpu, r0, n):
+def _oracle_layer(w, hw, x, logits, fp8: bool):
     import oracle
+    if fp8:
+        oracle.fused_moe_fp8(x, logits, hw["bias"], hw["w13_q"], hw["w13_s"], hw["w2_q"],
+                             hw["w2_s"], hw["shared_w13_q"], hw["shared_w13_s"],
+                             hw["shared_w2_q"], hw["shared_w2_s"], **oracle_cfg(w))
+    else:
+        oracle.fused_moe_rows(x, logits, hw["bias"], hw["w13"], hw["w2"], hw["shared_w13"],
+                              hw["shared_w2"], **oracle_cfg(w))
+
+
+def _oracle_rows(w, hw, x_cpu, logits_cpu, r0, n, fp8=False):
     t0 = time.perf_counter()
-    oracle.fused_moe_rows(x_cpu[r0:r0 + n], logits_cpu[r0:r0 + n], hw["bias"], hw["w13"],
-                          hw["w2"], hw["shared_w13"], hw["shared_w2"], **oracle_cfg(w))
+    _oracle_layer(w, hw, x_cpu[r0:r0 + n], logits_cpu[r0:r0 + n], fp8)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(w, wts, x_cpu, logits_cpu, n_tokens: int, target_s: float = 12.0) -> dict:
+def cpu_baseline(w, wts, x_cpu, logits_cpu, n_tokens: int, target_s: float = 12.0,
+                 fp8: bool = False) -> dict:
     """The CPU oracle, as it stands, on a leading sample of the batch sized to ~target_s."""
     hw = _host_weights(w, wts)
     T = x_cpu.shape[0]
     n = min(n_tokens, T)
-    dt = _oracle_rows(w, hw, x_cpu, logits_cpu, 0, n)
+    dt = _oracle_rows(w, hw, x_cpu, logits_cpu, 0, n, fp8)
     if dt < target_s / 4 and n < T:                 # grow the sample to ~target_s of work
         n = int(min(T, max(n + 1, n * target_s / max(dt, 1e-3))))
-        dt = _oracle_rows(w, hw, x_cpu, logits_cpu, 0, n)
+        dt = _oracle_rows(w, hw, x_cpu, logits_cpu, 0, n, fp8)
     return {"value": round(n / dt, 4), "unit": "tokens/s",
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
             "sample": f"first {n} of the step's {T} tokens, full weights, fp64 numpy "
@@ -400,13 +434,14 @@ def run_reference(args, w, T):
     if rank != 0:
         return None
     n = args.ref_sample if args.ref_sample > 0 else 1
-    hw = inputs.make_weights(w, 0)           # CPU-generated: the oracle arm needs no GPU
+    fp8 = args.quant == "fp8"
+    # CPU-generated: the oracle arm needs no GPU
+    hw = inputs.make_fp8_weights(w, 0) if fp8 else inputs.make_weights(w, 0)
     x_cpu, logits_cpu = inputs.make_tokens(w, T, seed=0)
 
     def step(i):
         r0 = (i * n) % max(T - n + 1, 1)
-        oracle.fused_moe_rows(x_cpu[r0:r0 + n], logits_cpu[r0:r0 + n], hw["bias"], hw["w13"],
-                              hw["w2"], hw["shared_w13"], hw["shared_w2"], **oracle_cfg(w))
+        _oracle_layer(w, hw, x_cpu[r0:r0 + n], logits_cpu[r0:r0 + n], fp8)
 
     # size each step's sample so one step is ~1.5 s of oracle work (the whole run then
     # stays within a few minutes for the usual K, W)
@@ -429,7 +464,8 @@ def run_reference(args, w, T):
             "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": f"{w.name}: FusedMoE layer H={w.hidden_size} "
-                                   f"I={w.intermediate_size} E={w.num_experts} k={w.top_k}",
+                                   f"I={w.intermediate_size} E={w.num_experts} k={w.top_k}"
+                                   + (" w8a8 fp8 block-128" if fp8 else ""),
                        "tokens_per_gpu": T, "sample_tokens_per_step": n},
             "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
@@ -445,6 +481,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral")
     ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--quant", choices=["none", "fp8"], default="none",
+                    help="expert weights: bf16 (none) or e4m3 with 128 x 128 fp32 block scales")
     ap.add_argument("--cpu-sample", type=int, default=4,
                     help="initial oracle sample (tokens); grown to ~12 s of CPU work")
     ap.add_argument("--ref-sample", type=int, default=0,

@@ -63,6 +63,13 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// wait_bounded with the first try inline (the common case: the phase has completed).
+__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bounded(bar, parity, abort_flag, status);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
