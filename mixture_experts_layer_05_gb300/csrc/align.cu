@@ -25,6 +25,8 @@ namespace gbmoe {
 __global__ void __launch_bounds__(256) align_count_kernel(const int* __restrict__ ids, int n,
                                                           int E, int* __restrict__ counts,
                                                           int* status) {
+  pdl_trigger();  // the next kernel may start its launch now
+  pdl_wait();     // inputs written by the previous kernel are visible
   extern __shared__ int sc[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) sc[e] = 0;
   __syncthreads();
@@ -50,6 +52,8 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(const int* __restrict_
                                                           int* __restrict__ expert_ids,
                                                           int max_blocks, int* __restrict__ npp,
                                                           int2* __restrict__ block_seg) {
+  pdl_trigger();  // the next kernel may start its launch now
+  pdl_wait();     // inputs written by the previous kernel are visible
   __shared__ int warp_tot[32];
   __shared__ int s_total;
   const int e = threadIdx.x;
@@ -107,6 +111,8 @@ constexpr int kSliceLen = kAlignChunk / kScatterWarps;
 __global__ void __launch_bounds__(kScatterWarps * 32)
     align_scatter_kernel(const int* __restrict__ ids, int n, int E, const int* __restrict__ offs,
                          int* __restrict__ sorted, int* __restrict__ inv) {
+  pdl_trigger();  // the next kernel may start its launch now
+  pdl_wait();     // inputs written by the previous kernel are visible
   extern __shared__ int wcnt[];  // [kScatterWarps][E]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int* cnt = wcnt + warp * E;
@@ -173,6 +179,8 @@ __global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restric
                                                           int k, int max_rows,
                                                           const float* __restrict__ row_scale,
                                                           uint4* __restrict__ xp) {
+  pdl_trigger();  // the next kernel may start its launch now
+  pdl_wait();     // inputs written by the previous kernel are visible
   for (int f = blockIdx.x; f < n; f += gridDim.x) {
     const int p = inv[f];
     if (p < 0 || p >= max_rows) continue;
@@ -211,6 +219,8 @@ __global__ void __launch_bounds__(kSmallThreads)
                              int2* __restrict__ block_seg, int* __restrict__ inv,
                              const uint4* __restrict__ x, int H8, uint4* __restrict__ xp,
                              const float* __restrict__ row_scale) {
+  pdl_trigger();  // the next kernel may start its launch now
+  pdl_wait();     // inputs written by the previous kernel are visible
   extern __shared__ int sm[];
   const int n = a.T * a.k, E = a.E;
   int* s_ids = sm;                                   // [n]
@@ -356,8 +366,8 @@ struct RouteAlignSmall {
   void operator()() {
     const int n = a.T * a.k;
     const size_t shm = (size_t)(((n + 31) & ~31) + kSmallWarps * a.E) * sizeof(int);
-    route_align_small_kernel<EPT><<<1, kSmallThreads, shm, stream>>>(
-        a, bs, sorted, expert_ids, max_blocks, npp, block_seg, inv, x, H8, xp, row_scale);
+    launch_kernel(route_align_small_kernel<EPT>, dim3(1), dim3(kSmallThreads), shm, stream, a, bs,
+                  sorted, expert_ids, max_blocks, npp, block_seg, inv, x, H8, xp, row_scale);
   }
 };
 
@@ -395,12 +405,13 @@ cudaError_t launch_align(const int* ids, int n, int E, int bs, int* sorted, int*
   int* counts = static_cast<int*>(scratch);
   int* offs = counts + (size_t)C * E;
   const size_t shm = (size_t)E * sizeof(int);
-  if (C > 0) align_count_kernel<<<C, 256, shm, stream>>>(ids, n, E, counts, status);
-  align_scan_kernel<<<1, 1024, 0, stream>>>(counts, C, E, bs, n, offs, sorted, expert_ids,
-                                            max_blocks, npp, block_seg);
+  if (C > 0) launch_kernel(align_count_kernel, dim3(C), dim3(256), shm, stream, ids, n, E, counts,
+                           status);
+  launch_kernel(align_scan_kernel, dim3(1), dim3(1024), 0, stream, counts, C, E, bs, n, offs, sorted,
+                expert_ids, max_blocks, npp, block_seg);
   if (C > 0)
-    align_scatter_kernel<<<C, kScatterWarps * 32, shm * kScatterWarps, stream>>>(ids, n, E, offs,
-                                                                              sorted, inv);
+    launch_kernel(align_scatter_kernel, dim3(C), dim3(kScatterWarps * 32), shm * kScatterWarps,
+                  stream, ids, n, E, offs, sorted, inv);
   return cudaGetLastError();
 }
 
@@ -409,9 +420,9 @@ cudaError_t launch_gather(const void* x, int H, const int* inv, int n, int k, in
   int blocks = num_sms() * 8;
   if (blocks > n) blocks = n;
   if (blocks < 1) return cudaSuccess;
-  gather_rows_kernel<<<blocks, 128, 0, stream>>>(static_cast<const uint4*>(x), H / 8, inv, n, k,
-                                                  max_rows, row_scale,
-                                                  static_cast<uint4*>(x_perm));
+  launch_kernel(gather_rows_kernel, dim3(blocks), dim3(128), 0, stream,
+                static_cast<const uint4*>(x), H / 8, inv, n, k, max_rows, row_scale,
+                static_cast<uint4*>(x_perm));
   return cudaGetLastError();
 }
 

@@ -80,6 +80,7 @@ GBMOE_API gbmoe_status_t moe_align_block_size_no_workspace(
   if (scratch_address(&scratch) != cudaSuccess) return GBMOE_ERR_CUDA;
   const int max_sorted = n + num_experts * (block_size - 1);
   const int max_blocks = max_sorted / block_size + 1;
+  PdlChain chain;
   return launch_align(topk_ids, n, num_experts, block_size, sorted_token_ids, expert_ids,
                       max_blocks, num_tokens_post_padded, scratch, nullptr,
                       (cudaStream_t)stream) == cudaSuccess

@@ -14,6 +14,11 @@
 
 namespace gbmoe {
 
+bool& pdl_next() {
+  static thread_local bool next = false;
+  return next;
+}
+
 int num_sms() {
   static int cached[64] = {0};
   int dev = 0;
@@ -31,7 +36,10 @@ namespace {
 
 constexpr int kMaxTokens = 1 << 22;
 constexpr int kSplitMaxTokens = 64;  // split-K only at decode-sized batches
-constexpr size_t kMaxSplits = 8;
+#ifndef GBMOE_MAX_SPLITS
+#define GBMOE_MAX_SPLITS 8
+#endif
+constexpr size_t kMaxSplits = GBMOE_MAX_SPLITS;  // largest split-K factor
 constexpr size_t kAlign = 256;
 
 size_t up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
@@ -258,6 +266,7 @@ GBMOE_API gbmoe_status_t moe_topk(const gbmoe_config_t* cfg, int32_t num_tokens,
   if (num_tokens < 0 || num_tokens > kMaxTokens) return GBMOE_ERR_INVALID_ARG;
   if (num_tokens == 0) return GBMOE_OK;
   if (!router_logits || !topk_weights || !topk_ids) return GBMOE_ERR_INVALID_ARG;
+  PdlChain chain;
   return cuda_status(launch_topk(*cfg, num_tokens, router_logits, e_score_correction_bias,
                                  topk_weights, topk_ids, nullptr, (cudaStream_t)stream));
 }
@@ -286,6 +295,7 @@ GBMOE_API gbmoe_status_t moe_align_block_size(const int32_t* topk_ids, int32_t n
   const int n = num_tokens * top_k;
   const int max_sorted = n + num_experts * (block_size - 1);
   const int max_blocks = max_sorted / block_size + 1;
+  PdlChain chain;
   return cuda_status(launch_align(topk_ids, n, num_experts, block_size, sorted_token_ids,
                                   expert_ids, max_blocks, num_tokens_post_padded,
                                   at<char>(workspace, kAlign), at<int>(workspace, 0),
@@ -370,6 +380,7 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
   cudaStream_t stream = (cudaStream_t)stream_;
   const int T = num_tokens, E = c.num_experts, k = c.top_k, H = c.hidden_size,
             I = c.intermediate_size;
+  PdlChain chain;  // the forward's kernels overlap their predecessors' tails
   int* status = at<int>(workspace, L.status);
   float* tw = at<float>(workspace, L.topk_weights);
   int* tids = at<int>(workspace, L.topk_ids);
@@ -386,6 +397,7 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
   if (events && cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return GBMOE_ERR_CUDA;
   auto rec = [&](int i) -> cudaError_t {
     if (!events || !events[i]) return cudaSuccess;
+    pdl_next() = false;  // the kernel after a stage event starts after it
     return cap == cudaStreamCaptureStatusActive
                ? cudaEventRecordWithFlags((cudaEvent_t)events[i], stream, cudaEventRecordExternal)
                : cudaEventRecord((cudaEvent_t)events[i], stream);
@@ -806,6 +818,7 @@ GBMOE_API gbmoe_status_t moe_router_logits(int32_t num_tokens, int32_t hidden_si
   P.out = router_logits;
   P.ldo = E;
   P.store_rows = T;
+  PdlChain chain;
   return cuda_status(launch_gemm(kGemmRouter, kGemmBM, gr, (cudaStream_t)stream, false, T));
 }
 
@@ -818,6 +831,7 @@ GBMOE_API gbmoe_status_t moe_quant_fp8_per_token_group(int32_t num_rows, int32_t
   if (!x || !q || !scale || !aligned16(x) || !aligned16(q) ||
       (reinterpret_cast<uintptr_t>(scale) & 3u))
     return GBMOE_ERR_INVALID_ARG;
+  PdlChain chain;
   return cuda_status(
       launch_quant_fp8(x, num_rows, hidden_size, q, scale, num_rows, (cudaStream_t)stream));
 }

@@ -15,6 +15,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
                                                       int splits_last,
                                                       long long split_stride4,
                                                       uint4* __restrict__ y) {
+  pdl_trigger();  // the next kernel may start its launch now
+  pdl_wait();     // inputs written by the previous kernel are visible
   const size_t total = (size_t)T * H8;
   const int copies = splits > splits_last ? splits : splits_last;
   const int terms = copies * slots;
@@ -63,6 +65,8 @@ __global__ void __launch_bounds__(256) combine_small_kernel(const float4* __rest
                                                             int T, int splits, int splits_last,
                                                             long long split_stride4,
                                                             uint4* __restrict__ y) {
+  pdl_trigger();  // the next kernel may start its launch now
+  pdl_wait();     // inputs written by the previous kernel are visible
   const size_t groups = (size_t)T * H8;
   const int lane8 = threadIdx.x & (kTermLanes - 1);
   const int copies = splits > splits_last ? splits : splits_last;
@@ -77,13 +81,24 @@ __global__ void __launch_bounds__(256) combine_small_kernel(const float4* __rest
     const size_t t = g / H8, h = g % H8;
     const float4* row = ytok + (t * slots * H8 + h) * 2;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-    for (int i = lane8; valid && i < terms; i += kTermLanes) {
-      const int c = i / slots, sl = i % slots;
-      if (c < (sl < routed_slots ? splits : splits_last)) {
-        const float4* src = row + (size_t)c * split_stride4 + (size_t)sl * H8 * 2;
-        const float4 u = __ldg(src), v = __ldg(src + 1);
-        a.x += u.x; a.y += u.y; a.z += u.z; a.w += u.w;
-        b.x += v.x; b.y += v.y; b.z += v.z; b.w += v.w;
+    // this lane's terms in increasing order, four loads issued before their adds
+    for (int i0 = lane8; valid && i0 < terms; i0 += 4 * kTermLanes) {
+      float4 u[4], v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = i0 + q * kTermLanes;
+        const int c = i / slots, sl = i % slots;
+        u[q] = v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < terms && c < (sl < routed_slots ? splits : splits_last)) {
+          const float4* src = row + (size_t)c * split_stride4 + (size_t)sl * H8 * 2;
+          u[q] = __ldg(src);
+          v[q] = __ldg(src + 1);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        a.x += u[q].x; a.y += u[q].y; a.z += u[q].z; a.w += u[q].w;
+        b.x += v[q].x; b.y += v[q].y; b.z += v[q].z; b.w += v[q].w;
       }
     }
 #pragma unroll
@@ -116,9 +131,9 @@ cudaError_t launch_combine(const void* ytok, int slots, int routed_slots, int H,
     const size_t threads_needed = total * kTermLanes;
     size_t blocks = (threads_needed + 255) / 256;
     if (blocks < 1) blocks = 1;
-    combine_small_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-        static_cast<const float4*>(ytok), slots, routed_slots, H / 8, T, splits, splits_last,
-        split_stride / 4, static_cast<uint4*>(y));
+    launch_kernel(combine_small_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                  static_cast<const float4*>(ytok), slots, routed_slots, H / 8, T, splits,
+                  splits_last, split_stride / 4, static_cast<uint4*>(y));
     return cudaGetLastError();
   }
   const int threads = total < (size_t)num_sms() * 256 ? 64 : 256;  // spread small T over SMs
@@ -126,9 +141,9 @@ cudaError_t launch_combine(const void* ytok, int slots, int routed_slots, int H,
   const size_t cap = (size_t)num_sms() * (2048 / threads);
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  combine_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
-      static_cast<const float4*>(ytok), slots, routed_slots, H / 8, T, splits, splits_last,
-      split_stride / 4, static_cast<uint4*>(y));
+  launch_kernel(combine_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                static_cast<const float4*>(ytok), slots, routed_slots, H / 8, T, splits,
+                splits_last, split_stride / 4, static_cast<uint4*>(y));
   return cudaGetLastError();
 }
 

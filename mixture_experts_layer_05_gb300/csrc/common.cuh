@@ -14,6 +14,17 @@ namespace gbmoe {
 // in these kernels last microseconds.
 constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;
 
+// Programmatic dependent launch. A kernel launched with programmatic stream serialization
+// (launch_kernel below, inside one forward) may start while the kernel before it in the
+// stream is still running: pdl_wait() blocks until that kernel has completed and its
+// writes are visible (a no-op for an ordinary launch), and pdl_trigger() lets the next
+// kernel begin launching. Every kernel calls pdl_wait() before it reads anything an
+// earlier kernel of the stream wrote.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void record_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }

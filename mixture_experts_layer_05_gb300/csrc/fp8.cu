@@ -36,6 +36,8 @@ __device__ __forceinline__ GroupQ quant_group_warp(const __nv_bfloat16* src, int
 __global__ void __launch_bounds__(256) quant_fp8_kernel(const __nv_bfloat16* __restrict__ x,
                                                         int rows, int H, uint8_t* __restrict__ q,
                                                         float* __restrict__ s_out, int s_ld) {
+  pdl_trigger();  // the next kernel may start its launch now
+  pdl_wait();     // inputs written by the previous kernel are visible
   const int lane = threadIdx.x & 31;
   const int groups = H / kFp8Block;
   const long long items = (long long)rows * groups;
@@ -55,6 +57,8 @@ __global__ void __launch_bounds__(256)
                             const int* __restrict__ inv, int k, int T, int max_rows,
                             uint8_t* __restrict__ xp, float* __restrict__ xs_perm, int perm_ld,
                             uint8_t* __restrict__ xq_tok, float* __restrict__ xs_tok) {
+  pdl_trigger();  // the next kernel may start its launch now
+  pdl_wait();     // inputs written by the previous kernel are visible
   const int lane = threadIdx.x & 31;
   const int groups = H / kFp8Block;
   const long long items = (long long)T * groups;
@@ -82,6 +86,8 @@ __global__ void __launch_bounds__(256)
 // its amax with four xor-shuffles. Every lane runs every step (shuffles stay converged).
 __global__ void __launch_bounds__(128) silu_reduce_fp8_kernel(const GemmLaunch L, const int* npp,
                                                               int max_routed_rows) {
+  pdl_trigger();  // the next kernel may start its launch now
+  pdl_wait();     // inputs written by the previous kernel are visible
   const GemmProblem& R = L.p[0];
   int routed_rows = npp ? *npp : R.m_rows_host;
   if (routed_rows > max_routed_rows) routed_rows = max_routed_rows;
@@ -157,8 +163,9 @@ cudaError_t launch_quant_fp8(const void* x, int rows, int H, uint8_t* q, float* 
                              cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
   if (H % kFp8Block) return cudaErrorInvalidValue;
-  quant_fp8_kernel<<<grid_for_warps((long long)rows * (H / kFp8Block)), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(x), rows, H, q, s_out, s_ld);
+  launch_kernel(quant_fp8_kernel, dim3(grid_for_warps((long long)rows * (H / kFp8Block))),
+                dim3(256), 0, stream, static_cast<const __nv_bfloat16*>(x), rows, H, q, s_out,
+                s_ld);
   return cudaGetLastError();
 }
 
@@ -167,9 +174,9 @@ cudaError_t launch_quant_gather_fp8(const void* x, int H, const int* inv, int n,
                                     uint8_t* xq_tok, float* xs_tok, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
   if (H % kFp8Block || n != T * k) return cudaErrorInvalidValue;
-  quant_gather_fp8_kernel<<<grid_for_warps((long long)T * (H / kFp8Block)), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(x), H, inv, k, T, perm_ld, x_perm_q, xs_perm, perm_ld,
-      xq_tok, xs_tok);
+  launch_kernel(quant_gather_fp8_kernel, dim3(grid_for_warps((long long)T * (H / kFp8Block))),
+                dim3(256), 0, stream, static_cast<const __nv_bfloat16*>(x), H, inv, k, T, perm_ld,
+                x_perm_q, xs_perm, perm_ld, xq_tok, xs_tok);
   return cudaGetLastError();
 }
 
@@ -179,7 +186,7 @@ cudaError_t launch_silu_reduce_fp8(const GemmLaunch& L, const int* npp, int max_
   int grid = num_sms() * 4;
   if (rows < grid) grid = rows;
   if (grid < 1) return cudaSuccess;
-  silu_reduce_fp8_kernel<<<grid, 128, 0, stream>>>(L, npp, max_routed_rows);
+  launch_kernel(silu_reduce_fp8_kernel, dim3(grid), dim3(128), 0, stream, L, npp, max_routed_rows);
   return cudaGetLastError();
 }
 

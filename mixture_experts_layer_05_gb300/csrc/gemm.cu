@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                 const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                 const GemmLaunch args) {
+  if (threadIdx.x == 0) pdl_trigger();
   using S = Shape<KIND, BN, AROWS>;
   constexpr int kStages = S::kNumStages;
   extern __shared__ uint8_t smem_raw[];
@@ -117,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the set-up above overlapped the previous kernel; its outputs are now visible
 
   Schedule sched;
   sched.init(args);
@@ -607,6 +609,8 @@ __global__ void wait_selftest_kernel(int* status, unsigned long long timeout_ns)
 // act = silu(sum_s gate_s) * sum_s up_s, one CTA per output row, 8 columns per step.
 __global__ void __launch_bounds__(128) silu_reduce_kernel(const GemmLaunch L, const int* npp,
                                                           int max_routed_rows, int gated) {
+  pdl_trigger();  // the next kernel may start its launch now
+  pdl_wait();     // inputs written by the previous kernel are visible
   const GemmProblem& R = L.p[0];
   int routed_rows = npp ? *npp : R.m_rows_host;
   if (routed_rows > max_routed_rows) routed_rows = max_routed_rows;
@@ -702,9 +706,8 @@ cudaError_t launch_typed(const CUtensorMap* tm, const GemmLaunch& args, int grid
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  gemm_kernel<KIND, BN, AROWS>
-      <<<grid, kThreads, S::kSmem, stream>>>(tm[0], tm[1], tm[2], tm[3], args);
-  return cudaGetLastError();
+  return launch_kernel(gemm_kernel<KIND, BN, AROWS>, dim3(grid), dim3(kThreads), S::kSmem, stream,
+                       tm[0], tm[1], tm[2], tm[3], args);
 }
 
 template <int AROWS>
@@ -744,7 +747,10 @@ cudaError_t launch_pair_typed(const CUtensorMap* tm, const GemmLaunch& args, int
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<KIND>, tm[0], tm[1], tm[2], tm[3], args);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<KIND>, tm[0], tm[1], tm[2],
+                                           tm[3], args);
+  pdl_next() = true;
+  return e;
 }
 
 }  // namespace
@@ -795,8 +801,8 @@ cudaError_t launch_silu_reduce(const GemmLaunch& L, const int* npp, int max_rout
   int grid = num_sms() * 4;
   if (rows < grid) grid = rows;
   if (grid < 1) return cudaSuccess;
-  silu_reduce_kernel<<<grid, 128, 0, stream>>>(L, npp, max_routed_rows, gated ? 1 : 0);
-  return cudaGetLastError();
+  return launch_kernel(silu_reduce_kernel, dim3(grid), dim3(128), 0, stream, L, npp,
+                       max_routed_rows, gated ? 1 : 0);
 }
 
 }  // namespace gbmoe

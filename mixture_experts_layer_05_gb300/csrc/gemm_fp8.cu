@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmA1,
                     const __grid_constant__ CUtensorMap tmB1, const GemmLaunch args) {
+  if (threadIdx.x == 0) pdl_trigger();
   constexpr int kStages = kF8Stages;
   constexpr int kBN = KIND == kGemmW13 ? 128 : 256;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
@@ -113,6 +114,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the set-up above overlapped the previous kernel; its outputs are now visible
 
   Schedule sched;
   sched.init(args);
@@ -377,6 +379,7 @@ __global__ void __launch_bounds__(kSwThreads, 1)
                          const __grid_constant__ CUtensorMap tmB0,
                          const __grid_constant__ CUtensorMap tmA1,
                          const __grid_constant__ CUtensorMap tmB1, const GemmLaunch args) {
+  if (threadIdx.x == 0) pdl_trigger();
   constexpr int kStages = kSwStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -425,6 +428,7 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the set-up above overlapped the previous kernel; its outputs are now visible
 
   Schedule sched;
   sched.init(args);
@@ -678,9 +682,8 @@ cudaError_t launch_fp8_swap_typed(const CUtensorMap* tm, const GemmLaunch& args,
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  gemm_fp8_swap_kernel<KIND>
-      <<<grid, kSwThreads, kSwSmem, stream>>>(tm[0], tm[1], tm[2], tm[3], args);
-  return cudaGetLastError();
+  return launch_kernel(gemm_fp8_swap_kernel<KIND>, dim3(grid), dim3(kSwThreads), kSwSmem, stream,
+                       tm[0], tm[1], tm[2], tm[3], args);
 }
 
 template <int KIND>
@@ -696,8 +699,8 @@ cudaError_t launch_fp8_typed(const CUtensorMap* tm, const GemmLaunch& args, int 
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  gemm_fp8_kernel<KIND><<<grid, kF8Threads, kF8Smem, stream>>>(tm[0], tm[1], tm[2], tm[3], args);
-  return cudaGetLastError();
+  return launch_kernel(gemm_fp8_kernel<KIND>, dim3(grid), dim3(kF8Threads), kF8Smem, stream,
+                       tm[0], tm[1], tm[2], tm[3], args);
 }
 
 }  // namespace

@@ -22,6 +22,39 @@ constexpr int kGemmBK = 64;        // K elements per pipeline stage (one 128-byt
 
 int num_sms();
 
+// Whether the next launch_kernel() of this host thread may overlap the kernel before it in
+// the stream (programmatic stream serialization). The forward clears it for its first
+// kernel and after each stage event; every launch sets it for the next one.
+bool& pdl_next();
+
+// One C-ABI call: its first kernel launches normally, the later ones may overlap their
+// predecessor, and nothing carries over to the next call.
+struct PdlChain {
+  PdlChain() { pdl_next() = false; }
+  ~PdlChain() { pdl_next() = false; }
+};
+
+// Launch `k` on `stream`; with pdl_next() set, with programmatic stream serialization.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (pdl_next()) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
+  pdl_next() = true;
+  return e;
+}
+
 // logits may arrive as logit_splits fp32 copies, logit_split_stride floats apart, whose sum
 // is the logit (the split-K router GEMM); 1 = plain logits.
 cudaError_t launch_topk(const gbmoe_config_t& c, int T, const float* logits, const float* bias,

@@ -6,6 +6,8 @@ namespace gbmoe {
 
 template <int EPT>
 __global__ void __launch_bounds__(256) topk_kernel(TopkArgs a) {
+  pdl_trigger();  // the next kernel may start its launch now
+  pdl_wait();     // inputs written by the previous kernel are visible
   const int lane = threadIdx.x & 31;
   const int warps_total = gridDim.x * (blockDim.x >> 5);
   for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < a.T; t += warps_total)
@@ -18,7 +20,7 @@ struct TopkLaunch {
   cudaStream_t stream;
   template <int EPT>
   void operator()() {
-    topk_kernel<EPT><<<blocks, 256, 0, stream>>>(a);
+    launch_kernel(topk_kernel<EPT>, dim3(blocks), dim3(256), 0, stream, a);
   }
 };
 
