@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restric
 // offsets in slice order, and each warp scatters its slice in order (stable).
 constexpr int kSmallWarps = 8;
 constexpr int kSmallThreads = kSmallWarps * 32;
+constexpr int kBlockRouteMaxTokens = 4;  // route token by token with the whole CTA up to here
 
 template <int EPT>
 __global__ void __launch_bounds__(kSmallThreads)
@@ -229,10 +230,20 @@ __global__ void __launch_bounds__(kSmallThreads)
   __shared__ int s_total;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) wcnt[i] = 0;
-  // 1. routing
-  for (int t = warp; t < a.T; t += kSmallWarps) {
-    const int id = route_token_warp<EPT>(a, t, lane);
-    if (lane < a.k) s_ids[t * a.k + lane] = id;
+  // 1. routing: EPT = 0 (the tiniest batches) routes token by token with the whole CTA, in
+  //    compact code (this kernel starts each forward, and its code is fetched cold after the
+  //    expert GEMMs have streamed through L2); else a warp per token
+  if constexpr (EPT == 0) {
+    float* rsm = reinterpret_cast<float*>(wcnt + kSmallWarps * E);
+    for (int t = 0; t < a.T; ++t) {
+      const int id = route_token_block(a, t, rsm);
+      if (threadIdx.x < a.k) s_ids[t * a.k + threadIdx.x] = id;
+    }
+  } else {
+    for (int t = warp; t < a.T; t += kSmallWarps) {
+      const int id = route_token_warp<EPT>(a, t, lane);
+      if (lane < a.k) s_ids[t * a.k + lane] = id;
+    }
   }
   __syncthreads();
   // 2. per-warp slice counts
@@ -365,7 +376,10 @@ struct RouteAlignSmall {
   template <int EPT>
   void operator()() {
     const int n = a.T * a.k;
-    const size_t shm = (size_t)(((n + 31) & ~31) + kSmallWarps * a.E) * sizeof(int);
+    // s_ids, the per-warp expert counts, and the CTA-wide routing's scratch (tiny batches)
+    const size_t shm = (size_t)(((n + 31) & ~31) + kSmallWarps * a.E +
+                                (a.T <= kBlockRouteMaxTokens ? 2 * ((a.E + 3) & ~3) + 128 : 0)) *
+                       sizeof(int);
     launch_kernel(route_align_small_kernel<EPT>, dim3(1), dim3(kSmallThreads), shm, stream, a, bs,
                   sorted, expert_ids, max_blocks, npp, block_seg, inv, x, H8, xp, row_scale);
   }
@@ -389,7 +403,10 @@ cudaError_t launch_route_align_small(const gbmoe_config_t& c, int T, const float
                     expert_ids, max_blocks, npp, block_seg, inv,
                     static_cast<const uint4*>(x), c.hidden_size / 8,
                     static_cast<uint4*>(x_perm), row_scale, stream};
-  dispatch_ept(c.num_experts, L);
+  if (T <= kBlockRouteMaxTokens)
+    L.template operator()<0>();
+  else
+    dispatch_ept(c.num_experts, L);
   return cudaGetLastError();
 }
 

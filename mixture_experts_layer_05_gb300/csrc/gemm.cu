@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      const uint64_t wpolicy = l2_evict_first_policy();
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
@@ -151,9 +152,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sb = sa + S::kARegion;
           mbar_expect_tx(full_bar(s), S::kTxBytes);
           tma_load_2d(sa, ta, full_bar(s), kb * kGemmBK, a_row);
-          tma_load_2d(sb, tb, full_bar(s), kb * kGemmBK, b_row);
-          if (KIND == kGemmW13)
-            tma_load_2d(sb + BN * 128, tb, full_bar(s), kb * kGemmBK, b_row + P.up_offset);
+          if (AROWS < kGemmBM) {
+            // decode: each weight tile has a single reader; stream it through L2 first-out
+            tma_load_2d_hint(sb, tb, full_bar(s), kb * kGemmBK, b_row, wpolicy);
+            if (KIND == kGemmW13)
+              tma_load_2d_hint(sb + BN * 128, tb, full_bar(s), kb * kGemmBK, b_row + P.up_offset,
+                               wpolicy);
+          } else {
+            tma_load_2d(sb, tb, full_bar(s), kb * kGemmBK, b_row);
+            if (KIND == kGemmW13)
+              tma_load_2d(sb + BN * 128, tb, full_bar(s), kb * kGemmBK, b_row + P.up_offset);
+          }
         }
       }
     }

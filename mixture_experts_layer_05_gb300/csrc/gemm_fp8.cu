@@ -437,6 +437,7 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      const uint64_t wpolicy = l2_evict_first_policy();
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
@@ -460,8 +461,9 @@ __global__ void __launch_bounds__(kSwThreads, 1)
           }
           const uint32_t sw = base + s * kSwStageBytes;
           mbar_expect_tx(full_bar(s), kSwStageBytes);
-          tma_load_2d(sw, tb, full_bar(s), kb * kF8BK, b_row);
-          tma_load_2d(sw + 128 * kF8BK, tb, full_bar(s), kb * kF8BK, b_row1);
+          // each weight tile has a single reader here: stream it through L2 first-out
+          tma_load_2d_hint(sw, tb, full_bar(s), kb * kF8BK, b_row, wpolicy);
+          tma_load_2d_hint(sw + 128 * kF8BK, tb, full_bar(s), kb * kF8BK, b_row1, wpolicy);
           tma_load_2d(sw + 256 * kF8BK, ta, full_bar(s), kb * kF8BK, w.mb * kGemmBM);
         }
       }
