@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(kSmallThreads)
   __shared__ int s_total;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) wcnt[i] = 0;
+  for (int i = threadIdx.x; i < a.zero_count; i += blockDim.x) a.zero[i] = 0;
   // 1. routing: EPT = 0 (the tiniest batches) routes token by token with the whole CTA, in
   //    compact code (this kernel starts each forward, and its code is fetched cold after the
   //    expert GEMMs have streamed through L2); else a warp per token
@@ -395,8 +396,11 @@ cudaError_t launch_route_align_small(const gbmoe_config_t& c, int T, const float
                                      int* sorted, int* expert_ids, int max_blocks, int* npp,
                                      int2* block_seg, int* inv, const void* x, void* x_perm,
                                      const float* row_scale, int* status, cudaStream_t stream,
-                                     int logit_splits, long long logit_split_stride) {
+                                     int logit_splits, long long logit_split_stride,
+                                     int* zero, int zero_count) {
   TopkArgs ta = make_topk_args(c, T, logits, bias, weights, ids, status);
+  ta.zero = zero;
+  ta.zero_count = zero_count;
   ta.logit_splits = logit_splits;
   ta.logit_split_stride = logit_split_stride;
   RouteAlignSmall L{ta, bs, sorted,

@@ -143,7 +143,8 @@ struct Layout {
   bool small, fused_copy;
   int w2_bn, splits13, splits13_shared, splits2, splits2_shared, splits_router, launches;
   size_t status, topk_weights, topk_ids, sorted, expert_ids, npp, block_seg, inv, scratch,
-      x_perm, act, ytok, act_s, part_r, part_s, logits, xq, total;
+      x_perm, act, ytok, act_s, part_r, part_s, logits, xq, tile_cnt, total;
+  int tile_cnt_r, tile_cnt_s;  // counters of the fused split reduce (routed, shared); 0 = none
   // fp8: byte offsets of the scales inside x_perm / act / act_s / xq
   size_t xs_perm, act_scale, act_s_scale, xs_tok;
 };
@@ -207,6 +208,7 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   L.act_scale = L.fp8 ? up((size_t)L.max_sorted * I) : 0;
   L.act_s_scale = L.fp8 ? up((size_t)T * Is) : 0;
   L.xs_tok = L.fp8 ? up((size_t)T * H) : 0;
+  L.tile_cnt = o;                     // filled in with the launch plan below
   L.total = o;
 
   // launch plan
@@ -228,8 +230,20 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
     L.splits2 = b.r;
     L.splits2_shared = b.s;
   }
-  L.launches = (L.small ? (L.fused_copy ? 1 : 2) : 5) + 1 +
-               (L.splits13 > 1 || (Is && L.splits13_shared > 1) ? 1 : 0) + 1 + 1;
+  // bf16 split-K first GEMMs with two splits finish the activation in their last split
+  // (per-tile counters, cleared by the routing kernel). With more splits the units are short
+  // and their fence + atomic each cost more than the separate reduce kernel saves (measured:
+  // Mixtral T = 1 with 2 splits 175 -> 153 us, DeepSeek-V2 T = 1 with 3 splits 115 -> 120 us),
+  // so those, and the fp8 ones, keep the reduce kernel.
+  const bool split13 = L.splits13 > 1 || (Is && L.splits13_shared > 1);
+  const int max_split13 = L.splits13 > (Is ? L.splits13_shared : 1) ? L.splits13
+                                                                     : (Is ? L.splits13_shared : 1);
+  const bool fused_reduce = split13 && !L.fp8 && max_split13 <= 2;
+  L.tile_cnt_r = fused_reduce ? (L.max_sorted / L.bs) * (I / kGemmBM) * 4 : 0;
+  L.tile_cnt_s = fused_reduce && Is ? (int)t_blocks * (Is / kGemmBM) * 4 : 0;
+  L.total = up(L.tile_cnt + (size_t)(L.tile_cnt_r + L.tile_cnt_s) * 4);
+  L.launches = (L.small ? (L.fused_copy ? 1 : 2) : 5) + 1 + (split13 && !fused_reduce ? 1 : 0) +
+               1 + 1;
   L.splits_router = choose_splits(t_blocks_128(T) * ((E + kGemmBM - 1) / kGemmBM), H / kGemmBK, T);
   return L;
 }
@@ -446,6 +460,7 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
   }
   int2* bseg = at<int2>(workspace, L.block_seg);
   int* inv = at<int>(workspace, L.inv);
+  int* tile_cnt = at<int>(workspace, L.tile_cnt);
   // apply_router_weight_on_input: the gathered rows carry the routing weight instead
   const float* row_scale = c.apply_router_weight_on_input ? tw : nullptr;
   const bool gated = c.is_act_and_mul != 0;
@@ -467,11 +482,12 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
     GBMOE_TRY(launch_route_align_small(c, T, router_logits, e_score_correction_bias, tw, tids,
                                        L.bs, sorted, eids, L.max_blocks, npp, bseg, inv,
                                        hidden_states, fused_copy ? x_perm : nullptr, row_scale,
-                                       status, stream, logit_splits, logit_stride));
+                                       status, stream, logit_splits, logit_stride, tile_cnt,
+                                       L.tile_cnt_r + L.tile_cnt_s));
     if (!fused_copy) GBMOE_TRY(gather());
   } else {
     GBMOE_TRY(launch_topk(c, T, router_logits, e_score_correction_bias, tw, tids, status, stream,
-                          logit_splits, logit_stride));
+                          logit_splits, logit_stride, tile_cnt, L.tile_cnt_r + L.tile_cnt_s));
     GBMOE_TRY(launch_align(tids, L.n, E, L.bs, sorted, eids, L.max_blocks, npp,
                            at<char>(workspace, L.scratch), status, stream, bseg, inv));
     GBMOE_TRY(gather());
@@ -680,9 +696,13 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
   }
   g1.splits = L.splits13;
   g1.splits_p1 = L.splits13_shared;
+  if (L.tile_cnt_r) {
+    g1.p[0].tile_count = tile_cnt;
+    if (Is) g1.p[1].tile_count = tile_cnt + L.tile_cnt_r;
+  }
   // a row block holds at most T real rows (a token meets an expert once)
   GBMOE_TRY(launch_gemm(gated ? kGemmW13 : kGemmW1, kGemmBM, g1, stream, L.pair, T));
-  if (g1.splits > 1 || (Is && g1.splits_p1 > 1))
+  if ((g1.splits > 1 || (Is && g1.splits_p1 > 1)) && !L.tile_cnt_r)
     GBMOE_TRY(launch_silu_reduce(g1, npp, L.max_sorted, gated, stream));
   GBMOE_TRY(rec(2));
 

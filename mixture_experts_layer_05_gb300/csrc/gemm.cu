@@ -274,10 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          // raw K-slice sums; bias and activation are applied by the split reduce
+          // raw K-slice sums; bias and activation follow once every split is in
+          const size_t prow = kGated ? 2 * (size_t)P.ldo : (size_t)P.ldo;
           float* dst = P.part + (size_t)w.split * P.part_split_stride +
-                       (size_t)(f < 0 ? 0 : f) * (kGated ? 2 * P.ldo : P.ldo) +
-                       (size_t)w.nt * BN;
+                       (size_t)(f < 0 ? 0 : f) * prow + (size_t)w.nt * BN;
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
             uint32_t g[32], up[32];
@@ -288,6 +288,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (f >= 0) {
               store_f32x32(dst + c * 32, g, 1.f);
               if (kGated) store_f32x32(dst + P.ldo + c * 32, up, 1.f);
+            }
+          }
+          if (P.tile_count) {
+            // the last split to arrive at this (row block, N tile, lane quarter) sums all
+            // splits' partials of its 32 rows in split order and finishes the activation
+            __threadfence();
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) {
+              int* cnt = P.tile_count + ((size_t)w.mb * P.n_tiles + w.nt) * 4 + quarter;
+              last = atomicAdd(cnt, 1) == splits_of(args, w.p) - 1;
+              if (last) *cnt = 0;                  // every split has arrived: reset for reuse
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+              __threadfence();
+              const int nsp = splits_of(args, w.p);
+              const float* src0 = P.part + (size_t)(f < 0 ? 0 : f) * prow + (size_t)w.nt * BN;
+              __nv_bfloat16* act = static_cast<__nv_bfloat16*>(P.out) + (size_t)m * P.ldo +
+                                   (size_t)w.nt * BN;
+#pragma unroll 1
+              for (int c = 0; c < BN / 32 && f >= 0; ++c) {
+                float gs[32], us[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) gs[i] = us[i] = 0.f;
+                for (int sp = 0; sp < nsp; ++sp) {
+                  const float4* q = reinterpret_cast<const float4*>(
+                      src0 + (size_t)sp * P.part_split_stride + c * 32);
+#pragma unroll
+                  for (int v = 0; v < 8; ++v) {
+                    const float4 a4 = __ldcg(q + v);
+                    gs[4 * v] += a4.x; gs[4 * v + 1] += a4.y; gs[4 * v + 2] += a4.z; gs[4 * v + 3] += a4.w;
+                    if (kGated) {
+                      const float4 b4 = __ldcg(q + P.ldo / 4 + v);
+                      us[4 * v] += b4.x; us[4 * v + 1] += b4.y; us[4 * v + 2] += b4.z; us[4 * v + 3] += b4.w;
+                    }
+                  }
+                }
+                float gb[32], ub[32];
+                load_bias32(bg ? bg + c * 32 : nullptr, gb);
+                if (kGated) load_bias32(bg ? bg + P.ldo + c * 32 : nullptr, ub);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  float a0, a1;
+                  if (kGated) {
+                    a0 = act_gated(gs[2 * i] + gb[2 * i], us[2 * i] + ub[2 * i], P.alpha, P.clamp_limit);
+                    a1 = act_gated(gs[2 * i + 1] + gb[2 * i + 1], us[2 * i + 1] + ub[2 * i + 1], P.alpha,
+                                   P.clamp_limit);
+                  } else {
+                    a0 = silu_f(gs[2 * i] + gb[2 * i]);
+                    a1 = silu_f(gs[2 * i + 1] + gb[2 * i + 1]);
+                  }
+                  pk[i] = pack_bf16x2(a0, a1);
+                }
+                uint4* o = reinterpret_cast<uint4*>(act + c * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                  o[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+              }
             }
           }
         }

@@ -59,7 +59,8 @@ cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t sme
 // is the logit (the split-K router GEMM); 1 = plain logits.
 cudaError_t launch_topk(const gbmoe_config_t& c, int T, const float* logits, const float* bias,
                         float* weights, int* ids, int* status, cudaStream_t stream,
-                        int logit_splits = 1, long long logit_split_stride = 0);
+                        int logit_splits = 1, long long logit_split_stride = 0,
+                        int* zero = nullptr, int zero_count = 0);
 
 size_t align_scratch_bytes(int n, int E);
 // block_seg (optional): per block, (first block, block count) of its expert's run.
@@ -74,7 +75,8 @@ cudaError_t launch_route_align_small(const gbmoe_config_t& c, int T, const float
                                      int* sorted, int* expert_ids, int max_blocks, int* npp,
                                      int2* block_seg, int* inv, const void* x, void* x_perm,
                                      const float* row_scale, int* status, cudaStream_t stream,
-                                     int logit_splits = 1, long long logit_split_stride = 0);
+                                     int logit_splits = 1, long long logit_split_stride = 0,
+                                     int* zero = nullptr, int zero_count = 0);
 // x_perm[inv[f]] = x[f / k] (times row_scale[f] when row_scale is not NULL) for f < n
 // (x_perm == NULL in the small launch: no copy there).
 cudaError_t launch_gather(const void* x, int H, const int* inv, int n, int k, int max_rows,
@@ -130,6 +132,9 @@ struct GemmProblem {
                            // [row][ldo] non-gated), row = flat index (routed) or token
   long long part_split_stride;
   long long out_split_stride;  // w2: elements between the per-split copies of out
+  int* tile_count;         // bf16 first GEMM with splits > 1: per (row block, N tile, TMEM lane
+                           // quarter) arrival counters, zero at launch; the last split of each
+                           // finishes the activation (no separate reduce). NULL: reduce kernel
   // FP8 (e4m3 w8a8, 128 x 128 weight blocks) problems only: A and B are e4m3 bytes,
   // K blocks are 128 wide, and out (w13) is e4m3 act with fp32 scales.
   const float* a_scale;    // A scales, K-block major: a_scale[kb * a_scale_ld + row]

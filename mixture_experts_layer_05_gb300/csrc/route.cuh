@@ -28,6 +28,8 @@ struct TopkArgs {
   float rsf;
   int logit_splits;              // logits arrive as this many fp32 partial copies (>= 1),
   long long logit_split_stride;  // summed in copy order on load (split-K router GEMM)
+  int* zero;                     // the forward's split counters, cleared by the routing
+  int zero_count;                // kernel (it runs before any GEMM of the forward)
 };
 
 // (key, index) pair maximum: larger key wins, equal keys go to the lower index.
@@ -404,6 +406,8 @@ inline TopkArgs make_topk_args(const gbmoe_config_t& c, int T, const float* logi
   a.rsf = c.routed_scaling_factor;
   a.logit_splits = 1;
   a.logit_split_stride = 0;
+  a.zero = nullptr;
+  a.zero_count = 0;
   return a;
 }
 

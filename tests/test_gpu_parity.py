@@ -388,14 +388,26 @@ VARIANTS = {
     "non_gated_bias": dict(gated=False, bias=True),
     "weight_on_input": dict(apply_router_weight_on_input=True),
 }
+# two-way split-K of the first GEMM: its last split finishes the activation in the GEMM
+FUSED2 = _small(configs.MIXTRAL, num_experts=8, hidden_size=512, intermediate_size=1024)
 VARIANT_SHAPES = {
     "dsv3": SMALL["dsv3"],        # grouped sigmoid routing + shared expert
-    "split": SPLIT,               # decode shapes: split-K and the split reduce
+    "split": SPLIT,               # decode shapes: split-K and the split reduce kernel
+    "fused2": FUSED2,             # decode shapes: split-K reduced inside the GEMM
 }
 
 
+def test_two_way_split_reduces_in_the_gemm(cuda_lib):
+    """The two-split decode shape launches no separate reduce kernel: routing + align with
+    the row copy, w13, w2, combine."""
+    cfg = binding.config_from_workload(FUSED2)
+    assert binding.moe_forward_num_launches(cfg, 1) == 4
+    assert binding.moe_forward_num_launches(binding.config_from_workload(SPLIT), 1) == 5
+
+
 @pytest.mark.parametrize("vname", list(VARIANTS))
-@pytest.mark.parametrize("sname,T", [("dsv3", 203), ("split", 1), ("split", 17)])
+@pytest.mark.parametrize("sname,T", [("dsv3", 203), ("split", 1), ("split", 17), ("fused2", 1),
+                                     ("fused2", 5)])
 def test_forward_variants(cuda_lib, vname, sname, T):
     v = dict(VARIANTS[vname])
     w = VARIANT_SHAPES[sname]
