@@ -196,3 +196,82 @@ def test_fp8_cuda_graph_replay(cuda_lib):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, y_eager)
+
+
+# ------------------------------------------------------------------ edge cases and options
+def test_fp8_empty_batch_and_single_expert(cuda_lib):
+    w = SMALL["mixtral"]
+    layer, _ = _fp8_layer(w, inputs.make_fp8_weights(w, 0), 4)
+    out = torch.full((0, w.hidden_size), 1.0, dtype=torch.bfloat16, device=DEV)
+    layer(torch.empty(0, w.hidden_size, dtype=torch.bfloat16, device=DEV),
+          torch.empty(0, w.num_experts, device=DEV), out=out)          # T = 0: a no-op
+    # E = 1, k = 1: one dense fp8 SwiGLU MLP over more than one row block
+    w1 = _shrink(configs.MIXTRAL, num_experts=1, top_k=1, hidden_size=512, intermediate_size=256)
+    wts = inputs.make_fp8_weights(w1, 0)
+    x, logits = tokens(w1, 200, None)
+    layer1, _ = _fp8_layer(w1, wts, 200)
+    y = layer1(x.to(DEV), logits.to(DEV))
+    torch.cuda.synchronize()
+    assert layer1.device_status() == binding.OK
+    check_close(y, _oracle(w1, wts, x, logits, None), "fp8 E=1 k=1")
+
+
+def test_fp8_skewed_routing(cuda_lib):
+    """Zipf-skewed DeepSeek-V3 routing (small shapes): hot experts span several row blocks."""
+    w = _shrink(configs.SKEW, hidden_size=512, intermediate_size=256, shared_intermediate_size=256)
+    wts = inputs.make_fp8_weights(w, 0)
+    x, logits = tokens(w, 300, wts["bias"])
+    layer, _ = _fp8_layer(w, wts, 300)
+    y = layer(x.to(DEV), logits.to(DEV))
+    torch.cuda.synchronize()
+    assert layer.device_status() == binding.OK
+    check_close(y, _oracle(w, wts, x, logits, wts["bias"]), "fp8 skew T=300")
+
+
+@pytest.mark.parametrize("T", [1, 77])
+def test_fp8_from_gate_weight(cuda_lib, T):
+    """The router GEMM in front of the fp8 layer: logits = x @ W_gate^T in fp32 first. Ids
+    must match wherever the oracle's decision margin exceeds 1e-4 (far above the fp32 logit
+    error); closer rows are only checked for a valid choice."""
+    w = SMALL["dsv3"]
+    wts = inputs.make_fp8_weights(w, 0)
+    gate = inputs.normal((w.num_experts, w.hidden_size), w.hidden_size ** -0.5,
+                         inputs.tensor_seed(w.name, "gate", 0), torch.bfloat16)
+    x = inputs.normal((T, w.hidden_size), 1.0, 5, torch.bfloat16)
+    layer, _ = _fp8_layer(w, wts, T)
+    y = layer(x.to(DEV), gate_weight=gate.to(DEV))
+    torch.cuda.synchronize()
+    assert layer.device_status() == binding.OK
+    logits = oracle.router_logits(x, gate)
+    safe = oracle.decision_margins(logits, wts["bias"], **oracle_cfg(w)) >= 1e-4
+    ids, _ = _routing_from_ws(layer, T, w.top_k)
+    for t in range(T):
+        assert len(set(ids[t].tolist())) == w.top_k
+    rows = np.flatnonzero(safe).tolist()
+    if rows:
+        y_ref, parts = _oracle(w, wts, x[rows], logits[rows], wts["bias"], return_parts=True)
+        assert np.array_equal(ids[rows], parts["topk_ids"])
+        check_close(y[rows], y_ref, f"fp8 gate T={T}")
+    if T > 1:
+        assert safe.mean() > 0.9
+
+
+def test_fp8_stage_events_in_a_graph(cuda_lib):
+    w = SMALL["dsv3"]
+    wts = inputs.make_fp8_weights(w, 0)
+    x, logits = tokens(w, 16, wts["bias"])
+    layer, _ = _fp8_layer(w, wts, 16)
+    xd, ld = x.to(DEV), logits.to(DEV)
+    y_eager = layer(xd, ld).clone()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(binding.NUM_STAGE_EVENTS)]
+    out = torch.empty_like(y_eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer(xd, ld, out=out, events=evs)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, y_eager)
+    times = [evs[i].elapsed_time(evs[i + 1]) for i in range(len(evs) - 1)]
+    assert all(t >= 0 for t in times) and sum(times) > 0
