@@ -143,8 +143,9 @@ struct Layout {
   bool small, fused_copy;
   int w2_bn, splits13, splits13_shared, splits2, splits2_shared, splits_router, launches;
   size_t status, topk_weights, topk_ids, sorted, expert_ids, npp, block_seg, inv, scratch,
-      x_perm, act, ytok, act_s, part_r, part_s, logits, xq, tile_cnt, total;
+      x_perm, act, ytok, act_s, part_r, part_s, logits, xq, tile_cnt, tail_part, total;
   int tile_cnt_r, tile_cnt_s;  // counters of the fused split reduce (routed, shared); 0 = none
+  int tail_cnt;                // counters of the w2 stream-K tail (after those); 0 = none
   // fp8: byte offsets of the scales inside x_perm / act / act_s / xq
   size_t xs_perm, act_scale, act_s_scale, xs_tok;
 };
@@ -241,7 +242,12 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   const bool fused_reduce = split13 && !L.fp8 && max_split13 <= 2;
   L.tile_cnt_r = fused_reduce ? (L.max_sorted / L.bs) * (I / kGemmBM) * 4 : 0;
   L.tile_cnt_s = fused_reduce && Is ? (int)t_blocks * (Is / kGemmBM) * 4 : 0;
-  L.total = up(L.tile_cnt + (size_t)(L.tile_cnt_r + L.tile_cnt_s) * 4);
+  // bf16 w2 without split-K: a stream-K tail evens out the last round of tiles (up to one
+  // 128 x N-tile fp32 partial per SM)
+  const bool tail = T > kSplitMaxTokens && !L.fp8 && !L.pair;
+  L.tail_cnt = tail ? num_sms() * 4 : 0;
+  L.tail_part = up(L.tile_cnt + (size_t)(L.tile_cnt_r + L.tile_cnt_s + L.tail_cnt) * 4);
+  L.total = up(L.tail_part + (tail ? (size_t)num_sms() * kGemmBM * L.w2_bn * 4 : 0));
   L.launches = (L.small ? (L.fused_copy ? 1 : 2) : 5) + 1 + (split13 && !fused_reduce ? 1 : 0) +
                1 + 1;
   L.splits_router = choose_splits(t_blocks_128(T) * ((E + kGemmBM - 1) / kGemmBM), H / kGemmBK, T);
@@ -483,11 +489,12 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
                                        L.bs, sorted, eids, L.max_blocks, npp, bseg, inv,
                                        hidden_states, fused_copy ? x_perm : nullptr, row_scale,
                                        status, stream, logit_splits, logit_stride, tile_cnt,
-                                       L.tile_cnt_r + L.tile_cnt_s));
+                                       L.tile_cnt_r + L.tile_cnt_s + L.tail_cnt));
     if (!fused_copy) GBMOE_TRY(gather());
   } else {
     GBMOE_TRY(launch_topk(c, T, router_logits, e_score_correction_bias, tw, tids, status, stream,
-                          logit_splits, logit_stride, tile_cnt, L.tile_cnt_r + L.tile_cnt_s));
+                          logit_splits, logit_stride, tile_cnt,
+                          L.tile_cnt_r + L.tile_cnt_s + L.tail_cnt));
     GBMOE_TRY(launch_align(tids, L.n, E, L.bs, sorted, eids, L.max_blocks, npp,
                            at<char>(workspace, L.scratch), status, stream, bseg, inv));
     GBMOE_TRY(gather());
@@ -763,6 +770,11 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
   }
   g2.splits = L.splits2;
   g2.splits_p1 = L.splits2_shared;
+  if (L.tail_cnt) {
+    g2.tail_part = at<float>(workspace, L.tail_part);
+    g2.tail_count = tile_cnt + L.tile_cnt_r + L.tile_cnt_s;
+    g2.tail_max_splits = 8;
+  }
   GBMOE_TRY(launch_gemm(kGemmW2, w2_bn, g2, stream, L.pair, T));
   GBMOE_TRY(rec(3));
   GBMOE_TRY(launch_combine(ytok, L.slots, k, H, T, g2.splits, Is ? g2.splits_p1 : g2.splits,

@@ -383,24 +383,77 @@ __global__ void __launch_bounds__(kThreads, 1)
             dest = f * P.slots + P.slot_offset;
           }
         }
-        // the expert's output bias enters once (split 0), inside the routing weight
-        const __nv_bfloat16* b2 = (P.bias && w.split == 0)
-                                      ? P.bias + (size_t)e_tile * P.ldo + (size_t)w.nt * BN
-                                      : nullptr;
-        float* dst = static_cast<float*>(P.out) + (size_t)w.split * P.out_split_stride +
-                     (size_t)(dest < 0 ? 0 : dest) * P.ldo + (size_t)w.nt * BN;
+        if (w.tail >= 0) {
+          // stream-K tail range: the raw partial goes to its scratch slot; the last range of
+          // this tile and lane quarter sums the ranges in order and finishes the epilogue
+          float* part = args.tail_part +
+                        ((size_t)(w.tail * w.tail_splits + w.split) * kGemmBM + row) * BN;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tbase + c * 32, r);
-          tmem_wait_ld(r);
-          if (b2) {
-            float bb[32];
-            load_bias32(b2 + c * 32, bb);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + bb[i]);
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tbase + c * 32, r);
+            tmem_wait_ld(r);
+            store_f32x32(part + c * 32, r, 1.f);
           }
-          if (dest >= 0) store_f32x32(dst + c * 32, r, wt);
+          __threadfence();
+          __syncwarp();
+          int last = 0;
+          if (lane == 0) {
+            int* cnt = args.tail_count + (size_t)w.tail * 4 + quarter;
+            last = atomicAdd(cnt, 1) == w.tail_splits - 1;
+            if (last) *cnt = 0;                      // every range has arrived: reset
+          }
+          last = __shfl_sync(0xffffffffu, last, 0);
+          if (last) {
+            __threadfence();
+            const __nv_bfloat16* b2 =
+                P.bias ? P.bias + (size_t)e_tile * P.ldo + (size_t)w.nt * BN : nullptr;
+            float* dst = static_cast<float*>(P.out) + (size_t)(dest < 0 ? 0 : dest) * P.ldo +
+                         (size_t)w.nt * BN;
+            const float* src0 = args.tail_part +
+                                ((size_t)(w.tail * w.tail_splits) * kGemmBM + row) * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32 && dest >= 0; ++c) {
+              float acc[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+              for (int sp = 0; sp < w.tail_splits; ++sp) {
+                const float4* q = reinterpret_cast<const float4*>(
+                    src0 + (size_t)sp * kGemmBM * BN + c * 32);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                  const float4 a4 = __ldcg(q + v);
+                  acc[4 * v] += a4.x; acc[4 * v + 1] += a4.y; acc[4 * v + 2] += a4.z; acc[4 * v + 3] += a4.w;
+                }
+              }
+              uint32_t r[32];
+              float bb[32];
+              load_bias32(b2 ? b2 + c * 32 : nullptr, bb);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(acc[i] + bb[i]);
+              store_f32x32(dst + c * 32, r, wt);
+            }
+          }
+        } else {
+          // the expert's output bias enters once (split 0), inside the routing weight
+          const __nv_bfloat16* b2 = (P.bias && w.split == 0)
+                                        ? P.bias + (size_t)e_tile * P.ldo + (size_t)w.nt * BN
+                                        : nullptr;
+          float* dst = static_cast<float*>(P.out) + (size_t)w.split * P.out_split_stride +
+                       (size_t)(dest < 0 ? 0 : dest) * P.ldo + (size_t)w.nt * BN;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tbase + c * 32, r);
+            tmem_wait_ld(r);
+            if (b2) {
+              float bb[32];
+              load_bias32(b2 + c * 32, bb);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + bb[i]);
+            }
+            if (dest >= 0) store_f32x32(dst + c * 32, r, wt);
+          }
         }
       }
       tc_fence_before();

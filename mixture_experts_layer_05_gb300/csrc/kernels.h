@@ -152,6 +152,14 @@ struct GemmLaunch {
   int splits;       // split-K factor of problem 0
   int splits_p1;    // split-K factor of problem 1 (0 = same as problem 0)
   int* status;
+  // Stream-K tail (bf16 w2): when the tiles leave a last round of at most half the grid, the
+  // kernel cuts those tail tiles into up to tail_max_splits K ranges; each range writes an fp32
+  // partial tile to tail_part ([range slot][128 rows][N tile]) and the last range to arrive
+  // (per tile and TMEM lane quarter, counted in tail_count, zero at launch) sums them in range
+  // order and runs the epilogue. tail_max_splits 0: no tail splitting.
+  float* tail_part;
+  int* tail_count;
+  int tail_max_splits;
 };
 
 __host__ __device__ inline int splits_of(const GemmLaunch& L, int p) {

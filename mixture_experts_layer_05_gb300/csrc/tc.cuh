@@ -345,10 +345,13 @@ __device__ __forceinline__ void tile_coords(const GemmProblem& a, int m_blocks, 
 // Work unit u -> (problem, split, row block, N tile, K-block range).
 struct Unit {
   int p, split, mb, nt, kb0, kb1;
+  int tail;          // stream-K tail tile index (its K ranges are `split` of tail_splits), or -1
+  int tail_splits;
 };
 
 struct Schedule {
   int mblk[2], tiles[2], total_tiles, units, units0;
+  int dp_units, tail, tail_splits;  // stream-K tail: units [dp_units, units) are tail ranges
 
   __device__ void init(const GemmLaunch& L, int bm = kGemmBM) {
     total_tiles = 0;
@@ -367,11 +370,49 @@ struct Schedule {
     }
     units0 = tiles[0] * splits_of(L, 0);
     units = units0 + tiles[1] * splits_of(L, 1);
+    dp_units = units;
+    tail = 0;
+    tail_splits = 1;
+    // stream-K tail: only without split-K, and only when the tail tiles all belong to the
+    // last problem
+    const int G = gridDim.x;
+    const int last = L.num_problems - 1;
+    if (L.tail_max_splits > 1 && units == total_tiles && total_tiles >= G) {
+      const int tl = total_tiles % G;
+      if (tl > 0 && 2 * tl <= G && tl <= tiles[last]) {
+        int sp = G / tl;
+        if (sp > L.tail_max_splits) sp = L.tail_max_splits;
+        if (sp > L.p[last].k_blocks / 4) sp = L.p[last].k_blocks / 4;
+        if (sp >= 2) {
+          tail = tl;
+          tail_splits = sp;
+          dp_units = total_tiles - tl;
+          units = dp_units + tl * sp;
+        }
+      }
+    }
   }
 
-  // units: problem 0 first, then problem 1; within a problem split-major
+  // units: problem 0 first, then problem 1; within a problem split-major; then the tail ranges
+  // (range-major, so one tile's ranges run on different CTAs of the same round)
   __device__ Unit unit(const GemmLaunch& L, int u) const {
     Unit r;
+    r.tail = -1;
+    r.tail_splits = 1;
+    if (u >= dp_units) {
+      const int v = u - dp_units;
+      const int j = v % tail, s = v / tail;
+      r.p = L.num_problems - 1;
+      const int t = dp_units + j - (r.p ? tiles[0] : 0);
+      const GemmProblem& P = L.p[r.p];
+      tile_coords(P, mblk[r.p], t, L.status, r.mb, r.nt);
+      r.split = s;
+      r.tail = j;
+      r.tail_splits = tail_splits;
+      r.kb0 = (s * P.k_blocks) / tail_splits;
+      r.kb1 = ((s + 1) * P.k_blocks) / tail_splits;
+      return r;
+    }
     r.p = u < units0 ? 0 : 1;
     const int local = r.p ? u - units0 : u;
     const int sp = splits_of(L, r.p);

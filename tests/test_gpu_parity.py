@@ -405,6 +405,41 @@ def test_two_way_split_reduces_in_the_gemm(cuda_lib):
     assert binding.moe_forward_num_launches(binding.config_from_workload(SPLIT), 1) == 5
 
 
+# w2 with more tiles than SMs and a short last round: the stream-K tail splits those tiles
+TAIL = _small(configs.MIXTRAL, hidden_size=2048, intermediate_size=512)
+
+
+@pytest.mark.parametrize("use_bias", [False, True], ids=["plain", "bias"])
+@pytest.mark.parametrize("T", [1024, 1100])
+def test_forward_w2_stream_k_tail(cuda_lib, use_bias, T):
+    """Prefill shapes whose w2 tiles leave a last round of at most half the SMs: those tiles
+    run as K ranges summed by the last range (checked against the oracle and for run-to-run
+    determinism)."""
+    w = TAIL
+    wts = inputs.make_weights(w, 0)
+    x, logits = tokens(w, T, None)
+    _, ids = oracle.select_experts(logits, None, **oracle_cfg(w))
+    blocks = sum((c + 127) // 128 for c in np.bincount(ids.reshape(-1), minlength=w.num_experts))
+    tiles = blocks * (w.hidden_size // 256)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert tiles >= sms and 0 < tiles % sms <= sms // 2      # the shape takes the tail path
+    extra = inputs.make_expert_extras(w, 0) if use_bias else {}
+    b13 = extra.get("w13_bias")
+    b2 = extra.get("w2_bias")
+    cfg = binding.config_from_workload(w)
+    dv = lambda t: None if t is None else t.to(DEV)
+    layer = binding.FusedMoE(cfg, wts["w13"].to(DEV), wts["w2"].to(DEV), max_tokens=T,
+                             w13_bias=dv(b13), w2_bias=dv(b2))
+    y = layer(x.to(DEV), logits.to(DEV)).clone()
+    torch.cuda.synchronize()
+    assert layer.device_status() == binding.OK
+    rows = sorted({0, T - 1, *np.random.default_rng(T).choice(T, size=30, replace=False).tolist()})
+    y_ref = oracle.fused_moe(x[rows], logits[rows], None, wts["w13"], wts["w2"],
+                             w13_bias=b13, w2_bias=b2, **oracle_cfg(w))
+    check_close(y[rows], y_ref, f"w2 tail T={T}")
+    assert torch.equal(y, layer(x.to(DEV), logits.to(DEV)))
+
+
 @pytest.mark.parametrize("vname", list(VARIANTS))
 @pytest.mark.parametrize("sname,T", [("dsv3", 203), ("split", 1), ("split", 17), ("fused2", 1),
                                      ("fused2", 5)])
