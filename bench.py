@@ -220,25 +220,31 @@ def run_ours(args, w, T):
              for n, a, b in (("route_align_gather", 0, 1), ("w13_gemm", 1, 2),
                              ("w2_gemm", 2, 3), ("combine", 3, 4))}
 
-    # timed region: K forwards captured once into a CUDA graph and replayed; the w13
-    # GEMM of every step is bracketed by two events inside the graph
+    # timed region: K forwards captured once into a CUDA graph and replayed (no events in
+    # it: a stage event would break the kernels' programmatic launch chain). The w13 GEMM's
+    # duration for the roofline comes from a second graph of K forwards whose w13 launches
+    # are bracketed by events, replayed untimed right after the timed region.
     wevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     for pair in wevs:
         for ev in pair:
             ev.record(stream)
     torch.cuda.synchronize()
-    graph = None
+    graph = graph_w13 = None
     try:
         graph = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream()
         cap.wait_stream(stream)
         with torch.cuda.graph(graph, stream=cap):
             for i in range(K):
+                layer(x, logits, out=out)
+        graph_w13 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_w13, stream=cap):
+            for i in range(K):
                 layer(x, logits, out=out, events=[None, wevs[i][0], wevs[i][1], None, None])
         torch.cuda.synchronize()
     except Exception as exc:                        # eager timing if capture is refused
         print(f"[bench] CUDA graph capture failed ({exc}); timing eager steps", file=sys.stderr)
-        graph = None
+        graph = graph_w13 = None
         torch.cuda.synchronize()
 
     def timed_steps():
@@ -246,10 +252,18 @@ def run_ours(args, w, T):
             graph.replay()
         else:
             for i in range(K):
+                layer(x, logits, out=out)
+
+    def w13_steps():
+        if graph_w13 is not None:
+            graph_w13.replay()
+        else:
+            for i in range(K):
                 layer(x, logits, out=out, events=[None, wevs[i][0], wevs[i][1], None, None])
 
     if graph is not None:
-        graph.replay()                               # one untimed replay
+        graph.replay()                               # one untimed replay of each graph
+        graph_w13.replay()
     torch.cuda.synchronize()
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
@@ -270,12 +284,15 @@ def run_ours(args, w, T):
         dist.barrier()
     ms = t_start.elapsed_time(t_end) / K
     ms_max = reduce_max(ms, dev)
+    w13_steps()                                     # untimed: the w13 events for the roofline
+    torch.cuda.synchronize()
     status = layer.device_status()
     if status != binding.OK:
         raise RuntimeError(f"device status {binding.STATUS.get(status, status)} after the run")
     try:
         w13_ms = statistics.mean(a.elapsed_time(b) for a, b in wevs)
-        w13_src = "w13 GEMM bracketed by events inside every timed step"
+        w13_src = ("w13 GEMM bracketed by events in a graph of K forwards replayed right "
+                   "after the timed region")
     except RuntimeError as exc:                     # events not readable: use the eager ones
         print(f"[bench] w13 events unreadable ({exc}); using the stage pass", file=sys.stderr)
         w13_ms = stage["w13_gemm"]
@@ -315,10 +332,15 @@ def run_ours(args, w, T):
               .view(torch.int32).item())
     work = layer_work(w, T, n_active, fp8)
     peaks, peak_src = load_peaks()
-    # the e4m3 tensor peak: the measured bf16 peak times the nominal dense ratio 4.5 / 2.25
-    tc_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
-    tc_src = f"{peak_src} bf16 (burst) x 2, the nominal e4m3/bf16 ratio" if fp8 else \
-        f"{peak_src} (burst)"
+    # The timed region follows >= 0.5 s of back-to-back forwards, so the GEMMs run in the
+    # power-capped steady state: the sustained measured peak is the denominator (the burst
+    # fraction is reported beside it). The e4m3 peak is the bf16 one times the nominal dense
+    # ratio 4.5 / 2.25.
+    ratio = 2.0 if fp8 else 1.0
+    tc_peak = peaks["bf16_tflops_sustained"] * ratio
+    tc_burst = peaks["bf16_tflops"] * ratio
+    tc_src = (f"{peak_src} bf16 sustained (back-to-back GEMMs for 4 s)"
+              + (" x 2, the nominal e4m3/bf16 ratio" if fp8 else ""))
     kname = ("gemm_fp8_kernel<w13> (grouped e4m3 w13 GEMM + SiLU*mul + act quant)" if fp8
              else "gemm_kernel<w13> (grouped w13 GEMM + SiLU*mul)")
     value = aggregate_tokens_per_s(T, world, ms_max)
@@ -333,7 +355,7 @@ def run_ours(args, w, T):
             ach = work["flops_w13"] / t_w13 / 1e12
             roof = {"kernel": kname, "bound": "tensor", "achieved": round(ach, 1),
                     "peak": round(tc_peak, 1), "unit": "TFLOP/s", "frac": round(ach / tc_peak, 4),
-                    "peak_source": tc_src}
+                    "peak_source": tc_src, "frac_of_burst_peak": round(ach / tc_burst, 4)}
         else:
             ach = work["bytes_w13"] / t_w13 / 1e9
             roof = {"kernel": kname, "bound": "hbm", "achieved": round(ach, 1),
@@ -414,8 +436,10 @@ def cpu_baseline(w, wts, x_cpu, logits_cpu, n_tokens: int, target_s: float = 12.
     T = x_cpu.shape[0]
     n = min(n_tokens, T)
     dt = _oracle_rows(w, hw, x_cpu, logits_cpu, 0, n, fp8)
-    if dt < target_s / 4 and n < T:                 # grow the sample to ~target_s of work
-        n = int(min(T, max(n + 1, n * target_s / max(dt, 1e-3))))
+    for _ in range(4):                              # grow the sample to ~target_s of work
+        if dt >= target_s / 2 or n >= T:
+            break
+        n = int(min(T, max(2 * n, n * target_s / max(dt, 1e-3))))
         dt = _oracle_rows(w, hw, x_cpu, logits_cpu, 0, n, fp8)
     return {"value": round(n / dt, 4), "unit": "tokens/s",
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
@@ -448,8 +472,13 @@ def run_reference(args, w, T):
     t0 = time.perf_counter()
     step(0)
     dt0 = time.perf_counter() - t0
-    if args.ref_sample <= 0:
-        n = max(1, min(T, int(n * 1.5 / max(dt0, 1e-3))))
+    for _ in range(4):                              # a fixed cost per call makes one guess short
+        if args.ref_sample > 0 or dt0 >= 0.75 or n >= T:
+            break
+        n = max(n + 1, min(T, int(n * 1.5 / max(dt0, 1e-3))))
+        t0 = time.perf_counter()
+        step(0)
+        dt0 = time.perf_counter() - t0
     for i in range(args.warmup):
         step(i)
     t0 = time.perf_counter()
