@@ -85,18 +85,30 @@ def layer_work(w, T: int, n_active: int, fp8: bool = False) -> dict:
             "bytes_w2": float(w2_bytes + act_bytes + T * k * H * 4)}
 
 
+KERNEL_SOURCES = {"gemm.cu": ("gemm.cu", "tc.cuh", "common.cuh", "kernels.h"),
+                  "gemm_fp8.cu": ("gemm_fp8.cu", "tc.cuh", "fp8.cuh", "common.cuh", "kernels.h")}
+
+
+def source_digest(source: str) -> str:
+    """sha1 over a GEMM translation unit and the headers it compiles in."""
+    import hashlib
+    h = hashlib.sha1()
+    for name in KERNEL_SOURCES.get(source, (source,)):
+        with open(os.path.join(ROOT, "mixture_experts_layer_05_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def kernel_traffic(kernel: str, workload: str, tokens: int, source: str = "gemm.cu"):
     """DRAM bytes per launch of `kernel` from a committed ncu summary, if it was captured on
-    this workload with the current kernel source (sha1 of csrc/<source>); else None.
+    this workload with the current kernel source (source_digest of csrc/<source> and its
+    headers); else None.
 
-    A summary states it on a line `traffic: <kernel> <workload> <tokens> <bytes> <sha1>`.
+    A summary states it on a line `traffic: <kernel> <workload> <tokens> <bytes> <digest>`.
     """
     import glob
-    import hashlib
-    src = os.path.join(ROOT, "mixture_experts_layer_05_gb300", "csrc", source)
     try:
-        with open(src, "rb") as f:
-            sha = hashlib.sha1(f.read()).hexdigest()
+        sha = source_digest(source)
     except OSError:
         return None
     for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
