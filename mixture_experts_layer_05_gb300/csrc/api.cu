@@ -40,6 +40,14 @@ constexpr int kSplitMaxTokens = 64;  // split-K only at decode-sized batches
 #define GBMOE_MAX_SPLITS 8
 #endif
 constexpr size_t kMaxSplits = GBMOE_MAX_SPLITS;  // largest split-K factor
+#ifndef GBMOE_UNIT_COST_KB
+#define GBMOE_UNIT_COST_KB 4
+#endif
+// Fixed cost of one unit of a persistent GEMM round (pipeline fill, accumulator hand-off and
+// epilogue), in K blocks of streaming. Measured (graph replay): 4 takes DeepSeek-V2 T = 1
+// from 95.6 to 93.1 us and T = 16 from 592 to 561 us, and the fp8 DeepSeek-V3 T = 1 from
+// 105.5 to 100.7 us; 2 and 8 were no better.
+constexpr double kUnitCostKb = GBMOE_UNIT_COST_KB;
 constexpr size_t kAlign = 256;
 
 size_t up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
@@ -105,9 +113,10 @@ bool use_pair(const gbmoe_config_t& c, int T) {
 
 // Split-K factors of a launch with a routed problem (tiles_r tiles of kb_r K blocks) and
 // an optional shared problem (tiles_s of kb_s): the persistent grid runs
-// ceil(units / SMs) rounds, each as long as the longest unit, so pick (s_r, s_s)
-// minimising rounds * max(kb_r / s_r, kb_s / s_s); a split keeps >= 4 K blocks and must
-// beat the best so far by 3 %. Only at decode-sized batches.
+// ceil(units / SMs) rounds, each as long as the longest unit plus a fixed cost per unit,
+// so pick (s_r, s_s) minimising rounds * (max(kb_r / s_r, kb_s / s_s) + kUnitCostKb); a
+// split keeps >= 4 K blocks and must beat the best so far by 3 %. Only at decode-sized
+// batches.
 struct Splits {
   int r, s;
 };
@@ -119,7 +128,7 @@ Splits choose_splits2(long tiles_r, int kb_r, long tiles_s, int kb_s, int T) {
     const long units = tiles_r * sr + tiles_s * ss;
     double len = tiles_r ? (double)kb_r / sr : 0.0;
     if (tiles_s && (double)kb_s / ss > len) len = (double)kb_s / ss;
-    return (double)((units + sms - 1) / sms) * len;
+    return (double)((units + sms - 1) / sms) * (len + kUnitCostKb);
   };
   double best_t = cost(1, 1);
   for (int sr = 1; sr <= (int)kMaxSplits && kb_r / sr >= 4; ++sr)
