@@ -379,7 +379,7 @@ struct RouteAlignSmall {
     const int n = a.T * a.k;
     // s_ids, the per-warp expert counts, and the CTA-wide routing's scratch (tiny batches)
     const size_t shm = (size_t)(((n + 31) & ~31) + kSmallWarps * a.E +
-                                (a.T <= kBlockRouteMaxTokens ? 2 * ((a.E + 3) & ~3) + 128 : 0)) *
+                                (a.T <= kBlockRouteMaxTokens ? ((a.E + 3) & ~3) + ((a.E + 15) & ~15) + 128 : 0)) *
                        sizeof(int);
     launch_kernel(route_align_small_kernel<EPT>, dim3(1), dim3(kSmallThreads), shm, stream, a, bs,
                   sorted, expert_ids, max_blocks, npp, block_seg, inv, x, H8, xp, row_scale);

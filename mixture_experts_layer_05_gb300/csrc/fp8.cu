@@ -84,7 +84,8 @@ __global__ void __launch_bounds__(256)
 // One CTA (128 threads) per output row; thread i owns 8 consecutive columns of each
 // 1024-column step, so the 16 threads of a half-warp hold one 128-column group and find
 // its amax with four xor-shuffles. Every lane runs every step (shuffles stay converged).
-__global__ void __launch_bounds__(128) silu_reduce_fp8_kernel(const GemmLaunch L, const int* npp,
+__global__ void __launch_bounds__(128) silu_reduce_fp8_kernel(const __grid_constant__ GemmLaunch L,
+                                                              const int* npp,
                                                               int max_routed_rows) {
   pdl_trigger();  // the next kernel may start its launch now
   pdl_wait();     // inputs written by the previous kernel are visible

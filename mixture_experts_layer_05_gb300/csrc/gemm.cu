@@ -729,7 +729,8 @@ __global__ void wait_selftest_kernel(int* status, unsigned long long timeout_ns)
 }
 
 // act = silu(sum_s gate_s) * sum_s up_s, one CTA per output row, 8 columns per step.
-__global__ void __launch_bounds__(128) silu_reduce_kernel(const GemmLaunch L, const int* npp,
+__global__ void __launch_bounds__(128) silu_reduce_kernel(const __grid_constant__ GemmLaunch L,
+                                                          const int* npp,
                                                           int max_routed_rows, int gated) {
   pdl_trigger();  // the next kernel may start its launch now
   pdl_wait();     // inputs written by the previous kernel are visible

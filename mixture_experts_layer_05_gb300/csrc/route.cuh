@@ -265,10 +265,11 @@ __device__ __forceinline__ int route_token_warp(const TopkArgs& a, int t, int la
 __device__ __forceinline__ int route_token_block(const TopkArgs& a, int t, float* smem) {
   const int E = a.E, tid = threadIdx.x, nt = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-  const int E4 = (E + 3) & ~3;  // keys start on a 16-byte boundary (read as float4)
-  float* sc = smem;             // [E] scores
-  float* key = sc + E4;         // [E] selection keys (-inf once excluded)
-  float* gsc = key + E4;        // [G] group scores
+  const int E4 = (E + 3) & ~3;     // keys start on a 16-byte boundary (read as float4)
+  const int E16 = (E + 15) & ~15;  // and run to a multiple of 16 (-inf past E)
+  float* sc = smem;                // [E] scores
+  float* key = sc + E4;            // [E16] selection keys (-inf once excluded)
+  float* gsc = key + E16;          // [G] group scores
   float* ow = gsc + 32;         // [k] chosen weights
   int* oid = reinterpret_cast<int*>(ow + 32);  // [k] chosen experts
   float* red = ow + 64;         // [32] reduction scratch
@@ -277,6 +278,7 @@ __device__ __forceinline__ int route_token_block(const TopkArgs& a, int t, float
   float mx = -INFINITY;
   for (int e = tid; e < E; e += nt) {
     float l = __ldg(row + e);
+    if (a.bias) key[e] = __ldg(a.bias + e);  // the bias is fetched with the logits
     for (int sp = 1; sp < a.logit_splits; ++sp) l += __ldg(row + sp * a.logit_split_stride + e);
     sc[e] = l;
     mx = fmaxf(mx, l);
@@ -303,8 +305,8 @@ __device__ __forceinline__ int route_token_block(const TopkArgs& a, int t, float
   } else {
     for (int e = tid; e < E; e += nt) sc[e] = 1.f / (1.f + expf(-sc[e]));
   }
-  for (int e = tid; e < E4; e += nt)       // the padded tail never outranks a real key
-    key[e] = e >= E ? -INFINITY : (a.bias ? sc[e] + __ldg(a.bias + e) : sc[e]);
+  for (int e = tid; e < E16; e += nt)      // the padded tail never outranks a real key
+    key[e] = e >= E ? -INFINITY : (a.bias ? sc[e] + key[e] : sc[e]);
   __syncthreads();
   if (a.grouped) {
     const int gsize = E / a.G;
@@ -342,12 +344,21 @@ __device__ __forceinline__ int route_token_block(const TopkArgs& a, int t, float
     const float ke = key[e];
     if (ke == -INFINITY) continue;
     int rank = 0;
-    // four keys per 16-byte read; a plain loop keeps the code short
+    // sixteen keys per step, four 16-byte reads in flight; the outer loop stays rolled to
+    // keep the code short
 #pragma unroll 1
-    for (int f = 0; f < E4 && rank < a.k; f += 4) {
-      const float4 kv = *reinterpret_cast<const float4*>(key + f);
-      rank += (kv.x > ke || (kv.x == ke && f < e)) + (kv.y > ke || (kv.y == ke && f + 1 < e)) +
-              (kv.z > ke || (kv.z == ke && f + 2 < e)) + (kv.w > ke || (kv.w == ke && f + 3 < e));
+    for (int f0 = 0; f0 < E16 && rank < a.k; f0 += 16) {
+      float4 kv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) kv[q] = *reinterpret_cast<const float4*>(key + f0 + 4 * q);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int f = f0 + 4 * q;
+        rank += (kv[q].x > ke || (kv[q].x == ke && f < e)) +
+                (kv[q].y > ke || (kv[q].y == ke && f + 1 < e)) +
+                (kv[q].z > ke || (kv[q].z == ke && f + 2 < e)) +
+                (kv[q].w > ke || (kv[q].w == ke && f + 3 < e));
+      }
     }
     if (rank < a.k) {
       oid[rank] = e;
