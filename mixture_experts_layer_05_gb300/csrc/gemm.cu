@@ -72,7 +72,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                 const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                 const GemmLaunch args) {
-  if (threadIdx.x == 0) pdl_trigger();
   using S = Shape<KIND, BN, AROWS>;
   constexpr int kStages = S::kNumStages;
   extern __shared__ uint8_t smem_raw[];
@@ -118,7 +117,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();  // the set-up above overlapped the previous kernel; its outputs are now visible
+  // Decode w2: the producer sends the weight boxes of its first stages before it waits on
+  // the previous kernel. They depend only on the routing's expert blocks, and this kernel is
+  // launched only after the previous one got past its own wait, i.e. after the routing
+  // finished. Every other thread waits here.
+  constexpr bool kEarlyB = KIND == kGemmW2 && AROWS < kGemmBM;
+  if (!kEarlyB || warp != 0) pdl_wait();  // the set-up above overlapped the previous kernel
+  // the next kernel may launch once this one's inputs are complete (so that it, too, may
+  // rely on everything before this kernel having finished)
+  if (!kEarlyB && threadIdx.x == 0) pdl_trigger();
 
   Schedule sched;
   sched.init(args);
@@ -127,6 +134,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t wpolicy = l2_evict_first_policy();
+      uint32_t npre = 0;  // leading stages whose weight box went out before the wait
+      if (kEarlyB) {
+        for (int u = blockIdx.x; npre < (uint32_t)kStages && u < sched.units; u += gridDim.x) {
+          const Unit w = sched.unit(args, u);
+          const GemmProblem& P = args.p[w.p];
+          const CUtensorMap* tb = w.p ? &tmB1 : &tmB0;
+          int e = P.expert_ids ? P.expert_ids[w.mb] : 0;
+          if ((unsigned)e >= (unsigned)P.num_experts) e = 0;  // recorded below
+          const int b_row = e * P.b_rows_per_expert + w.nt * BN;
+          for (int kb = w.kb0; kb < w.kb1 && npre < (uint32_t)kStages; ++kb, ++npre) {
+            // the ring is empty: stage npre takes the npre-th K block
+            const uint32_t sb = base + npre * S::kStageBytes + S::kARegion;
+            mbar_expect_tx(full_bar(npre), S::kTxBytes);
+            tma_load_2d_hint(sb, tb, full_bar(npre), kb * kGemmBK, b_row, wpolicy);
+          }
+        }
+        pdl_wait();  // the A rows are the previous kernel's output
+        pdl_trigger();
+      }
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
@@ -144,12 +170,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
+          const uint32_t sa = base + s * S::kStageBytes;
+          const uint32_t sb = sa + S::kARegion;
+          if (it < npre) {  // its weight box is on its way already
+            tma_load_2d(sa, ta, full_bar(s), kb * kGemmBK, a_row);
+            continue;
+          }
           if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
           }
-          const uint32_t sa = base + s * S::kStageBytes;
-          const uint32_t sb = sa + S::kARegion;
           mbar_expect_tx(full_bar(s), S::kTxBytes);
           tma_load_2d(sa, ta, full_bar(s), kb * kGemmBK, a_row);
           if (AROWS < kGemmBM) {
