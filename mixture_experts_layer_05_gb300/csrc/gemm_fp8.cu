@@ -64,7 +64,6 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmA1,
                     const __grid_constant__ CUtensorMap tmB1, const GemmLaunch args) {
-  if (threadIdx.x == 0) pdl_trigger();
   constexpr int kStages = kF8Stages;
   constexpr int kBN = KIND == kGemmW13 ? 128 : 256;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
@@ -115,6 +114,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // the set-up above overlapped the previous kernel; its outputs are now visible
+  // the next kernel may launch once this one's inputs are complete (so that it, too, may
+  // rely on everything before this kernel having finished)
+  if (threadIdx.x == 0) pdl_trigger();
 
   Schedule sched;
   sched.init(args);
@@ -379,7 +381,6 @@ __global__ void __launch_bounds__(kSwThreads, 1)
                          const __grid_constant__ CUtensorMap tmB0,
                          const __grid_constant__ CUtensorMap tmA1,
                          const __grid_constant__ CUtensorMap tmB1, const GemmLaunch args) {
-  if (threadIdx.x == 0) pdl_trigger();
   constexpr int kStages = kSwStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -428,7 +429,13 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();  // the set-up above overlapped the previous kernel; its outputs are now visible
+  // w2: the producer sends the weight boxes of its first stages before it waits on the
+  // previous kernel. They depend only on the routing's expert blocks, and this kernel is
+  // launched only after the previous one got past its own wait, i.e. after the routing
+  // finished. Every other thread waits here.
+  constexpr bool kEarlyB = KIND == kGemmW2;
+  if (!kEarlyB || warp != 0) pdl_wait();  // the set-up above overlapped the previous kernel
+  if (!kEarlyB && threadIdx.x == 0) pdl_trigger();  // see the prefill kernel
 
   Schedule sched;
   sched.init(args);
@@ -438,6 +445,27 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t wpolicy = l2_evict_first_policy();
+      uint32_t npre = 0;  // leading stages whose weight boxes went out before the wait
+      if (kEarlyB) {
+        for (int u = blockIdx.x; npre < (uint32_t)kStages && u < sched.units; u += gridDim.x) {
+          const Unit w = sched.unit(args, u);
+          const GemmProblem& P = args.p[w.p];
+          const CUtensorMap* tb = w.p ? &tmB1 : &tmB0;
+          int e = P.expert_ids ? P.expert_ids[w.mb] : 0;
+          if ((unsigned)e >= (unsigned)P.num_experts) e = 0;  // recorded below
+          const int b_row = e * P.b_rows_per_expert + w.nt * kTileCols;
+          for (int kb = w.kb0; kb < w.kb1 && npre < (uint32_t)kStages; ++kb, ++npre) {
+            // the ring is empty: stage npre takes the npre-th K block
+            const uint32_t sw = base + npre * kSwStageBytes;
+            mbar_expect_tx(full_bar(npre), kSwStageBytes);
+            tma_load_2d_hint(sw, tb, full_bar(npre), kb * kF8BK, b_row, wpolicy);
+            tma_load_2d_hint(sw + 128 * kF8BK, tb, full_bar(npre), kb * kF8BK, b_row + 128,
+                             wpolicy);
+          }
+        }
+        pdl_wait();  // the token rows are the previous kernel's output
+        pdl_trigger();
+      }
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
@@ -455,11 +483,15 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
+          const uint32_t sw = base + s * kSwStageBytes;
+          if (it < npre) {  // its weight boxes are on their way already
+            tma_load_2d(sw + 256 * kF8BK, ta, full_bar(s), kb * kF8BK, w.mb * kGemmBM);
+            continue;
+          }
           if (!wait_fast(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
           }
-          const uint32_t sw = base + s * kSwStageBytes;
           mbar_expect_tx(full_bar(s), kSwStageBytes);
           // each weight tile has a single reader here: stream it through L2 first-out
           tma_load_2d_hint(sw, tb, full_bar(s), kb * kF8BK, b_row, wpolicy);
