@@ -16,6 +16,8 @@
 //   scatter one CTA per chunk; its warps own consecutive slices, count them, take
 //           start offsets in slice order, and walk their slices in order, ranking
 //           equal experts in each 32-wide step with __match_any_sync: stable order.
+#include <climits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "route.cuh"
@@ -204,6 +206,33 @@ __global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restric
   }
 }
 
+// One warp copies one bf16 row of H8 16-byte vectors (times `scale` when `scaled`), with up
+// to eight loads in flight per lane.
+__device__ __forceinline__ void copy_row_warp(const uint4* __restrict__ src,
+                                              uint4* __restrict__ dst, int H8, int lane,
+                                              bool scaled, float scale) {
+  if (scaled) {
+    for (int j = lane; j < H8; j += 32) dst[j] = scale_bf16x8(__ldg(src + j), scale);
+    return;
+  }
+  int j = lane;
+  for (; j + 224 < H8; j += 256) {
+    uint4 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = __ldg(src + j + 32 * q);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) dst[j + 32 * q] = v[q];
+  }
+  for (; j + 96 < H8; j += 128) {
+    uint4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = __ldg(src + j + 32 * q);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[j + 32 * q] = v[q];
+  }
+  for (; j < H8; j += 32) dst[j] = __ldg(src + j);
+}
+
 // Small batches (T*k <= kAlignChunk): routing and the whole align in one CTA of
 // kSmallWarps warps, no global scratch. Warps route tokens (route.cuh) into shared
 // memory, count their slices of the flat indices per expert, the CTA scans the padded
@@ -214,7 +243,7 @@ constexpr int kSmallThreads = kSmallWarps * 32;
 constexpr int kBlockRouteMaxTokens = 4;  // route token by token with the whole CTA up to here
 
 template <int EPT>
-__global__ void __launch_bounds__(kSmallThreads)
+__global__ void __launch_bounds__(kSmallThreads, 1)
     route_align_small_kernel(TopkArgs a, int bs, int* __restrict__ sorted,
                              int* __restrict__ expert_ids, int max_blocks, int* __restrict__ npp,
                              int2* __restrict__ block_seg, int* __restrict__ inv,
@@ -247,6 +276,58 @@ __global__ void __launch_bounds__(kSmallThreads)
     }
   }
   __syncthreads();
+  // 1'. at most 32 rows (the tiniest batches, T <= kBlockRouteMaxTokens): every active
+  //     expert holds fewer rows than a block, so each gets exactly one block, in ascending
+  //     expert order. One warp ranks the experts and places the rows (stable: a row's
+  //     place in its block counts the lower flat indices of its expert); no pass over all
+  //     E experts.
+  if constexpr (EPT == 0) {
+    if (n <= 32 && bs >= 32) {
+      int* s_slot = wcnt;       // [32] slot of each flat index
+      int* s_bcnt = wcnt + 32;  // [32] rows of each block
+      __shared__ int s_nact;
+      if (warp == 0) {
+        const int f = lane;
+        const bool v = f < n;
+        int e = v ? s_ids[f] : INT_MAX;
+        if (v && (unsigned)e >= (unsigned)E) e = 0;
+        const unsigned lt = (1u << lane) - 1u;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const bool first = v && (peers & lt) == 0u;
+        const unsigned firsts = __ballot_sync(0xffffffffu, first);
+        int rank = 0;  // active experts below e
+        for (int i = 0; i < 32; ++i) {
+          const int ei = __shfl_sync(0xffffffffu, e, i);
+          rank += ((firsts >> i) & 1u) && ei < e;
+        }
+        if (v) {
+          const int slot = rank * bs + __popc(peers & lt);
+          s_slot[f] = slot;
+          sorted[slot] = f;
+          if (inv) inv[f] = slot;
+        }
+        if (first) {
+          expert_ids[rank] = e;
+          if (block_seg) block_seg[rank] = make_int2(rank, 1);
+          s_bcnt[rank] = __popc(peers);
+        }
+        if (lane == 0) {
+          s_nact = __popc(firsts);
+          *npp = __popc(firsts) * bs;
+        }
+      }
+      __syncthreads();
+      const int nact = s_nact;
+      for (int b = nact + threadIdx.x; b < max_blocks; b += blockDim.x) expert_ids[b] = -1;
+      for (int q = threadIdx.x; q < nact * bs; q += blockDim.x)
+        if (q % bs >= s_bcnt[q / bs]) sorted[q] = n;  // the padding slots
+      if (xp)
+        for (int f = warp; f < n; f += kSmallWarps)  // the weights were written above
+          copy_row_warp(x + (size_t)(f / a.k) * H8, xp + (size_t)s_slot[f] * H8, H8, lane,
+                        row_scale != nullptr, row_scale ? a.weights[f] : 1.f);
+      return;
+    }
+  }
   // 2. per-warp slice counts
   const unsigned lt = (1u << lane) - 1u;
   const int slice = (n + kSmallWarps - 1) / kSmallWarps;
@@ -332,29 +413,15 @@ __global__ void __launch_bounds__(kSmallThreads)
       if ((peers & lt) == 0u) cnt[e] += __popc(peers);
     }
     __syncwarp();
-    // 5. tiny batches: the warp also copies its rows into expert order
+    // 5. tiny batches: the warp also copies its rows into expert order (the weights were
+    //    written by this CTA's routing)
     if (xp) {
       for (int i = 0; i < 32; ++i) {
         const int fi = base + i;
         if (fi >= s1) break;
         const int pi = __shfl_sync(0xffffffffu, slot, i);
-        const uint4* src = x + (size_t)(fi / a.k) * H8;
-        uint4* dst = xp + (size_t)pi * H8;
-        if (row_scale) {                 // the weights were written by this CTA's routing
-          const float sc = a.weights[fi];
-          for (int jj = lane; jj < H8; jj += 32) dst[jj] = scale_bf16x8(__ldg(src + jj), sc);
-          continue;
-        }
-        int j = lane;
-        for (; j + 96 < H8; j += 128) {             // four 16-byte loads in flight per lane
-          const uint4 v0 = __ldg(src + j), v1 = __ldg(src + j + 32);
-          const uint4 v2 = __ldg(src + j + 64), v3 = __ldg(src + j + 96);
-          dst[j] = v0;
-          dst[j + 32] = v1;
-          dst[j + 64] = v2;
-          dst[j + 96] = v3;
-        }
-        for (; j < H8; j += 32) dst[j] = __ldg(src + j);
+        copy_row_warp(x + (size_t)(fi / a.k) * H8, xp + (size_t)pi * H8, H8, lane,
+                      row_scale != nullptr, row_scale ? a.weights[fi] : 1.f);
       }
     }
   }

@@ -130,6 +130,37 @@ def _layer(w, wts, T):
                             max_tokens=max(T, 1)), d
 
 
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 16])
+def test_forward_small_batch_align_bitexact(cuda_lib, name, T):
+    """The one-CTA routing + align of small batches (a one-warp align for at most 32 rows,
+    the per-warp slices above that) writes exactly the oracle's sorted_token_ids,
+    expert_ids and num_tokens_post_padded into the forward's workspace."""
+    w = SMALL[name]
+    wts = inputs.make_weights(w, 0)
+    x, logits = tokens(w, T, wts["bias"], 3)
+    layer, _ = _layer(w, wts, T)
+    y = layer(x.to(DEV), logits.to(DEV))
+    torch.cuda.synchronize()
+    assert layer.device_status() == binding.OK
+    bs = binding.moe_forward_block_size(layer.cfg, T)
+    y_ref, parts = oracle.fused_moe(x, logits, wts["bias"], wts["w13"], wts["w2"],
+                                    wts["shared_w13"], wts["shared_w2"], return_parts=True,
+                                    **oracle_cfg(w))
+    s_ref, e_ref, n_ref = oracle.moe_align_block_size(parts["topk_ids"], w.num_experts, bs)
+    lay = binding.moe_forward_workspace_layout(layer.cfg, T)
+    ws = layer.workspace
+    npp = int(ws[lay.num_tokens_post_padded:lay.num_tokens_post_padded + 4].view(torch.int32))
+    assert npp == n_ref
+    srt = ws[lay.sorted_token_ids:lay.sorted_token_ids + npp * 4].view(torch.int32).cpu().numpy()
+    assert np.array_equal(srt, s_ref)
+    max_blocks = (T * w.top_k + w.num_experts * (bs - 1)) // bs + 1
+    eid = ws[lay.expert_ids:lay.expert_ids + max_blocks * 4].view(torch.int32).cpu().numpy()
+    assert np.array_equal(eid[:npp // bs], e_ref)
+    assert (eid[npp // bs:] == -1).all()
+    check_close(y, y_ref, f"{name} T={T}")
+
+
 def _routing_from_ws(layer, T, k):
     lay = binding.moe_forward_workspace_layout(layer.cfg, T)
     ws = layer.workspace
