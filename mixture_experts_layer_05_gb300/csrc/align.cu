@@ -193,16 +193,15 @@ __global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restric
       for (int i = threadIdx.x; i < H8; i += blockDim.x) dst[i] = scale_bf16x8(__ldg(src + i), sc);
       continue;
     }
-    int i = threadIdx.x;
-    for (; i + 3 * 128 < H8; i += 4 * 128) {       // four 16-byte loads in flight per thread
-      const uint4 v0 = __ldg(src + i), v1 = __ldg(src + i + 128);
-      const uint4 v2 = __ldg(src + i + 256), v3 = __ldg(src + i + 384);
-      dst[i] = v0;
-      dst[i + 128] = v1;
-      dst[i + 256] = v2;
-      dst[i + 384] = v3;
+    for (int i0 = threadIdx.x; i0 < H8; i0 += 8 * 128) {  // up to eight loads in flight
+      uint4 v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (i0 + 128 * q < H8) v[q] = __ldg(src + i0 + 128 * q);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (i0 + 128 * q < H8) dst[i0 + 128 * q] = v[q];
     }
-    for (; i < H8; i += 128) dst[i] = __ldg(src + i);
   }
 }
 

@@ -546,6 +546,7 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
       P.num_flat = L.n;
       P.part = at<float>(workspace, L.part_r);
       P.part_split_stride = (long long)L.n * 2 * I;
+      P.flat_row = inv;
     }
     if (Is) {
       GemmProblem& P = g1.p[1];
@@ -669,6 +670,7 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
     P.clamp_limit = c.swiglu_limit;
     P.alpha = alpha;
     P.expert_of_flat = tids;
+    P.flat_row = inv;
     P.k_blocks = H / kGemmBK;
     P.m_rows_dev = npp;
     P.max_m_blocks = L.max_sorted / L.bs;

@@ -93,21 +93,29 @@ __global__ void __launch_bounds__(128) silu_reduce_fp8_kernel(const __grid_const
   int routed_rows = npp ? *npp : R.m_rows_host;
   if (routed_rows > max_routed_rows) routed_rows = max_routed_rows;
   const int shared_rows = L.num_problems > 1 ? L.p[1].store_rows : 0;
-  for (int r = blockIdx.x; r < max_routed_rows + shared_rows; r += gridDim.x) {
+  // routed work items: the flat indices (through their sorted rows) or every sorted row
+  const int routed_items = R.flat_row ? R.num_flat : max_routed_rows;
+  for (int r = blockIdx.x; r < routed_items + shared_rows; r += gridDim.x) {
     const GemmProblem* P;
     int src, dst_row, pi;
-    if (r < max_routed_rows) {
-      if (r >= routed_rows) continue;
+    if (r < routed_items) {
       P = &L.p[0];
       pi = 0;
-      const int f = P->sorted_ids ? P->sorted_ids[r] : r;
-      if (f < 0 || f >= P->num_flat) continue;  // padding rows are never read back
-      src = f;
-      dst_row = r;
+      if (P->flat_row) {
+        src = r;
+        dst_row = P->flat_row[r];
+        if (dst_row < 0 || dst_row >= routed_rows) continue;
+      } else {
+        if (r >= routed_rows) continue;
+        const int f = P->sorted_ids ? P->sorted_ids[r] : r;
+        if (f < 0 || f >= P->num_flat) continue;  // padding rows are never read back
+        src = f;
+        dst_row = r;
+      }
     } else {
       P = &L.p[1];
       pi = 1;
-      src = dst_row = r - max_routed_rows;
+      src = dst_row = r - routed_items;
     }
     const int N = P->ldo;
     const int nsp = splits_of(L, pi);
@@ -183,7 +191,8 @@ cudaError_t launch_quant_gather_fp8(const void* x, int H, const int* inv, int n,
 
 cudaError_t launch_silu_reduce_fp8(const GemmLaunch& L, const int* npp, int max_routed_rows,
                                    cudaStream_t stream) {
-  const int rows = max_routed_rows + (L.num_problems > 1 ? L.p[1].store_rows : 0);
+  const int rows = (L.p[0].flat_row ? L.p[0].num_flat : max_routed_rows) +
+                   (L.num_problems > 1 ? L.p[1].store_rows : 0);
   int grid = num_sms() * 4;
   if (rows < grid) grid = rows;
   if (grid < 1) return cudaSuccess;

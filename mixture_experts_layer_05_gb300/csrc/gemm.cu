@@ -768,17 +768,26 @@ __global__ void __launch_bounds__(128) silu_reduce_kernel(const __grid_constant_
   int routed_rows = npp ? *npp : R.m_rows_host;
   if (routed_rows > max_routed_rows) routed_rows = max_routed_rows;
   const int shared_rows = L.num_problems > 1 ? L.p[1].store_rows : 0;
-  for (int r = blockIdx.x; r < max_routed_rows + shared_rows; r += gridDim.x) {
+  // routed work items: the flat indices (through their sorted rows) or every sorted row
+  const int routed_items = R.flat_row ? R.num_flat : max_routed_rows;
+  for (int r = blockIdx.x; r < routed_items + shared_rows; r += gridDim.x) {
     const GemmProblem* P;
     int src, dst_row, row_gated = gated;
     const __nv_bfloat16* bias = nullptr;
-    if (r < max_routed_rows) {
-      if (r >= routed_rows) continue;
+    if (r < routed_items) {
       P = &L.p[0];
-      const int f = P->sorted_ids ? P->sorted_ids[r] : r;
-      if (f < 0 || f >= P->num_flat) continue;          // padding rows are never read back
+      int f;
+      if (P->flat_row) {
+        f = r;
+        dst_row = P->flat_row[r];
+        if (dst_row < 0 || dst_row >= routed_rows) continue;
+      } else {
+        if (r >= routed_rows) continue;
+        f = P->sorted_ids ? P->sorted_ids[r] : r;
+        if (f < 0 || f >= P->num_flat) continue;        // padding rows are never read back
+        dst_row = r;
+      }
       src = f;
-      dst_row = r;
       if (P->bias && P->expert_of_flat) {
         int e = P->expert_of_flat[f];
         if ((unsigned)e >= (unsigned)P->num_experts) e = 0;
@@ -786,7 +795,7 @@ __global__ void __launch_bounds__(128) silu_reduce_kernel(const __grid_constant_
       }
     } else {
       P = &L.p[1];                                      // the shared expert: always gated
-      src = dst_row = r - max_routed_rows;
+      src = dst_row = r - routed_items;
       row_gated = 1;
     }
     const int N = P->ldo;
@@ -950,7 +959,8 @@ cudaError_t launch_wait_selftest(int* status, int timeout_us, cudaStream_t strea
 
 cudaError_t launch_silu_reduce(const GemmLaunch& L, const int* npp, int max_routed_rows,
                                bool gated, cudaStream_t stream) {
-  const int rows = max_routed_rows + (L.num_problems > 1 ? L.p[1].store_rows : 0);
+  const int rows = (L.p[0].flat_row ? L.p[0].num_flat : max_routed_rows) +
+                   (L.num_problems > 1 ? L.p[1].store_rows : 0);
   int grid = num_sms() * 4;
   if (rows < grid) grid = rows;
   if (grid < 1) return cudaSuccess;

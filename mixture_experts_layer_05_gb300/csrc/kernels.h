@@ -128,6 +128,8 @@ struct GemmProblem {
   float clamp_limit;         // gated first GEMM: > 0 clamps gate <= L and up to [-L, L]
   float alpha;               // gated first GEMM: act = g * sigmoid(alpha g) * u
   const int* expert_of_flat; // split reduce: expert of each flat index (for the bias)
+  const int* flat_row;       // split reduce: sorted row of each flat index, or NULL (then
+                             // the reduce walks every sorted row)
   float* part;             // first GEMM with splits > 1: fp32 [splits][row][2 ldo] (gate | up;
                            // [row][ldo] non-gated), row = flat index (routed) or token
   long long part_split_stride;
