@@ -90,12 +90,18 @@ KERNEL_SOURCES = {"gemm.cu": ("gemm.cu", "tc.cuh", "common.cuh", "kernels.h"),
 
 
 def source_digest(source: str) -> str:
-    """sha1 over a GEMM translation unit and the headers it compiles in."""
+    """sha1 over the code of a GEMM translation unit and the headers it compiles in, with
+    comments and blank lines dropped (a comment-only edit keeps the digest)."""
     import hashlib
+    import re
     h = hashlib.sha1()
     for name in KERNEL_SOURCES.get(source, (source,)):
-        with open(os.path.join(ROOT, "mixture_experts_layer_05_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "mixture_experts_layer_05_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(code.encode())
     return h.hexdigest()
 
 

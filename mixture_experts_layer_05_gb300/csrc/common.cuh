@@ -19,7 +19,10 @@ constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;
 // stream is still running: pdl_wait() blocks until that kernel has completed and its
 // writes are visible (a no-op for an ordinary launch), and pdl_trigger() lets the next
 // kernel begin launching. Every kernel calls pdl_wait() before it reads anything an
-// earlier kernel of the stream wrote.
+// earlier kernel of the stream wrote, with one exception: the decode w2 GEMMs read the
+// routing's expert blocks before they wait. That is safe because the GEMMs trigger their
+// dependents only after their own wait, so a w2 GEMM starts only once everything before
+// the w13 GEMM (the routing included) has finished; the small kernels trigger at entry.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
