@@ -38,3 +38,20 @@ def test_layer_work_counts():
 
 def test_traffic_lookup_needs_matching_source():
     assert bench.kernel_traffic("gemm_w13", "no-such-workload", 1) is None
+
+
+def test_source_digest_ignores_comments_not_code(tmp_path, monkeypatch):
+    """The traffic digest keys on code: a comment-only edit keeps it, a code edit changes it."""
+    csrc = tmp_path / "mixture_experts_layer_05_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    src_dir = os.path.join(ROOT, "mixture_experts_layer_05_gb300", "csrc")
+    for name in bench.KERNEL_SOURCES["gemm.cu"]:
+        (csrc / name).write_text(open(os.path.join(src_dir, name)).read())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    d0 = bench.source_digest("gemm.cu")
+    common = csrc / "common.cuh"
+    text = common.read_text()
+    common.write_text("// a new comment line\n" + text.replace("\n", "  // trailing note\n", 1))
+    assert bench.source_digest("gemm.cu") == d0
+    common.write_text(text + "\nconstexpr int kDigestProbe = 1;\n")
+    assert bench.source_digest("gemm.cu") != d0
