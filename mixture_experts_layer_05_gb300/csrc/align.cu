@@ -262,9 +262,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) wcnt[i] = 0;
   for (int i = threadIdx.x; i < a.zero_count; i += blockDim.x) a.zero[i] = 0;
-  // 1. routing: EPT = 0 (the tiniest batches) routes token by token with the whole CTA, in
-  //    compact code (this kernel starts each forward, and its code is fetched cold after the
-  //    expert GEMMs have streamed through L2); else a warp per token
+  // 1. routing: EPT = 0 (a single token) routes it with the whole CTA, in compact code (this
+  //    kernel starts each forward, and its code may have to come from HBM after the expert
+  //    GEMMs streamed through L2); else a warp per token
   if constexpr (EPT == 0) {
     float* rsm = reinterpret_cast<float*>(wcnt + kSmallWarps * E);
     for (int t = 0; t < a.T; ++t) {
