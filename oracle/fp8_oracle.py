@@ -159,14 +159,17 @@ def expert_mlp_fp8(xd, w13_q, w13_s, w2_q, w2_s) -> np.ndarray:
     return quant_dequant(act) @ W2.T
 
 
-def fused_moe_fp8(x, logits, bias, w13_q, w13_s, w2_q, w2_s, shared_w13_q=None,
-                  shared_w13_s=None, shared_w2_q=None, shared_w2_s=None, *,
-                  return_parts=False, **cfg):
-    """y [T, H] fp64 of the fp8 layer: routing as the bf16 layer, x quantized once."""
+def experts_combine_fp8(x, topk_weights, topk_ids, w13_q, w13_s, w2_q, w2_s,
+                        shared_w13_q=None, shared_w13_s=None, shared_w2_q=None,
+                        shared_w2_s=None, *, return_parts=False, top_k=None):
+    """y [T, H] fp64 of the fp8 experts and the combine for a routing given as input (the
+    precomputed top-k of ``FusedMoE.forward(hidden_states, topk_output)``): x is quantized
+    once per token and group of 128 and feeds the routed and the shared experts."""
     X = _mo._f64(x)
     T, H = X.shape
-    W, ids = _mo.select_experts(logits, bias, **cfg)
-    k = cfg["top_k"]
+    W = np.atleast_2d(np.asarray(topk_weights, dtype=np.float64))
+    ids = np.atleast_2d(np.asarray(topk_ids, dtype=np.int64))
+    k = ids.shape[1] if top_k is None else top_k
     xd = quant_dequant(X) if T else np.zeros((0, H))
     o = np.zeros((T, k, H), dtype=np.float64)
     for e in sorted(set(ids.reshape(-1).tolist())):
@@ -187,3 +190,14 @@ def fused_moe_fp8(x, logits, bias, w13_q, w13_s, w2_q, w2_s, shared_w13_q=None,
         return y, {"topk_weights": W, "topk_ids": ids, "expert_out": o, "shared": shared,
                    "x_dequant": xd}
     return y
+
+
+def fused_moe_fp8(x, logits, bias, w13_q, w13_s, w2_q, w2_s, shared_w13_q=None,
+                  shared_w13_s=None, shared_w2_q=None, shared_w2_s=None, *,
+                  return_parts=False, **cfg):
+    """y [T, H] fp64 of the fp8 layer: routing as the bf16 layer, then
+    ``experts_combine_fp8``."""
+    W, ids = _mo.select_experts(logits, bias, **cfg)
+    return experts_combine_fp8(x, W, ids, w13_q, w13_s, w2_q, w2_s, shared_w13_q,
+                               shared_w13_s, shared_w2_q, shared_w2_s,
+                               return_parts=return_parts, top_k=cfg["top_k"])

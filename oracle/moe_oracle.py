@@ -231,19 +231,25 @@ def expert_mlp(h, w13_e, w2_e, *, b13_e=None, b2_e=None, gated=True, swiglu_limi
 
 
 # ---------------------------------------------------------------- 8. the layer
-def fused_moe(x, logits, bias, w13, w2, shared_w13=None, shared_w2=None, *,
-              return_parts=False, w13_bias=None, w2_bias=None, gated=True, swiglu_limit=None,
-              gemm1_alpha=1.0, apply_router_weight_on_input=False, **cfg):
-    """y [T, H] fp64 = routed experts (weighted, combined) + shared expert.
+def experts_combine(x, topk_weights, topk_ids, w13, w2, shared_w13=None, shared_w2=None, *,
+                    return_parts=False, w13_bias=None, w2_bias=None, gated=True,
+                    swiglu_limit=None, gemm1_alpha=1.0, apply_router_weight_on_input=False,
+                    top_k=None):
+    """y [T, H] fp64 of the experts and the combine for a routing given as input.
 
-    With ``apply_router_weight_on_input`` (FusedMoE constructor argument) the routing
-    weight scales the expert's input instead of its output. The shared expert
-    (``DeepseekV2MLP``: no bias, alpha 1) shares the SwiGLU limit.
+    This is the layer behind a precomputed top-k (``FusedMoE.forward(hidden_states,
+    topk_output)`` with a ``StandardTopKOutput(topk_weights, topk_ids, ...)`` on the sglang
+    ``fused_moe_triton/layer.py`` page): each (token, slot) runs its expert's MLP, the
+    outputs are summed with the routing weights over slots j ascending, then the shared
+    expert is added unscaled. With ``apply_router_weight_on_input`` (FusedMoE constructor
+    argument) the routing weight scales the expert's input instead of its output. The
+    shared expert (``DeepseekV2MLP``: no bias, alpha 1) shares the SwiGLU limit.
     """
     X = _f64(x)
     T, H = X.shape
-    W, ids = select_experts(logits, bias, **cfg)
-    k = cfg["top_k"]
+    W = np.atleast_2d(np.asarray(topk_weights, dtype=np.float64))
+    ids = np.atleast_2d(np.asarray(topk_ids, dtype=np.int64))
+    k = ids.shape[1] if top_k is None else top_k
     o = np.zeros((T, k, H), dtype=np.float64)
     for e in sorted(set(ids.reshape(-1).tolist())):           # each expert's weights once
         rows = [(t, j) for t in range(T) for j in range(k) if ids[t, j] == e]
@@ -268,6 +274,19 @@ def fused_moe(x, logits, bias, w13, w2, shared_w13=None, shared_w2=None, *,
     if return_parts:
         return y, {"topk_weights": W, "topk_ids": ids, "expert_out": o, "shared": shared}
     return y
+
+
+def fused_moe(x, logits, bias, w13, w2, shared_w13=None, shared_w2=None, *,
+              return_parts=False, w13_bias=None, w2_bias=None, gated=True, swiglu_limit=None,
+              gemm1_alpha=1.0, apply_router_weight_on_input=False, **cfg):
+    """y [T, H] fp64 = routed experts (weighted, combined) + shared expert: the routing of
+    ``select_experts`` followed by ``experts_combine``."""
+    W, ids = select_experts(logits, bias, **cfg)
+    return experts_combine(x, W, ids, w13, w2, shared_w13, shared_w2,
+                           return_parts=return_parts, w13_bias=w13_bias, w2_bias=w2_bias,
+                           gated=gated, swiglu_limit=swiglu_limit, gemm1_alpha=gemm1_alpha,
+                           apply_router_weight_on_input=apply_router_weight_on_input,
+                           top_k=cfg["top_k"])
 
 
 def fused_moe_rows(x_rows, logits_rows, bias, w13, w2, shared_w13=None, shared_w2=None,

@@ -347,12 +347,131 @@ def test_empty_batch():
     assert y.shape == (0, 4)
 
 
+# ------------------------------------------------------------------ decision margins
+MARGINS = os.path.join(os.path.dirname(__file__), "golden", "margin_hand_examples.json")
+
+
+def pin_hand_margins():
+    """decision_margins on hand-worked rows, one per kind of decision: a softmax top-k gap
+    (logit units), a biased sigmoid key gap, a kept/dropped group gap under each group rule."""
+    with open(MARGINS) as f:
+        cases = json.load(f)["cases"]
+    for case in cases:
+        logits = np.log(np.array(case["exp_logits"], dtype=np.float64))[None]
+        bias = None if case["bias"] is None else np.array(case["bias"])
+        m = oracle.decision_margins(logits, bias, **_cfg(**case["cfg"]))
+        assert abs(m[0] - case["margin"]) <= 1e-9, (case["name"], m[0], case["margin"])
+
+
+def _decision_plain(logits, bias, cfg):
+    """(kept groups, ordered ids) of one row by plain sorting, written apart from the oracle:
+    scores by scipy, group scores (largest score, or the two largest biased keys), the
+    topk_group best groups, then the top_k best eligible keys in descending order."""
+    E, k = cfg["num_experts"], cfg["top_k"]
+    s = expit(logits) if cfg["scoring_func"] == "sigmoid" else softmax(logits)
+    q = s + bias if bias is not None else s
+    elig = list(range(E))
+    kept = None
+    if cfg["use_grouped_topk"]:
+        G, g = cfg["num_expert_group"], cfg["topk_group"]
+        size = E // G
+        gs = []
+        for x in range(G):
+            mem = q[x * size:(x + 1) * size] if bias is not None else s[x * size:(x + 1) * size]
+            top = sorted(mem, reverse=True)
+            gs.append(top[0] + top[1] if bias is not None else top[0])
+        kept = frozenset(sorted(range(G), key=lambda x: (-gs[x], x))[:g])
+        elig = [e for e in elig if e // size in kept]
+    return kept, tuple(sorted(elig, key=lambda e: (-q[e], e))[:k])
+
+
+def _perturbed(logits, bias, cfg, e, delta):
+    """Move the selection key of expert e by delta: in logit units for softmax without a bias
+    (shift the logit), in key units otherwise (shift the bias entry, or, for unbiased sigmoid
+    scores, the logit that moves the score by delta). None if the score would leave (0, 1)."""
+    lg = logits.copy()
+    if bias is not None:
+        b = bias.copy()
+        b[e] += delta
+        return lg, b
+    if cfg["scoring_func"] == "softmax":
+        lg[e] += delta
+        return lg, None
+    s = expit(lg[e]) + delta
+    if not 0.0 < s < 1.0:
+        return None
+    lg[e] = math.log(s / (1.0 - s))
+    return lg, None
+
+
+def _brute_margin(logits, bias, cfg, span=4.0, steps=48):
+    """Smallest move of one selection key that changes the decision, by bisection over each
+    expert and direction (a key moved one way changes its rank monotonically)."""
+    base = _decision_plain(logits, bias, cfg)
+    best = math.inf
+    for e in range(cfg["num_experts"]):
+        for sign in (1.0, -1.0):
+            def changed(d):
+                p = _perturbed(logits, bias, cfg, e, sign * d)
+                return p is not None and _decision_plain(p[0], p[1], cfg) != base
+            hi = span
+            if not changed(hi):
+                # unbiased sigmoid: the score range caps the move; shrink to the largest valid
+                while hi > 1e-6 and _perturbed(logits, bias, cfg, e, sign * hi) is None:
+                    hi /= 2
+                if not changed(hi):
+                    continue
+            lo = 0.0
+            for _ in range(steps):
+                mid = 0.5 * (lo + hi)
+                if changed(mid):
+                    hi = mid
+                else:
+                    lo = mid
+            best = min(best, hi)
+    return best
+
+
+def pin_margins_bruteforce(n_cases=36):
+    """decision_margins equals the smallest single-key move that changes which groups
+    survive or which experts are chosen (in which order), on small random rows of every
+    routing branch."""
+    rng = np.random.default_rng(12)
+    kinds = ["softmax", "softmax_bias", "softmax_grouped", "sigmoid_grouped_bias",
+             "sigmoid_grouped"]
+    for c in range(n_cases):
+        kind = kinds[c % len(kinds)]
+        G = int(rng.choice([2, 3, 4]))
+        size = int(rng.choice([2, 3]))
+        E = G * size
+        grouped = "grouped" in kind
+        g = int(rng.integers(1, G + 1)) if grouped else 0
+        k = int(rng.integers(1, min((g * size) if grouped else E, 3) + 1))
+        cfg = _cfg(num_experts=E, top_k=k, use_grouped_topk=grouped,
+                   num_expert_group=G if grouped else 0, topk_group=g,
+                   scoring_func="sigmoid" if kind.startswith("sigmoid") else "softmax")
+        logits = rng.normal(size=E)
+        bias = rng.normal(scale=0.1, size=E) if "bias" in kind else None
+        m = oracle.decision_margins(logits[None], bias, **cfg)[0]
+        want = _brute_margin(logits, bias, cfg)
+        assert abs(m - want) <= 1e-9 * max(1.0, want), (c, kind, m, want)
+
+
+def test_hand_margins():
+    pin_hand_margins()
+
+
+def test_margins_bruteforce():
+    pin_margins_bruteforce()
+
+
 # ------------------------------------------------------------------ planted mistakes
 ALL_PINS = [pin_hand_routing, pin_hand_align, pin_hand_expert_mlp, pin_bruteforce_ungrouped,
             pin_bruteforce_grouped, pin_renormalized_softmax_closed_form,
             pin_sigmoid_weights_unbiased, pin_grouped_reduces_to_ungrouped,
             pin_routing_invariants, pin_align_bruteforce, pin_dense_swiglu_single_expert,
-            pin_identity_like_experts, pin_scaling_and_shared, pin_expert_relabeling]
+            pin_identity_like_experts, pin_scaling_and_shared, pin_expert_relabeling,
+            pin_hand_margins, pin_margins_bruteforce]
 
 
 def _caught(monkeypatch, name, fn):
@@ -415,3 +534,48 @@ def test_planted_mistake_is_caught(monkeypatch, name, fn):
     monkeypatch.setattr(oracle, name, fn, raising=False)
     caught = _caught(monkeypatch, name, fn)
     assert caught, f"no pin caught a planted mistake in {name}"
+
+
+def _margins_mutant(log_units=True, group_gap=True, extra=1):
+    """A copy of decision_margins with one step changed: gaps in score units instead of
+    logit units, the group gap left out, or the key order checked over top_k + extra."""
+    def margins(logits, bias, **cfg):
+        L = np.asarray(logits, dtype=np.float64)
+        out = np.full(L.shape[0], np.inf)
+        soft_log = log_units and cfg.get("scoring_func", "softmax") == "softmax" and bias is None
+        for t in range(L.shape[0]):
+            _, _, info = om.route_token(L[t], bias, **cfg)
+            q = np.log(info["keys"]) if soft_log else info["keys"]
+            m = np.inf
+            if group_gap and info["kept_groups"] is not None:
+                gsc = np.log(info["group_scores"]) if soft_log else info["group_scores"]
+                order = om._rank_desc(gsc, range(len(gsc)))
+                nk = len(info["kept_groups"])
+                if nk < len(order):
+                    m = min(m, gsc[order[nk - 1]] - gsc[order[nk]])
+            order = om._rank_desc(q, info["eligible"])[: cfg["top_k"] + extra]
+            for a, b in zip(order[:-1], order[1:]):
+                m = min(m, q[a] - q[b])
+            out[t] = m
+        return out
+    return margins
+
+
+@pytest.mark.parametrize("mutant", [dict(log_units=False), dict(group_gap=False),
+                                    dict(extra=2), dict(extra=0)],
+                         ids=["score_units", "no_group_gap", "k_plus_2", "k_only"])
+def test_planted_margin_mistake_is_caught(monkeypatch, mutant):
+    fn = _margins_mutant(**mutant)
+    monkeypatch.setattr(oracle, "decision_margins", fn, raising=False)
+    caught = _caught(monkeypatch, "decision_margins", fn)
+    assert caught, f"no pin caught the planted margin mistake {mutant}"
+
+
+def test_margin_mutant_copy_is_faithful(monkeypatch):
+    """The unmutated copy passes the margin pins (so each caught mutant is caught for its
+    change, not for a difference in the copy)."""
+    fn = _margins_mutant()
+    monkeypatch.setattr(oracle, "decision_margins", fn, raising=False)
+    monkeypatch.setattr(om, "decision_margins", fn)
+    pin_hand_margins()
+    pin_margins_bruteforce()
