@@ -1,17 +1,20 @@
 """Benchmark of the FusedMoE layer forward on GB300 (one JSON line on stdout).
 
-Default workload: the Mixtral-8x7B-shaped MoE layer (H=4096, I=14336, E=8, top_k=2,
-softmax + renormalize) at T=4096 tokens, bf16 weights ~N(0, 0.02) (2.8 GB, larger
-than L2, so no flush is needed between steps), activations ~N(0, 1), fp32 router
-logits ~N(0, 1), seed = rank.
+Default workload: the DeepSeek-V3-shaped MoE layer (H=7168, I=2048, E=256 routed experts,
+top_k=8, sigmoid scores + e_score_correction_bias, grouped top-k 8/4, renormalize,
+routed_scaling_factor 2.5, one shared expert of I=2048) at T=8192 tokens, the largest
+workload that fits one GPU: bf16 weights ~N(0, 0.02) (22.5 GB, far larger than L2, so no
+flush is needed between steps), activations ~N(0, 1), fp32 router logits ~N(0, 1), bias
+~N(0, 0.1), seed = rank.
 
 A step is one full forward through the C ABI (routing, align, gather, w13 GEMM +
 SiLU*mul, w2 GEMM, combine) on inputs resident in HBM. W warm-up steps, then K
 timed steps between a barrier + synchronize on both sides, CUDA events on the
 launching stream, max over ranks; ``value`` = tokens of all ranks / that time.
-``e2e`` is the same metric with pinned host inputs copied in and the output copied
-out inside each timed step. ``--impl reference`` times the CPU oracle instead, on a
-bounded token sample per step.
+``eager`` times the same steps launched without a graph; ``e2e`` is the same metric with
+pinned host inputs copied in and the output copied out inside each timed step.
+``--impl reference`` times the CPU oracle instead, on a bounded token sample per step.
+``--sweep T1,T2,...`` prints one line per token count instead (the skewed-routing sweep).
 
 Multi-GPU (torchrun): independent data-parallel replicas, each rank its own batch
 and a full copy of the weights; no collective on the data path (weak scaling).
@@ -191,6 +194,64 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- arms
+L2_BYTES = 129 * 2 ** 20          # GB300 L2
+
+
+def routing_stats(layer, cfg, w, T) -> dict:
+    """Routing facts of the last forward, read from its workspace: distinct experts, padded
+    row count, and the per-expert load (rows routed to each expert) relative to the mean."""
+    import torch
+    from mixture_experts_layer_05_gb300 import binding
+    lay = binding.moe_forward_workspace_layout(cfg, T)
+    ids = layer.workspace[lay.topk_ids:lay.topk_ids + T * w.top_k * 4].view(torch.int32)
+    cnt = torch.bincount(ids.long(), minlength=w.num_experts).cpu()
+    npp = int(layer.workspace[lay.num_tokens_post_padded:lay.num_tokens_post_padded + 4]
+              .view(torch.int32).item())
+    mean = T * w.top_k / w.num_experts
+    rel = cnt.double() / mean
+    edges = [0.0, 0.5, 1.0, 2.0, 4.0, 8.0, 16.0]
+    hist = {}
+    for a, b in zip(edges, edges[1:] + [float("inf")]):
+        n = int(((rel > a) & (rel <= b)).sum()) if a > 0 else int((rel <= b).sum())
+        hist[f"({a:g},{b:g}]" if a > 0 else f"[0,{b:g}]"] = n
+    return {"active_experts": int((cnt > 0).sum()), "rows_post_padded": npp,
+            "padding_frac": round(npp / (T * w.top_k) - 1.0, 4),
+            "max_load_over_mean": round(float(rel.max()), 3),
+            "top8_loads": sorted(cnt.tolist(), reverse=True)[:8],
+            "load_over_mean_hist": hist}
+
+
+def roofline_of(work: dict, t_s: float, peaks: dict, peak_src: str, fp8: bool, kname: str,
+                which: str = "w13") -> dict:
+    """Roofline of one kernel (its algorithmic flops and bytes over its duration): bound by
+    the larger of flops / tensor peak and bytes / HBM peak, both at the burst peak (a kernel
+    inside a short step); the sustained tensor fraction is reported beside it."""
+    ratio = 2.0 if fp8 else 1.0                      # e4m3 = 2 x the bf16 peak (nominal ratio)
+    burst = peaks["bf16_tflops"] * ratio
+    sustained = peaks["bf16_tflops_sustained"] * ratio
+    flops, byts = work[f"flops_{which}"], work[f"bytes_{which}"]
+    t_tc, t_hbm = flops / (burst * 1e12), byts / (peaks["hbm_gbs"] * 1e9)
+    tflops = flops / t_s / 1e12
+    gbs = byts / t_s / 1e9
+    src = f"{peak_src} bf16 burst (best of 10 cuBLAS GEMMs)" + (
+        " x 2, the nominal e4m3/bf16 ratio" if fp8 else "")
+    if t_tc >= t_hbm:
+        roof = {"kernel": kname, "bound": "tensor", "achieved": round(tflops, 1),
+                "peak": round(burst, 1), "unit": "TFLOP/s", "frac": round(tflops / burst, 4),
+                "peak_source": src}
+    else:
+        roof = {"kernel": kname, "bound": "hbm", "achieved": round(gbs, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm_gbs"], 4),
+                "peak_source": f"{peak_src} HBM copy bandwidth"}
+    roof.update({"tensor_frac_of_burst": round(tflops / burst, 4),
+                 "tensor_frac_of_sustained": round(tflops / sustained, 4),
+                 "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                 "ridge_frac": round(max(t_tc, t_hbm) / t_s, 4),
+                 "ms": round(t_s * 1e3, 4)})
+    return roof
+
+
 def run_ours(args, w, T):
     import torch
     import torch.distributed as dist
@@ -237,6 +298,7 @@ def run_ours(args, w, T):
     stage = {n: statistics.mean(e[a].elapsed_time(e[b]) for e in sevs)
              for n, a, b in (("route_align_gather", 0, 1), ("w13_gemm", 1, 2),
                              ("w2_gemm", 2, 3), ("combine", 3, 4))}
+    step_est_s = max(sum(stage.values()) * 1e-3, 1e-6)
 
     # timed region: K forwards captured once into a CUDA graph and replayed (no events in
     # it: a stage event would break the kernels' programmatic launch chain). The w13 GEMM's
@@ -265,12 +327,15 @@ def run_ours(args, w, T):
         graph = graph_w13 = None
         torch.cuda.synchronize()
 
+    def eager_steps():
+        for i in range(K):
+            layer(x, logits, out=out)
+
     def timed_steps():
         if graph is not None:
             graph.replay()
         else:
-            for i in range(K):
-                layer(x, logits, out=out)
+            eager_steps()
 
     def w13_steps():
         if graph_w13 is not None:
@@ -279,14 +344,31 @@ def run_ours(args, w, T):
             for i in range(K):
                 layer(x, logits, out=out, events=[None, wevs[i][0], wevs[i][1], None, None])
 
+    def warm(fn, seconds=0.5):
+        """Back-to-back steps until the GPU settles in its loaded power state."""
+        for _ in range(max(1, int(seconds / (step_est_s * K)))):
+            fn()
+
+    def timed(fn, s=None):
+        """(ms per step, wall start, wall end) of one K-step call on `s`, device-timed."""
+        s = s or stream
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        w0 = time.time()
+        a.record(s)
+        fn()
+        b.record(s)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / K, w0, time.time()
+
     if graph is not None:
         graph.replay()                               # one untimed replay of each graph
         graph_w13.replay()
     torch.cuda.synchronize()
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
-    for _ in range(max(1, int(0.5 / max(stage["w13_gemm"] * 1e-3 * K, 1e-6)))):
-        timed_steps()                                # warm the clocks for the sampler
+    warm(timed_steps)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -302,6 +384,9 @@ def run_ours(args, w, T):
         dist.barrier()
     ms = t_start.elapsed_time(t_end) / K
     ms_max = reduce_max(ms, dev)
+    # the same K forwards launched eagerly, in the same loaded state (informational)
+    warm(eager_steps, 0.2)
+    eager_ms, ew0, ew1 = timed(eager_steps)
     w13_steps()                                     # untimed: the w13 events for the roofline
     torch.cuda.synchronize()
     status = layer.device_status()
@@ -316,9 +401,6 @@ def run_ours(args, w, T):
         w13_ms = stage["w13_gemm"]
         w13_src = "w13 GEMM events of the eager stage pass"
         torch.cuda.synchronize()
-    clocks = sampler.summary(wall0, wall1) if sampler else None
-    if sampler:
-        sampler.stop()
 
     # end to end: pinned host inputs in, output out, inside each timed step; copies of
     # neighbouring steps overlap the forward (binding.HostPipeline)
@@ -332,57 +414,62 @@ def run_ours(args, w, T):
 
     e2e_run(W)
     torch.cuda.synchronize()
+    warm(lambda: e2e_run(K), 0.3)
+    torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    xw0 = time.time()
     e0.record(pipe.h2d)
     e2e_run(K)
     e1.record(pipe.d2h)
     torch.cuda.synchronize()
+    xw1 = time.time()
     e2e_ms = reduce_max(e0.elapsed_time(e1) / K, dev)
+    clocks = e_clocks = x_clocks = None
+    if sampler:
+        time.sleep(0.1)
+        clocks = sampler.summary(wall0, wall1)
+        e_clocks = sampler.summary(ew0, ew1)
+        x_clocks = sampler.summary(xw0, xw1)
+        sampler.stop()
 
-    # routing facts for the algorithmic work
-    lay = binding.moe_forward_workspace_layout(cfg, T)
-    ids = layer.workspace[lay.topk_ids:lay.topk_ids + T * w.top_k * 4].view(torch.int32)
-    n_active = int(torch.unique(ids).numel())
-    npp = int(layer.workspace[lay.num_tokens_post_padded:lay.num_tokens_post_padded + 4]
-              .view(torch.int32).item())
-    work = layer_work(w, T, n_active, fp8)
+    # cold L2 for working sets that fit in L2: each step after writing a buffer larger than
+    # L2, the forward alone timed by events (informational)
+    cold = None
+    weight_bytes = sum(v.numel() * v.element_size() for v in wts.values() if v is not None)
+    if weight_bytes < 3 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        for a, b in evs:
+            flush.fill_(1.0)
+            a.record(stream)
+            layer(x, logits, out=out)
+            b.record(stream)
+        torch.cuda.synchronize()
+        cold = {"ms_per_step": round(statistics.mean(a.elapsed_time(b) for a, b in evs), 4),
+                "how": "eager forwards, a 258 MB buffer written before each, events around "
+                       "the forward only"}
+
+    rs = routing_stats(layer, cfg, w, T)
+    work = layer_work(w, T, rs["active_experts"], fp8)
     peaks, peak_src = load_peaks()
-    # The timed region follows >= 0.5 s of back-to-back forwards, so the GEMMs run in the
-    # power-capped steady state: the sustained measured peak is the denominator (the burst
-    # fraction is reported beside it). The e4m3 peak is the bf16 one times the nominal dense
-    # ratio 4.5 / 2.25.
-    ratio = 2.0 if fp8 else 1.0
-    tc_peak = peaks["bf16_tflops_sustained"] * ratio
-    tc_burst = peaks["bf16_tflops"] * ratio
-    tc_src = (f"{peak_src} bf16 sustained (back-to-back GEMMs for 4 s)"
-              + (" x 2, the nominal e4m3/bf16 ratio" if fp8 else ""))
     kname = ("gemm_fp8_kernel<w13> (grouped e4m3 w13 GEMM + SiLU*mul + act quant)" if fp8
              else "gemm_kernel<w13> (grouped w13 GEMM + SiLU*mul)")
     value = aggregate_tokens_per_s(T, world, ms_max)
+    ratio = 2.0 if fp8 else 1.0
 
     res = None
     if rank == 0:
         # dominant kernel: the w13 grouped GEMM (two thirds of the flops and weight bytes)
-        t_w13 = w13_ms / 1e3
-        tensor_bound = work["flops_w13"] / (tc_peak * 1e12) >= \
-            work["bytes_w13"] / (peaks["hbm_gbs"] * 1e9)
-        if tensor_bound:
-            ach = work["flops_w13"] / t_w13 / 1e12
-            roof = {"kernel": kname, "bound": "tensor", "achieved": round(ach, 1),
-                    "peak": round(tc_peak, 1), "unit": "TFLOP/s", "frac": round(ach / tc_peak, 4),
-                    "peak_source": tc_src, "frac_of_burst_peak": round(ach / tc_burst, 4)}
-        else:
-            ach = work["bytes_w13"] / t_w13 / 1e9
-            roof = {"kernel": kname, "bound": "hbm", "achieved": round(ach, 1),
-                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": f"{peak_src}"}
+        roof = roofline_of(work, w13_ms / 1e3, peaks, peak_src, fp8, kname)
         roof["traffic"] = args.traffic if args.traffic is not None else (
             kernel_traffic("gemm_fp8_w13", w.name, T, "gemm_fp8.cu") if fp8
             else kernel_traffic("gemm_w13", w.name, T))
         step_s = ms_max / 1e3
+        tc_burst = peaks["bf16_tflops"] * ratio
         res = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
@@ -390,32 +477,117 @@ def run_ours(args, w, T):
             "data": "synthetic",
             "config": {"workload": f"{w.name}: FusedMoE layer H={w.hidden_size} "
                                    f"I={w.intermediate_size} E={w.num_experts} k={w.top_k}"
+                                   + (f" shared I={w.shared_intermediate_size}"
+                                      if w.shared_intermediate_size else "")
                                    + (" w8a8 fp8 block-128" if fp8 else ""),
                        "tokens_per_gpu": T, "global_batch": T * world,
                        "parallelism": f"dp{world} replicas",
-                       "l2": "inputs larger than L2 (expert weights streamed every step)",
+                       "l2": ("inputs larger than L2 (expert weights streamed every step)"
+                              if weight_bytes >= 3 * L2_BYTES else
+                              "weights fit in L2: value is warm-L2; cold_l2 flushes L2"),
                        "seed": "weights 0, tokens = rank"},
             "layer": {"tflops": round(work["flops"] / step_s / 1e12, 1),
-                      "tflops_frac": round(work["flops"] / step_s / 1e12 / tc_peak, 4),
+                      "tensor_frac_of_burst": round(work["flops"] / step_s / 1e12 / tc_burst, 4),
                       "hbm_gbs": round(work["bytes"] / step_s / 1e9, 1),
                       "hbm_frac": round(work["bytes"] / step_s / 1e9 / peaks["hbm_gbs"], 4),
-                      "active_experts": n_active, "rows_post_padded": npp,
+                      "ridge_frac": round(max(work["flops"] / (tc_burst * 1e12),
+                                              work["bytes"] / (peaks["hbm_gbs"] * 1e9))
+                                          / step_s, 4),
+                      **rs,
                       "stages_ms": {k: round(v, 4) for k, v in stage.items()},
                       "stages_note": "eager forwards with events at every stage boundary, "
                                      "outside the timed region"},
             "roofline": roof,
-            "timing": {"value": "one CUDA-graph replay of K captured forwards"
-                                if graph is not None else "K eager forwards",
+            "timing": {"value": "one CUDA-graph replay of K captured forwards, after >= 0.5 s "
+                                "of back-to-back replays" if graph is not None
+                                else "K eager forwards",
                        "roofline": w13_src},
+            "eager": {"ms_per_step": round(eager_ms, 4),
+                      "value": round(aggregate_tokens_per_s(T, 1, eager_ms), 1),
+                      "clocks": e_clocks,
+                      "note": "the same K forwards launched one by one (no graph), right after "
+                              "the timed region"},
             "e2e": {"value": round(aggregate_tokens_per_s(T, world, e2e_ms), 1),
                     "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
-                    "d2h_bytes_per_step": out.numel() * 2},
+                    "d2h_bytes_per_step": out.numel() * 2, "ms_per_step": round(e2e_ms, 4),
+                    "clocks": x_clocks},
             "gpu_launches": K * binding.moe_forward_num_launches(cfg, T),
             "clocks": clocks,
         }
+        if cold is not None:
+            res["cold_l2"] = cold
         if args.cpu_baseline and world == 1:
             res["cpu_baseline"] = cpu_baseline(w, wts, x_cpu, logits_cpu, args.cpu_sample, fp8=fp8)
     return res
+
+
+def run_sweep(args, w, token_counts):
+    """One JSON line per token count: graph-replayed forwards on the same weights, with the
+    routing's per-expert load histogram (the skewed-routing sweep)."""
+    import torch
+
+    from mixture_experts_layer_05_gb300 import binding, inputs
+    from mixture_experts_layer_05_gb300 import build as build_mod
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    build_mod.build()
+    binding.load()
+    fp8 = args.quant == "fp8"
+    Tmax = max(token_counts)
+    if fp8:
+        wts = inputs.make_fp8_weights(w, 0, device=dev)
+        cfg = binding.config_from_workload(w, weight_quant="fp8")
+        layer = binding.FusedMoE(cfg, wts["w13_q"], wts["w2_q"], wts["bias"], wts["shared_w13_q"],
+                                 wts["shared_w2_q"], max_tokens=Tmax, w13_scale=wts["w13_s"],
+                                 w2_scale=wts["w2_s"], shared_w13_scale=wts["shared_w13_s"],
+                                 shared_w2_scale=wts["shared_w2_s"])
+    else:
+        wts = inputs.make_weights(w, 0, device=dev)
+        cfg = binding.config_from_workload(w)
+        layer = binding.FusedMoE(cfg, wts["w13"], wts["w2"], wts["bias"], wts["shared_w13"],
+                                 wts["shared_w2"], max_tokens=Tmax)
+    peaks, peak_src = load_peaks()
+    ratio = 2.0 if fp8 else 1.0
+    K = args.steps
+    for T in token_counts:
+        x_cpu, l_cpu = inputs.make_tokens(w, T, seed=0)
+        x, lg = x_cpu.to(dev), l_cpu.to(dev)
+        out = torch.empty_like(x)
+        for _ in range(max(3, args.warmup)):
+            layer(x, lg, out=out)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream()
+        cs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=cs):
+            for _ in range(K):
+                layer(x, lg, out=out)
+        g.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / K
+        if layer.device_status() != binding.OK:
+            raise RuntimeError(f"device status error at T={T}")
+        rs = routing_stats(layer, cfg, w, T)
+        work = layer_work(w, T, rs["active_experts"], fp8)
+        t = ms / 1e3
+        print(json.dumps({
+            "sweep": w.name, "tokens": T, "dtype": "e4m3" if fp8 else "bf16",
+            "ms_per_step": round(ms, 4), "tokens_per_s": round(T / t, 1),
+            "layer_tflops": round(work["flops"] / t / 1e12, 1),
+            "tensor_frac_of_burst": round(work["flops"] / t / 1e12
+                                          / (peaks["bf16_tflops"] * ratio), 4),
+            "hbm_frac": round(work["bytes"] / t / 1e9 / peaks["hbm_gbs"], 4),
+            "ridge_frac": round(max(work["flops"] / (peaks["bf16_tflops"] * ratio * 1e12),
+                                    work["bytes"] / (peaks["hbm_gbs"] * 1e9)) / t, 4),
+            **rs}), flush=True)
+        del g
 
 
 def _host_weights(w, wts):
@@ -477,8 +649,13 @@ def run_reference(args, w, T):
         return None
     n = args.ref_sample if args.ref_sample > 0 else 1
     fp8 = args.quant == "fp8"
-    # CPU-generated: the oracle arm needs no GPU
-    hw = inputs.make_fp8_weights(w, 0) if fp8 else inputs.make_weights(w, 0)
+    # drawn where the GPU arm draws them (the same values), then held on the host; on a
+    # machine without a GPU, drawn on the CPU. Only the oracle's work is timed.
+    gen = "cuda" if torch.cuda.is_available() else "cpu"
+    hw = inputs.make_fp8_weights(w, 0, device=gen) if fp8 else inputs.make_weights(w, 0, device=gen)
+    hw = {key: (None if v is None else v.to("cpu")) for key, v in hw.items()}
+    if gen == "cuda":
+        torch.cuda.empty_cache()
     x_cpu, logits_cpu = inputs.make_tokens(w, T, seed=0)
 
     def step(i):
@@ -523,11 +700,14 @@ def run_reference(args, w, T):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mixtral")
-    ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--workload", default="dsv3")
+    ap.add_argument("--tokens", type=int, default=8192)
+    ap.add_argument("--sweep", default=None,
+                    help="comma-separated token counts: one JSON line per count (no contract "
+                         "line); e.g. the skewed-routing sweep 1,2,4,...,16384")
     ap.add_argument("--quant", choices=["none", "fp8"], default="none",
                     help="expert weights: bf16 (none) or e4m3 with 128 x 128 fp32 block scales")
     ap.add_argument("--cpu-sample", type=int, default=4,
@@ -541,6 +721,9 @@ def main(argv=None):
     args.warmup = max(args.warmup, 3)
     from mixture_experts_layer_05_gb300 import configs
     w = configs.get(args.workload)
+    if args.sweep:
+        run_sweep(args, w, [int(t) for t in args.sweep.split(",")])
+        return
     res = run_reference(args, w, args.tokens) if args.impl == "reference" \
         else run_ours(args, w, args.tokens)
     if res is not None:

@@ -240,7 +240,7 @@ __device__ __forceinline__ void copy_row_warp(const uint4* __restrict__ src,
 constexpr int kSmallWarps = 8;
 constexpr int kSmallThreads = kSmallWarps * 32;
 // A single token is routed by the whole CTA; from two tokens on a warp per token routes
-// them side by side (measured: DeepSeek-V3 T = 4 388 -> 377 us per forward, while T = 1
+// them side by side (measured: DeepSeek-V3 T = 4 388 -> 369 us per forward, while T = 1
 // stays 2-3 us faster on the CTA-wide path).
 constexpr int kBlockRouteMaxTokens = 1;
 

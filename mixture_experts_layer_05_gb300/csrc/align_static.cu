@@ -13,8 +13,8 @@
 //  - the array holds kNoWorkspaceScratchBytes (1 MiB) on every GPU that loads the
 //    library, until the process exits;
 //  - a request whose scratch, 2 * ceil(T*top_k / 2048) * num_experts * 4 bytes, is larger
-//    is rejected with GBMOE_ERR_WORKSPACE (for example E = 256 allows up to 1,046,528
-//    flat indices T*top_k);
+//    is rejected with GBMOE_ERR_WORKSPACE (for example E = 256 allows up to 1,048,576
+//    flat indices T*top_k: 512 chunks of 2048);
 //  - every call on a device shares the one array, and the array keeps the last call's
 //    contents. Each call overwrites every byte it reads before reading it (counts, then
 //    offsets), so nothing has to start at zero; calls whose kernels overlap on the GPU

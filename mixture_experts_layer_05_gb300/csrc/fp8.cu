@@ -87,6 +87,9 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(128) silu_reduce_fp8_kernel(const __grid_constant__ GemmLaunch L,
                                                               const int* npp,
                                                               int max_routed_rows) {
+  // Triggering at entry is safe for the decode w2 GEMM that follows (it reads the routing's
+  // expert blocks before its wait): this kernel launched only after the w13 GEMM in front of
+  // it passed its wait, i.e. after the routing finished.
   pdl_trigger();  // the next kernel may start its launch now
   pdl_wait();     // inputs written by the previous kernel are visible
   const GemmProblem& R = L.p[0];

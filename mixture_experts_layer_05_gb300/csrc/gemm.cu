@@ -124,7 +124,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kEarlyB = KIND == kGemmW2 && AROWS < kGemmBM;
   if (!kEarlyB || warp != 0) pdl_wait();  // the set-up above overlapped the previous kernel
   // the next kernel may launch once this one's inputs are complete (so that it, too, may
-  // rely on everything before this kernel having finished)
+  // rely on everything before this kernel having finished). DEPENDENCE: the decode w2 GEMM
+  // (kEarlyB) reads the routing's expert blocks and schedule before its own wait; that is
+  // safe only because this trigger comes after this kernel's wait. Moving it earlier (e.g. to
+  // kernel entry) lets a w2 GEMM read stale expert ids.
   if (!kEarlyB && threadIdx.x == 0) pdl_trigger();
 
   Schedule sched;
@@ -151,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         pdl_wait();  // the A rows are the previous kernel's output
-        pdl_trigger();
+        pdl_trigger();  // after the wait, like every GEMM (see the DEPENDENCE note above)
       }
       uint32_t it = 0;
       bool ok = true;
@@ -762,6 +765,9 @@ __global__ void wait_selftest_kernel(int* status, unsigned long long timeout_ns)
 __global__ void __launch_bounds__(128) silu_reduce_kernel(const __grid_constant__ GemmLaunch L,
                                                           const int* npp,
                                                           int max_routed_rows, int gated) {
+  // Triggering at entry is safe for the decode w2 GEMM that follows (it reads the routing's
+  // expert blocks before its wait): this kernel itself launched only after the w13 GEMM in
+  // front of it passed its wait, i.e. after the routing finished.
   pdl_trigger();  // the next kernel may start its launch now
   pdl_wait();     // inputs written by the previous kernel are visible
   const GemmProblem& R = L.p[0];

@@ -115,7 +115,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // the set-up above overlapped the previous kernel; its outputs are now visible
   // the next kernel may launch once this one's inputs are complete (so that it, too, may
-  // rely on everything before this kernel having finished)
+  // rely on everything before this kernel having finished). DEPENDENCE: the decode w2 GEMM
+  // reads the routing's expert blocks before its own wait; that is safe only because this
+  // trigger comes after this kernel's wait.
   if (threadIdx.x == 0) pdl_trigger();
 
   Schedule sched;
@@ -435,7 +437,8 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   // finished. Every other thread waits here.
   constexpr bool kEarlyB = KIND == kGemmW2;
   if (!kEarlyB || warp != 0) pdl_wait();  // the set-up above overlapped the previous kernel
-  if (!kEarlyB && threadIdx.x == 0) pdl_trigger();  // see the prefill kernel
+  // after the wait: the decode w2 GEMM relies on it (DEPENDENCE note of the prefill kernel)
+  if (!kEarlyB && threadIdx.x == 0) pdl_trigger();
 
   Schedule sched;
   sched.init(args);
@@ -464,7 +467,7 @@ __global__ void __launch_bounds__(kSwThreads, 1)
           }
         }
         pdl_wait();  // the token rows are the previous kernel's output
-        pdl_trigger();
+        pdl_trigger();  // after the wait, like every GEMM
       }
       uint32_t it = 0;
       bool ok = true;

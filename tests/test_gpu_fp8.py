@@ -16,7 +16,8 @@ import torch
 
 import oracle
 from mixture_experts_layer_05_gb300 import binding, configs, inputs
-from tests.moe_cases import check_close, oracle_cfg, tokens
+from tests.moe_cases import (check_close, check_routing_valid, gate_logit_error_bound,
+                              oracle_cfg, tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -230,9 +231,11 @@ def test_fp8_skewed_routing(cuda_lib):
 
 @pytest.mark.parametrize("T", [1, 77])
 def test_fp8_from_gate_weight(cuda_lib, T):
-    """The router GEMM in front of the fp8 layer: logits = x @ W_gate^T in fp32 first. Ids
-    must match wherever the oracle's decision margin exceeds 1e-4 (far above the fp32 logit
-    error); closer rows are only checked for a valid choice."""
+    """The router GEMM in front of the fp8 layer: logits = x @ W_gate^T in fp32 first. Rows
+    whose decision margin exceeds 1e-4 (far above the fp32 logit error) must route exactly
+    like the oracle and match its output; closer rows must hold a valid routing for logits
+    within the GEMM's fp32 error bound and match the oracle's fp8 experts and combine run
+    on the GPU's own ids and weights."""
     w = SMALL["dsv3"]
     wts = inputs.make_fp8_weights(w, 0)
     gate = inputs.normal((w.num_experts, w.hidden_size), w.hidden_size ** -0.5,
@@ -244,14 +247,23 @@ def test_fp8_from_gate_weight(cuda_lib, T):
     assert layer.device_status() == binding.OK
     logits = oracle.router_logits(x, gate)
     safe = oracle.decision_margins(logits, wts["bias"], **oracle_cfg(w)) >= 1e-4
-    ids, _ = _routing_from_ws(layer, T, w.top_k)
-    for t in range(T):
-        assert len(set(ids[t].tolist())) == w.top_k
+    ids, lay = _routing_from_ws(layer, T, w.top_k)
+    tw = layer.workspace[lay.topk_weights:lay.topk_weights + T * w.top_k * 4] \
+        .view(torch.float32).cpu().numpy().reshape(T, w.top_k)
+    check_routing_valid(w, ids, tw, logits, wts["bias"], gate_logit_error_bound(x, gate),
+                        f"fp8 gate T={T}")
     rows = np.flatnonzero(safe).tolist()
     if rows:
         y_ref, parts = _oracle(w, wts, x[rows], logits[rows], wts["bias"], return_parts=True)
         assert np.array_equal(ids[rows], parts["topk_ids"])
         check_close(y[rows], y_ref, f"fp8 gate T={T}")
+    close = np.flatnonzero(~safe).tolist()
+    if close:
+        y_own = oracle.experts_combine_fp8(x[close], tw[close], ids[close], wts["w13_q"],
+                                           wts["w13_s"], wts["w2_q"], wts["w2_s"],
+                                           wts["shared_w13_q"], wts["shared_w13_s"],
+                                           wts["shared_w2_q"], wts["shared_w2_s"])
+        check_close(y[close], y_own, f"fp8 gate T={T}, close rows on the GPU's routing")
     if T > 1:
         assert safe.mean() > 0.9
 

@@ -35,8 +35,9 @@ def _outputs(T, k, E, bs):
             torch.zeros(1, dtype=torch.int32, device="cuda"))
 
 
-def _compare(lib, T, k, E, bs, seed, skew):
-    ids = _ids(T, k, E, seed, skew)
+def _compare(lib, T, k, E, bs, seed, skew, ids=None):
+    if ids is None:
+        ids = _ids(T, k, E, seed, skew)
     ref = _outputs(T, k, E, bs)
     ws = binding.alloc_workspace(binding.moe_align_block_size_workspace_size(T, k, E))
     binding.moe_align_block_size(ids, E, bs, *ref, ws)
@@ -63,3 +64,19 @@ def test_no_workspace_matches_workspace_entry_point(cuda_lib):
     too_big = lib.moe_align_block_size_no_workspace(P(256), 1 << 20, 8, 1024, 128, P(256),
                                                     P(256), P(256), None)
     assert too_big == binding.ERR_WORKSPACE
+
+
+def test_no_workspace_size_limit_is_exact(cuda_lib):
+    """The scratch limit is inclusive: with E = 256, 1,048,576 flat indices (512 chunks of
+    2048, exactly 1 MiB of counts and offsets) are accepted and match the workspace entry
+    point; one token more needs a 513th chunk and is refused before anything is enqueued."""
+    lib = cuda_lib
+    T, k, E = 131072, 8, 256
+    rng = np.random.default_rng(3)
+    # k distinct experts per token: a random start plus k offsets 32 apart
+    ids = (rng.integers(0, E, size=(T, 1)) + 32 * np.arange(k)[None, :]) % E
+    _compare(lib, T, k, E, 128, 0, False, torch.from_numpy(ids.astype(np.int32)).cuda())
+    P = ctypes.c_void_p
+    refused = lib.moe_align_block_size_no_workspace(P(256), T + 1, k, E, 128, P(256), P(256),
+                                                    P(256), None)
+    assert refused == binding.ERR_WORKSPACE
