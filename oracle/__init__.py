@@ -1,7 +1,7 @@
 """CPU oracle of the FusedMoE layer forward (test infrastructure only; see moe_oracle)."""
 from .moe_oracle import (  # noqa: F401
     router_logits, score, group_score, route_token, select_experts, decision_margins,
-    moe_align_block_size, silu, swiglu_mlp, expert_mlp, experts_combine, fused_moe,
+    moe_align_block_size, round_bf16, silu, swiglu_mlp, expert_mlp, experts_combine, fused_moe,
     fused_moe_rows,
 )
 from .fp8_oracle import (  # noqa: F401

@@ -34,13 +34,18 @@ What it computes, step by step, and where each step is defined:
 7. Expert MLP (``swiglu_mlp``): ``w13[e]`` rows [0, I) are the gate (w1) and rows
    [I, 2I) the up projection (w3) (``FusedMoE._load_w13``); ``act = silu(gate) * up``
    (``SiluAndMul`` in ``DeepseekV2MLP``); ``o = w2[e] @ act`` with ``w2 [E, H, I]``
-   (``FusedMoE._load_w2``).
+   (``FusedMoE._load_w2``). ``act``, the tensor between the two GEMMs, is held in the
+   layer's dtype, bf16: ``DeepseekV2MLP.forward`` hands ``act_fn(gate_up)`` (or the buffer
+   ``gate_up.new_empty(...)`` that ``silu_and_mul_clamp`` fills) to ``down_proj``, and the
+   activations entering ``FusedMoE`` are the model dtype (``moe_in_dtype`` on the vLLM
+   page). The layer functions therefore round ``act`` to the nearest bf16 value, ties to
+   even (``round_bf16``), and compute everything else exactly.
 8. Combine: ``y[t] = sum_j w[t, j] * o[t, j]`` over j ascending, plus the shared expert
    (one dense SwiGLU, ``DeepseekV2MLP``) added without the routed scaling factor
    (``DeepseekV2MoE.forward_normal`` / ``maybe_fuse_routed_scale_and_shared_add``).
 
-Everything is fp64; bf16 inputs are widened exactly. Parity of every function is
-pinned by the CPU tests (brute force, closed forms, invariants, hand-worked examples).
+Everything is fp64 (bf16 inputs widened exactly) except the bf16 act of step 7. Parity
+of every function is pinned by the CPU tests (brute force, closed forms, invariants, hand-worked examples).
 """
 from __future__ import annotations
 
@@ -188,6 +193,20 @@ def moe_align_block_size(topk_ids, num_experts: int, block_size: int):
 
 
 # ---------------------------------------------------------------- 7. expert MLP
+BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127        # largest finite bfloat16
+
+
+def round_bf16(a) -> np.ndarray:
+    """Nearest bfloat16 value of each fp64 value, ties to even: 8 significant bits over
+    fp32's exponent range (spacing 2^(e-7) for 2^e <= |a| < 2^(e+1), e >= -126; 2^-133 below
+    2^-126), values past the largest finite bf16 to +-inf. Written from the format."""
+    a = np.asarray(a, dtype=np.float64)
+    _, e = np.frexp(a)                               # a = m 2^e with 1/2 <= |m| < 1
+    e = np.maximum(e, -125)                          # subnormal spacing stays 2^-133
+    q = np.ldexp(np.rint(np.ldexp(a, 8 - e)), e - 8)  # rint: ties to even
+    return np.where(np.abs(q) > BF16_MAX, np.copysign(np.inf, a), q)
+
+
 def silu(z: np.ndarray) -> np.ndarray:
     return z / (1.0 + np.exp(-z))
 
@@ -198,7 +217,7 @@ def swiglu_mlp(h: np.ndarray, w13_e, w2_e) -> np.ndarray:
 
 
 def expert_mlp(h, w13_e, w2_e, *, b13_e=None, b2_e=None, gated=True, swiglu_limit=None,
-               gemm1_alpha=1.0) -> np.ndarray:
+               gemm1_alpha=1.0, act_dtype=None) -> np.ndarray:
     """One expert's MLP with the layer's optional variants (sglang ``fused_moe_triton/layer``
     page, ``FusedMoE.__init__``: ``with_bias``, ``is_gated``, ``gemm1_alpha``,
     ``gemm1_clamp_limit``; ``DeepseekV2MLP.forward``: ``swiglu_limit``).
@@ -208,6 +227,7 @@ def expert_mlp(h, w13_e, w2_e, *, b13_e=None, b2_e=None, gated=True, swiglu_limi
     Not gated (w13_e is [I, H]): act = silu(z). o = act @ w2^T (+ b2).
     The pages name these parameters without their arithmetic; this is the reading the
     NPU clipped-SwiGLU call's arguments (alpha, limit, bias) point to.
+    act_dtype "bf16" rounds act to bf16 (the layer's intermediate tensor); None keeps it exact.
     """
     W13 = _f64(w13_e)
     W2 = _f64(w2_e)
@@ -224,6 +244,10 @@ def expert_mlp(h, w13_e, w2_e, *, b13_e=None, b2_e=None, gated=True, swiglu_limi
         act = gate / (1.0 + np.exp(-gemm1_alpha * gate)) * up
     else:
         act = silu(z)
+    if act_dtype == "bf16":
+        act = round_bf16(act)
+    elif act_dtype is not None:
+        raise ValueError(f"unknown act_dtype {act_dtype!r}")
     o = act @ W2.T
     if b2_e is not None:
         o = o + _f64(b2_e)
@@ -234,7 +258,7 @@ def expert_mlp(h, w13_e, w2_e, *, b13_e=None, b2_e=None, gated=True, swiglu_limi
 def experts_combine(x, topk_weights, topk_ids, w13, w2, shared_w13=None, shared_w2=None, *,
                     return_parts=False, w13_bias=None, w2_bias=None, gated=True,
                     swiglu_limit=None, gemm1_alpha=1.0, apply_router_weight_on_input=False,
-                    top_k=None):
+                    top_k=None, act_dtype="bf16"):
     """y [T, H] fp64 of the experts and the combine for a routing given as input.
 
     This is the layer behind a precomputed top-k (``FusedMoE.forward(hidden_states,
@@ -243,7 +267,8 @@ def experts_combine(x, topk_weights, topk_ids, w13, w2, shared_w13=None, shared_
     outputs are summed with the routing weights over slots j ascending, then the shared
     expert is added unscaled. With ``apply_router_weight_on_input`` (FusedMoE constructor
     argument) the routing weight scales the expert's input instead of its output. The
-    shared expert (``DeepseekV2MLP``: no bias, alpha 1) shares the SwiGLU limit.
+    shared expert (``DeepseekV2MLP``: no bias, alpha 1) shares the SwiGLU limit. Every
+    expert's act is rounded to bf16 (``act_dtype``; None keeps it exact).
     """
     X = _f64(x)
     T, H = X.shape
@@ -259,7 +284,8 @@ def experts_combine(x, topk_weights, topk_ids, w13, w2, shared_w13=None, shared_
         out = expert_mlp(h, w13[e], w2[e],
                          b13_e=None if w13_bias is None else w13_bias[e],
                          b2_e=None if w2_bias is None else w2_bias[e], gated=gated,
-                         swiglu_limit=swiglu_limit, gemm1_alpha=gemm1_alpha)
+                         swiglu_limit=swiglu_limit, gemm1_alpha=gemm1_alpha,
+                         act_dtype=act_dtype)
         for (t, j), r in zip(rows, out):
             o[t, j] = r
     y = np.zeros((T, H), dtype=np.float64)
@@ -268,8 +294,8 @@ def experts_combine(x, topk_weights, topk_ids, w13, w2, shared_w13=None, shared_
             y[t] += o[t, j] if apply_router_weight_on_input else W[t, j] * o[t, j]
     shared = None
     if shared_w13 is not None:
-        shared = (expert_mlp(X, shared_w13, shared_w2, swiglu_limit=swiglu_limit) if T
-                  else np.zeros((0, H)))
+        shared = (expert_mlp(X, shared_w13, shared_w2, swiglu_limit=swiglu_limit,
+                             act_dtype=act_dtype) if T else np.zeros((0, H)))
         y = y + shared
     if return_parts:
         return y, {"topk_weights": W, "topk_ids": ids, "expert_out": o, "shared": shared}
@@ -278,15 +304,16 @@ def experts_combine(x, topk_weights, topk_ids, w13, w2, shared_w13=None, shared_
 
 def fused_moe(x, logits, bias, w13, w2, shared_w13=None, shared_w2=None, *,
               return_parts=False, w13_bias=None, w2_bias=None, gated=True, swiglu_limit=None,
-              gemm1_alpha=1.0, apply_router_weight_on_input=False, **cfg):
+              gemm1_alpha=1.0, apply_router_weight_on_input=False, act_dtype="bf16", **cfg):
     """y [T, H] fp64 = routed experts (weighted, combined) + shared expert: the routing of
-    ``select_experts`` followed by ``experts_combine``."""
+    ``select_experts`` followed by ``experts_combine`` (act rounded to bf16 unless
+    ``act_dtype`` is None)."""
     W, ids = select_experts(logits, bias, **cfg)
     return experts_combine(x, W, ids, w13, w2, shared_w13, shared_w2,
                            return_parts=return_parts, w13_bias=w13_bias, w2_bias=w2_bias,
                            gated=gated, swiglu_limit=swiglu_limit, gemm1_alpha=gemm1_alpha,
                            apply_router_weight_on_input=apply_router_weight_on_input,
-                           top_k=cfg["top_k"])
+                           top_k=cfg["top_k"], act_dtype=act_dtype)
 
 
 def fused_moe_rows(x_rows, logits_rows, bias, w13, w2, shared_w13=None, shared_w2=None,

@@ -177,7 +177,7 @@ def pin_layer_near_bf16_layer_on_dequantized_operands():
     W13, W2 = _dequant_stack(d["w13_q"], d["w13_s"]), _dequant_stack(d["w2_q"], d["w2_s"])
     S13 = oracle.dequant_block(d["sw13_q"], d["sw13_s"])
     S2 = oracle.dequant_block(d["sw2_q"], d["sw2_s"])
-    y_ref = om.fused_moe(xd, logits, None, W13, W2, S13, S2, **cfg)
+    y_ref = om.fused_moe(xd, logits, None, W13, W2, S13, S2, act_dtype=None, **cfg)
     W, ids = om.select_experts(logits, None, **cfg)
 
     def act_err(h, w13):

@@ -255,7 +255,7 @@ def pin_dense_swiglu_single_expert():
     x = rng.normal(size=(7, 12))
     w13, w2, _, _ = _rand_layer(rng, 1, 12, 5)
     y = oracle.fused_moe(x, rng.normal(size=(7, 1)), None, w13, w2,
-                         **_cfg(num_experts=1, top_k=1))
+                         act_dtype=None, **_cfg(num_experts=1, top_k=1))
     X, W13, W2 = (torch.tensor(a) for a in (x, w13[0], w2[0]))
     ref = torch.nn.functional.silu(X @ W13[:5].T) * (X @ W13[5:].T) @ W2.T
     np.testing.assert_allclose(y, ref.numpy(), rtol=1e-12, atol=1e-14)
@@ -272,7 +272,7 @@ def pin_identity_like_experts():
     x = rng.normal(size=(T, n))
     logits = rng.normal(size=(T, E))
     cfg = _cfg(num_experts=E, top_k=2)
-    y = oracle.fused_moe(x, logits, None, w13, w2, **cfg)
+    y = oracle.fused_moe(x, logits, None, w13, w2, act_dtype=None, **cfg)
     W, ids = oracle.select_experts(logits, None, **cfg)
     for t in range(T):
         for i in range(n):
@@ -293,13 +293,13 @@ def pin_scaling_and_shared():
     logits = rng.normal(size=(T, E))
     c1 = _cfg(num_experts=E, top_k=2, routed_scaling_factor=1.0)
     c2 = _cfg(num_experts=E, top_k=2, routed_scaling_factor=2.5)
-    y1 = oracle.fused_moe(x, logits, None, w13, w2, sw13, sw2, **c1)
-    y2 = oracle.fused_moe(x, logits, None, w13, w2, sw13, sw2, **c2)
+    y1 = oracle.fused_moe(x, logits, None, w13, w2, sw13, sw2, act_dtype=None, **c1)
+    y2 = oracle.fused_moe(x, logits, None, w13, w2, sw13, sw2, act_dtype=None, **c2)
     shared = torch.nn.functional.silu(torch.tensor(x) @ torch.tensor(sw13[:Is]).T) \
         * (torch.tensor(x) @ torch.tensor(sw13[Is:]).T) @ torch.tensor(sw2).T
     shared = shared.numpy()
     np.testing.assert_allclose(y2 - shared, 2.5 * (y1 - shared), rtol=1e-10, atol=1e-12)
-    y0 = oracle.fused_moe(x, logits, None, w13, np.zeros_like(w2), sw13, sw2, **c1)
+    y0 = oracle.fused_moe(x, logits, None, w13, np.zeros_like(w2), sw13, sw2, act_dtype=None, **c1)
     np.testing.assert_allclose(y0, shared, rtol=1e-12, atol=1e-14)
 
 
@@ -345,6 +345,75 @@ def test_empty_batch():
     y = oracle.fused_moe(np.zeros((0, 4)), np.zeros((0, 8)), None, np.zeros((8, 4, 4)),
                          np.zeros((8, 4, 2)), **_cfg())
     assert y.shape == (0, 4)
+
+
+# ------------------------------------------------------------------ bf16 act
+BF16 = os.path.join(os.path.dirname(__file__), "golden", "bf16_round_examples.json")
+
+
+def _rne_bits(a):
+    """bfloat16 rounding by bit surgery on the fp64 pattern (a second, independent way):
+    keep the top 7 of the 52 stored fraction bits, rounding the dropped 45 to nearest, ties
+    to even, by adding 2^44 - 1 plus the lowest kept bit; for normal fp32-range values."""
+    a = np.asarray(a, dtype=np.float64)
+    bits = a.view(np.uint64).copy()
+    lsb = (bits >> np.uint64(45)) & np.uint64(1)
+    bits = bits + np.uint64((1 << 44) - 1) + lsb
+    bits &= ~np.uint64((1 << 45) - 1)
+    return bits.view(np.float64)
+
+
+def pin_round_bf16():
+    """round_bf16 on hand-worked values (ties, subnormals), against bit surgery on random
+    fp64 values, and against torch's float32 -> bfloat16 conversion on fp32 values."""
+    with open(BF16) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        got = float(oracle.round_bf16(math.ldexp(*c["x"])))
+        assert got == math.ldexp(*c["want"]), c
+    rng = np.random.default_rng(13)
+    v = rng.normal(size=4000) * np.exp2(rng.integers(-100, 100, size=4000))
+    np.testing.assert_array_equal(oracle.round_bf16(v), _rne_bits(v))
+    f32 = (rng.normal(size=4000) * 3.0).astype(np.float32)
+    f32[:64] = (np.arange(64, dtype=np.float32) + 0.5) * np.float32(2.0 ** -7) + 1  # ties
+    want = torch.from_numpy(f32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle.round_bf16(f32.astype(np.float64)), want)
+
+
+def pin_layer_rounds_act_only():
+    """Identity-like experts (w1 = a Id, w3 = b Id, w2 = Id) and a shared expert: the layer
+    equals sum_j w_j bf16(silu(a x) (b x)) + bf16(silu(c x) (d x)), the act rounded and
+    nothing else (gate, up and output exact)."""
+    rng = np.random.default_rng(14)
+    E, n, T = 4, 6, 7
+    a = rng.uniform(0.5, 2.0, E)
+    b = rng.uniform(-2.0, 2.0, E)
+    w13 = np.stack([np.vstack([a[e] * np.eye(n), b[e] * np.eye(n)]) for e in range(E)])
+    w2 = np.stack([np.eye(n)] * E)
+    c, d = 1.3, -0.7
+    sw13, sw2 = np.vstack([c * np.eye(n), d * np.eye(n)]), np.eye(n)
+    x = rng.normal(size=(T, n)) * 3.0
+    logits = rng.normal(size=(T, E))
+    cfg = _cfg(num_experts=E, top_k=2)
+    y = oracle.fused_moe(x, logits, None, w13, w2, sw13, sw2, **cfg)
+    W, ids = oracle.select_experts(logits, None, **cfg)
+    for t in range(T):
+        want = _rne_bits(om.silu(c * x[t]) * (d * x[t]))
+        for j in range(2):
+            e = ids[t, j]
+            want = want + W[t, j] * _rne_bits(om.silu(a[e] * x[t]) * (b[e] * x[t]))
+        np.testing.assert_allclose(y[t], want, rtol=1e-13, atol=1e-15)
+    # and the act really is rounded: the exact layer differs
+    y_exact = oracle.fused_moe(x, logits, None, w13, w2, sw13, sw2, act_dtype=None, **cfg)
+    assert np.abs(y - y_exact).max() > 1e-4
+
+
+def test_round_bf16():
+    pin_round_bf16()
+
+
+def test_layer_rounds_act_only():
+    pin_layer_rounds_act_only()
 
 
 # ------------------------------------------------------------------ decision margins
@@ -471,7 +540,8 @@ ALL_PINS = [pin_hand_routing, pin_hand_align, pin_hand_expert_mlp, pin_bruteforc
             pin_sigmoid_weights_unbiased, pin_grouped_reduces_to_ungrouped,
             pin_routing_invariants, pin_align_bruteforce, pin_dense_swiglu_single_expert,
             pin_identity_like_experts, pin_scaling_and_shared, pin_expert_relabeling,
-            pin_hand_margins, pin_margins_bruteforce]
+            pin_hand_margins, pin_margins_bruteforce, pin_round_bf16,
+            pin_layer_rounds_act_only]
 
 
 def _caught(monkeypatch, name, fn):
@@ -579,3 +649,39 @@ def test_margin_mutant_copy_is_faithful(monkeypatch):
     monkeypatch.setattr(om, "decision_margins", fn)
     pin_hand_margins()
     pin_margins_bruteforce()
+
+
+
+def _round_half_away(a):
+    a = np.asarray(a, dtype=np.float64)
+    _, e = np.frexp(a)
+    e = np.maximum(e, -125)
+    m = np.ldexp(a, 8 - e)
+    return np.ldexp(np.sign(m) * np.floor(np.abs(m) + 0.5), e - 8)
+
+
+def _expert_act_unrounded(h, w13_e, w2_e, **kw):
+    kw.pop("act_dtype", None)
+    return _orig_expert(h, w13_e, w2_e, **kw)
+
+
+def _expert_rounds_gate_up(h, w13_e, w2_e, act_dtype=None, **kw):
+    if act_dtype is None:
+        return _orig_expert(h, w13_e, w2_e, **kw)
+    W13 = om.round_bf16(np.atleast_2d(om._f64(h)) @ om._f64(w13_e).T)   # z rounded as well
+    I = W13.shape[1] // 2
+    act = om.round_bf16(om.silu(W13[:, :I]) * W13[:, I:])
+    return act @ om._f64(w2_e).T
+
+
+_orig_expert = om.expert_mlp
+
+
+@pytest.mark.parametrize("name,fn", [("round_bf16", _round_half_away),
+                                     ("expert_mlp", _expert_act_unrounded),
+                                     ("expert_mlp", _expert_rounds_gate_up)],
+                         ids=["half_away", "act_not_rounded", "gate_up_rounded"])
+def test_planted_bf16_mistake_is_caught(monkeypatch, name, fn):
+    monkeypatch.setattr(oracle, name, fn, raising=False)
+    caught = _caught(monkeypatch, name, fn)
+    assert caught, f"no pin caught the planted bf16 mistake in {name}"

@@ -62,7 +62,7 @@ def pin_bias_dense():
     w13, w2 = rng.normal(size=(1, 10, 8)), rng.normal(size=(1, 8, 5))
     b13, b2 = rng.normal(size=(1, 10)), rng.normal(size=(1, 8))
     y = oracle.fused_moe(x, rng.normal(size=(6, 1)), None, w13, w2, w13_bias=b13, w2_bias=b2,
-                         **_cfg(num_experts=1, top_k=1))
+                         act_dtype=None, **_cfg(num_experts=1, top_k=1))
     X = torch.tensor(x)
     F = torch.nn.functional
     g = F.linear(X, torch.tensor(w13[0, :5]), torch.tensor(b13[0, :5]))
@@ -81,7 +81,7 @@ def pin_bias_zero_weights():
     w2 = np.stack([np.eye(n)] * E)
     x = rng.normal(size=(5, n))
     logits = rng.normal(size=(5, E))
-    y = oracle.fused_moe(x, logits, None, w13, w2, w13_bias=b13, w2_bias=b2, **_cfg())
+    y = oracle.fused_moe(x, logits, None, w13, w2, w13_bias=b13, w2_bias=b2, act_dtype=None, **_cfg())
     W, ids = oracle.select_experts(logits, None, **_cfg())
     for t in range(5):
         want = sum(W[t, j] * (om.silu(b13[e, :n]) * b13[e, n:] + b2[e])
@@ -94,7 +94,7 @@ def pin_non_gated_dense():
     x = rng.normal(size=(4, 6))
     w1, w2 = rng.normal(size=(1, 5, 6)), rng.normal(size=(1, 6, 5))
     y = oracle.fused_moe(x, rng.normal(size=(4, 1)), None, w1, w2, gated=False,
-                         **_cfg(num_experts=1, top_k=1))
+                         act_dtype=None, **_cfg(num_experts=1, top_k=1))
     ref = torch.nn.functional.silu(torch.tensor(x) @ torch.tensor(w1[0]).T) @ \
         torch.tensor(w2[0]).T
     np.testing.assert_allclose(y, ref.numpy(), rtol=1e-12)
@@ -110,7 +110,7 @@ def pin_router_weight_on_input():
     w2 = np.stack([np.eye(n)] * E)
     x = rng.normal(size=(6, n))
     logits = rng.normal(size=(6, E))
-    y = oracle.fused_moe(x, logits, None, w13, w2, apply_router_weight_on_input=True, **_cfg())
+    y = oracle.fused_moe(x, logits, None, w13, w2, apply_router_weight_on_input=True, act_dtype=None, **_cfg())
     W, ids = oracle.select_experts(logits, None, **_cfg())
     for t in range(6):
         want = sum(om.silu(a[e] * W[t, j] * x[t]) * (b[e] * W[t, j] * x[t])
@@ -126,7 +126,7 @@ def pin_shared_expert_clamped_unbiased():
     w13, w2 = np.zeros((2, 4, 4)), np.zeros((2, 4, 2))
     y = oracle.fused_moe(x, rng.normal(size=(3, 2)), None, w13, w2, sw13, sw2,
                          w13_bias=np.zeros((2, 4)), w2_bias=np.zeros((2, 4)),
-                         swiglu_limit=0.3, **_cfg(num_experts=2, top_k=1))
+                         swiglu_limit=0.3, act_dtype=None, **_cfg(num_experts=2, top_k=1))
     np.testing.assert_allclose(y, oracle.expert_mlp(x, sw13, sw2, swiglu_limit=0.3),
                                rtol=1e-12, atol=1e-15)
 
