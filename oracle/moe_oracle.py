@@ -267,8 +267,10 @@ def experts_combine(x, topk_weights, topk_ids, w13, w2, shared_w13=None, shared_
     outputs are summed with the routing weights over slots j ascending, then the shared
     expert is added unscaled. With ``apply_router_weight_on_input`` (FusedMoE constructor
     argument) the routing weight scales the expert's input instead of its output. The
-    shared expert (``DeepseekV2MLP``: no bias, alpha 1) shares the SwiGLU limit. Every
-    expert's act is rounded to bf16 (``act_dtype``; None keeps it exact).
+    shared expert (``DeepseekV2MLP``: no bias, alpha 1) shares the SwiGLU limit. The
+    tensors the layer holds between its steps are of its dtype (``act_dtype`` "bf16"): every
+    expert's act, and with ``apply_router_weight_on_input`` the weighted input rows, are
+    rounded to bf16 (None keeps them exact).
     """
     X = _f64(x)
     T, H = X.shape
@@ -281,6 +283,8 @@ def experts_combine(x, topk_weights, topk_ids, w13, w2, shared_w13=None, shared_
         h = X[[t for t, _ in rows]]
         if apply_router_weight_on_input:
             h = h * np.array([W[t, j] for t, j in rows])[:, None]
+            if act_dtype == "bf16":
+                h = round_bf16(h)            # the scaled input is a tensor of the layer dtype
         out = expert_mlp(h, w13[e], w2[e],
                          b13_e=None if w13_bias is None else w13_bias[e],
                          b2_e=None if w2_bias is None else w2_bias[e], gated=gated,

@@ -131,8 +131,35 @@ def pin_shared_expert_clamped_unbiased():
                                rtol=1e-12, atol=1e-15)
 
 
+def pin_router_weight_on_input_bf16():
+    """The weighted input is a tensor of the layer dtype: identity-like experts give
+    y = sum_j bf16(silu(a r) (b r)) with r = bf16(w_j x), both roundings to nearest even."""
+    rng = np.random.default_rng(26)
+    E, n = 4, 5
+    a = rng.uniform(0.5, 2.0, E)
+    b = rng.uniform(-2.0, 2.0, E)
+    w13 = np.stack([np.vstack([a[e] * np.eye(n), b[e] * np.eye(n)]) for e in range(E)])
+    w2 = np.stack([np.eye(n)] * E)
+    x = rng.normal(size=(6, n)) * 2.0
+    logits = rng.normal(size=(6, E))
+    y = oracle.fused_moe(x, logits, None, w13, w2, apply_router_weight_on_input=True, **_cfg())
+    W, ids = oracle.select_experts(logits, None, **_cfg())
+    bf = lambda v: torch.tensor(v, dtype=torch.float32).to(torch.bfloat16).double().numpy()
+    for t in range(6):
+        want = 0.0
+        for j, e in enumerate(ids[t]):
+            r = bf((W[t, j] * x[t]).astype(np.float32))
+            want = want + bf((om.silu(a[e] * r) * (b[e] * r)).astype(np.float32))
+        # float32 detours: the exact fp64 values round through fp32 first; compare loosely
+        np.testing.assert_allclose(y[t], want, rtol=2e-7, atol=1e-7)
+    y_exact = oracle.fused_moe(x, logits, None, w13, w2, apply_router_weight_on_input=True,
+                               act_dtype=None, **_cfg())
+    assert np.abs(y - y_exact).max() > 1e-4
+
+
 PINS = [pin_clamp_hand_example, pin_clamp_reduces_to_plain, pin_bias_dense,
         pin_bias_zero_weights, pin_non_gated_dense, pin_router_weight_on_input,
+        pin_router_weight_on_input_bf16,
         pin_shared_expert_clamped_unbiased]
 
 
@@ -205,3 +232,25 @@ def test_router_logits_is_a_matmul():
     np.testing.assert_array_equal(oracle.router_logits(np.array([[1.0, 2.0]]),
                                                        np.array([[3.0, 4.0], [5.0, 6.0]])),
                                   [[11.0, 17.0]])
+
+
+def test_planted_unrounded_weighted_input_is_caught(monkeypatch):
+    """A layer that rounds the act but leaves the weighted input rows exact fails the
+    bf16 weight-on-input pin."""
+    def combine(x, topk_weights, topk_ids, w13, w2, shared_w13=None, shared_w2=None, *,
+                return_parts=False, apply_router_weight_on_input=False, top_k=None,
+                act_dtype="bf16", **kw):
+        X = om._f64(x)
+        W = np.atleast_2d(np.asarray(topk_weights, dtype=np.float64))
+        ids = np.atleast_2d(np.asarray(topk_ids))
+        y = np.zeros_like(X)
+        for t in range(X.shape[0]):
+            for j in range(ids.shape[1]):
+                h = X[t:t + 1] * (W[t, j] if apply_router_weight_on_input else 1.0)
+                o = om.expert_mlp(h, w13[ids[t, j]], w2[ids[t, j]], act_dtype=act_dtype)[0]
+                y[t] += o if apply_router_weight_on_input else W[t, j] * o
+        return y
+
+    monkeypatch.setattr(om, "experts_combine", combine)
+    with pytest.raises(AssertionError):
+        pin_router_weight_on_input_bf16()
