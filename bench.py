@@ -89,6 +89,7 @@ def layer_work(w, T: int, n_active: int, fp8: bool = False) -> dict:
 
 
 KERNEL_SOURCES = {"gemm.cu": ("gemm.cu", "tc.cuh", "common.cuh", "kernels.h"),
+                  "gemm_tn.cu": ("gemm_tn.cu", "tc.cuh", "common.cuh", "kernels.h"),
                   "gemm_fp8.cu": ("gemm_fp8.cu", "tc.cuh", "fp8.cuh", "common.cuh", "kernels.h")}
 
 
@@ -199,7 +200,9 @@ L2_BYTES = 129 * 2 ** 20          # GB300 L2
 
 def routing_stats(layer, cfg, w, T) -> dict:
     """Routing facts of the last forward, read from its workspace: distinct experts, padded
-    row count, and the per-expert load (rows routed to each expert) relative to the mean."""
+    row count of the align, the rows the expert GEMMs' MMAs cover (the padded rows for
+    128-row blocks; each 256-row block's real rows rounded up to 16 for the token-N GEMMs),
+    and the per-expert load (rows routed to each expert) relative to the mean."""
     import torch
     from mixture_experts_layer_05_gb300 import binding
     lay = binding.moe_forward_workspace_layout(cfg, T)
@@ -207,6 +210,11 @@ def routing_stats(layer, cfg, w, T) -> dict:
     cnt = torch.bincount(ids.long(), minlength=w.num_experts).cpu()
     npp = int(layer.workspace[lay.num_tokens_post_padded:lay.num_tokens_post_padded + 4]
               .view(torch.int32).item())
+    bs = binding.moe_forward_block_size(cfg, T)
+    if bs == 256:
+        mma_rows = int(sum(c // 256 * 256 + (-(-(c % 256) // 16) * 16) for c in cnt.tolist()))
+    else:
+        mma_rows = npp
     mean = T * w.top_k / w.num_experts
     rel = cnt.double() / mean
     edges = [0.0, 0.5, 1.0, 2.0, 4.0, 8.0, 16.0]
@@ -215,7 +223,8 @@ def routing_stats(layer, cfg, w, T) -> dict:
         n = int(((rel > a) & (rel <= b)).sum()) if a > 0 else int((rel <= b).sum())
         hist[f"({a:g},{b:g}]" if a > 0 else f"[0,{b:g}]"] = n
     return {"active_experts": int((cnt > 0).sum()), "rows_post_padded": npp,
-            "padding_frac": round(npp / (T * w.top_k) - 1.0, 4),
+            "block_rows": bs, "mma_rows": mma_rows,
+            "mma_padding_frac": round(mma_rows / (T * w.top_k) - 1.0, 4),
             "max_load_over_mean": round(float(rel.max()), 3),
             "top8_loads": sorted(cnt.tolist(), reverse=True)[:8],
             "load_over_mean_hist": hist}
@@ -456,8 +465,11 @@ def run_ours(args, w, T):
     rs = routing_stats(layer, cfg, w, T)
     work = layer_work(w, T, rs["active_experts"], fp8)
     peaks, peak_src = load_peaks()
+    # which w13 kernel the forward runs: the token-N CTA-pair GEMM when its blocks are 256
+    tn = not fp8 and binding.moe_forward_block_size(cfg, T) == 256
     kname = ("gemm_fp8_kernel<w13> (grouped e4m3 w13 GEMM + SiLU*mul + act quant)" if fp8
-             else "gemm_kernel<w13> (grouped w13 GEMM + SiLU*mul)")
+             else "gemm_tn_kernel<w13> (grouped w13 GEMM + SiLU*mul, tokens on N, CTA pairs)"
+             if tn else "gemm_kernel<w13> (grouped w13 GEMM + SiLU*mul)")
     value = aggregate_tokens_per_s(T, world, ms_max)
     ratio = 2.0 if fp8 else 1.0
 
@@ -467,6 +479,7 @@ def run_ours(args, w, T):
         roof = roofline_of(work, w13_ms / 1e3, peaks, peak_src, fp8, kname)
         roof["traffic"] = args.traffic if args.traffic is not None else (
             kernel_traffic("gemm_fp8_w13", w.name, T, "gemm_fp8.cu") if fp8
+            else kernel_traffic("gemm_tn_w13", w.name, T, "gemm_tn.cu") if tn
             else kernel_traffic("gemm_w13", w.name, T))
         step_s = ms_max / 1e3
         tc_burst = peaks["bf16_tflops"] * ratio
@@ -715,12 +728,18 @@ def main(argv=None):
     ap.add_argument("--ref-sample", type=int, default=0,
                     help="tokens per reference step (0: sized to ~1.5 s per step)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--num-experts", type=int, default=0,
+                    help="reduced-expert stand-in of the workload (profiling captures only)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     from mixture_experts_layer_05_gb300 import configs
     w = configs.get(args.workload)
+    if args.num_experts:
+        # a reduced-expert stand-in of the same shapes (for counter captures that must stay
+        # small): the same hidden, intermediate, top_k and group count, fewer experts
+        w = configs.shrink(w, num_experts=args.num_experts, name=f"{w.name}-E{args.num_experts}")
     if args.sweep:
         run_sweep(args, w, [int(t) for t in args.sweep.split(",")])
         return

@@ -12,7 +12,8 @@
 //           order-free);
 //   scan    one CTA: per-expert totals, padded runs, exclusive scan over experts,
 //           per-(chunk, expert) start offsets, sentinel padding, expert_ids, and
-//           (for the GEMMs) each block's expert segment (first block, block count);
+//           (for the GEMMs) each block's expert segment (first block, block count) and
+//           its real rows;
 //   scatter one CTA per chunk; its warps own consecutive slices, count them, take
 //           start offsets in slice order, and walk their slices in order, ranking
 //           equal experts in each 32-wide step with __match_any_sync: stable order.
@@ -53,11 +54,13 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(const int* __restrict_
                                                           int* __restrict__ sorted,
                                                           int* __restrict__ expert_ids,
                                                           int max_blocks, int* __restrict__ npp,
-                                                          int2* __restrict__ block_seg) {
+                                                          int2* __restrict__ block_seg,
+                                                          int* __restrict__ block_rows) {
   pdl_trigger();  // the next kernel may start its launch now
   pdl_wait();     // inputs written by the previous kernel are visible
   __shared__ int warp_tot[32];
   __shared__ int s_total;
+  __shared__ int s_pad0[1024], s_pad1[1024];  // each expert's padding slots [s_pad0, s_pad1)
   const int e = threadIdx.x;
   const int lane = e & 31, wid = e >> 5;
   int tot = 0;
@@ -92,15 +95,21 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(const int* __restrict_
       offs[(size_t)c * E + e] = run;
       run += counts[(size_t)c * E + e];
     }
-    for (int p = start + tot; p < start + pad; ++p) sorted[p] = n;
+    s_pad0[e] = start + tot;
+    s_pad1[e] = start + pad;
     for (int b = start / bs; b < (start + pad) / bs; ++b) {
       expert_ids[b] = e;
       if (block_seg) block_seg[b] = make_int2(start / bs, pad / bs);
+      if (block_rows) block_rows[b] = min(bs, tot - (b - start / bs) * bs);
     }
   }
   const int total = s_total;
   if (e == 0) *npp = total;
   for (int b = total / bs + e; b < max_blocks; b += blockDim.x) expert_ids[b] = -1;
+  // the padding slots get the sentinel n, one expert at a time across the whole CTA
+  __syncthreads();
+  for (int x = 0; x < E; ++x)
+    for (int p = s_pad0[x] + e; p < s_pad1[x]; p += blockDim.x) sorted[p] = n;
 }
 
 // One CTA per chunk, kScatterWarps warps, each owning a contiguous slice of the chunk.
@@ -489,7 +498,7 @@ size_t align_scratch_bytes(int n, int E) {
 
 cudaError_t launch_align(const int* ids, int n, int E, int bs, int* sorted, int* expert_ids,
                          int max_blocks, int* npp, void* scratch, int* status,
-                         cudaStream_t stream, int2* block_seg, int* inv) {
+                         cudaStream_t stream, int2* block_seg, int* inv, int* block_rows) {
   const int C = (n + kAlignChunk - 1) / kAlignChunk;
   int* counts = static_cast<int*>(scratch);
   int* offs = counts + (size_t)C * E;
@@ -497,7 +506,7 @@ cudaError_t launch_align(const int* ids, int n, int E, int bs, int* sorted, int*
   if (C > 0) launch_kernel(align_count_kernel, dim3(C), dim3(256), shm, stream, ids, n, E, counts,
                            status);
   launch_kernel(align_scan_kernel, dim3(1), dim3(1024), 0, stream, counts, C, E, bs, n, offs, sorted,
-                expert_ids, max_blocks, npp, block_seg);
+                expert_ids, max_blocks, npp, block_seg, block_rows);
   if (C > 0)
     launch_kernel(align_scatter_kernel, dim3(C), dim3(kScatterWarps * 32), shm * kScatterWarps,
                   stream, ids, n, E, offs, sorted, inv);

@@ -36,6 +36,16 @@ namespace {
 
 constexpr int kMaxTokens = 1 << 22;
 constexpr int kSplitMaxTokens = 64;  // split-K only at decode-sized batches
+#ifndef GBMOE_TN_MIN_TOKENS
+#define GBMOE_TN_MIN_TOKENS 65
+#endif
+// bf16 prefill batches of at least this many tokens may run the token-N GEMMs
+constexpr int kTnMinTokens = GBMOE_TN_MIN_TOKENS;
+#ifndef GBMOE_TN_MIN_ROWS
+#define GBMOE_TN_MIN_ROWS 128
+#endif
+// ... when their experts average at least this many routed rows
+constexpr int kTnMinRowsPerExpert = GBMOE_TN_MIN_ROWS;
 #ifndef GBMOE_MAX_SPLITS
 #define GBMOE_MAX_SPLITS 8
 #endif
@@ -101,14 +111,22 @@ gbmoe_status_t check_layer(const gbmoe_config_t* c) {
   return GBMOE_OK;
 }
 
-// CTA-pair GEMMs (row blocks of 256) when the experts average >= kPairMinRowsPerExpert
-// rows and the w2 output tiles are 256 wide.
-bool use_pair(const gbmoe_config_t& c, int T) {
-  const bool plain = c.is_act_and_mul && c.swiglu_limit == 0.f &&
-                     (c.gemm1_alpha == 0.f || c.gemm1_alpha == 1.f) &&
-                     c.weight_quant == GBMOE_QUANT_NONE;
-  return plain && (long)T * c.top_k >= (long)kPairMinRowsPerExpert * c.num_experts &&
-         c.hidden_size % 256 == 0;
+bool use_tn(const gbmoe_config_t& c, int T);
+
+// bf16 prefill whose experts average at least kTnMinRowsPerExpert rows runs the token-N
+// GEMMs on CTA pairs: row blocks of 256 rows whose MMA width follows each block's real
+// rows, so the padding of the align costs no tensor time. Measured against the tokens-on-M
+// GEMMs (graph replay, same box): DeepSeek-V2 T = 4096 (154 rows per expert) 2.13 -> 1.89
+// ms, DeepSeek-V3 T = 8192 (256) 6.82 -> 6.66, Mixtral T = 4096 (1024) 2.19 -> 2.12, the
+// Zipf-skewed T = 16384 (512) 12.4 -> 11.9; with fewer rows per expert the pair streams
+// each weight tile with less in flight per SM and loses (DeepSeek-V3 T = 2048, 64 rows:
+// 3.28 -> 3.43).
+bool use_tn(const gbmoe_config_t& c, int T) {
+  return c.weight_quant == GBMOE_QUANT_NONE && T > kSplitMaxTokens && T >= kTnMinTokens &&
+         (long)T * c.top_k >= (long)kTnMinRowsPerExpert * c.num_experts &&
+         !route_align_small_ok(T, c.top_k, c.num_experts) &&
+         gemm_tn_supported(c.is_act_and_mul ? kGemmW13 : kGemmW1, c.intermediate_size) &&
+         gemm_tn_supported(kGemmW2, c.hidden_size);
 }
 
 // Split-K factors of a launch with a routed problem (tiles_r tiles of kb_r K blocks) and
@@ -147,11 +165,13 @@ long t_blocks_128(int T) { return ((long)T + kGemmBM - 1) / kGemmBM; }
 
 struct Layout {
   int bs, n, max_sorted, max_blocks, slots;
-  bool pair, fp8;
-  // launch plan of one forward: small-batch routing, fused row copy, split factors
-  bool small, fused_copy;
+  bool fp8;
+  // launch plan of one forward: small-batch routing, fused row copy, token-N GEMMs (tn),
+  // split factors
+  bool small, fused_copy, tn;
   int w2_bn, splits13, splits13_shared, splits2, splits2_shared, splits_router, launches;
-  size_t status, topk_weights, topk_ids, sorted, expert_ids, npp, block_seg, inv, scratch,
+  size_t status, topk_weights, topk_ids, sorted, expert_ids, npp, block_seg, block_rows, inv,
+      scratch,
       x_perm, act, ytok, act_s, part_r, part_s, logits, xq, tile_cnt, tail_part, total;
   int tile_cnt_r, tile_cnt_s;  // counters of the fused split reduce (routed, shared); 0 = none
   int tail_cnt;                // counters of the w2 stream-K tail (after those); 0 = none
@@ -163,9 +183,9 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   Layout L;
   const int E = c.num_experts, k = c.top_k, H = c.hidden_size, I = c.intermediate_size;
   const int Is = c.shared_intermediate_size;
-  L.pair = use_pair(c, T);
+  L.tn = use_tn(c, T);
   L.fp8 = c.weight_quant == GBMOE_QUANT_FP8_BLOCK128;
-  L.bs = L.pair ? 2 * kGemmBM : kGemmBM;
+  L.bs = L.tn ? 2 * kGemmBM : kGemmBM;
   L.n = T * k;
   L.max_sorted = L.n + E * (L.bs - 1);
   L.max_blocks = L.max_sorted / L.bs + 1;
@@ -185,6 +205,8 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   o = up(o + 4);
   L.block_seg = o;
   o = up(o + (size_t)L.max_blocks * 8);
+  L.block_rows = o;
+  o = up(o + (size_t)L.max_blocks * 4);
   L.inv = o;
   o = up(o + (size_t)L.n * 4);
   L.scratch = o;
@@ -228,7 +250,7 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   const int kblk = L.fp8 ? kFp8Block : kGemmBK;  // K elements per GEMM pipeline stage
   const long est_blocks = (long)(L.n < E ? L.n : E) + L.n / kGemmBM;  // >= 1 partial per expert
   const long t_blocks = ((long)T + L.bs - 1) / L.bs;
-  if (L.pair) {
+  if (L.tn) {
     L.splits13 = L.splits13_shared = L.splits2 = L.splits2_shared = 1;
   } else {
     const Splits a = choose_splits2(est_blocks * (I / kGemmBM), H / kblk,
@@ -253,7 +275,7 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   L.tile_cnt_s = fused_reduce && Is ? (int)t_blocks * (Is / kGemmBM) * 4 : 0;
   // bf16 w2 without split-K: a stream-K tail evens out the last round of tiles (up to one
   // 128 x N-tile fp32 partial per SM)
-  const bool tail = T > kSplitMaxTokens && !L.fp8 && !L.pair;
+  const bool tail = T > kSplitMaxTokens && !L.fp8 && !L.tn;
   L.tail_cnt = tail ? num_sms() * 4 : 0;
   L.tail_part = up(L.tile_cnt + (size_t)(L.tile_cnt_r + L.tile_cnt_s + L.tail_cnt) * 4);
   L.total = up(L.tail_part + (tail ? (size_t)num_sms() * kGemmBM * L.w2_bn * 4 : 0));
@@ -338,7 +360,7 @@ GBMOE_API size_t moe_forward_workspace_size(const gbmoe_config_t* cfg, int32_t m
 
 GBMOE_API int32_t moe_forward_block_size(const gbmoe_config_t* cfg, int32_t num_tokens) {
   if (check_layer(cfg) != GBMOE_OK || num_tokens < 0) return kGemmBM;
-  return use_pair(*cfg, num_tokens) ? 2 * kGemmBM : kGemmBM;
+  return use_tn(*cfg, num_tokens) ? 2 * kGemmBM : kGemmBM;
 }
 
 GBMOE_API gbmoe_status_t moe_forward_workspace_layout(const gbmoe_config_t* cfg,
@@ -468,12 +490,13 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
     P.ldo = E;
     P.store_rows = T;
     P.out_split_stride = (long long)T * E;
-    GBMOE_TRY(launch_gemm(kGemmRouter, kGemmBM, gr, stream, false, T));
+    GBMOE_TRY(launch_gemm(kGemmRouter, kGemmBM, gr, stream, T));
     router_logits = at<float>(workspace, L.logits);
     logit_splits = gr.splits;
     logit_stride = (long long)T * E;
   }
   int2* bseg = at<int2>(workspace, L.block_seg);
+  int* brows = L.tn ? at<int>(workspace, L.block_rows) : nullptr;
   int* inv = at<int>(workspace, L.inv);
   int* tile_cnt = at<int>(workspace, L.tile_cnt);
   // apply_router_weight_on_input: the gathered rows carry the routing weight instead
@@ -505,7 +528,7 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
                           logit_splits, logit_stride, tile_cnt,
                           L.tile_cnt_r + L.tile_cnt_s + L.tail_cnt));
     GBMOE_TRY(launch_align(tids, L.n, E, L.bs, sorted, eids, L.max_blocks, npp,
-                           at<char>(workspace, L.scratch), status, stream, bseg, inv));
+                           at<char>(workspace, L.scratch), status, stream, bseg, inv, brows));
     GBMOE_TRY(gather());
   }
   GBMOE_TRY(rec(1));
@@ -687,6 +710,7 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
     P.num_flat = L.n;
     P.part = at<float>(workspace, L.part_r);
     P.part_split_stride = (long long)L.n * (gated ? 2 : 1) * I;
+    P.block_rows = brows;
   }
   if (Is) {
     GemmProblem& P = g1.p[1];
@@ -719,7 +743,13 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
     if (Is) g1.p[1].tile_count = tile_cnt + L.tile_cnt_r;
   }
   // a row block holds at most T real rows (a token meets an expert once)
-  GBMOE_TRY(launch_gemm(gated ? kGemmW13 : kGemmW1, kGemmBM, g1, stream, L.pair, T));
+  if (L.tn) {
+    if (gated) g1.p[0].n_tiles = I / kGemmBM;    // units of 128 features (64 per CTA)
+    else g1.p[0].n_tiles = I / 256;              // units of 256 features
+    GBMOE_TRY(launch_gemm_tn(gated ? kGemmW13 : kGemmW1, g1, stream));
+  } else {
+    GBMOE_TRY(launch_gemm(gated ? kGemmW13 : kGemmW1, kGemmBM, g1, stream, T));
+  }
   if ((g1.splits > 1 || (Is && g1.splits_p1 > 1)) && !L.tile_cnt_r)
     GBMOE_TRY(launch_silu_reduce(g1, npp, L.max_sorted, gated, stream));
   GBMOE_TRY(rec(2));
@@ -755,6 +785,7 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
     P.top_k = k;
     P.slots = L.slots;
     P.out_split_stride = slot_copy;
+    P.block_rows = brows;
   }
   if (Is) {
     GemmProblem& P = g2.p[1];
@@ -786,7 +817,13 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
     g2.tail_count = tile_cnt + L.tile_cnt_r + L.tile_cnt_s;
     g2.tail_max_splits = 8;
   }
-  GBMOE_TRY(launch_gemm(kGemmW2, w2_bn, g2, stream, L.pair, T));
+  if (L.tn) {
+    g2.p[0].n_tiles = H / 256;                   // units of 256 output rows
+    if (Is) g2.p[1].n_tiles = H / 256;
+    GBMOE_TRY(launch_gemm_tn(kGemmW2, g2, stream));
+  } else {
+    GBMOE_TRY(launch_gemm(kGemmW2, w2_bn, g2, stream, T));
+  }
   GBMOE_TRY(rec(3));
   GBMOE_TRY(launch_combine(ytok, L.slots, k, H, T, g2.splits, Is ? g2.splits_p1 : g2.splits,
                            slot_copy, output, stream));
@@ -862,7 +899,7 @@ GBMOE_API gbmoe_status_t moe_router_logits(int32_t num_tokens, int32_t hidden_si
   P.ldo = E;
   P.store_rows = T;
   PdlChain chain;
-  return cuda_status(launch_gemm(kGemmRouter, kGemmBM, gr, (cudaStream_t)stream, false, T));
+  return cuda_status(launch_gemm(kGemmRouter, kGemmBM, gr, (cudaStream_t)stream, T));
 }
 
 GBMOE_API gbmoe_status_t moe_quant_fp8_per_token_group(int32_t num_rows, int32_t hidden_size,

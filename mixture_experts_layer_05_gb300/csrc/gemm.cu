@@ -503,250 +503,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ---------------------------------------------------------------- the CTA-pair GEMM
-// One work unit = 256 rows (a 256-row block of one expert) x one N tile of 256 MMA
-// columns, computed by a cluster of two CTAs with tcgen05.mma.cta_group::2 (M = 256):
-// CTA r loads A rows [256 b + 128 r, +128) and half r of the B tile, so each SM stages
-// 32 KB per K step instead of 48 KB and half of each weight tile. w13: half 0 = the
-// gate rows, half 1 = the up rows (D columns [0,128) gate, [128,256) up); w2: the
-// two 128-row halves of a 256-row weight tile. The leader CTA (rank 0) issues the
-// MMAs; both CTAs' loads complete on the leader's full barrier; commits arrive on the
-// barriers of both CTAs. Each CTA has two 256-column accumulators; its 8 epilogue
-// warps copy one to registers, release it, and only then apply SiLU*mul or the
-// routing weight and store, while the MMAs of the next units run.
-constexpr int kPairStages = 6;
-constexpr int kPairEpiWarps = 8;
-constexpr int kPairThreads = 64 + 32 * kPairEpiWarps;
-constexpr uint32_t kPairTmemCols = 512;  // two 256-column accumulators
-constexpr uint32_t kPairStageBytes = kABytes + 128 * kGemmBK * 2;
-constexpr size_t kPairSmem = (size_t)kPairStages * kPairStageBytes + 1024 + 256;
-constexpr int kPairBM = 2 * kGemmBM;
-
-template <int KIND>
-__global__ void __launch_bounds__(kPairThreads, 1)
-    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0,
-                     const __grid_constant__ CUtensorMap tmB0,
-                     const __grid_constant__ CUtensorMap tmA1,
-                     const __grid_constant__ CUtensorMap tmB1, const GemmLaunch args) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairStages * kPairStageBytes);
-  // bars: full[kPairStages] empty[kPairStages] tfull[2] tempty[2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 4);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const uint32_t bar0 = smem_addr(bars);
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (kPairStages + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kPairStages + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kPairStages + 2 + a); };
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kPairStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 2 * kPairEpiWarps);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch(&tmA0);
-    tma_prefetch(&tmB0);
-    if (args.num_problems > 1) {
-      tma_prefetch(&tmA1);
-      tma_prefetch(&tmB1);
-    }
-  }
-  if (warp == 1) {
-    tmem_alloc_pair(smem_addr(tmem_slot), kPairTmemCols);
-    tmem_relinquish_pair();
-  }
-  tc_fence_before();
-  cluster_sync();             // barriers of both CTAs initialised, TMEM allocated
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  const uint32_t leader_full0 = mapa_shared(full_bar(0), 0);
-  const uint32_t leader_tempty0 = mapa_shared(tempty_bar(0), 0);
-
-  Schedule sched;
-  sched.init(args, kPairBM);
-  const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (both CTAs)
-    if (lane == 0) {
-      uint32_t it = 0;
-      bool ok = true;
-      for (int u = cluster_id; ok && u < sched.units; u += num_clusters) {
-        const Unit w = sched.unit(args, u);
-        const GemmProblem& P = args.p[w.p];
-        const CUtensorMap* ta = w.p ? &tmA1 : &tmA0;
-        const CUtensorMap* tb = w.p ? &tmB1 : &tmB0;
-        int e = P.expert_ids ? P.expert_ids[w.mb] : 0;
-        if ((unsigned)e >= (unsigned)P.num_experts) {
-          record_status(args.status, GBMOE_ERR_DEVICE_CHECK);
-          e = 0;
-        }
-        const int a_row = w.mb * kPairBM + (int)rank * kGemmBM;
-        const int b_row = KIND == kGemmW13
-                              ? e * P.b_rows_per_expert + w.nt * 128 + (rank ? P.up_offset : 0)
-                              : e * P.b_rows_per_expert + w.nt * 256 + (int)rank * 128;
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          const int s = it % kPairStages;
-          const uint32_t ph = (it / kPairStages) & 1u;
-          if (!wait_bounded_cluster(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sa = base + s * kPairStageBytes;
-          if (leader) mbar_expect_tx(full_bar(s), 2 * kPairStageBytes);
-          const uint32_t fb = leader_full0 + 8u * s;
-          tma_load_2d_pair(sa, ta, fb, kb * kGemmBK, a_row);
-          tma_load_2d_pair(sa + kABytes, tb, fb, kb * kGemmBK, b_row);
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (leader only)
-    if (leader && lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(kPairBM, 256);
-      uint32_t it = 0;
-      int local = 0;
-      bool ok = true;
-      for (int u = cluster_id; ok && u < sched.units; u += num_clusters, ++local) {
-        const Unit w = sched.unit(args, u);
-        const int acc = local & 1;
-        const uint32_t use = (uint32_t)(local >> 1);
-        if (!wait_bounded_cluster(tempty_bar(acc), (use & 1u) ^ 1u, abort_flag, args.status))
-          break;
-        tc_fence_after();
-        const uint32_t d = tmem_base + acc * kAccStride;
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          const int s = it % kPairStages;
-          const uint32_t ph = (it / kPairStages) & 1u;
-          if (!wait_bounded_cluster(full_bar(s), ph, abort_flag, args.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = base + s * kPairStageBytes;
-          const uint32_t sb = sa + kABytes;
-#pragma unroll
-          for (int kk = 0; kk < kGemmBK / 16; ++kk)
-            mma_bf16_pair(d, sdesc_sw128(sa + kk * 32), sdesc_sw128(sb + kk * 32), idesc,
-                          (kb > w.kb0 || kk != 0) ? 1u : 0u);
-          mma_commit_pair(empty_bar(s));
-        }
-        if (!ok) break;
-        mma_commit_pair(tfull_bar(acc));
-      }
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ epilogue (both CTAs)
-    const int ew = warp - 2;
-    const int quarter = warp & 3;             // TMEM lanes [32*quarter, 32*quarter + 32)
-    const int half = ew >> 2;                 // which half of this thread's columns
-    const int row = quarter * 32 + lane;
-    int local = 0;
-    for (int u = cluster_id; u < sched.units; u += num_clusters, ++local) {
-      const Unit w = sched.unit(args, u);
-      const GemmProblem& P = args.p[w.p];
-      const int acc = local & 1;
-      const uint32_t use = (uint32_t)(local >> 1);
-      if (!wait_bounded_cluster(tfull_bar(acc), use & 1u, abort_flag, args.status)) break;
-      tc_fence_after();
-      const int m = w.mb * kPairBM + (int)rank * kGemmBM + row;
-      const uint32_t tl = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kAccStride;
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      if (KIND == kGemmW13) {         // gate cols [64 h, +64), up cols [128 + 64 h, +64)
-        tmem_ld32(tl + half * 64, r0);
-        tmem_ld32(tl + half * 64 + 32, r1);
-        tmem_ld32(tl + 128 + half * 64, r2);
-        tmem_ld32(tl + 128 + half * 64 + 32, r3);
-      } else {                        // output cols [128 h, +128)
-        tmem_ld32(tl + half * 128, r0);
-        tmem_ld32(tl + half * 128 + 32, r1);
-        tmem_ld32(tl + half * 128 + 64, r2);
-        tmem_ld32(tl + half * 128 + 96, r3);
-      }
-      tmem_wait_ld(r0);
-      reg_fence(r1);
-      reg_fence(r2);
-      reg_fence(r3);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8u * acc);  // accumulator free again
-      int f = -1;
-      if (P.sorted_ids) {
-        const int v = P.sorted_ids[m];
-        if (v >= 0 && v < P.num_flat) f = v;
-      } else if (m < P.store_rows) {
-        f = m;
-      }
-      if (KIND == kGemmW13) {
-        const bool store = P.sorted_ids ? true : (m < P.store_rows);
-        if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.out) +
-                                                (size_t)m * P.ldo + (size_t)w.nt * 128 + half * 64);
-          // 64 consecutive activations -> 8 x 16-byte stores
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const uint32_t* g = c ? r1 : r0;
-            const uint32_t* up = c ? r3 : r2;
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t q[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                q[i] = pack_bf16x2(silu_mul(__uint_as_float(g[8 * v + 2 * i]),
-                                            __uint_as_float(up[8 * v + 2 * i])),
-                                   silu_mul(__uint_as_float(g[8 * v + 2 * i + 1]),
-                                            __uint_as_float(up[8 * v + 2 * i + 1])));
-              dst[c * 4 + v] = make_uint4(q[0], q[1], q[2], q[3]);
-            }
-          }
-        }
-      } else {
-        int dest = -1;
-        float wt = 1.f;
-        if (f >= 0) {
-          if (P.sorted_ids) {
-            dest = (f / P.top_k) * P.slots + (f % P.top_k);
-            wt = P.row_weight ? P.row_weight[f] : 1.f;
-          } else {
-            dest = f * P.slots + P.slot_offset;
-          }
-        }
-        if (dest >= 0) {
-          float* dst = static_cast<float*>(P.out) + (size_t)dest * P.ldo + (size_t)w.nt * 256 +
-                       half * 128;
-          store_f32x32(dst, r0, wt);
-          store_f32x32(dst + 32, r1, wt);
-          store_f32x32(dst + 64, r2, wt);
-          store_f32x32(dst + 96, r3, wt);
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  cluster_sync();             // no CTA leaves while its peer may still signal or read it
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc_pair(tmem_base, kPairTmemCols);
-  }
-}
-
 // Self test of the bounded wait: one thread waits on an mbarrier nobody arrives on; the
 // wait gives up after timeout_ns and records GBMOE_ERR_TIMEOUT in the status word.
 __global__ void wait_selftest_kernel(int* status, unsigned long long timeout_ns) {
@@ -890,66 +646,23 @@ cudaError_t launch_rows(int kind, int bn, const CUtensorMap* tm, const GemmLaunc
   return cudaErrorInvalidValue;
 }
 
-template <int KIND>
-cudaError_t launch_pair_typed(const CUtensorMap* tm, const GemmLaunch& args, int clusters,
-                              cudaStream_t stream) {
-  static int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<KIND>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kPairSmem);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * clusters, 1, 1);
-  cfg.blockDim = dim3(kPairThreads, 1, 1);
-  cfg.dynamicSmemBytes = kPairSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<KIND>, tm[0], tm[1], tm[2],
-                                           tm[3], args);
-  pdl_next() = true;
-  return e;
-}
-
 }  // namespace
 
-cudaError_t launch_gemm(int kind, int bn, const GemmLaunch& L, cudaStream_t stream, bool pair,
+cudaError_t launch_gemm(int kind, int bn, const GemmLaunch& L, cudaStream_t stream,
                         int max_rows_per_block) {
-  const int arows = (!pair && max_rows_per_block <= 32) ? 32 : kGemmBM;
+  const int arows = max_rows_per_block <= 32 ? 32 : kGemmBM;
   if (L.num_problems < 1 || L.num_problems > 2 || L.splits < 1) return cudaErrorInvalidValue;
-  if (pair && (L.splits != 1 || splits_of(L, 1) != 1 || (kind == kGemmW2 && bn != 256) ||
-               (kind == kGemmW13 && bn != 128) ||
-               kind == kGemmW1 || kind == kGemmRouter))
-    return cudaErrorInvalidValue;
   CUtensorMap tm[4];
   long units = 0;
-  const uint32_t b_box = pair ? 128u : (uint32_t)bn;
   for (int p = 0; p < 2; ++p) {
     const GemmProblem& P = L.p[L.num_problems > p ? p : 0];
     if (!make_map(&tm[2 * p], P.A, (uint64_t)P.K, (uint64_t)P.a_rows, (uint32_t)arows) ||
-        !make_map(&tm[2 * p + 1], P.B, (uint64_t)P.K, (uint64_t)P.b_rows, b_box))
+        !make_map(&tm[2 * p + 1], P.B, (uint64_t)P.K, (uint64_t)P.b_rows, (uint32_t)bn))
       return cudaErrorInvalidValue;
     if (p < L.num_problems) {
       if (splits_of(L, p) < 1 || P.k_blocks < splits_of(L, p)) return cudaErrorInvalidValue;
       units += (long)P.max_m_blocks * P.n_tiles * splits_of(L, p);
     }
-  }
-  if (pair) {
-    int clusters = num_sms() / 2;
-    if (units < clusters) clusters = (int)units;
-    if (clusters < 1) clusters = 1;
-    return kind == kGemmW13 ? launch_pair_typed<kGemmW13>(tm, L, clusters, stream)
-                            : launch_pair_typed<kGemmW2>(tm, L, clusters, stream);
   }
   int grid = num_sms();
   if (units < grid) grid = (int)units;

@@ -13,11 +13,6 @@ namespace gbmoe {
 
 constexpr int kAlignChunk = 2048;  // flat indices per align chunk (one scatter warp each)
 constexpr int kGemmBM = 128;       // token rows per GEMM tile (= align block size)
-#ifndef GBMOE_PAIR_MIN_ROWS
-#define GBMOE_PAIR_MIN_ROWS 2048
-#endif
-// CTA-pair GEMMs when the experts average at least this many rows.
-constexpr int kPairMinRowsPerExpert = GBMOE_PAIR_MIN_ROWS;
 constexpr int kGemmBK = 64;        // K elements per pipeline stage (one 128-byte swizzle row)
 
 int num_sms();
@@ -65,9 +60,11 @@ cudaError_t launch_topk(const gbmoe_config_t& c, int T, const float* logits, con
 size_t align_scratch_bytes(int n, int E);
 // block_seg (optional): per block, (first block, block count) of its expert's run.
 // inv (optional): per flat index, its position in sorted order.
+// block_rows (optional): per block, its real (non-padding) rows.
 cudaError_t launch_align(const int* ids, int n, int E, int bs, int* sorted, int* expert_ids,
                          int max_blocks, int* npp, void* scratch, int* status,
-                         cudaStream_t stream, int2* block_seg = nullptr, int* inv = nullptr);
+                         cudaStream_t stream, int2* block_seg = nullptr, int* inv = nullptr,
+                         int* block_rows = nullptr);
 // Routing + align of a small batch in one launch (when route_align_small_ok).
 bool route_align_small_ok(int T, int k, int E);
 cudaError_t launch_route_align_small(const gbmoe_config_t& c, int T, const float* logits,
@@ -110,6 +107,8 @@ struct GemmProblem {
   const int* expert_ids;   // expert per row block, or NULL (all expert 0)
   const int2* block_seg;   // per row block: (first block, block count) of its expert run,
                            // or NULL (one run over all blocks)
+  const int* block_rows;   // token-N GEMMs: real rows of each row block (routed problems),
+                           // or NULL (identity rows: store_rows bounds them)
   int group_m;             // row blocks walked together across all N tiles (L2 reuse)
   int num_experts;
   int b_rows_per_expert;   // rows of B per expert
@@ -168,12 +167,19 @@ __host__ __device__ inline int splits_of(const GemmLaunch& L, int p) {
   return (p == 0 || L.splits_p1 <= 0) ? L.splits : L.splits_p1;
 }
 
-// pair: the CTA-pair kernel (clusters of 2, M = 256 per unit, row blocks of 256; w13 with
-// bn = 128, w2 with bn = 256; no split-K).
+// Tokens-on-M grouped GEMM (128-row blocks, the token rows on the MMA's M side).
 // max_rows_per_block: an upper bound on the real rows of any row block (<= 32 lets the
 // kernel load 32-row A boxes and run a deeper pipeline).
 cudaError_t launch_gemm(int kind, int bn, const GemmLaunch& L, cudaStream_t stream,
-                        bool pair = false, int max_rows_per_block = kGemmBM);
+                        int max_rows_per_block = kGemmBM);
+
+// Token-N grouped GEMMs on CTA pairs (prefill, no split-K): row blocks of 256 rows, each
+// block's tokens on the MMA's N side, N = its real rows (GemmProblem.block_rows, or
+// store_rows for identity problems) rounded up to 16. Units: kGemmW13 128 features
+// (n_tiles = I / 128), kGemmW1 256 features (I / 256), kGemmW2 256 output rows (H / 256).
+// gemm_tn_supported(kind, I or H): whether the sizes tile that way.
+bool gemm_tn_supported(int kind, int hidden_or_inter);
+cudaError_t launch_gemm_tn(int kind, const GemmLaunch& L, cudaStream_t stream);
 
 // One mbarrier wait that nothing completes; gives up after timeout_us and records
 // GBMOE_ERR_TIMEOUT in *status.

@@ -83,6 +83,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Bring a tile of `map` into L2 without writing shared memory (no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // The same load with an L2 eviction policy (createpolicy); streaming operands that no
 // other CTA will read again go first, so they do not push everything else out of L2.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
@@ -291,6 +299,15 @@ __device__ __forceinline__ float act_gated(float g, float u, float alpha, float 
     u = fminf(fmaxf(u, -limit), limit);
   }
   return g / (1.f + __expf(-alpha * g)) * u;
+}
+// act_gated with the fast single-precision division (__fdividef, a couple of ulp): the
+// result is rounded to bf16 right after, 2^16 times coarser.
+__device__ __forceinline__ float act_gated_fast(float g, float u, float alpha, float limit) {
+  if (limit > 0.f) {
+    g = fminf(g, limit);
+    u = fminf(fmaxf(u, -limit), limit);
+  }
+  return __fdividef(g, 1.f + __expf(-alpha * g)) * u;
 }
 // 32 consecutive bf16 biases as fp32 (zeros when b is NULL).
 __device__ __forceinline__ void load_bias32(const __nv_bfloat16* b, float (&out)[32]) {

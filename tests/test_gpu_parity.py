@@ -353,10 +353,13 @@ PAIR_SHARED = _small(configs.DSV3, num_experts=8, top_k=4, num_expert_group=4, t
                      hidden_size=256, intermediate_size=256, shared_intermediate_size=384)
 
 
-@pytest.mark.parametrize("w,T", [(PAIR_ROUTED, 4096), (PAIR_ROUTED, 4501), (PAIR_SHARED, 4100)],
-                         ids=["routed-4096", "routed-4501", "shared-4100"])
+@pytest.mark.parametrize("w,T", [(PAIR_ROUTED, 4096), (PAIR_ROUTED, 4501), (PAIR_SHARED, 4100),
+                                 (PAIR_SHARED, 300)],
+                         ids=["routed-4096", "routed-4501", "shared-4100", "shared-300"])
 def test_forward_pair_mode(cuda_lib, w, T):
-    """Experts averaging >= 2048 rows: row blocks of 256 on CTA pairs (cta_group::2)."""
+    """Experts averaging >= 128 rows: the token-N GEMMs on CTA pairs (cta_group::2), row
+    blocks of 256 whose MMA width follows their real rows; the forward's align must match
+    the oracle's at block size 256."""
     cfg = binding.config_from_workload(w)
     assert binding.moe_forward_block_size(cfg, T) == 256
     wts = inputs.make_weights(w, 0)
@@ -502,7 +505,11 @@ VARIANTS = {
 }
 # two-way split-K of the first GEMM: its last split finishes the activation in the GEMM
 FUSED2 = _small(configs.MIXTRAL, num_experts=8, hidden_size=512, intermediate_size=1024)
+# experts averaging >= 128 rows: the token-N CTA-pair GEMMs (w1 too: I % 256 == 0)
+TN = _small(configs.DSV3, num_experts=16, top_k=4, num_expert_group=4, topk_group=2,
+            hidden_size=512, intermediate_size=256, shared_intermediate_size=256)
 VARIANT_SHAPES = {
+    "tn": TN,                     # token-N CTA-pair GEMMs, shared expert included
     "dsv3": SMALL["dsv3"],        # grouped sigmoid routing + shared expert
     "split": SPLIT,               # decode shapes: split-K and the split reduce kernel
     "fused2": FUSED2,             # decode shapes: split-K reduced inside the GEMM
@@ -553,11 +560,13 @@ def test_forward_w2_stream_k_tail(cuda_lib, use_bias, T):
 
 
 @pytest.mark.parametrize("vname", list(VARIANTS))
-@pytest.mark.parametrize("sname,T", [("dsv3", 203), ("split", 1), ("split", 17), ("fused2", 1),
-                                     ("fused2", 5)])
+@pytest.mark.parametrize("sname,T", [("tn", 600), ("dsv3", 203), ("split", 1), ("split", 17),
+                                     ("fused2", 1), ("fused2", 5)])
 def test_forward_variants(cuda_lib, vname, sname, T):
     v = dict(VARIANTS[vname])
     w = VARIANT_SHAPES[sname]
+    if sname == "tn":
+        assert binding.moe_forward_block_size(binding.config_from_workload(w), T) == 256
     gated = v.pop("gated", True)
     use_bias = v.pop("bias", False)
     if not gated:
