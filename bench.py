@@ -294,15 +294,27 @@ def run_ours(args, w, T):
     out = torch.empty_like(x)
     stream = torch.cuda.current_stream()
     K, W = args.steps, args.warmup
+    gate = None
+    if args.router == "gate":
+        # the router GEMM inside the forward: a synthetic gate ~N(0, 1/sqrt(H)), so the
+        # logits of the N(0, 1) hidden states are about N(0, 1) as in the logits workloads
+        gate = inputs.normal((w.num_experts, w.hidden_size), w.hidden_size ** -0.5,
+                             inputs.tensor_seed(w.name, "gate", 0), torch.bfloat16, dev)
+
+    def fwd(**kw):
+        if gate is not None:
+            return layer(x, gate_weight=gate, out=out, **kw)
+        return layer(x, logits, out=out, **kw)
+
     for _ in range(W):
-        layer(x, logits, out=out)
+        fwd()
     torch.cuda.synchronize()
 
     # stage breakdown (informational, untimed): events at every stage boundary
     sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(binding.NUM_STAGE_EVENTS)]
             for _ in range(W)]
     for i in range(W):
-        layer(x, logits, out=out, events=sevs[i])
+        fwd(events=sevs[i])
     torch.cuda.synchronize()
     stage = {n: statistics.mean(e[a].elapsed_time(e[b]) for e in sevs)
              for n, a, b in (("route_align_gather", 0, 1), ("w13_gemm", 1, 2),
@@ -325,11 +337,11 @@ def run_ours(args, w, T):
         cap.wait_stream(stream)
         with torch.cuda.graph(graph, stream=cap):
             for i in range(K):
-                layer(x, logits, out=out)
+                fwd()
         graph_w13 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph_w13, stream=cap):
             for i in range(K):
-                layer(x, logits, out=out, events=[None, wevs[i][0], wevs[i][1], None, None])
+                fwd(events=[None, wevs[i][0], wevs[i][1], None, None])
         torch.cuda.synchronize()
     except Exception as exc:                        # eager timing if capture is refused
         print(f"[bench] CUDA graph capture failed ({exc}); timing eager steps", file=sys.stderr)
@@ -338,7 +350,7 @@ def run_ours(args, w, T):
 
     def eager_steps():
         for i in range(K):
-            layer(x, logits, out=out)
+            fwd()
 
     def timed_steps():
         if graph is not None:
@@ -351,7 +363,7 @@ def run_ours(args, w, T):
             graph_w13.replay()
         else:
             for i in range(K):
-                layer(x, logits, out=out, events=[None, wevs[i][0], wevs[i][1], None, None])
+                fwd(events=[None, wevs[i][0], wevs[i][1], None, None])
 
     def warm(fn, seconds=0.5):
         """Back-to-back steps until the GPU settles in its loaded power state."""
@@ -416,7 +428,7 @@ def run_ours(args, w, T):
     x_h = x_cpu.pin_memory()
     l_h = logits_cpu.pin_memory()
     y_h = [torch.empty(x_cpu.shape, dtype=x_cpu.dtype).pin_memory() for _ in range(2)]
-    pipe = binding.HostPipeline(layer, T)
+    pipe = binding.HostPipeline(layer, T, gate_weight=gate)
 
     def e2e_run(n):
         pipe.run([x_h] * n, [l_h] * n, [y_h[i & 1] for i in range(n)])
@@ -455,7 +467,7 @@ def run_ours(args, w, T):
         for a, b in evs:
             flush.fill_(1.0)
             a.record(stream)
-            layer(x, logits, out=out)
+            fwd()
             b.record(stream)
         torch.cuda.synchronize()
         cold = {"ms_per_step": round(statistics.mean(a.elapsed_time(b) for a, b in evs), 4),
@@ -492,7 +504,9 @@ def run_ours(args, w, T):
                                    f"I={w.intermediate_size} E={w.num_experts} k={w.top_k}"
                                    + (f" shared I={w.shared_intermediate_size}"
                                       if w.shared_intermediate_size else "")
-                                   + (" w8a8 fp8 block-128" if fp8 else ""),
+                                   + (" w8a8 fp8 block-128" if fp8 else "")
+                                   + (", router GEMM from the gate weight" if gate is not None
+                                      else ""),
                        "tokens_per_gpu": T, "global_batch": T * world,
                        "parallelism": f"dp{world} replicas",
                        "l2": ("inputs larger than L2 (expert weights streamed every step)"
@@ -521,10 +535,11 @@ def run_ours(args, w, T):
                       "note": "the same K forwards launched one by one (no graph), right after "
                               "the timed region"},
             "e2e": {"value": round(aggregate_tokens_per_s(T, world, e2e_ms), 1),
-                    "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
+                    "unit": "tokens/s",
+                    "h2d_bytes_per_step": x.numel() * 2 + (0 if gate is not None else logits.numel() * 4),
                     "d2h_bytes_per_step": out.numel() * 2, "ms_per_step": round(e2e_ms, 4),
                     "clocks": x_clocks},
-            "gpu_launches": K * binding.moe_forward_num_launches(cfg, T),
+            "gpu_launches": K * binding.moe_forward_num_launches_ex(cfg, T, gate is not None),
             "clocks": clocks,
         }
         if cold is not None:
@@ -728,6 +743,9 @@ def main(argv=None):
     ap.add_argument("--ref-sample", type=int, default=0,
                     help="tokens per reference step (0: sized to ~1.5 s per step)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--router", choices=["logits", "gate"], default="logits",
+                    help="router logits as input (the FusedMoE layer's signature), or the "
+                         "gate weight with the router GEMM inside the forward")
     ap.add_argument("--num-experts", type=int, default=0,
                     help="reduced-expert stand-in of the workload (profiling captures only)")
     ap.add_argument("--traffic", type=float, default=None,

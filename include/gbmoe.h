@@ -261,8 +261,13 @@ typedef struct {
   void* const* events;
   int32_t num_events;
   const void* gate_weight;   /* [E, H] bf16: when router_logits is NULL, the logits are
-                                computed first as hidden_states @ gate_weight^T in fp32
-                                (moe_router_logits); exactly one of the two is given */
+                                computed first as hidden_states @ gate_weight^T with fp32
+                                sums (`MoEGate.forward`); exactly one of the two is given.
+                                Batches of at most 16 tokens compute them inside the routing
+                                launch (no [T, E] logits pass of their own), larger ones with
+                                the tensor-core GEMM of moe_router_logits. Uses the int32 at
+                                byte 4 of the workspace as an arrival counter (zero between
+                                calls, like the status word) */
   /* weight_quant == FP8_BLOCK128 only (else NULL): the weights above are e4m3fn bytes and
      these their fp32 block scales, row-major per matrix:
      w13_scale [E, 2I/128, H/128], w2_scale [E, H/128, I/128],
@@ -336,6 +341,16 @@ gbmoe_status_t moe_get_device_status(void* workspace, int32_t* status, gbmoe_str
  * Returns -1 for an invalid configuration.
  */
 int32_t moe_forward_num_launches(const gbmoe_config_t* cfg, int32_t num_tokens);
+
+/*
+ * moe_forward_num_launches_ex: moe_forward_num_launches for a moe_forward_ex call that
+ * passes the gate weight instead of router logits when from_gate_weight != 0. Batches of
+ * at most 16 tokens (when num_tokens * top_k <= 2048) compute the router logits inside
+ * their routing launch (the count is unchanged); larger ones add one router GEMM launch.
+ * Returns -1 for an invalid configuration.
+ */
+int32_t moe_forward_num_launches_ex(const gbmoe_config_t* cfg, int32_t num_tokens,
+                                    int32_t from_gate_weight);
 
 /*
  * moe_selftest_bounded_wait: failure-detection self test. Enqueues one kernel whose

@@ -28,7 +28,8 @@ EXPORTS = ("moe_topk", "moe_align_block_size_workspace_size", "moe_align_block_s
            "moe_align_block_size_no_workspace",
            "moe_forward_workspace_size", "moe_forward_block_size", "moe_forward",
            "moe_forward_events", "moe_forward_workspace_layout", "moe_get_device_status",
-           "moe_forward_num_launches", "moe_selftest_bounded_wait", "moe_forward_ex",
+           "moe_forward_num_launches", "moe_forward_num_launches_ex",
+           "moe_selftest_bounded_wait", "moe_forward_ex",
            "moe_router_logits", "moe_quant_fp8_per_token_group", "gbmoe_version")
 
 
@@ -122,6 +123,7 @@ def load() -> ctypes.CDLL:
         "moe_forward_workspace_layout": (I32, [CP, I32, ctypes.POINTER(WorkspaceLayout)]),
         "moe_get_device_status": (I32, [P, ctypes.POINTER(I32), P]),
         "moe_forward_num_launches": (I32, [CP, I32]),
+        "moe_forward_num_launches_ex": (I32, [CP, I32, I32]),
         "moe_forward_ex": (I32, [CP, I32, ctypes.POINTER(ForwardArgs), P]),
         "moe_router_logits": (I32, [I32, I32, I32, P, P, P, P]),
         "moe_quant_fp8_per_token_group": (I32, [I32, I32, P, P, P, P]),
@@ -249,6 +251,11 @@ def moe_forward(cfg: Config, hidden_states, router_logits, e_score_correction_bi
 
 def moe_forward_num_launches(cfg: Config, num_tokens: int) -> int:
     return load().moe_forward_num_launches(ctypes.byref(cfg), num_tokens)
+
+
+def moe_forward_num_launches_ex(cfg: Config, num_tokens: int, from_gate_weight: bool) -> int:
+    return load().moe_forward_num_launches_ex(ctypes.byref(cfg), num_tokens,
+                                              int(bool(from_gate_weight)))
 
 
 def moe_selftest_bounded_wait(workspace, timeout_us: int, stream=None):
@@ -398,8 +405,9 @@ class HostPipeline:
     computes. Every batch still pays its own copies; they are only overlapped.
     """
 
-    def __init__(self, layer: FusedMoE, max_tokens: int):
+    def __init__(self, layer: FusedMoE, max_tokens: int, gate_weight=None):
         dev = layer.w13.device
+        self.gate = gate_weight                       # route from the gate weight: no logits
         H = layer.cfg.hidden_size
         E = layer.cfg.num_experts
         layer.reserve(max_tokens)
@@ -421,11 +429,15 @@ class HostPipeline:
             self.h2d.wait_event(self.comp_done[b])         # batch i-2 no longer reads x[b]
             with torch.cuda.stream(self.h2d):
                 x.copy_(xs[i], non_blocking=True)
-                lg.copy_(logits[i], non_blocking=True)
+                if self.gate is None:
+                    lg.copy_(logits[i], non_blocking=True)
                 self.in_ready[b].record(self.h2d)
             self.comp.wait_event(self.in_ready[b])
             self.comp.wait_event(self.d2h_done[b])         # batch i-2 has left y[b]
-            self.layer(x, lg, out=y, stream=self.comp)
+            if self.gate is None:
+                self.layer(x, lg, out=y, stream=self.comp)
+            else:
+                self.layer(x, out=y, stream=self.comp, gate_weight=self.gate)
             self.comp_done[b].record(self.comp)
             self.d2h.wait_event(self.comp_done[b])
             with torch.cuda.stream(self.d2h):

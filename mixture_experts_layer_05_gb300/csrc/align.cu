@@ -253,15 +253,106 @@ constexpr int kSmallThreads = kSmallWarps * 32;
 // stays 2-3 us faster on the CTA-wide path).
 constexpr int kBlockRouteMaxTokens = 1;
 
+// The router GEMM of a small batch on CUDA cores (a few tokens against E x H weights is a
+// weight stream, not a tensor-core problem): this CTA's warp w takes expert
+// 8 * (blockIdx.x / splits) + w over K split blockIdx.x % splits; lane l sums eight
+// consecutive products per 256-wide K step for every token, then the warp adds its lanes.
+constexpr int kGateMaxTokens = 16;
+// TM >= T token rows per pass, U K steps at a time: all loads of a pass (U weight vectors,
+// U x TM token vectors) are issued before its FMAs, so a pass costs about one load latency.
+// Rows past T re-read row T - 1 (an L1 hit; their sums are not stored); steps past the split
+// re-read its last vector and count zero.
+template <int TM, int U>
+__device__ __forceinline__ void gate_logits_rows(const uint4* __restrict__ wr,
+                                                 const uint4* __restrict__ x, int H8, int T,
+                                                 int k0, int k1, int lane, float* out) {
+  float acc[TM];
+#pragma unroll
+  for (int t = 0; t < TM; ++t) acc[t] = 0.f;
+  for (int kb = k0 + lane; kb < k1; kb += 32 * U) {
+    uint4 wv[U], xv[U][TM];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int k = min(kb + 32 * u, k1 - 1);
+      wv[u] = __ldg(wr + k);
+#pragma unroll
+      for (int t = 0; t < TM; ++t) xv[u][t] = __ldg(x + (size_t)min(t, T - 1) * H8 + k);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const bool live = kb + 32 * u < k1;
+      const uint32_t wu[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+      float w[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = unpack_bf16x2(wu[i]);
+        w[2 * i] = live ? f.x : 0.f;
+        w[2 * i + 1] = live ? f.y : 0.f;
+      }
+#pragma unroll
+      for (int t = 0; t < TM; ++t) {
+        const uint32_t xu[4] = {xv[u][t].x, xv[u][t].y, xv[u][t].z, xv[u][t].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = unpack_bf16x2(xu[i]);
+          acc[t] = fmaf(f.x, w[2 * i], acc[t]);
+          acc[t] = fmaf(f.y, w[2 * i + 1], acc[t]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TM; ++t) out[t] = acc[t];
+}
+
+__device__ __forceinline__ void gate_logits_slice(const GateArgs& ga, const uint4* __restrict__ x,
+                                                  int H8, int T, int E) {
+  const int splits = ga.splits;
+  const int grp = blockIdx.x / splits, sp = blockIdx.x % splits;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = grp * kSmallWarps + warp;
+  if (e >= E) return;
+  const int kper = (H8 + splits - 1) / splits;
+  const int k0 = sp * kper, k1 = min(H8, k0 + kper);
+  const uint4* wr = static_cast<const uint4*>(ga.gate) + (size_t)e * H8;
+  float acc[kGateMaxTokens];
+  if (T <= 1) gate_logits_rows<1, 4>(wr, x, H8, T, k0, k1, lane, acc);
+  else if (T <= 2) gate_logits_rows<2, 4>(wr, x, H8, T, k0, k1, lane, acc);
+  else if (T <= 4) gate_logits_rows<4, 2>(wr, x, H8, T, k0, k1, lane, acc);
+  else if (T <= 8) gate_logits_rows<8, 2>(wr, x, H8, T, k0, k1, lane, acc);
+  else gate_logits_rows<kGateMaxTokens, 1>(wr, x, H8, T, k0, k1, lane, acc);
+#pragma unroll
+  for (int t = 0; t < kGateMaxTokens; ++t) {
+    if (t < T) {
+      const float v = warp_sum(acc[t]);
+      if (lane == 0) ga.part[((size_t)sp * T + t) * E + e] = v;
+    }
+  }
+}
+
 template <int EPT>
 __global__ void __launch_bounds__(kSmallThreads, 1)
     route_align_small_kernel(TopkArgs a, int bs, int* __restrict__ sorted,
                              int* __restrict__ expert_ids, int max_blocks, int* __restrict__ npp,
                              int2* __restrict__ block_seg, int* __restrict__ inv,
                              const uint4* __restrict__ x, int H8, uint4* __restrict__ xp,
-                             const float* __restrict__ row_scale) {
+                             const float* __restrict__ row_scale, GateArgs ga) {
   pdl_trigger();  // the next kernel may start its launch now
   pdl_wait();     // inputs written by the previous kernel are visible
+  if (ga.gate) {
+    // 0. every CTA computes its slice of the router logits; the last to finish routes
+    __shared__ int s_last;
+    gate_logits_slice(ga, x, H8, a.T, a.E);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      s_last = atomicAdd(ga.counter, 1) == (int)gridDim.x - 1;
+      if (s_last) *ga.counter = 0;           // all have arrived: reset for the next forward
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+  }
   extern __shared__ int sm[];
   const int n = a.T * a.k, E = a.E;
   int* s_ids = sm;                                   // [n]
@@ -450,6 +541,7 @@ struct RouteAlignSmall {
   int H8;
   uint4* xp;
   const float* row_scale;
+  GateArgs ga;
   cudaStream_t stream;
   template <int EPT>
   void operator()() {
@@ -458,14 +550,25 @@ struct RouteAlignSmall {
     const size_t shm = (size_t)(((n + 31) & ~31) + (kSmallWarps * a.E > 64 ? kSmallWarps * a.E : 64) +
                                 (a.T <= kBlockRouteMaxTokens ? ((a.E + 3) & ~3) + ((a.E + 15) & ~15) + 128 : 0)) *
                        sizeof(int);
-    launch_kernel(route_align_small_kernel<EPT>, dim3(1), dim3(kSmallThreads), shm, stream, a, bs,
-                  sorted, expert_ids, max_blocks, npp, block_seg, inv, x, H8, xp, row_scale);
+    const int grid = ga.gate ? ((a.E + kSmallWarps - 1) / kSmallWarps) * ga.splits : 1;
+    launch_kernel(route_align_small_kernel<EPT>, dim3(grid), dim3(kSmallThreads), shm, stream, a,
+                  bs, sorted, expert_ids, max_blocks, npp, block_seg, inv, x, H8, xp, row_scale,
+                  ga);
   }
 };
 
 // One CTA routes all tokens here (8 warps), so only batches of a few tokens qualify.
 bool route_align_small_ok(int T, int k, int E) {
-  return T <= 16 && T * k <= kAlignChunk && E <= 1024;
+  return T <= kGateMaxTokens && T * k <= kAlignChunk && E <= 1024;
+}
+
+int gate_splits(int E, int H) {
+  const int groups = (E + kSmallWarps - 1) / kSmallWarps;
+  int s = num_sms() / groups;
+  const int ksteps = (H / 8 + 31) / 32;           // 256-wide K steps of a warp
+  if (s > ksteps) s = ksteps;
+  if (s > kGateMaxSplits) s = kGateMaxSplits;
+  return s < 1 ? 1 : s;
 }
 
 cudaError_t launch_route_align_small(const gbmoe_config_t& c, int T, const float* logits,
@@ -474,16 +577,21 @@ cudaError_t launch_route_align_small(const gbmoe_config_t& c, int T, const float
                                      int2* block_seg, int* inv, const void* x, void* x_perm,
                                      const float* row_scale, int* status, cudaStream_t stream,
                                      int logit_splits, long long logit_split_stride,
-                                     int* zero, int zero_count) {
+                                     int* zero, int zero_count, GateArgs gate) {
   TopkArgs ta = make_topk_args(c, T, logits, bias, weights, ids, status);
   ta.zero = zero;
   ta.zero_count = zero_count;
   ta.logit_splits = logit_splits;
   ta.logit_split_stride = logit_split_stride;
+  if (gate.gate) {                       // the routing reads the launch's own partial logits
+    ta.logits = gate.part;
+    ta.logit_splits = gate.splits;
+    ta.logit_split_stride = (long long)T * c.num_experts;
+  }
   RouteAlignSmall L{ta, bs, sorted,
                     expert_ids, max_blocks, npp, block_seg, inv,
                     static_cast<const uint4*>(x), c.hidden_size / 8,
-                    static_cast<uint4*>(x_perm), row_scale, stream};
+                    static_cast<uint4*>(x_perm), row_scale, gate, stream};
   if (T <= kBlockRouteMaxTokens)
     L.template operator()<0>();
   else

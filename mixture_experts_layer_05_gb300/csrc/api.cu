@@ -59,6 +59,14 @@ constexpr size_t kMaxSplits = GBMOE_MAX_SPLITS;  // largest split-K factor
 // 105.5 to 100.7 us; 2 and 8 were no better.
 constexpr double kUnitCostKb = GBMOE_UNIT_COST_KB;
 constexpr size_t kAlign = 256;
+// byte offset, inside the status region, of the fused router's arrival counter
+constexpr size_t kGateCounterOffset = 4;
+#ifndef GBMOE_GATE_FUSED
+#define GBMOE_GATE_FUSED 1
+#endif
+// small batches given the gate weight compute their router logits inside the routing launch
+// (0: with the tensor-core router GEMM first, as larger batches)
+constexpr bool kGateFused = GBMOE_GATE_FUSED != 0;
 
 size_t up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
 
@@ -464,10 +472,17 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
   } while (0)
 
   GBMOE_TRY(rec(0));
-  // router GEMM when the caller passes the gate weight instead of logits
+  // router GEMM when the caller passes the gate weight instead of logits: inside the routing
+  // launch for small batches (GateArgs), else a tensor-core GEMM before it
   int logit_splits = 1;
   long long logit_stride = 0;
-  if (!router_logits) {
+  GateArgs gate_args{nullptr, 1, nullptr, nullptr};
+  if (!router_logits && L.small && kGateFused) {
+    gate_args.gate = gate_weight;
+    gate_args.splits = gate_splits(E, H);
+    gate_args.part = at<float>(workspace, L.logits);
+    gate_args.counter = at<int>(workspace, L.status + kGateCounterOffset);
+  } else if (!router_logits) {
     GemmLaunch gr;
     std::memset(&gr, 0, sizeof(gr));
     gr.status = status;
@@ -521,7 +536,7 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
                                        L.bs, sorted, eids, L.max_blocks, npp, bseg, inv,
                                        hidden_states, fused_copy ? x_perm : nullptr, row_scale,
                                        status, stream, logit_splits, logit_stride, tile_cnt,
-                                       L.tile_cnt_r + L.tile_cnt_s + L.tail_cnt));
+                                       L.tile_cnt_r + L.tile_cnt_s + L.tail_cnt, gate_args));
     if (!fused_copy) GBMOE_TRY(gather());
   } else {
     GBMOE_TRY(launch_topk(c, T, router_logits, e_score_correction_bias, tw, tids, status, stream,
@@ -920,6 +935,14 @@ GBMOE_API int32_t moe_forward_num_launches(const gbmoe_config_t* cfg, int32_t nu
   if (check_layer(cfg) != GBMOE_OK || num_tokens < 0 || num_tokens > kMaxTokens) return -1;
   if (num_tokens == 0) return 0;
   return layout_for(*cfg, num_tokens).launches;
+}
+
+GBMOE_API int32_t moe_forward_num_launches_ex(const gbmoe_config_t* cfg, int32_t num_tokens,
+                                              int32_t from_gate_weight) {
+  const int32_t n = moe_forward_num_launches(cfg, num_tokens);
+  if (n <= 0 || !from_gate_weight) return n;
+  // small batches compute the logits inside the routing launch; others add the router GEMM
+  return (layout_for(*cfg, num_tokens).small && kGateFused) ? n : n + 1;
 }
 
 GBMOE_API gbmoe_status_t moe_selftest_bounded_wait(void* workspace, int32_t timeout_us,

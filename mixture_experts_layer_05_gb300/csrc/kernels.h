@@ -65,6 +65,19 @@ cudaError_t launch_align(const int* ids, int n, int E, int bs, int* sorted, int*
                          int max_blocks, int* npp, void* scratch, int* status,
                          cudaStream_t stream, int2* block_seg = nullptr, int* inv = nullptr,
                          int* block_rows = nullptr);
+// Router logits of a small batch computed inside its routing launch, from the gate weight
+// (MoEGate's x @ W_gate^T, bf16 operands, fp32 sums): CTA c takes experts 8 * (c / splits)
+// + [0, 8) (a warp each) over K split c % splits, writes fp32 partial logits, and the last
+// CTA to finish routes the batch from their split-ordered sum. gate == NULL: logits given.
+struct GateArgs {
+  const void* gate;   // [E, H] bf16
+  int splits;         // K splits; the launch has ceil(E / 8) * splits CTAs
+  float* part;        // [splits][T][E] fp32 partial logits (written)
+  int* counter;       // CTAs that have finished their slice; zero between forwards
+};
+constexpr int kGateMaxSplits = 8;
+// Gate K splits for a fused small-batch routing launch: about one CTA per SM.
+int gate_splits(int E, int H);
 // Routing + align of a small batch in one launch (when route_align_small_ok).
 bool route_align_small_ok(int T, int k, int E);
 cudaError_t launch_route_align_small(const gbmoe_config_t& c, int T, const float* logits,
@@ -73,7 +86,8 @@ cudaError_t launch_route_align_small(const gbmoe_config_t& c, int T, const float
                                      int2* block_seg, int* inv, const void* x, void* x_perm,
                                      const float* row_scale, int* status, cudaStream_t stream,
                                      int logit_splits = 1, long long logit_split_stride = 0,
-                                     int* zero = nullptr, int zero_count = 0);
+                                     int* zero = nullptr, int zero_count = 0,
+                                     GateArgs gate = GateArgs{nullptr, 1, nullptr, nullptr});
 // x_perm[inv[f]] = x[f / k] (times row_scale[f] when row_scale is not NULL) for f < n
 // (x_perm == NULL in the small launch: no copy there).
 cudaError_t launch_gather(const void* x, int H, const int* inv, int n, int k, int max_rows,

@@ -27,7 +27,8 @@ struct TopkArgs {
   int T, E, k, renorm, grouped, G, g, sigmoid;
   float rsf;
   int logit_splits;              // logits arrive as this many fp32 partial copies (>= 1),
-  long long logit_split_stride;  // summed in copy order on load (split-K router GEMM)
+  long long logit_split_stride;  // summed in copy order on load (split-K router GEMM); read
+                                 // through L2 (they may come from the same launch)
   int* zero;                     // the forward's split counters, cleared by the routing
   int zero_count;                // kernel (it runs before any GEMM of the forward)
 };
@@ -72,9 +73,9 @@ __device__ __forceinline__ int route_token_warp(const TopkArgs& a, int t, int la
     float l = -INFINITY;
     bias[i] = 0.f;
     if (e < a.E) {
-      l = __ldg(row + e);
+      l = __ldcg(row + e);
       if (a.bias) bias[i] = __ldg(a.bias + e);
-      for (int sp = 1; sp < a.logit_splits; ++sp) l += __ldg(row + sp * a.logit_split_stride + e);
+      for (int sp = 1; sp < a.logit_splits; ++sp) l += __ldcg(row + sp * a.logit_split_stride + e);
     }
     s[i] = l;
     mx = fmaxf(mx, s[i]);
@@ -277,9 +278,9 @@ __device__ __forceinline__ int route_token_block(const TopkArgs& a, int t, float
   if (tid < a.k) oid[tid] = -1;            // set before the first barrier below
   float mx = -INFINITY;
   for (int e = tid; e < E; e += nt) {
-    float l = __ldg(row + e);
+    float l = __ldcg(row + e);
     if (a.bias) key[e] = __ldg(a.bias + e);  // the bias is fetched with the logits
-    for (int sp = 1; sp < a.logit_splits; ++sp) l += __ldg(row + sp * a.logit_split_stride + e);
+    for (int sp = 1; sp < a.logit_splits; ++sp) l += __ldcg(row + sp * a.logit_split_stride + e);
     sc[e] = l;
     mx = fmaxf(mx, l);
   }

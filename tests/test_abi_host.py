@@ -153,6 +153,11 @@ def test_launch_count_host(lib):
         cfg = binding.config_from_workload(w)
         counts = [lib.moe_forward_num_launches(ctypes.byref(cfg), T) for T in (1, 16, 64, 4096)]
         assert all(4 <= c <= 9 for c in counts), (w.name, counts)
+        # from the gate weight: small batches route inside the same launch, others add one
+        for T, c in zip((1, 16, 64, 4096), counts):
+            small = T <= 16 and T * w.top_k <= 2048
+            assert lib.moe_forward_num_launches_ex(ctypes.byref(cfg), T, 1) == c + (0 if small else 1)
+            assert lib.moe_forward_num_launches_ex(ctypes.byref(cfg), T, 0) == c
 
 
 def _fwd_ex(lib, cfg, T=4, ptr=256, **fields):

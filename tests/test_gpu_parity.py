@@ -640,8 +640,9 @@ def test_router_logits(cuda_lib, E, H, T):
     assert (err <= bound).all(), float((err / bound).max())
 
 
-@pytest.mark.parametrize("name,T", [("dsv3", 1), ("dsv3", 77), ("mixtral", 16), ("dsv2", 300),
-                                    ("skew", 200)])
+@pytest.mark.parametrize("name,T", [("dsv3", 1), ("dsv3", 5), ("dsv3", 16), ("dsv3", 77),
+                                    ("mixtral", 1), ("mixtral", 16), ("dsv2", 3), ("dsv2", 300),
+                                    ("skew", 200), ("tiny", 16)])
 def test_forward_from_gate_weight(cuda_lib, name, T):
     """moe_forward_ex with the gate weight: router GEMM (split-K at decode), routing,
     experts. Rows whose oracle decision margin exceeds 1e-4 (far above the fp32 logit
@@ -676,12 +677,13 @@ def test_forward_from_gate_weight(cuda_lib, name, T):
     assert T == 1 or safe.mean() > 0.9
 
 
-def test_forward_from_gate_weight_near_ties(cuda_lib):
+@pytest.mark.parametrize("T", [16, 64])
+def test_forward_from_gate_weight_near_ties(cuda_lib, T):
     """Gate weights whose logits are built to land near routing ties: many rows fall under
     the 1e-4 margin, and every one of them must still hold a valid routing and the output
-    of its own routing."""
+    of its own routing (T = 16: logits inside the routing launch; T = 64: the router
+    GEMM)."""
     w = SMALL["dsv3"]
-    T = 64
     wts = inputs.make_weights(w, 0)
     x = inputs.normal((T, w.hidden_size), 1.0, 6, torch.bfloat16)
     base = _gate(w)
@@ -705,3 +707,45 @@ def test_forward_from_gate_weight_near_ties(cuda_lib):
     y_own = oracle.experts_combine(x, tw, ids, wts["w13"], wts["w2"], wts["shared_w13"],
                                    wts["shared_w2"])
     check_close(y, y_own, "near ties, on the GPU's routing")
+
+
+@pytest.mark.parametrize("name", ["dsv3", "mixtral", "dsv2"])
+def test_gate_weight_adds_no_launch_for_small_batches(cuda_lib, name):
+    """With the gate weight, batches of at most 16 tokens compute the router logits inside
+    their routing launch: the same number of kernels as from logits; larger ones add the
+    router GEMM."""
+    cfg = binding.config_from_workload(configs.WORKLOADS[name])
+    for T in (1, 4, 16):
+        assert binding.moe_forward_num_launches_ex(cfg, T, True) == \
+            binding.moe_forward_num_launches(cfg, T)
+    assert binding.moe_forward_num_launches_ex(cfg, 200, True) == \
+        binding.moe_forward_num_launches(cfg, 200) + 1
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_gate_weight_graph_replay(cuda_lib, T):
+    """The fused router's arrival counter returns to zero after every forward: a captured
+    forward from the gate weight replayed on new tokens equals eager calls."""
+    w = SMALL["dsv3"]
+    wts = inputs.make_weights(w, 0)
+    wg = _gate(w).to(DEV)
+    layer, _ = _layer(w, wts, T)
+    xs = [inputs.normal((T, w.hidden_size), 1.0, 40 + s, torch.bfloat16) for s in range(3)]
+    xd = xs[0].to(DEV)
+    out = torch.empty_like(xd)
+    layer(xd, gate_weight=wg, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=cs):
+        layer(xd, gate_weight=wg, out=out)
+    for x in xs:
+        xd.copy_(x)
+        g.replay()
+        torch.cuda.synchronize()
+        got = out.clone()
+        eager = layer(x.to(DEV), gate_weight=wg)
+        torch.cuda.synchronize()
+        assert torch.equal(got, eager)
+    assert layer.device_status() == binding.OK
