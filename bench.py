@@ -64,17 +64,18 @@ def aggregate_tokens_per_s(tokens_per_rank: int, world: int, ms_max: float) -> f
     return tokens_per_rank * world / (ms_max / 1e3)
 
 
-def layer_work(w, T: int, n_active: int, fp8: bool = False) -> dict:
+def layer_work(w, T: int, n_active: int, quant: str = "none") -> dict:
     """Algorithmic flops and bytes of one forward (no padding rows).
 
     bf16: weights, gathered rows and act 2 bytes per element. fp8 (w8a8, block 128):
     weights, gathered rows and act 1 byte per element plus one fp32 scale per 128 x 128
-    weight block and per 128-element activation group.
+    weight block and per 128-element activation group. nvfp4 (w4a4, block 16): weights,
+    gathered rows and act half a byte per element plus one e4m3 byte per 16 elements.
     """
     H, I, k, E, Is = w.hidden_size, w.intermediate_size, w.top_k, w.num_experts, \
         w.shared_intermediate_size
-    wb = 1.0 + 4.0 / (128 * 128) if fp8 else 2.0        # bytes per weight element
-    ab = 1.0 + 4.0 / 128 if fp8 else 2.0                # bytes per activation element
+    wb = {"fp8": 1.0 + 4.0 / (128 * 128), "nvfp4": 0.5 + 1.0 / 16}.get(quant, 2.0)
+    ab = {"fp8": 1.0 + 4.0 / 128, "nvfp4": 0.5 + 1.0 / 16}.get(quant, 2.0)
     flops_w13 = 4.0 * T * k * H * I + 4.0 * T * H * Is
     flops_w2 = 2.0 * T * k * H * I + 2.0 * T * H * Is
     w13_bytes = (n_active * 2 * I * H + 2 * Is * H) * wb
@@ -90,7 +91,14 @@ def layer_work(w, T: int, n_active: int, fp8: bool = False) -> dict:
 
 KERNEL_SOURCES = {"gemm.cu": ("gemm.cu", "tc.cuh", "common.cuh", "kernels.h"),
                   "gemm_tn.cu": ("gemm_tn.cu", "tc.cuh", "common.cuh", "kernels.h"),
-                  "gemm_fp8.cu": ("gemm_fp8.cu", "tc.cuh", "fp8.cuh", "common.cuh", "kernels.h")}
+                  "gemm_fp8.cu": ("gemm_fp8.cu", "tc.cuh", "fp8.cuh", "common.cuh", "kernels.h"),
+                  "gemm_fp4.cu": ("gemm_fp4.cu", "tc.cuh", "fp4.cuh", "common.cuh", "kernels.h")}
+
+# tensor peak of each path's contraction dtype: the measured bf16 peak times the nominal
+# dense ratio (e4m3 4.5 / 2.25, fp4 13.5 / 2.25 PFLOP/s)
+QUANT_PEAK_RATIO = {"none": 1.0, "fp8": 2.0, "nvfp4": 6.0}
+QUANT_DTYPE = {"none": "bf16", "fp8": "e4m3", "nvfp4": "e2m1"}
+QUANT_TAG = {"none": "", "fp8": " w8a8 fp8 block-128", "nvfp4": " w4a4 nvfp4 block-16"}
 
 
 def source_digest(source: str) -> str:
@@ -230,12 +238,13 @@ def routing_stats(layer, cfg, w, T) -> dict:
             "load_over_mean_hist": hist}
 
 
-def roofline_of(work: dict, t_s: float, peaks: dict, peak_src: str, fp8: bool, kname: str,
+def roofline_of(work: dict, t_s: float, peaks: dict, peak_src: str, quant: str, kname: str,
                 which: str = "w13") -> dict:
     """Roofline of one kernel (its algorithmic flops and bytes over its duration): bound by
     the larger of flops / tensor peak and bytes / HBM peak, both at the burst peak (a kernel
-    inside a short step); the sustained tensor fraction is reported beside it."""
-    ratio = 2.0 if fp8 else 1.0                      # e4m3 = 2 x the bf16 peak (nominal ratio)
+    inside a short step); the sustained tensor fraction is reported beside it. The tensor
+    peak is that of the path's own contraction dtype (QUANT_PEAK_RATIO)."""
+    ratio = QUANT_PEAK_RATIO[quant]
     burst = peaks["bf16_tflops"] * ratio
     sustained = peaks["bf16_tflops_sustained"] * ratio
     flops, byts = work[f"flops_{which}"], work[f"bytes_{which}"]
@@ -243,7 +252,7 @@ def roofline_of(work: dict, t_s: float, peaks: dict, peak_src: str, fp8: bool, k
     tflops = flops / t_s / 1e12
     gbs = byts / t_s / 1e9
     src = f"{peak_src} bf16 burst (best of 10 cuBLAS GEMMs)" + (
-        " x 2, the nominal e4m3/bf16 ratio" if fp8 else "")
+        f" x {ratio:g}, the nominal {QUANT_DTYPE[quant]}/bf16 dense ratio" if ratio != 1.0 else "")
     if t_tc >= t_hbm:
         roof = {"kernel": kname, "bound": "tensor", "achieved": round(tflops, 1),
                 "peak": round(burst, 1), "unit": "TFLOP/s", "frac": round(tflops / burst, 4),
@@ -261,6 +270,43 @@ def roofline_of(work: dict, t_s: float, peaks: dict, peak_src: str, fp8: bool, k
     return roof
 
 
+def make_layer(w, quant: str, dev, T: int):
+    """Seeded weights of the workload and the resident layer: bf16, fp8 block-128 or nvfp4
+    (prepared once, as a loader would)."""
+    from mixture_experts_layer_05_gb300 import binding, inputs
+    if quant == "fp8":
+        wts = inputs.make_fp8_weights(w, 0, device=dev)
+        cfg = binding.config_from_workload(w, weight_quant="fp8")
+        layer = binding.FusedMoE(cfg, wts["w13_q"], wts["w2_q"], wts["bias"], wts["shared_w13_q"],
+                                 wts["shared_w2_q"], max_tokens=T, w13_scale=wts["w13_s"],
+                                 w2_scale=wts["w2_s"], shared_w13_scale=wts["shared_w13_s"],
+                                 shared_w2_scale=wts["shared_w2_s"])
+    elif quant == "nvfp4":
+        wts = inputs.make_fp4_weights(w, 0, device=dev)
+        cfg = binding.config_from_workload(w, weight_quant="nvfp4")
+
+        def prep(q, sf):
+            return binding.moe_nvfp4_prepare_weight(q.reshape(-1, q.shape[-1]),
+                                                    sf.reshape(-1, sf.shape[-1]))
+        kw = dict(w13_weight_scale_2=wts["w13_s2"], w2_weight_scale_2=wts["w2_s2"],
+                  input_scale=wts["input_scale"], act_scale=wts["act_scale"])
+        sw13 = sw2 = None
+        if w.shared_intermediate_size:
+            sw13 = prep(wts["shared_w13"], wts["shared_w13_sf"])
+            sw2 = prep(wts["shared_w2"], wts["shared_w2_sf"])
+            kw.update(shared_weight_scale_2=wts["shared_s2"],
+                      shared_input_scale=wts["shared_input_scale"],
+                      shared_act_scale=wts["shared_act_scale"])
+        layer = binding.FusedMoE(cfg, prep(wts["w13"], wts["w13_sf"]), prep(wts["w2"], wts["w2_sf"]),
+                                 wts["bias"], sw13, sw2, max_tokens=T, **kw)
+    else:
+        wts = inputs.make_weights(w, 0, device=dev)
+        cfg = binding.config_from_workload(w)
+        layer = binding.FusedMoE(cfg, wts["w13"], wts["w2"], wts["bias"], wts["shared_w13"],
+                                 wts["shared_w2"], max_tokens=T)
+    return wts, cfg, layer
+
+
 def run_ours(args, w, T):
     import torch
     import torch.distributed as dist
@@ -276,21 +322,11 @@ def run_ours(args, w, T):
     build_mod.build()
     binding.load()
 
-    fp8 = args.quant == "fp8"
+    quant = args.quant
+    fp8 = quant == "fp8"
     x_cpu, logits_cpu = inputs.make_tokens(w, T, seed=rank_seed(rank))
     x, logits = x_cpu.to(dev), logits_cpu.to(dev)
-    if fp8:
-        wts = inputs.make_fp8_weights(w, 0, device=dev)
-        cfg = binding.config_from_workload(w, weight_quant="fp8")
-        layer = binding.FusedMoE(cfg, wts["w13_q"], wts["w2_q"], wts["bias"], wts["shared_w13_q"],
-                                 wts["shared_w2_q"], max_tokens=T, w13_scale=wts["w13_s"],
-                                 w2_scale=wts["w2_s"], shared_w13_scale=wts["shared_w13_s"],
-                                 shared_w2_scale=wts["shared_w2_s"])
-    else:
-        wts = inputs.make_weights(w, 0, device=dev)
-        cfg = binding.config_from_workload(w)
-        layer = binding.FusedMoE(cfg, wts["w13"], wts["w2"], wts["bias"], wts["shared_w13"],
-                                 wts["shared_w2"], max_tokens=T)
+    wts, cfg, layer = make_layer(w, quant, dev, T)
     out = torch.empty_like(x)
     stream = torch.cuda.current_stream()
     K, W = args.steps, args.warmup
@@ -459,7 +495,7 @@ def run_ours(args, w, T):
     # cold L2 for working sets that fit in L2: each step after writing a buffer larger than
     # L2, the forward alone timed by events (informational)
     cold = None
-    weight_bytes = sum(v.numel() * v.element_size() for v in wts.values() if v is not None)
+    weight_bytes = sum(v.numel() * v.element_size() for v in wts.values() if hasattr(v, "numel"))
     if weight_bytes < 3 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -475,22 +511,25 @@ def run_ours(args, w, T):
                        "the forward only"}
 
     rs = routing_stats(layer, cfg, w, T)
-    work = layer_work(w, T, rs["active_experts"], fp8)
+    work = layer_work(w, T, rs["active_experts"], quant)
     peaks, peak_src = load_peaks()
     # which w13 kernel the forward runs: the token-N CTA-pair GEMM when its blocks are 256
-    tn = not fp8 and binding.moe_forward_block_size(cfg, T) == 256
+    tn = quant == "none" and binding.moe_forward_block_size(cfg, T) == 256
     kname = ("gemm_fp8_kernel<w13> (grouped e4m3 w13 GEMM + SiLU*mul + act quant)" if fp8
+             else "gemm_fp4_kernel<w13> (grouped nvfp4 w13 GEMM, fp4 -> f16 in shared memory)"
+             if quant == "nvfp4"
              else "gemm_tn_kernel<w13> (grouped w13 GEMM + SiLU*mul, tokens on N, CTA pairs)"
              if tn else "gemm_kernel<w13> (grouped w13 GEMM + SiLU*mul)")
     value = aggregate_tokens_per_s(T, world, ms_max)
-    ratio = 2.0 if fp8 else 1.0
+    ratio = QUANT_PEAK_RATIO[quant]
 
     res = None
     if rank == 0:
         # dominant kernel: the w13 grouped GEMM (two thirds of the flops and weight bytes)
-        roof = roofline_of(work, w13_ms / 1e3, peaks, peak_src, fp8, kname)
+        roof = roofline_of(work, w13_ms / 1e3, peaks, peak_src, quant, kname)
         roof["traffic"] = args.traffic if args.traffic is not None else (
             kernel_traffic("gemm_fp8_w13", w.name, T, "gemm_fp8.cu") if fp8
+            else kernel_traffic("gemm_fp4_w13", w.name, T, "gemm_fp4.cu") if quant == "nvfp4"
             else kernel_traffic("gemm_tn_w13", w.name, T, "gemm_tn.cu") if tn
             else kernel_traffic("gemm_w13", w.name, T))
         step_s = ms_max / 1e3
@@ -498,13 +537,13 @@ def run_ours(args, w, T):
         res = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": QUANT_DTYPE[quant],
             "data": "synthetic",
             "config": {"workload": f"{w.name}: FusedMoE layer H={w.hidden_size} "
                                    f"I={w.intermediate_size} E={w.num_experts} k={w.top_k}"
                                    + (f" shared I={w.shared_intermediate_size}"
                                       if w.shared_intermediate_size else "")
-                                   + (" w8a8 fp8 block-128" if fp8 else "")
+                                   + QUANT_TAG[quant]
                                    + (", router GEMM from the gate weight" if gate is not None
                                       else ""),
                        "tokens_per_gpu": T, "global_batch": T * world,
@@ -545,7 +584,8 @@ def run_ours(args, w, T):
         if cold is not None:
             res["cold_l2"] = cold
         if args.cpu_baseline and world == 1:
-            res["cpu_baseline"] = cpu_baseline(w, wts, x_cpu, logits_cpu, args.cpu_sample, fp8=fp8)
+            res["cpu_baseline"] = cpu_baseline(w, wts, x_cpu, logits_cpu, args.cpu_sample,
+                                               quant=quant)
     return res
 
 
@@ -561,22 +601,11 @@ def run_sweep(args, w, token_counts):
     dev = torch.device("cuda", 0)
     build_mod.build()
     binding.load()
-    fp8 = args.quant == "fp8"
+    quant = args.quant
     Tmax = max(token_counts)
-    if fp8:
-        wts = inputs.make_fp8_weights(w, 0, device=dev)
-        cfg = binding.config_from_workload(w, weight_quant="fp8")
-        layer = binding.FusedMoE(cfg, wts["w13_q"], wts["w2_q"], wts["bias"], wts["shared_w13_q"],
-                                 wts["shared_w2_q"], max_tokens=Tmax, w13_scale=wts["w13_s"],
-                                 w2_scale=wts["w2_s"], shared_w13_scale=wts["shared_w13_s"],
-                                 shared_w2_scale=wts["shared_w2_s"])
-    else:
-        wts = inputs.make_weights(w, 0, device=dev)
-        cfg = binding.config_from_workload(w)
-        layer = binding.FusedMoE(cfg, wts["w13"], wts["w2"], wts["bias"], wts["shared_w13"],
-                                 wts["shared_w2"], max_tokens=Tmax)
+    wts, cfg, layer = make_layer(w, quant, dev, Tmax)
     peaks, peak_src = load_peaks()
-    ratio = 2.0 if fp8 else 1.0
+    ratio = QUANT_PEAK_RATIO[quant]
     K = args.steps
     for T in token_counts:
         x_cpu, l_cpu = inputs.make_tokens(w, T, seed=0)
@@ -603,10 +632,10 @@ def run_sweep(args, w, token_counts):
         if layer.device_status() != binding.OK:
             raise RuntimeError(f"device status error at T={T}")
         rs = routing_stats(layer, cfg, w, T)
-        work = layer_work(w, T, rs["active_experts"], fp8)
+        work = layer_work(w, T, rs["active_experts"], quant)
         t = ms / 1e3
         print(json.dumps({
-            "sweep": w.name, "tokens": T, "dtype": "e4m3" if fp8 else "bf16",
+            "sweep": w.name, "tokens": T, "dtype": QUANT_DTYPE[quant],
             "ms_per_step": round(ms, 4), "tokens_per_s": round(T / t, 1),
             "layer_tflops": round(work["flops"] / t / 1e12, 1),
             "tensor_frac_of_burst": round(work["flops"] / t / 1e12
@@ -619,8 +648,7 @@ def run_sweep(args, w, token_counts):
 
 
 def _host_weights(w, wts):
-    import torch
-    return {k: (None if v is None else v.to("cpu")) for k, v in wts.items()}
+    return {k: (v.to("cpu") if hasattr(v, "to") else v) for k, v in wts.items()}
 
 
 def oracle_cfg(w):
@@ -630,9 +658,24 @@ def oracle_cfg(w):
                 routed_scaling_factor=w.routed_scaling_factor)
 
 
-def _oracle_layer(w, hw, x, logits, fp8: bool):
+def _fp4_oracle_weights(hw) -> dict:
+    """make_fp4_weights' tensors under the names the NVFP4 oracle takes."""
+    o = {k: hw[k] for k in ("w13", "w13_sf", "w2", "w2_sf", "input_scale", "act_scale")}
+    o["w13_s2"], o["w2_s2"] = hw["w13_s2"].numpy(), hw["w2_s2"].numpy()
+    if hw.get("shared_w13") is not None:
+        o.update(shared_w13=hw["shared_w13"], shared_w13_sf=hw["shared_w13_sf"],
+                 shared_w2=hw["shared_w2"], shared_w2_sf=hw["shared_w2_sf"],
+                 shared_w13_s2=float(hw["shared_s2"][0]), shared_w2_s2=float(hw["shared_s2"][1]),
+                 shared_input_scale=hw["shared_input_scale"],
+                 shared_act_scale=hw["shared_act_scale"])
+    return o
+
+
+def _oracle_layer(w, hw, x, logits, quant: str):
     import oracle
-    if fp8:
+    if quant == "nvfp4":
+        oracle.fused_moe_fp4(x, logits, hw["bias"], _fp4_oracle_weights(hw), **oracle_cfg(w))
+    elif quant == "fp8":
         oracle.fused_moe_fp8(x, logits, hw["bias"], hw["w13_q"], hw["w13_s"], hw["w2_q"],
                              hw["w2_s"], hw["shared_w13_q"], hw["shared_w13_s"],
                              hw["shared_w2_q"], hw["shared_w2_s"], **oracle_cfg(w))
@@ -641,24 +684,24 @@ def _oracle_layer(w, hw, x, logits, fp8: bool):
                               hw["shared_w2"], **oracle_cfg(w))
 
 
-def _oracle_rows(w, hw, x_cpu, logits_cpu, r0, n, fp8=False):
+def _oracle_rows(w, hw, x_cpu, logits_cpu, r0, n, quant="none"):
     t0 = time.perf_counter()
-    _oracle_layer(w, hw, x_cpu[r0:r0 + n], logits_cpu[r0:r0 + n], fp8)
+    _oracle_layer(w, hw, x_cpu[r0:r0 + n], logits_cpu[r0:r0 + n], quant)
     return time.perf_counter() - t0
 
 
 def cpu_baseline(w, wts, x_cpu, logits_cpu, n_tokens: int, target_s: float = 12.0,
-                 fp8: bool = False) -> dict:
+                 quant: str = "none") -> dict:
     """The CPU oracle, as it stands, on a leading sample of the batch sized to ~target_s."""
     hw = _host_weights(w, wts)
     T = x_cpu.shape[0]
     n = min(n_tokens, T)
-    dt = _oracle_rows(w, hw, x_cpu, logits_cpu, 0, n, fp8)
+    dt = _oracle_rows(w, hw, x_cpu, logits_cpu, 0, n, quant)
     for _ in range(4):                              # grow the sample to ~target_s of work
         if dt >= target_s / 2 or n >= T:
             break
         n = int(min(T, max(2 * n, n * target_s / max(dt, 1e-3))))
-        dt = _oracle_rows(w, hw, x_cpu, logits_cpu, 0, n, fp8)
+        dt = _oracle_rows(w, hw, x_cpu, logits_cpu, 0, n, quant)
     return {"value": round(n / dt, 4), "unit": "tokens/s",
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
             "sample": f"first {n} of the step's {T} tokens, full weights, fp64 numpy "
@@ -676,19 +719,21 @@ def run_reference(args, w, T):
     if rank != 0:
         return None
     n = args.ref_sample if args.ref_sample > 0 else 1
-    fp8 = args.quant == "fp8"
+    quant = args.quant
     # drawn where the GPU arm draws them (the same values), then held on the host; on a
     # machine without a GPU, drawn on the CPU. Only the oracle's work is timed.
     gen = "cuda" if torch.cuda.is_available() else "cpu"
-    hw = inputs.make_fp8_weights(w, 0, device=gen) if fp8 else inputs.make_weights(w, 0, device=gen)
-    hw = {key: (None if v is None else v.to("cpu")) for key, v in hw.items()}
+    make = {"fp8": inputs.make_fp8_weights, "nvfp4": inputs.make_fp4_weights}.get(
+        quant, inputs.make_weights)
+    hw = {key: (v.to("cpu") if hasattr(v, "to") else v)
+          for key, v in make(w, 0, device=gen).items()}
     if gen == "cuda":
         torch.cuda.empty_cache()
     x_cpu, logits_cpu = inputs.make_tokens(w, T, seed=0)
 
     def step(i):
         r0 = (i * n) % max(T - n + 1, 1)
-        _oracle_layer(w, hw, x_cpu[r0:r0 + n], logits_cpu[r0:r0 + n], fp8)
+        _oracle_layer(w, hw, x_cpu[r0:r0 + n], logits_cpu[r0:r0 + n], quant)
 
     # size each step's sample so one step is ~1.5 s of oracle work (the whole run then
     # stays within a few minutes for the usual K, W)
@@ -717,7 +762,7 @@ def run_reference(args, w, T):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": f"{w.name}: FusedMoE layer H={w.hidden_size} "
                                    f"I={w.intermediate_size} E={w.num_experts} k={w.top_k}"
-                                   + (" w8a8 fp8 block-128" if fp8 else ""),
+                                   + QUANT_TAG[quant],
                        "tokens_per_gpu": T, "sample_tokens_per_step": n},
             "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
@@ -736,8 +781,9 @@ def main(argv=None):
     ap.add_argument("--sweep", default=None,
                     help="comma-separated token counts: one JSON line per count (no contract "
                          "line); e.g. the skewed-routing sweep 1,2,4,...,16384")
-    ap.add_argument("--quant", choices=["none", "fp8"], default="none",
-                    help="expert weights: bf16 (none) or e4m3 with 128 x 128 fp32 block scales")
+    ap.add_argument("--quant", choices=["none", "fp8", "nvfp4"], default="none",
+                    help="expert weights: bf16 (none), e4m3 with 128 x 128 fp32 block scales, "
+                         "or nvfp4 (e2m1, e4m3 scales per 16 values, per-expert fp32 scales)")
     ap.add_argument("--cpu-sample", type=int, default=4,
                     help="initial oracle sample (tokens); grown to ~12 s of CPU work")
     ap.add_argument("--ref-sample", type=int, default=0,

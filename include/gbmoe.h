@@ -51,7 +51,11 @@ typedef enum {
 
 typedef enum { GBMOE_SCORE_SOFTMAX = 0, GBMOE_SCORE_SIGMOID = 1 } gbmoe_scoring_t;
 typedef enum { GBMOE_ACT_SILU = 0 } gbmoe_act_t;
-typedef enum { GBMOE_QUANT_NONE = 0, GBMOE_QUANT_FP8_BLOCK128 = 1 } gbmoe_weight_quant_t;
+typedef enum {
+  GBMOE_QUANT_NONE = 0,
+  GBMOE_QUANT_FP8_BLOCK128 = 1,
+  GBMOE_QUANT_NVFP4 = 2
+} gbmoe_weight_quant_t;
 
 /*
  * Layer configuration; field names follow the FusedMoE constructor (vLLM
@@ -95,6 +99,18 @@ typedef enum { GBMOE_QUANT_NONE = 0, GBMOE_QUANT_FP8_BLOCK128 = 1 } gbmoe_weight
  *                         same way before its w2 GEMM. Requires H % 256 == 0, gated SiLU
  *                         without clamp or alpha, no expert biases, no
  *                         apply_router_weight_on_input (else UNSUPPORTED).
+ *                         NVFP4: the w4a4 layer of FlashInferFP4MoE (sglang
+ *                         `fused_moe_triton/layer.py` page, `trtllm_fp4_block_scale_moe`):
+ *                         weights are e2m1 codes with one e4m3 scale per 16 values along K
+ *                         and a per-expert fp32 weight_scale_2 (w = q * sf * s2), passed in
+ *                         the layout moe_nvfp4_prepare_weight writes; the input is quantized
+ *                         per token and block of 16 with the per-tensor input_scale g
+ *                         (sf = e4m3(g * amax / 6), q = e2m1(x * g / sf), fp32 steps;
+ *                         dequantized q * sf / g), and each act the same way with act_scale
+ *                         before its w2 GEMM (moe_quant_nvfp4 is that quantization alone).
+ *                         Same restrictions as FP8_BLOCK128 (H % 128 suffices). The pages'
+ *                         layer casts e_score_correction_bias to the activations' dtype
+ *                         before routing; callers wanting that pass bf16-valued biases.
  */
 typedef struct {
   int32_t num_experts;
@@ -276,6 +292,19 @@ typedef struct {
   const float* w2_scale;
   const float* shared_w13_scale;
   const float* shared_w2_scale;
+  /* weight_quant == NVFP4 only (else NULL / 0): w13_weight, w2_weight, shared_w13 and
+     shared_w2 are prepared NVFP4 weights (moe_nvfp4_prepare_weight of the [E * 2I, H],
+     [E * H, I], [2 I_s, H] and [H, I_s] stacks); these their fp32 per-expert scales
+     (device): w13_weight_scale_2 [E], w2_weight_scale_2 [E], shared_weight_scale_2 [2]
+     (w13, w2); and the per-tensor scales (host values > 0) of the input's and the act's
+     quantization, routed and shared */
+  const float* w13_weight_scale_2;
+  const float* w2_weight_scale_2;
+  const float* shared_weight_scale_2;
+  float input_scale;
+  float act_scale;
+  float shared_input_scale;
+  float shared_act_scale;
 } gbmoe_forward_args_t;
 gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_tokens,
                               const gbmoe_forward_args_t* args, gbmoe_stream_t stream);
@@ -308,6 +337,42 @@ gbmoe_status_t moe_quant_fp8_per_token_group(int32_t num_rows, int32_t hidden_si
                                              gbmoe_stream_t stream);
 
 /*
+ * moe_quant_nvfp4: fp4_quantize(x, global_scale, 16) as the FlashInferFP4MoE layer applies
+ * it to its input (sglang `fused_moe_triton/layer.py` page, `_quantize_hidden_states_fp4`):
+ * for each row and block of 16 consecutive columns, amax = max |x|, sf = e4m3(g * (amax /
+ * 6)) (round to nearest even, saturating at 448), r = g / sf (0 when sf is 0), q =
+ * e2m1(x * r) (round to nearest even, saturating at +-6), every step one fp32 operation.
+ *   x      [num_rows, hidden_size] bf16, device, 16-byte aligned
+ *   q      [num_rows, hidden_size / 2] bytes, device (written): element 2i in the low
+ *          nibble of byte i; codes: bit 3 the sign, magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6
+ *   sf     [num_rows, hidden_size / 16] e4m3fn bytes, device (written)
+ * hidden_size a positive multiple of 16, global_scale > 0 and finite; num_rows = 0 is a
+ * no-op. Asynchronous on `stream`; INVALID_ARG for bad sizes or pointers.
+ */
+gbmoe_status_t moe_quant_nvfp4(int32_t num_rows, int32_t hidden_size, const void* x,
+                               float global_scale, uint8_t* q, uint8_t* sf,
+                               gbmoe_stream_t stream);
+
+/*
+ * moe_nvfp4_prepare_weight: rewrites one NVFP4 weight stack [rows, K] (the checkpoint
+ * layout: packed codes [rows, K / 2], low nibble first, and e4m3 block scales [rows,
+ * K / 16]) into the layout the NVFP4 expert GEMMs stream, as the pages' layer shuffles its
+ * fp4 weights once at load time: for each tile of 128 rows and stage of 64 K values one
+ * 4608-byte chunk, chunk (tile, kb) at byte (tile * K / 64 + kb) * 4608, holding
+ *   bytes [h * 2048 + r * 16, +16)  the codes of row tile * 128 + r, values kb * 64 + 32 h
+ *                                   .. + 31 (h = 0, 1)
+ *   bytes [4096 + r * 4, +4)        that row's four block scales of the stage.
+ * A permutation of bytes only. rows a positive multiple of 128, K of 64; packed, scales
+ * and out 16-byte aligned device buffers; out holds moe_nvfp4_prepared_bytes(rows, K)
+ * bytes (= rows * K * 9 / 16). Asynchronous on `stream`; INVALID_ARG for bad sizes or
+ * pointers.
+ */
+size_t moe_nvfp4_prepared_bytes(int32_t rows, int32_t K);
+gbmoe_status_t moe_nvfp4_prepare_weight(int32_t rows, int32_t K, const uint8_t* packed,
+                                        const uint8_t* block_scale, uint8_t* out,
+                                        gbmoe_stream_t stream);
+
+/*
  * Byte offsets of the intermediate results inside a moe_forward workspace
  * (for inspection and tests). Each is valid after the call completes.
  */
@@ -320,9 +385,13 @@ typedef struct {
   size_t num_tokens_post_padded; /* int32 [1] */
   size_t act;                    /* bf16 [rows, I]: silu(gate)*up in expert order
                                     (FP8_BLOCK128: e4m3fn [rows, I], then fp32 scales
-                                    [I/128][rows] at act_scale) */
+                                    [I/128][rows] at act_scale; NVFP4: f16 [rows, I], the
+                                    values q * sf of the act's block quantization) */
   size_t act_scale;              /* FP8_BLOCK128 only, else 0 */
   size_t total;                  /* == moe_forward_workspace_size() */
+  size_t act_shared;             /* the shared expert's act [T, I_s] in token order (bf16;
+                                    NVFP4: f16 values q * sf of the quantized act); 0 when
+                                    there is no shared expert */
 } gbmoe_workspace_layout_t;
 gbmoe_status_t moe_forward_workspace_layout(const gbmoe_config_t* cfg, int32_t max_num_tokens,
                                             gbmoe_workspace_layout_t* layout);

@@ -20,7 +20,7 @@ STATUS = {0: "GBMOE_OK", -1: "GBMOE_ERR_INVALID_ARG", -2: "GBMOE_ERR_UNSUPPORTED
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_CHECK, ERR_TIMEOUT = \
     0, -1, -2, -3, -4, -5, -6
 SCORE = {"softmax": 0, "sigmoid": 1}
-QUANT = {None: 0, "none": 0, "fp8": 1, "fp8_block128": 1}
+QUANT = {None: 0, "none": 0, "fp8": 1, "fp8_block128": 1, "nvfp4": 2}
 NUM_STAGE_EVENTS = 5
 
 # every entry point declared in include/gbmoe.h
@@ -30,7 +30,8 @@ EXPORTS = ("moe_topk", "moe_align_block_size_workspace_size", "moe_align_block_s
            "moe_forward_events", "moe_forward_workspace_layout", "moe_get_device_status",
            "moe_forward_num_launches", "moe_forward_num_launches_ex",
            "moe_selftest_bounded_wait", "moe_forward_ex",
-           "moe_router_logits", "moe_quant_fp8_per_token_group", "gbmoe_version")
+           "moe_router_logits", "moe_quant_fp8_per_token_group", "moe_quant_nvfp4",
+           "moe_nvfp4_prepared_bytes", "moe_nvfp4_prepare_weight", "gbmoe_version")
 
 
 class GbmoeError(RuntimeError):
@@ -64,14 +65,18 @@ class ForwardArgs(ctypes.Structure):
                 ("events", ctypes.c_void_p), ("num_events", ctypes.c_int32),
                 ("gate_weight", ctypes.c_void_p), ("w13_scale", ctypes.c_void_p),
                 ("w2_scale", ctypes.c_void_p), ("shared_w13_scale", ctypes.c_void_p),
-                ("shared_w2_scale", ctypes.c_void_p)]
+                ("shared_w2_scale", ctypes.c_void_p),
+                ("w13_weight_scale_2", ctypes.c_void_p), ("w2_weight_scale_2", ctypes.c_void_p),
+                ("shared_weight_scale_2", ctypes.c_void_p), ("input_scale", ctypes.c_float),
+                ("act_scale", ctypes.c_float), ("shared_input_scale", ctypes.c_float),
+                ("shared_act_scale", ctypes.c_float)]
 
 
 class WorkspaceLayout(ctypes.Structure):
     """gbmoe_workspace_layout_t."""
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "topk_weights", "topk_ids", "sorted_token_ids", "expert_ids",
-        "num_tokens_post_padded", "act", "act_scale", "total")]
+        "num_tokens_post_padded", "act", "act_scale", "total", "act_shared")]
 
 
 def make_config(num_experts, top_k, hidden_size, intermediate_size, renormalize=True,
@@ -80,7 +85,8 @@ def make_config(num_experts, top_k, hidden_size, intermediate_size, renormalize=
                 is_act_and_mul=1, shared_intermediate_size=0, swiglu_limit=None,
                 gemm1_alpha=1.0, apply_router_weight_on_input=False,
                 weight_quant=None) -> Config:
-    """weight_quant: None / "none", or "fp8" (e4m3 weights with 128 x 128 fp32 block scales)."""
+    """weight_quant: None / "none", "fp8" (e4m3 weights with 128 x 128 fp32 block scales) or
+    "nvfp4" (prepared e2m1 weights with e4m3 block scales and per-expert fp32 scales)."""
     return Config(int(num_experts), int(top_k), int(hidden_size), int(intermediate_size),
                   int(bool(renormalize)), int(bool(use_grouped_topk)), int(num_expert_group or 0),
                   int(topk_group or 0), SCORE.get(scoring_func, scoring_func),
@@ -127,6 +133,9 @@ def load() -> ctypes.CDLL:
         "moe_forward_ex": (I32, [CP, I32, ctypes.POINTER(ForwardArgs), P]),
         "moe_router_logits": (I32, [I32, I32, I32, P, P, P, P]),
         "moe_quant_fp8_per_token_group": (I32, [I32, I32, P, P, P, P]),
+        "moe_quant_nvfp4": (I32, [I32, I32, P, ctypes.c_float, P, P, P]),
+        "moe_nvfp4_prepared_bytes": (SZ, [I32, I32]),
+        "moe_nvfp4_prepare_weight": (I32, [I32, I32, P, P, P, P]),
         "moe_selftest_bounded_wait": (I32, [P, I32, P]),
         "gbmoe_version": (I32, []),
     }
@@ -283,23 +292,39 @@ def _fp8_bytes(t, name):
     return t
 
 
+NVFP4_KEYS = ("w13_weight_scale_2", "w2_weight_scale_2", "shared_weight_scale_2",
+              "input_scale", "act_scale", "shared_input_scale", "shared_act_scale")
+
+
 def moe_forward_ex(cfg: Config, hidden_states, router_logits, e_score_correction_bias,
                    w13_weight, w2_weight, shared_w13, shared_w2, output, workspace,
                    w13_bias=None, w2_bias=None, events=None, stream=None, gate_weight=None,
-                   w13_scale=None, w2_scale=None, shared_w13_scale=None, shared_w2_scale=None):
+                   w13_scale=None, w2_scale=None, shared_w13_scale=None, shared_w2_scale=None,
+                   w13_weight_scale_2=None, w2_weight_scale_2=None, shared_weight_scale_2=None,
+                   input_scale=0.0, act_scale=0.0, shared_input_scale=0.0,
+                   shared_act_scale=0.0):
     """moe_forward with the optional per-expert biases, stage events, (router_logits None)
-    the gate weight whose router GEMM runs first, or (cfg.weight_quant fp8) e4m3 weights
-    with their fp32 128 x 128 block scales."""
+    the gate weight whose router GEMM runs first, or quantized experts: (cfg.weight_quant
+    fp8) e4m3 weights with their fp32 128 x 128 block scales; (nvfp4) prepared fp4 weights
+    (moe_nvfp4_prepare_weight) with fp32 per-expert scales and the per-tensor scales."""
     _need(hidden_states, torch.bfloat16, "hidden_states")
     _need(router_logits, torch.float32, "router_logits")
     _need(e_score_correction_bias, torch.float32, "e_score_correction_bias")
     weights = ((w13_weight, "w13_weight"), (w2_weight, "w2_weight"), (shared_w13, "shared_w13"),
                (shared_w2, "shared_w2"))
-    if cfg.weight_quant:
+    if cfg.weight_quant == QUANT["fp8"]:
         for t, n in weights:
             _fp8_bytes(t, n)
         for t, n in ((w13_scale, "w13_scale"), (w2_scale, "w2_scale"),
                      (shared_w13_scale, "shared_w13_scale"), (shared_w2_scale, "shared_w2_scale")):
+            _need(t, torch.float32, n)
+        weights = ()
+    elif cfg.weight_quant == QUANT["nvfp4"]:
+        for t, n in weights:
+            _need(t, torch.uint8, n)
+        for t, n in ((w13_weight_scale_2, "w13_weight_scale_2"),
+                     (w2_weight_scale_2, "w2_weight_scale_2"),
+                     (shared_weight_scale_2, "shared_weight_scale_2")):
             _need(t, torch.float32, n)
         weights = ()
     for t, n in weights + ((w13_bias, "w13_bias"), (w2_bias, "w2_bias"),
@@ -319,7 +344,10 @@ def moe_forward_ex(cfg: Config, hidden_states, router_logits, e_score_correction
                     workspace.numel() * workspace.element_size(),
                     ctypes.cast(arr, ctypes.c_void_p) if arr is not None else None,
                     0 if events is None else len(events), ptr(gate_weight), ptr(w13_scale),
-                    ptr(w2_scale), ptr(shared_w13_scale), ptr(shared_w2_scale))
+                    ptr(w2_scale), ptr(shared_w13_scale), ptr(shared_w2_scale),
+                    ptr(w13_weight_scale_2), ptr(w2_weight_scale_2),
+                    ptr(shared_weight_scale_2), float(input_scale), float(act_scale),
+                    float(shared_input_scale), float(shared_act_scale))
     _check("moe_forward_ex", load().moe_forward_ex(ctypes.byref(cfg), hidden_states.shape[0],
                                                    ctypes.byref(a), _stream(stream)))
 
@@ -340,6 +368,43 @@ def moe_quant_fp8_per_token_group(x, q=None, scale=None, stream=None):
     return q, scale
 
 
+def moe_quant_nvfp4(x, global_scale: float, q=None, sf=None, stream=None):
+    """fp4_quantize(x, g, 16) of bf16 rows: packed e2m1 codes q [R, H / 2] uint8 (low nibble
+    first) and e4m3 block scales sf [R, H / 16] (float8_e4m3fn); returns (q, sf)."""
+    _need(x, torch.bfloat16, "x")
+    R, H = x.shape
+    if q is None:
+        q = torch.empty(R, H // 2, dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty(R, H // 16, dtype=torch.float8_e4m3fn, device=x.device)
+    _need(q, torch.uint8, "q")
+    _fp8_bytes(sf, "sf")
+    _check("moe_quant_nvfp4", load().moe_quant_nvfp4(R, H, _p(x), float(global_scale), _p(q),
+                                                     _p(sf), _stream(stream)))
+    return q, sf
+
+
+def moe_nvfp4_prepared_bytes(rows: int, K: int) -> int:
+    return int(load().moe_nvfp4_prepared_bytes(rows, K))
+
+
+def moe_nvfp4_prepare_weight(packed, block_scale, out=None, stream=None):
+    """The GEMMs' layout of one fp4 weight stack: packed [rows, K / 2] uint8 codes and
+    block_scale [rows, K / 16] e4m3 (float8_e4m3fn or uint8) -> out (uint8, returned)."""
+    _need(packed, torch.uint8, "packed")
+    _fp8_bytes(block_scale, "block_scale")
+    rows, K = packed.shape[0], packed.shape[1] * 2
+    nbytes = moe_nvfp4_prepared_bytes(rows, K)
+    if nbytes == 0:
+        raise GbmoeError("moe_nvfp4_prepared_bytes", ERR_INVALID_ARG)
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=packed.device)
+    _need(out, torch.uint8, "out")
+    _check("moe_nvfp4_prepare_weight", load().moe_nvfp4_prepare_weight(
+        rows, K, _p(packed), _p(block_scale), _p(out), _stream(stream)))
+    return out
+
+
 def moe_get_device_status(workspace, stream=None) -> int:
     v = ctypes.c_int32(0)
     _check("moe_get_device_status",
@@ -353,13 +418,17 @@ class FusedMoE:
     def __init__(self, cfg: Config, w13_weight, w2_weight, e_score_correction_bias=None,
                  shared_w13=None, shared_w2=None, max_tokens: int = 1, w13_bias=None,
                  w2_bias=None, w13_scale=None, w2_scale=None, shared_w13_scale=None,
-                 shared_w2_scale=None):
+                 shared_w2_scale=None, **nvfp4):
         self.cfg = cfg
         self.w13, self.w2 = w13_weight, w2_weight
         self.bias, self.shared_w13, self.shared_w2 = e_score_correction_bias, shared_w13, shared_w2
         self.w13_bias, self.w2_bias = w13_bias, w2_bias
         self.scales = dict(w13_scale=w13_scale, w2_scale=w2_scale,
                            shared_w13_scale=shared_w13_scale, shared_w2_scale=shared_w2_scale)
+        unknown = set(nvfp4) - set(NVFP4_KEYS)
+        if unknown:
+            raise TypeError(f"unexpected arguments {sorted(unknown)}")
+        self.scales.update(nvfp4)  # nvfp4: per-expert and per-tensor scales
         self.max_tokens = 0
         self.workspace = None
         self.reserve(max_tokens)

@@ -16,7 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgbmoe.so")
-SOURCES = ["api.cu", "topk.cu", "align.cu", "gemm.cu", "gemm_tn.cu", "gemm_fp8.cu", "fp8.cu", "combine.cu",
+SOURCES = ["api.cu", "topk.cu", "align.cu", "gemm.cu", "gemm_tn.cu", "gemm_fp8.cu", "fp8.cu", "gemm_fp4.cu", "fp4.cu",
+           "combine.cu",
            "align_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

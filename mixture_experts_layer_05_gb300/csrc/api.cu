@@ -106,13 +106,14 @@ gbmoe_status_t check_layer(const gbmoe_config_t* c) {
     return GBMOE_ERR_UNSUPPORTED;                  // clamp / alpha / shared need the gated form
   if (c->hidden_size % 128 || c->intermediate_size % 128 || c->shared_intermediate_size % 128)
     return GBMOE_ERR_UNSUPPORTED;
-  if (c->weight_quant != GBMOE_QUANT_NONE && c->weight_quant != GBMOE_QUANT_FP8_BLOCK128)
+  if (c->weight_quant != GBMOE_QUANT_NONE && c->weight_quant != GBMOE_QUANT_FP8_BLOCK128 &&
+      c->weight_quant != GBMOE_QUANT_NVFP4)
     return GBMOE_ERR_INVALID_ARG;
-  if (c->weight_quant == GBMOE_QUANT_FP8_BLOCK128 &&
+  if (c->weight_quant != GBMOE_QUANT_NONE &&
       (!c->is_act_and_mul || c->swiglu_limit > 0.f ||
        (c->gemm1_alpha != 0.f && c->gemm1_alpha != 1.f) || c->apply_router_weight_on_input ||
-       c->hidden_size % 256))
-    return GBMOE_ERR_UNSUPPORTED;                  // the fp8 layer is the plain gated one
+       (c->weight_quant == GBMOE_QUANT_FP8_BLOCK128 && c->hidden_size % 256)))
+    return GBMOE_ERR_UNSUPPORTED;                  // the quantized layers are the plain gated one
   if ((long long)c->num_experts * 2 * c->intermediate_size > INT_MAX / 2 ||
       (long long)c->num_experts * c->hidden_size > INT_MAX / 2)
     return GBMOE_ERR_UNSUPPORTED;
@@ -177,6 +178,7 @@ struct Layout {
   // launch plan of one forward: small-batch routing, fused row copy, token-N GEMMs (tn),
   // split factors
   bool small, fused_copy, tn;
+  bool nvfp4;
   int w2_bn, splits13, splits13_shared, splits2, splits2_shared, splits_router, launches;
   size_t status, topk_weights, topk_ids, sorted, expert_ids, npp, block_seg, block_rows, inv,
       scratch,
@@ -193,7 +195,8 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   const int Is = c.shared_intermediate_size;
   L.tn = use_tn(c, T);
   L.fp8 = c.weight_quant == GBMOE_QUANT_FP8_BLOCK128;
-  L.bs = L.tn ? 2 * kGemmBM : kGemmBM;
+  L.nvfp4 = c.weight_quant == GBMOE_QUANT_NVFP4;
+  L.bs = L.tn ? 2 * kGemmBM : (L.nvfp4 ? kFp4BS : kGemmBM);
   L.n = T * k;
   L.max_sorted = L.n + E * (L.bs - 1);
   L.max_blocks = L.max_sorted / L.bs + 1;
@@ -234,16 +237,19 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
     const size_t fp8_bytes = Is ? up((size_t)T * Is) + (size_t)(Is / 128) * T * 4 : 0;
     o = up(o + (bf16_bytes > fp8_bytes ? bf16_bytes : fp8_bytes));
   }
+  // the NVFP4 first GEMM always writes fp32 partials (its act is quantized by the reduce)
+  const size_t part_rows = L.nvfp4 && (size_t)T > kMaxSplits * ts ? (size_t)T : kMaxSplits * ts;
   L.part_r = o;
-  o = up(o + kMaxSplits * ts * k * (c.is_act_and_mul ? 2 : 1) * I * 4);
+  o = up(o + part_rows * k * (c.is_act_and_mul ? 2 : 1) * I * 4);
   L.part_s = o;
-  o = up(o + kMaxSplits * ts * 2 * Is * 4);
+  o = up(o + part_rows * 2 * Is * 4);
   L.logits = o;                       // router GEMM output (per-split copies at decode)
   o = up(o + ((size_t)T > kMaxSplits * ts ? (size_t)T : kMaxSplits * ts) * E * 4);
   // fp8: e4m3 rows then group-major fp32 scales, inside the bf16-sized regions above (a
   // byte plus 4/128 bytes per element fits in 2 bytes); the token-order input has its own
   L.xq = o;
   if (L.fp8) o = up(o + up((size_t)T * H) + (size_t)(H / kFp8Block) * T * 4);
+  if (L.nvfp4 && Is) o = up(o + (size_t)T * H * 2);  // f16 token-order rows (shared expert)
   L.xs_perm = L.fp8 ? up((size_t)L.max_sorted * H) : 0;
   L.act_scale = L.fp8 ? up((size_t)L.max_sorted * I) : 0;
   L.act_s_scale = L.fp8 ? up((size_t)T * Is) : 0;
@@ -253,7 +259,7 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
 
   // launch plan
   L.small = route_align_small_ok(T, k, E);
-  L.fused_copy = L.small && L.n <= kFusedCopyMaxRows && !L.fp8;
+  L.fused_copy = L.small && L.n <= kFusedCopyMaxRows && !L.fp8 && !L.nvfp4;
   L.w2_bn = (H % 256 == 0) ? 256 : 128;
   const int kblk = L.fp8 ? kFp8Block : kGemmBK;  // K elements per GEMM pipeline stage
   const long est_blocks = (long)(L.n < E ? L.n : E) + L.n / kGemmBM;  // >= 1 partial per expert
@@ -278,17 +284,17 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   const bool split13 = L.splits13 > 1 || (Is && L.splits13_shared > 1);
   const int max_split13 = L.splits13 > (Is ? L.splits13_shared : 1) ? L.splits13
                                                                      : (Is ? L.splits13_shared : 1);
-  const bool fused_reduce = split13 && !L.fp8 && max_split13 <= 2;
+  const bool fused_reduce = split13 && !L.fp8 && !L.nvfp4 && max_split13 <= 2;
   L.tile_cnt_r = fused_reduce ? (L.max_sorted / L.bs) * (I / kGemmBM) * 4 : 0;
   L.tile_cnt_s = fused_reduce && Is ? (int)t_blocks * (Is / kGemmBM) * 4 : 0;
   // bf16 w2 without split-K: a stream-K tail evens out the last round of tiles (up to one
   // 128 x N-tile fp32 partial per SM)
-  const bool tail = T > kSplitMaxTokens && !L.fp8 && !L.tn;
+  const bool tail = T > kSplitMaxTokens && !L.fp8 && !L.nvfp4 && !L.tn;
   L.tail_cnt = tail ? num_sms() * 4 : 0;
   L.tail_part = up(L.tile_cnt + (size_t)(L.tile_cnt_r + L.tile_cnt_s + L.tail_cnt) * 4);
   L.total = up(L.tail_part + (tail ? (size_t)num_sms() * kGemmBM * L.w2_bn * 4 : 0));
-  L.launches = (L.small ? (L.fused_copy ? 1 : 2) : 5) + 1 + (split13 && !fused_reduce ? 1 : 0) +
-               1 + 1;
+  L.launches = (L.small ? (L.fused_copy ? 1 : 2) : 5) + 1 +
+               ((split13 && !fused_reduce) || L.nvfp4 ? 1 : 0) + 1 + 1;
   L.splits_router = choose_splits(t_blocks_128(T) * ((E + kGemmBM - 1) / kGemmBM), H / kGemmBK, T);
   return L;
 }
@@ -387,6 +393,7 @@ GBMOE_API gbmoe_status_t moe_forward_workspace_layout(const gbmoe_config_t* cfg,
   out->act = L.act;
   out->act_scale = L.fp8 ? L.act + L.act_scale : 0;
   out->total = L.total;
+  out->act_shared = cfg->shared_intermediate_size ? L.act_s : 0;
   return GBMOE_OK;
 }
 
@@ -427,10 +434,18 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
       !aligned16(w13_bias) || !aligned16(w2_bias))
     return GBMOE_ERR_INVALID_ARG;
   const bool fp8 = c.weight_quant == GBMOE_QUANT_FP8_BLOCK128;
-  if (fp8 && (w13_bias || w2_bias)) return GBMOE_ERR_UNSUPPORTED;
+  const bool nvfp4 = c.weight_quant == GBMOE_QUANT_NVFP4;
+  if ((fp8 || nvfp4) && (w13_bias || w2_bias)) return GBMOE_ERR_UNSUPPORTED;
   if (fp8 ? (!args->w13_scale || !args->w2_scale ||
              (Is && (!args->shared_w13_scale || !args->shared_w2_scale)))
           : (args->w13_scale || args->w2_scale || args->shared_w13_scale || args->shared_w2_scale))
+    return GBMOE_ERR_INVALID_ARG;
+  auto scale_ok = [](float g) { return std::isfinite(g) && g > 0.f; };
+  if (nvfp4 ? (!args->w13_weight_scale_2 || !args->w2_weight_scale_2 ||
+               !scale_ok(args->input_scale) || !scale_ok(args->act_scale) ||
+               (Is && (!args->shared_weight_scale_2 || !scale_ok(args->shared_input_scale) ||
+                       !scale_ok(args->shared_act_scale))))
+            : (args->w13_weight_scale_2 || args->w2_weight_scale_2 || args->shared_weight_scale_2))
     return GBMOE_ERR_INVALID_ARG;
   const Layout L = layout_for(c, num_tokens);
   if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) % kAlign))
@@ -511,7 +526,7 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
     logit_stride = (long long)T * E;
   }
   int2* bseg = at<int2>(workspace, L.block_seg);
-  int* brows = L.tn ? at<int>(workspace, L.block_rows) : nullptr;
+  int* brows = (L.tn || L.nvfp4) ? at<int>(workspace, L.block_rows) : nullptr;
   int* inv = at<int>(workspace, L.inv);
   int* tile_cnt = at<int>(workspace, L.tile_cnt);
   // apply_router_weight_on_input: the gathered rows carry the routing weight instead
@@ -523,7 +538,12 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
   uint8_t* xq_tok = at<uint8_t>(workspace, L.xq);
   float* xs_tok = at<float>(workspace, L.xq + L.xs_tok);
   float* xs_perm = at<float>(workspace, L.x_perm + L.xs_perm);
+  void* x_tok16 = at<char>(workspace, L.xq);  // nvfp4: f16 token-order rows (shared expert)
   auto gather = [&]() -> cudaError_t {
+    if (nvfp4)
+      return launch_quant_gather_fp4(hidden_states, H, inv, L.n, k, T, L.max_sorted,
+                                     args->input_scale, x_perm, Is ? x_tok16 : nullptr,
+                                     args->shared_input_scale, stream);
     if (fp8)
       return launch_quant_gather_fp8(hidden_states, H, inv, L.n, k, T,
                                      static_cast<uint8_t*>(x_perm), xs_perm, L.max_sorted,
@@ -548,6 +568,143 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
   }
   GBMOE_TRY(rec(1));
   const long long slot_copy = (long long)T * L.slots * H;
+
+  if (nvfp4) {
+    // ---- w13 (nvfp4): alpha-scaled fp32 partials of [gate | up], routed and shared
+    GemmLaunch g1;
+    std::memset(&g1, 0, sizeof(g1));
+    g1.status = status;
+    g1.num_problems = Is ? 2 : 1;
+    {
+      GemmProblem& P = g1.p[0];
+      P.A = x_perm;
+      P.a_rows = L.max_sorted;
+      P.B = w13_weight;
+      P.b_rows = E * 2 * I;
+      P.K = H;
+      P.n_tiles = 2 * I / kGemmBM;
+      P.k_blocks = H / kGemmBK;
+      P.m_rows_dev = npp;
+      P.max_m_blocks = L.max_sorted / L.bs;
+      P.expert_ids = eids;
+      P.block_seg = bseg;
+      P.block_rows = L.small ? nullptr : brows;
+      P.rows_bound = T < kFp4BS ? T : kFp4BS;
+      P.group_m = group_m_for(H, L.bs);
+      P.num_experts = E;
+      P.b_rows_per_expert = 2 * I;
+      P.up_offset = I;
+      P.out = act;
+      P.ldo = I;
+      P.store_rows = L.max_sorted;
+      P.sorted_ids = sorted;
+      P.num_flat = L.n;
+      P.flat_row = inv;
+      P.part = at<float>(workspace, L.part_r);
+      P.part_split_stride = (long long)L.n * 2 * I;
+      P.scale2 = args->w13_weight_scale_2;
+      P.gscale = args->input_scale;
+    }
+    if (Is) {
+      GemmProblem& P = g1.p[1];
+      P.A = x_tok16;
+      P.a_rows = T;
+      P.B = shared_w13;
+      P.b_rows = 2 * Is;
+      P.K = H;
+      P.n_tiles = 2 * Is / kGemmBM;
+      P.k_blocks = H / kGemmBK;
+      P.m_rows_host = t_pad;
+      P.max_m_blocks = t_pad / L.bs;
+      P.group_m = group_m_for(H, L.bs);
+      P.num_experts = 1;
+      P.b_rows_per_expert = 2 * Is;
+      P.up_offset = Is;
+      P.out = act_s;
+      P.ldo = Is;
+      P.store_rows = T;
+      P.num_flat = L.n;
+      P.part = at<float>(workspace, L.part_s);
+      P.part_split_stride = (long long)T * 2 * Is;
+      P.scale2 = args->shared_weight_scale_2;
+      P.gscale = args->shared_input_scale;
+    }
+    g1.splits = L.splits13;
+    g1.splits_p1 = L.splits13_shared;
+    GBMOE_TRY(launch_gemm_fp4(kGemmW13, g1, stream));
+    GBMOE_TRY(launch_silu_quant_fp4(g1, npp, L.max_sorted, args->act_scale,
+                                    Is ? args->shared_act_scale : 1.f, stream));
+    GBMOE_TRY(rec(2));
+
+    // ---- w2 (nvfp4): weighted fp32 slot outputs; the shared expert to slot k
+    GemmLaunch g2;
+    std::memset(&g2, 0, sizeof(g2));
+    g2.status = status;
+    g2.num_problems = Is ? 2 : 1;
+    {
+      GemmProblem& P = g2.p[0];
+      P.A = act;
+      P.a_rows = L.max_sorted;
+      P.B = w2_weight;
+      P.b_rows = E * H;
+      P.K = I;
+      P.n_tiles = H / kGemmBM;
+      P.k_blocks = I / kGemmBK;
+      P.m_rows_dev = npp;
+      P.max_m_blocks = L.max_sorted / L.bs;
+      P.expert_ids = eids;
+      P.block_seg = bseg;
+      P.block_rows = L.small ? nullptr : brows;
+      P.rows_bound = T < kFp4BS ? T : kFp4BS;
+      P.group_m = group_m_for(I, L.bs);
+      P.num_experts = E;
+      P.b_rows_per_expert = H;
+      P.out = ytok;
+      P.ldo = H;
+      P.store_rows = L.max_sorted;
+      P.sorted_ids = sorted;
+      P.row_weight = tw;
+      P.num_flat = L.n;
+      P.top_k = k;
+      P.slots = L.slots;
+      P.out_split_stride = slot_copy;
+      P.scale2 = args->w2_weight_scale_2;
+      P.gscale = args->act_scale;
+    }
+    if (Is) {
+      GemmProblem& P = g2.p[1];
+      P.A = act_s;
+      P.a_rows = T;
+      P.B = shared_w2;
+      P.b_rows = H;
+      P.K = Is;
+      P.n_tiles = H / kGemmBM;
+      P.k_blocks = Is / kGemmBK;
+      P.m_rows_host = t_pad;
+      P.max_m_blocks = t_pad / L.bs;
+      P.group_m = group_m_for(Is, L.bs);
+      P.num_experts = 1;
+      P.b_rows_per_expert = H;
+      P.out = ytok;
+      P.ldo = H;
+      P.store_rows = T;
+      P.num_flat = L.n;
+      P.top_k = k;
+      P.slots = L.slots;
+      P.slot_offset = k;
+      P.out_split_stride = slot_copy;
+      P.scale2 = args->shared_weight_scale_2 + 1;
+      P.gscale = args->shared_act_scale;
+    }
+    g2.splits = L.splits2;
+    g2.splits_p1 = L.splits2_shared;
+    GBMOE_TRY(launch_gemm_fp4(kGemmW2, g2, stream));
+    GBMOE_TRY(rec(3));
+    GBMOE_TRY(launch_combine(ytok, L.slots, k, H, T, g2.splits, Is ? g2.splits_p1 : g2.splits,
+                             slot_copy, output, stream));
+    GBMOE_TRY(rec(4));
+    return GBMOE_OK;
+  }
 
   if (fp8) {
     // ---- w13 (fp8): e4m3 act + scales, routed and shared experts in one launch
@@ -929,6 +1086,35 @@ GBMOE_API gbmoe_status_t moe_quant_fp8_per_token_group(int32_t num_rows, int32_t
   PdlChain chain;
   return cuda_status(
       launch_quant_fp8(x, num_rows, hidden_size, q, scale, num_rows, (cudaStream_t)stream));
+}
+
+GBMOE_API gbmoe_status_t moe_quant_nvfp4(int32_t num_rows, int32_t hidden_size, const void* x,
+                                         float global_scale, uint8_t* q, uint8_t* sf,
+                                         gbmoe_stream_t stream) {
+  if (num_rows < 0 || hidden_size <= 0 || hidden_size % 16 ||
+      !std::isfinite(global_scale) || !(global_scale > 0.f))
+    return GBMOE_ERR_INVALID_ARG;
+  if (num_rows == 0) return GBMOE_OK;
+  if (!x || !q || !sf || !aligned16(x) || (reinterpret_cast<uintptr_t>(q) & 7u))
+    return GBMOE_ERR_INVALID_ARG;
+  PdlChain chain;
+  return cuda_status(launch_quant_fp4(x, num_rows, hidden_size, global_scale, q, sf,
+                                      (cudaStream_t)stream));
+}
+
+GBMOE_API size_t moe_nvfp4_prepared_bytes(int32_t rows, int32_t K) {
+  if (rows <= 0 || K <= 0 || rows % 128 || K % 64) return 0;
+  return (size_t)rows / 128 * (size_t)(K / 64) * kFp4ChunkBytes;
+}
+
+GBMOE_API gbmoe_status_t moe_nvfp4_prepare_weight(int32_t rows, int32_t K, const uint8_t* packed,
+                                                  const uint8_t* block_scale, uint8_t* out,
+                                                  gbmoe_stream_t stream) {
+  if (rows <= 0 || K <= 0 || rows % 128 || K % 64 || !packed || !block_scale || !out ||
+      !aligned16(packed) || !aligned16(block_scale) || !aligned16(out))
+    return GBMOE_ERR_INVALID_ARG;
+  PdlChain chain;
+  return cuda_status(launch_prepare_fp4(packed, block_scale, rows, K, out, (cudaStream_t)stream));
 }
 
 GBMOE_API int32_t moe_forward_num_launches(const gbmoe_config_t* cfg, int32_t num_tokens) {

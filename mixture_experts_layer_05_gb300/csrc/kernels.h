@@ -157,6 +157,11 @@ struct GemmProblem {
   const float* b_scale;    // B block scales [b_rows / 128][K / 128], row-major
   float* out_scale;        // w13: act scales, [ldo / 128][out_scale_ld] (group-major)
   int out_scale_ld;
+  // NVFP4 problems only: A is f16 (quantized values q * sf), B the prepared fp4 weights,
+  // each output scaled by alpha = scale2[expert] / gscale.
+  const float* scale2;     // per-expert weight_scale_2 (the shared expert: one value)
+  float gscale;            // per-tensor scale of the A rows' quantization
+  int rows_bound;          // routed problems without block_rows: real rows of any block <= it
 };
 
 // Up to two problems (the routed experts and the shared expert) in one persistent
@@ -226,5 +231,30 @@ cudaError_t launch_gemm_fp8(int kind, const GemmLaunch& L, cudaStream_t stream,
 // 128 columns into e4m3 act + group-major scales.
 cudaError_t launch_silu_reduce_fp8(const GemmLaunch& L, const int* npp, int max_routed_rows,
                                    cudaStream_t stream);
+
+// ---------------------------------------------------------------- NVFP4 (w4a4, block 16)
+constexpr int kFp4BS = 128;             // align block size of the NVFP4 forward (max MMA N)
+constexpr int kFp4ChunkBytes = 4608;    // prepared weights: 128 rows x 64 K (4096 B of codes
+                                        // + 512 B of block scales) per chunk
+
+// fp4_quantize(x, g, 16) of bf16 rows [rows, H]: packed e2m1 codes q [rows, H / 2] (low
+// nibble first) and e4m3 block scales sf [rows, H / 16].
+cudaError_t launch_quant_fp4(const void* x, int rows, int H, float g, uint8_t* q, uint8_t* sf,
+                             cudaStream_t stream);
+// The same quant once per token, its f16 values q * sf written to x_perm row inv[f] for each
+// of the token's k slots and, when x_tok is not NULL, to x_tok row t (with scale g_tok).
+cudaError_t launch_quant_gather_fp4(const void* x, int H, const int* inv, int n, int k, int T,
+                                    int max_rows, float g, void* x_perm, void* x_tok,
+                                    float g_tok, cudaStream_t stream);
+// NVFP4 grouped GEMMs (weights on M, the row block's tokens on N): kGemmW13 writes alpha-scaled
+// fp32 partials [split][row][2 ldo] (gate | up), kGemmW2 weighted fp32 slot outputs.
+cudaError_t launch_gemm_fp4(int kind, const GemmLaunch& L, cudaStream_t stream);
+// act = silu(sum gate) * sum up of an NVFP4 first-GEMM launch, block-quantized with g_act
+// (routed) / g_act_shared, written as f16 q * sf to out (routed rows through flat_row).
+cudaError_t launch_silu_quant_fp4(const GemmLaunch& L, const int* npp, int max_routed_rows,
+                                  float g_act, float g_act_shared, cudaStream_t stream);
+// The prepared layout of one [rows, K] fp4 weight: see moe_nvfp4_prepare_weight.
+cudaError_t launch_prepare_fp4(const uint8_t* packed, const uint8_t* scales, int rows, int K,
+                               uint8_t* out, cudaStream_t stream);
 
 }  // namespace gbmoe

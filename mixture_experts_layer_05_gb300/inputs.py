@@ -205,3 +205,75 @@ def make_fp8_weights(w: MoEWorkload, seed: int = 0, device="cpu") -> dict:
                                        device=device)
         out["shared_w2_s"] = scales((H // B, Is // B), "fp8/shared_w2_s")
     return out
+
+
+def fp4_packed(shape, seed: int, device="cpu") -> torch.Tensor:
+    """Random packed e2m1 pairs: uniform bytes (every 4-bit code equally likely) of
+    ``shape`` (the last dim is half the value count), drawn on ``device``."""
+    g = _gen(seed, torch.device(device))
+    return torch.randint(0, 256, shape, generator=g, dtype=torch.uint8, device=device)
+
+
+def fp4_block_scales(shape, seed: int, device="cpu") -> torch.Tensor:
+    """Random e4m3fn block scales (torch.float8_e4m3fn): byte codes uniform in [0x30, 0x40),
+    the e4m3 values 0.5 .. 1.875, drawn on ``device``."""
+    g = _gen(seed, torch.device(device))
+    return torch.randint(0x30, 0x40, shape, generator=g, dtype=torch.uint8,
+                         device=device).view(torch.float8_e4m3fn)
+
+
+def make_fp4_weights(w: MoEWorkload, seed: int = 0, device="cpu") -> dict:
+    """NVFP4 expert weights as a checkpoint stores them: packed e2m1 codes ``w13 [E, 2I, H/2]``,
+    ``w2 [E, H, I/2]`` (uint8, low nibble first), e4m3 block scales per 16 values along K
+    (``w13_sf [E, 2I, H/16]``, ``w2_sf [E, H, I/16]``) and per-expert fp32 scales
+    ``w13_s2 [E]``, ``w2_s2 [E]``; the shared expert's the same way (``shared_s2 [2]``).
+
+    Uniform codes have an rms of 2.93 and the block scales of about 1.1, so the per-expert
+    scales, U(0.8, 1.2) * w_std / 3.2, make the weights the codes stand for about w_std in
+    rms like the bf16 workloads'. The per-tensor scales of the input and the act are the
+    usual calibration form 448 * 6 / (expected amax): input amax 4 x_std, act amax
+    8 rms(z)^2 with rms(z) = sqrt(H) x_std w_std; the shared expert's are 0.75 and 1.25
+    times those. The bias is the bf16 workload's, rounded to bf16 as the FP4 layer of the
+    pages casts it.
+    """
+    E, H, I = w.num_experts, w.hidden_size, w.intermediate_size
+    base = w.w_std / 3.2
+
+    def s2(shape, tag):
+        g = _gen(tensor_seed(w.name, tag, seed), "cpu")
+        return ((0.8 + 0.4 * torch.rand(shape, generator=g, dtype=torch.float32)) * base).to(device)
+
+    rms_z = (H ** 0.5) * w.x_std * w.w_std
+    g_in = 448.0 * 6.0 / (4.0 * w.x_std)
+    g_act = 448.0 * 6.0 / (8.0 * rms_z * rms_z)
+    out = {
+        "w13": fp4_packed((E, 2 * I, H // 2), tensor_seed(w.name, "fp4/w13", seed), device),
+        "w13_sf": fp4_block_scales((E, 2 * I, H // 16), tensor_seed(w.name, "fp4/w13_sf", seed),
+                                   device),
+        "w13_s2": s2((E,), "fp4/w13_s2"),
+        "w2": fp4_packed((E, H, I // 2), tensor_seed(w.name, "fp4/w2", seed), device),
+        "w2_sf": fp4_block_scales((E, H, I // 16), tensor_seed(w.name, "fp4/w2_sf", seed),
+                                  device),
+        "w2_s2": s2((E,), "fp4/w2_s2"),
+        "input_scale": float(torch.tensor(g_in, dtype=torch.float32)),
+        "act_scale": float(torch.tensor(g_act, dtype=torch.float32)),
+        "bias": None, "shared_w13": None, "shared_w13_sf": None, "shared_w2": None,
+        "shared_w2_sf": None, "shared_s2": None, "shared_input_scale": 0.0,
+        "shared_act_scale": 0.0,
+    }
+    if w.has_bias:
+        out["bias"] = normal((E,), w.bias_std, tensor_seed(w.name, "bias", seed),
+                             torch.bfloat16, device).float()
+    Is = w.shared_intermediate_size
+    if Is:
+        out["shared_w13"] = fp4_packed((2 * Is, H // 2), tensor_seed(w.name, "fp4/sw13", seed),
+                                       device)
+        out["shared_w13_sf"] = fp4_block_scales((2 * Is, H // 16),
+                                                tensor_seed(w.name, "fp4/sw13_sf", seed), device)
+        out["shared_w2"] = fp4_packed((H, Is // 2), tensor_seed(w.name, "fp4/sw2", seed), device)
+        out["shared_w2_sf"] = fp4_block_scales((H, Is // 16),
+                                               tensor_seed(w.name, "fp4/sw2_sf", seed), device)
+        out["shared_s2"] = s2((2,), "fp4/shared_s2")
+        out["shared_input_scale"] = float(torch.tensor(0.75 * g_in, dtype=torch.float32))
+        out["shared_act_scale"] = float(torch.tensor(1.25 * g_act, dtype=torch.float32))
+    return out

@@ -9,6 +9,7 @@ from .fp8_oracle import (  # noqa: F401
     dequant_block, expert_mlp_fp8, experts_combine_fp8, fused_moe_fp8,
 )
 from .fp4_oracle import (  # noqa: F401
-    e2m1_value, e2m1_round, e2m1_code, pack_fp4, unpack_fp4, weight_dequant, expert_mlp_fp4,
+    e2m1_value, e2m1_round, e2m1_code, pack_fp4, unpack_fp4, weight_dequant, expert_act_fp4,
+    expert_down_fp4, expert_mlp_fp4,
     experts_combine_fp4, fused_moe_fp4,
 )

@@ -148,15 +148,25 @@ def weight_dequant(packed, scales, scale2) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- the layer
+def expert_act_fp4(xq, w13_packed, w13_sf, w13_s2) -> np.ndarray:
+    """The first half of an NVFP4 expert on dequantized input rows xq [n, H]:
+    z = xq @ W13^T, act = silu(gate) * up (fp64, before its quantization)."""
+    W13 = weight_dequant(w13_packed, w13_sf, w13_s2)
+    z = np.atleast_2d(xq) @ W13.T
+    I = W13.shape[0] // 2
+    return _mo.silu(z[:, :I]) * z[:, I:]
+
+
+def expert_down_fp4(aq, w2_packed, w2_sf, w2_s2) -> np.ndarray:
+    """The second GEMM of an NVFP4 expert on dequantized act rows aq [n, I]: o = aq @ W2^T."""
+    return np.atleast_2d(aq) @ weight_dequant(w2_packed, w2_sf, w2_s2).T
+
+
 def expert_mlp_fp4(xq, w13_packed, w13_sf, w13_s2, w2_packed, w2_sf, w2_s2, act_scale) -> np.ndarray:
     """One NVFP4 expert on already-dequantized input rows xq [n, H]: z = xq @ W13^T,
     act = silu(gate) * up, aq = dequantized fp4_quantize(fp32(act), act_scale), o = aq @ W2^T."""
-    W13 = weight_dequant(w13_packed, w13_sf, w13_s2)
-    W2 = weight_dequant(w2_packed, w2_sf, w2_s2)
-    z = np.atleast_2d(xq) @ W13.T
-    I = W13.shape[0] // 2
-    act = _mo.silu(z[:, :I]) * z[:, I:]
-    return quant_dequant(act, act_scale) @ W2.T
+    act = expert_act_fp4(xq, w13_packed, w13_sf, w13_s2)
+    return expert_down_fp4(quant_dequant(act, act_scale), w2_packed, w2_sf, w2_s2)
 
 
 def experts_combine_fp4(x, topk_weights, topk_ids, w, *, return_parts=False):

@@ -61,15 +61,19 @@ def test_roofline_picks_the_binding_bound():
     peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
     # 1.9 TFLOP and 1 GB in 2 ms: tensor time 1 ms > HBM time 0.147 ms -> tensor, frac 0.5
     r = bench.roofline_of({"flops_w13": 1.9e12, "bytes_w13": 1e9}, 2e-3, peaks, "measured",
-                          False, "k")
+                          "none", "k")
     assert r["bound"] == "tensor" and abs(r["frac"] - 0.5) < 1e-9
     assert abs(r["tensor_frac_of_sustained"] - 950.0 / 1700.0) < 1e-4
     assert abs(r["ridge_frac"] - 0.5) < 1e-9
     # 1.9 GFLOP and 13.6 GB in 4 ms: HBM time 2 ms -> hbm, frac 0.5
     r = bench.roofline_of({"flops_w13": 1.9e9, "bytes_w13": 13.6e9}, 4e-3, peaks, "measured",
-                          False, "k")
+                          "none", "k")
     assert r["bound"] == "hbm" and abs(r["frac"] - 0.5) < 1e-9
     # e4m3: the tensor peak doubles
     r = bench.roofline_of({"flops_w13": 3.8e12, "bytes_w13": 1e9}, 2e-3, peaks, "measured",
-                          True, "k")
+                          "fp8", "k")
+    assert r["bound"] == "tensor" and abs(r["frac"] - 0.5) < 1e-9
+    # nvfp4: six times the bf16 peak (13.5 / 2.25 nominal)
+    r = bench.roofline_of({"flops_w13": 11.4e12, "bytes_w13": 1e9}, 2e-3, peaks, "measured",
+                          "nvfp4", "k")
     assert r["bound"] == "tensor" and abs(r["frac"] - 0.5) < 1e-9
