@@ -261,7 +261,7 @@ Layout layout_for(const gbmoe_config_t& c, int T) {
   L.small = route_align_small_ok(T, k, E);
   L.fused_copy = L.small && L.n <= kFusedCopyMaxRows && !L.fp8 && !L.nvfp4;
   L.w2_bn = (H % 256 == 0) ? 256 : 128;
-  const int kblk = L.fp8 ? kFp8Block : kGemmBK;  // K elements per GEMM pipeline stage
+  const int kblk = L.fp8 ? kFp8Block : (L.nvfp4 ? kFp4StageK : kGemmBK);  // K per GEMM stage
   const long est_blocks = (long)(L.n < E ? L.n : E) + L.n / kGemmBM;  // >= 1 partial per expert
   const long t_blocks = ((long)T + L.bs - 1) / L.bs;
   if (L.tn) {
@@ -571,6 +571,8 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
 
   if (nvfp4) {
     // ---- w13 (nvfp4): alpha-scaled fp32 partials of [gate | up], routed and shared
+    const int un13 = fp4_unit_rows(2 * I, Is ? 2 * Is : 256);
+    const int un2 = fp4_unit_rows(H, H);
     GemmLaunch g1;
     std::memset(&g1, 0, sizeof(g1));
     g1.status = status;
@@ -582,8 +584,8 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
       P.B = w13_weight;
       P.b_rows = E * 2 * I;
       P.K = H;
-      P.n_tiles = 2 * I / kGemmBM;
-      P.k_blocks = H / kGemmBK;
+      P.n_tiles = 2 * I / un13;
+      P.k_blocks = H / kFp4StageK;
       P.m_rows_dev = npp;
       P.max_m_blocks = L.max_sorted / L.bs;
       P.expert_ids = eids;
@@ -612,8 +614,8 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
       P.B = shared_w13;
       P.b_rows = 2 * Is;
       P.K = H;
-      P.n_tiles = 2 * Is / kGemmBM;
-      P.k_blocks = H / kGemmBK;
+      P.n_tiles = 2 * Is / un13;
+      P.k_blocks = H / kFp4StageK;
       P.m_rows_host = t_pad;
       P.max_m_blocks = t_pad / L.bs;
       P.group_m = group_m_for(H, L.bs);
@@ -648,8 +650,8 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
       P.B = w2_weight;
       P.b_rows = E * H;
       P.K = I;
-      P.n_tiles = H / kGemmBM;
-      P.k_blocks = I / kGemmBK;
+      P.n_tiles = H / un2;
+      P.k_blocks = I / kFp4StageK;
       P.m_rows_dev = npp;
       P.max_m_blocks = L.max_sorted / L.bs;
       P.expert_ids = eids;
@@ -678,8 +680,8 @@ GBMOE_API gbmoe_status_t moe_forward_ex(const gbmoe_config_t* cfg, int32_t num_t
       P.B = shared_w2;
       P.b_rows = H;
       P.K = Is;
-      P.n_tiles = H / kGemmBM;
-      P.k_blocks = Is / kGemmBK;
+      P.n_tiles = H / un2;
+      P.k_blocks = Is / kFp4StageK;
       P.m_rows_host = t_pad;
       P.max_m_blocks = t_pad / L.bs;
       P.group_m = group_m_for(Is, L.bs);

@@ -12,18 +12,27 @@
 //
 // The weights arrive prepared (moe_nvfp4_prepare_weight): per tile of 128 rows and K stage
 // of 64 values one contiguous 4608-byte chunk, the packed codes of the stage's two K halves
-// (16 bytes per row each) then the row's four scale bytes. One bulk copy per stage streams
-// the chunk into a 16-deep ring; converter warps expand it to f16 (hardware e2m1x2 and
-// e4m3x2 conversions and one packed multiply per pair) in the 128-byte-swizzled K-major
-// layout the MMA reads, so HBM carries 0.5625 bytes per weight and the tensor cores see
-// ordinary kind::f16 operands. The weights are on the MMA's M side (128 rows per unit), the
-// row block's tokens on N (its real rows rounded up to 16, at most 128):
+// (16 bytes per row each) then the rows' four scale bytes. A unit is a row block of up to
+// 128 token rows (the MMA's M side) against 256 weight rows (N; 128 when the weight rows do
+// not split into 256s) over a K range. Per 64-value K stage:
 //
-//   warp 0       bulk copies of prepared weight chunks into the raw ring (16 x 4.5 KB)
-//   warp 1       TMEM (two 128-column accumulators) and the MMAs (M 128, N n, K 16)
-//   warp 2       TMA token tiles (boxes of 16 / 32 / 64 / 128 rows) into the stage ring
-//   warps 4..11  converters: warp c expands rows 32 (c & 3) .. +31, K half c >> 2
-//   warps 12..15 epilogue: TMEM lane quarter warp & 3, one weight row per thread
+//   warp 0       bulk copies of the stage's two prepared chunks into an 8-deep raw ring
+//   warp 1       TMEM (two 256-column accumulators) and the MMAs (M 128, or 64 for row
+//                blocks of at most 64 real rows; N 256; K 16)
+//   warp 2       TMA of the token tile (16 / 32 / 64 / 128 rows) into a dense token ring
+//   warp 3       the unit scheduler: reads each unit's metadata from global memory ahead
+//                of time and publishes it in shared memory
+//   warps 4..19  converters: every stage, thread t expands weight row t % 256, K half
+//                t / 256 (hardware e2m1x2 and e4m3x2 conversions and one packed multiply
+//                per pair) into the 128-byte-swizzled K-major f16 layout the MMA reads
+//   warps 20..23 epilogue: TMEM lane quarter warp & 3, one token row per thread
+//
+// Weights on N keep the tensor core at full width whatever the batch: an M = 128 MMA costs
+// about the same at N = 16 as at N = 256, so putting the few decode tokens on N (weights on
+// M) spent eight MMA issues per 16K weights where this layout spends four. The token ring
+// is dense: a 16-row tile takes 2 KB, and the MMA's 128-row A operand starting at a slot
+// reads the following slots as its (discarded) rows 16..127, so the ring's tail is padded
+// to keep that read inside the ring.
 // Every wait is bounded (kWaitTimeoutNs).
 #include "fp4.cuh"
 #include "tc.cuh"
@@ -31,27 +40,43 @@
 namespace gbmoe {
 namespace {
 
-constexpr int kF4M = 128;                         // weight rows per unit (MMA M)
-constexpr int kF4BK = 64;                         // K values per stage
-constexpr uint32_t kF4RawBytes = kFp4ChunkBytes;  // one prepared chunk
-constexpr int kF4RawStages = 16;
-constexpr int kF4Stages = 4;
-constexpr uint32_t kF4WBytes = kF4M * kF4BK * 2;          // f16 weights of a stage: 16 KB
-constexpr uint32_t kF4XBytes = kFp4BS * kF4BK * 2;        // up to 128 token rows: 16 KB
-constexpr uint32_t kF4StageBytes = kF4WBytes + kF4XBytes;
-constexpr int kF4CvtWarps = 8;
+constexpr int kF4TileRows = 128;                  // rows of a prepared tile
+constexpr int kF4MaxN = 256;                      // weight rows per unit (MMA N)
+constexpr int kF4M = 128;                         // token rows per unit (MMA M)
+constexpr int kF4BK = kFp4StageK;                 // K values per stage (one 128-byte atom)
+constexpr uint32_t kF4RawBytes = 2 * kFp4ChunkBytes;  // the stage's prepared chunks
+#ifndef GBMOE_F4_RAW_STAGES
+#define GBMOE_F4_RAW_STAGES 8
+#endif
+constexpr int kF4RawStages = GBMOE_F4_RAW_STAGES;
+constexpr int kF4MaxRawStages = 8;
+constexpr int kF4CvtSlots = 3;                    // f16 weight stages
+constexpr uint32_t kF4WBytes = kF4MaxN * 128;     // f16 weights of a stage: 32 KB
+constexpr uint32_t kF4ABytes = kF4M * 128;        // the MMA's A operand: 128 rows, 16 KB
+// token ring + the tail the last slot's 16 KB A read may cover
+constexpr uint32_t kF4TokArea = 48 * 1024;
+constexpr int kF4MaxTokStages = 16;
+constexpr int kF4CvtWarps = 16;
 constexpr int kF4EpiWarps = 4;
 constexpr int kF4Threads = 32 * (4 + kF4CvtWarps + kF4EpiWarps);
-constexpr uint32_t kF4TmemCols = 256;             // two 128-column accumulators
+constexpr uint32_t kF4TmemCols = 512;             // two 256-column accumulators
 constexpr int kF4Boxes = 4;                       // token boxes of 16, 32, 64, 128 rows
-constexpr uint32_t kF4BarBytes = 512;
-constexpr size_t kF4Smem = 1024 + (size_t)kF4Stages * kF4StageBytes +
+constexpr int kF4UnitRing = 8;                    // unit descriptors the scheduler runs ahead
+// arrivals that free a descriptor: the two producers, the MMA issuer, every converter warp
+// and every epilogue warp
+constexpr int kF4UnitReaders = 3 + kF4CvtWarps + kF4EpiWarps;
+constexpr uint32_t kF4BarBytes = 2048;
+constexpr size_t kF4Smem = 1024 + (size_t)kF4CvtSlots * kF4WBytes + kF4TokArea +
                            (size_t)kF4RawStages * kF4RawBytes + kF4BarBytes;
 static_assert(kF4Smem <= 232448, "shared memory per CTA exceeded");
 static_assert(kF4RawBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
+static_assert(kF4RawStages <= kF4MaxRawStages && kF4TokArea >= kF4ABytes, "ring sizes");
 
 struct F4Maps {
   CUtensorMap x[2][kF4Boxes];  // per problem: f16 token rows, box 64 values x (16 << i) rows
+  int tok_stages;              // token ring stages (<= kF4MaxTokStages)
+  int tok_slot_bytes;          // the widest token box of the launch (a multiple of 1024)
+  int un;                      // weight rows per unit: 256, or 128
 };
 
 // Instruction descriptor of kind::f16 with f16 A and B (format code 0), fp32 D, K-major.
@@ -68,6 +93,47 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+
+// The two e4m3 block scales of a 16-bit word (low byte first) as f16 pairs {s, s} (exact).
+__device__ __forceinline__ void e4m3x2_pairs(uint32_t w, uint32_t& s0, uint32_t& s1) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t.reg .b32 p;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 p, lo;\n\t"
+      "prmt.b32 %0, p, 0, 0x1010;\n\t"
+      "prmt.b32 %1, p, 0, 0x3232;\n\t}"
+      : "=r"(s0), "=r"(s1)
+      : "r"(w));
+}
+
+// The eight e2m1 values of a word (element 2i in the low nibble of byte i) as four f16
+// pairs, each multiplied by the f16 pair sc (exact: both factors have few significant bits).
+__device__ __forceinline__ void e2m1x8_scaled(uint32_t w, uint32_t sc, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .b32 h0, h1, h2, h3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h3, b3;\n\t"
+      "mul.rn.f16x2 %0, h0, %5;\n\t"
+      "mul.rn.f16x2 %1, h1, %5;\n\t"
+      "mul.rn.f16x2 %2, h2, %5;\n\t"
+      "mul.rn.f16x2 %3, h3, %5;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w), "r"(sc));
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -80,36 +146,60 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > 10000000ull) return;
 }
 
-struct F4Unit {
-  int p, split, mb, nt, kb0, kb1, n, box;
+// A unit as the scheduler warp publishes it in shared memory: the unit, its real token
+// rows, its MMA-side row count and token box, its expert's first weight tile, the output
+// scale.
+struct F4Desc {
+  int p, split, mb, nt, kb0, kb1, rows, n, box, tile;
+  float alpha;
+  int pad;
 };
+static_assert(sizeof(F4Desc) == 48, "descriptor size");
 
-// Unit u with its MMA width: the row block's real rows (the align's per-block counts,
-// else the launch's bound for routed problems; the identity rows left for the shared one)
-// rounded up to 16, and the smallest token box that holds them.
-__device__ __forceinline__ F4Unit f4_unit(const GemmLaunch& L, const Schedule& S, int u) {
+// Unit u: the row block's real rows (the align's per-block counts bounded by the launch's
+// rows_bound, for routed problems; the identity rows left, for the shared one), that count
+// rounded up to 16 and the smallest token box that holds them.
+__device__ __forceinline__ F4Desc f4_desc(const GemmLaunch& L, const Schedule& S, int u, int un) {
   const Unit w = S.unit(L, u);
-  F4Unit r{w.p, w.split, w.mb, w.nt, w.kb0, w.kb1, 16, 0};
   const GemmProblem& P = L.p[w.p];
   int rows;
   if (P.sorted_ids)
-    rows = P.block_rows ? P.block_rows[w.mb] : P.rows_bound;
+    rows = P.block_rows ? min(P.block_rows[w.mb], P.rows_bound) : P.rows_bound;
   else
     rows = P.store_rows - w.mb * kFp4BS;
   rows = rows < 1 ? 1 : (rows > kFp4BS ? kFp4BS : rows);
-  r.n = (rows + 15) & ~15;
-  r.box = r.n <= 16 ? 0 : (r.n <= 32 ? 1 : (r.n <= 64 ? 2 : 3));
-  return r;
-}
-
-__device__ __forceinline__ int f4_expert(const GemmProblem& P, int mb, int* status) {
-  int e = P.expert_ids ? P.expert_ids[mb] : 0;
+  int e = P.expert_ids ? P.expert_ids[w.mb] : 0;
   if ((unsigned)e >= (unsigned)P.num_experts) {
-    record_status(status, GBMOE_ERR_DEVICE_CHECK);
+    record_status(L.status, GBMOE_ERR_DEVICE_CHECK);
     e = 0;
   }
-  return e;
+  F4Desc d;
+  d.p = w.p;
+  d.split = w.split;
+  d.mb = w.mb;
+  d.nt = w.nt;
+  d.kb0 = w.kb0;
+  d.kb1 = w.kb1;
+  d.rows = rows;
+  d.n = (rows + 15) & ~15;
+  d.box = d.n <= 16 ? 0 : (d.n <= 32 ? 1 : (d.n <= 64 ? 2 : 3));
+  d.tile = (int)(((long long)e * P.b_rows_per_expert + (long long)w.nt * un) / kF4TileRows);
+  d.alpha = __fdiv_rn(P.scale2 ? P.scale2[e] : 1.f, P.gscale);
+  d.pad = 0;
+  return d;
 }
+
+// A ring position: slot and phase parity, advanced without division.
+struct RingPos {
+  int slot;
+  uint32_t phase;
+  __device__ __forceinline__ void next(int n) {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
 
 template <int KIND>
 __global__ void __launch_bounds__(kF4Threads, 1)
@@ -118,23 +208,34 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   const uint32_t raw0 = smem_addr(smem_raw);
   const uint32_t base = (raw0 + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw0);
-  // [stages: f16 weights 16 KB | token rows 16 KB] [raw ring] [barriers]
-  const uint32_t raw_base = base + kF4Stages * kF4StageBytes;
-  uint8_t* raw_ptr = smem + kF4Stages * kF4StageBytes;
+  // [f16 weight slots 3 x 32 KB] [token ring 48 KB] [raw ring] [barriers]
+  const int ts = maps.tok_stages;
+  const uint32_t tsb = (uint32_t)maps.tok_slot_bytes;
+  const int un = maps.un;
+  const int chunks = un / kF4TileRows;             // prepared chunks per stage: 1 or 2
+  const uint32_t tok_base = base + kF4CvtSlots * kF4WBytes;
+  const uint32_t raw_base = tok_base + kF4TokArea;
+  uint8_t* raw_ptr = smem + kF4CvtSlots * kF4WBytes + kF4TokArea;
   uint64_t* bars = reinterpret_cast<uint64_t*>(raw_ptr + kF4RawStages * kF4RawBytes);
-  // bars: raw_full[16] raw_empty[16] tok_full[4] cvt_full[4] stage_empty[4] tfull[2] tempty[2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 48);
+  // bars: raw_full[8] raw_empty[8] cvt_full[4] cvt_empty[4] tfull[2] tempty[2]
+  //       unit_full[8] unit_empty[8] tok_full[16] tok_empty[16]; then the TMEM slot, the
+  //       abort flag and (at byte 1024) the unit descriptors
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 44 + 2 * kF4MaxTokStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  F4Desc* descs = reinterpret_cast<F4Desc*>(reinterpret_cast<uint8_t*>(bars) + 1024);
   const uint32_t bar0 = smem_addr(bars);
   auto raw_full = [&](int s) { return bar0 + 8u * s; };
-  auto raw_empty = [&](int s) { return bar0 + 8u * (16 + s); };
-  auto tok_full = [&](int s) { return bar0 + 8u * (32 + s); };
-  auto cvt_full = [&](int s) { return bar0 + 8u * (36 + s); };
-  auto stage_empty = [&](int s) { return bar0 + 8u * (40 + s); };
-  auto tfull = [&](int b) { return bar0 + 8u * (44 + b); };
-  auto tempty = [&](int b) { return bar0 + 8u * (46 + b); };
-  auto w_stage = [&](int s) { return base + s * kF4StageBytes; };
-  auto x_stage = [&](int s) { return base + s * kF4StageBytes + kF4WBytes; };
+  auto raw_empty = [&](int s) { return bar0 + 8u * (8 + s); };
+  auto cvt_full = [&](int s) { return bar0 + 8u * (16 + s); };
+  auto cvt_empty = [&](int s) { return bar0 + 8u * (20 + s); };
+  auto tfull = [&](int b) { return bar0 + 8u * (24 + b); };
+  auto tempty = [&](int b) { return bar0 + 8u * (26 + b); };
+  auto unit_full = [&](int i) { return bar0 + 8u * (28 + i); };
+  auto unit_empty = [&](int i) { return bar0 + 8u * (36 + i); };
+  auto tok_full = [&](int s) { return bar0 + 8u * (44 + s); };
+  auto tok_empty = [&](int s) { return bar0 + 8u * (44 + kF4MaxTokStages + s); };
+  auto w_stage = [&](int s) { return base + s * kF4WBytes; };
+  auto x_stage = [&](int s) { return tok_base + s * tsb; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -142,14 +243,21 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       mbar_init(raw_full(s), 1);
       mbar_init(raw_empty(s), kF4CvtWarps);
     }
-    for (int s = 0; s < kF4Stages; ++s) {
-      mbar_init(tok_full(s), 1);
+    for (int s = 0; s < kF4CvtSlots; ++s) {
       mbar_init(cvt_full(s), kF4CvtWarps);
-      mbar_init(stage_empty(s), 1);
+      mbar_init(cvt_empty(s), 1);
+    }
+    for (int s = 0; s < ts; ++s) {
+      mbar_init(tok_full(s), 1);
+      mbar_init(tok_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull(b), 1);
       mbar_init(tempty(b), kF4EpiWarps);
+    }
+    for (int i = 0; i < kF4UnitRing; ++i) {
+      mbar_init(unit_full(i), 1);
+      mbar_init(unit_empty(i), kF4UnitReaders);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -171,199 +279,242 @@ __global__ void __launch_bounds__(kF4Threads, 1)
 
   Schedule sched;
   sched.init(args, kFp4BS);
+  // the next unit of this CTA from the scheduler warp's ring, as a copy in registers; every
+  // reading warp releases the slot once
+  auto get_unit = [&](const RingPos& q, F4Desc& d) -> bool {
+    if (!wait_fast(unit_full(q.slot), q.phase, abort_flag, args.status)) return false;
+    d = descs[q.slot];
+    return true;
+  };
+  auto release_unit = [&](RingPos& q) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(unit_empty(q.slot));
+    q.next(kF4UnitRing);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ prepared weight chunks
     if (lane == 0) {
       const uint64_t policy = l2_evict_first_policy();
-      uint32_t it = 0;
+      RingPos uq{0, 0}, rq{0, 0};
+      uint32_t issued = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        const Unit w = sched.unit(args, u);
+        F4Desc w;
+        if (!get_unit(uq, w)) break;
+        mbar_arrive(unit_empty(uq.slot));
+        uq.next(kF4UnitRing);
         const GemmProblem& P = args.p[w.p];
-        const int e = f4_expert(P, w.mb, args.status);
-        const size_t tile = ((size_t)e * P.b_rows_per_expert + (size_t)w.nt * kF4M) / kF4M;
         const uint8_t* src = static_cast<const uint8_t*>(P.B) +
-                             (tile * P.k_blocks + w.kb0) * (size_t)kF4RawBytes;
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it, src += kF4RawBytes) {
-          const int s = it % kF4RawStages;
-          const uint32_t ph = (it / kF4RawStages) & 1u;
-          if (!wait_fast(raw_empty(s), ph ^ 1u, abort_flag, args.status)) {
+                             ((size_t)w.tile * P.k_blocks + w.kb0) * (size_t)kFp4ChunkBytes;
+        const size_t tile_bytes = (size_t)P.k_blocks * kFp4ChunkBytes;  // next tile's chunk
+        for (int kb = w.kb0; kb < w.kb1;
+             ++kb, src += kFp4ChunkBytes, rq.next(kF4RawStages), ++issued) {
+          if (!wait_fast(raw_empty(rq.slot), rq.phase ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(raw_full(s), kF4RawBytes);
-          bulk_load(raw_base + s * kF4RawBytes, src, kF4RawBytes, raw_full(s), policy);
+          mbar_expect_tx(raw_full(rq.slot), chunks * kFp4ChunkBytes);
+          const uint32_t dst = raw_base + rq.slot * kF4RawBytes;
+          for (int c = 0; c < chunks; ++c)
+            bulk_load(dst + c * kFp4ChunkBytes, src + c * tile_bytes, kFp4ChunkBytes,
+                      raw_full(rq.slot), policy);
         }
       }
       // the last copies of each slot land before the CTA can exit
-      for (uint32_t j = it > (uint32_t)kF4RawStages ? it - kF4RawStages : 0; j < it; ++j)
+      for (uint32_t j = issued > (uint32_t)kF4RawStages ? issued - kF4RawStages : 0; j < issued; ++j)
         drain_wait(raw_full(j % kF4RawStages), (j / kF4RawStages) & 1u);
     }
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ token tiles
     if (lane == 0) {
-      uint32_t it = 0;
+      RingPos uq{0, 0}, tq{0, 0};
+      uint32_t issued = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        const F4Unit w = f4_unit(args, sched, u);
+        F4Desc w;
+        if (!get_unit(uq, w)) break;
+        mbar_arrive(unit_empty(uq.slot));
+        uq.next(kF4UnitRing);
         const CUtensorMap* map = &maps.x[w.p][w.box];
-        const uint32_t bytes = (uint32_t)(16 << w.box) * kF4BK * 2;
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          const int s = it % kF4Stages;
-          const uint32_t ph = (it / kF4Stages) & 1u;
-          if (!wait_fast(stage_empty(s), ph ^ 1u, abort_flag, args.status)) {
+        const uint32_t box_bytes = (uint32_t)(16 << w.box) * 128;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, tq.next(ts), ++issued) {
+          if (!wait_fast(tok_empty(tq.slot), tq.phase ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(tok_full(s), bytes);
-          tma_load_2d(x_stage(s), map, tok_full(s), kb * kF4BK, w.mb * kFp4BS);
+          mbar_expect_tx(tok_full(tq.slot), box_bytes);
+          tma_load_2d(x_stage(tq.slot), map, tok_full(tq.slot), kb * kF4BK, w.mb * kFp4BS);
         }
       }
-      for (uint32_t j = it > (uint32_t)kF4Stages ? it - kF4Stages : 0; j < it; ++j)
-        drain_wait(tok_full(j % kF4Stages), (j / kF4Stages) & 1u);
+      for (uint32_t j = issued > (uint32_t)ts ? issued - ts : 0; j < issued; ++j)
+        drain_wait(tok_full(j % ts), (j / ts) & 1u);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, uc = 0;
+      RingPos uq{0, 0}, cq{0, 0}, tq{0, 0};
+      uint32_t uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x, ++uc) {
-        const F4Unit w = f4_unit(args, sched, u);
-        const uint32_t idesc = idesc_f16(kF4M, w.n);
+        F4Desc w;
+        if (!get_unit(uq, w)) break;
+        mbar_arrive(unit_empty(uq.slot));
+        uq.next(kF4UnitRing);
         const int buf = uc & 1;
+        // row blocks of at most 64 real rows run M = 64 MMAs: half the tensor work
+        const uint32_t idesc = idesc_f16(w.rows <= 64 ? 64 : kF4M, un);
         if (!wait_fast(tempty(buf), ((uc >> 1) & 1u) ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + buf * 128;
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          const int s = it % kF4Stages;
-          const uint32_t ph = (it / kF4Stages) & 1u;
-          if (!wait_fast(tok_full(s), ph, abort_flag, args.status) ||
-              !wait_fast(cvt_full(s), ph, abort_flag, args.status)) {
+        const uint32_t d = tmem_base + buf * kF4MaxN;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, cq.next(kF4CvtSlots), tq.next(ts)) {
+          if (!wait_fast(tok_full(tq.slot), tq.phase, abort_flag, args.status) ||
+              !wait_fast(cvt_full(cq.slot), cq.phase, abort_flag, args.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const uint32_t xa = x_stage(tq.slot), wa = w_stage(cq.slot);
 #pragma unroll
           for (int kk = 0; kk < kF4BK / 16; ++kk)
-            mma_bf16(d, sdesc_sw128(w_stage(s) + kk * 32), sdesc_sw128(x_stage(s) + kk * 32),
-                     idesc, (kb != w.kb0 || kk != 0) ? 1u : 0u);
-          mma_commit(stage_empty(s));
+            mma_bf16(d, sdesc_sw128(xa + kk * 32), sdesc_sw128(wa + kk * 32), idesc,
+                     (kb != w.kb0 || kk != 0) ? 1u : 0u);
+          mma_commit(cvt_empty(cq.slot));
+          mma_commit(tok_empty(tq.slot));
         }
         if (ok) mma_commit(tfull(buf));
       }
     }
     __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ unit scheduler
+    // The global reads of a unit (its row block's expert segment, expert, real rows and the
+    // expert's weight scale) happen here, up to kF4UnitRing units ahead of the other roles.
+    if (lane == 0) {
+      RingPos q{0, 0};
+      for (int u = blockIdx.x; u < sched.units; u += gridDim.x, q.next(kF4UnitRing)) {
+        const F4Desc d = f4_desc(args, sched, u, un);
+        if (!wait_fast(unit_empty(q.slot), q.phase ^ 1u, abort_flag, args.status)) break;
+        descs[q.slot] = d;
+        mbar_arrive(unit_full(q.slot));
+      }
+    }
+    __syncwarp();
   } else if (warp >= 4 && warp < 4 + kF4CvtWarps) {
     // ------------------------------------------------------------ fp4 -> f16 expansion
-    const int c = warp - 4;
-    const int h = c >> 2;                 // K half of the stage: values 32 h .. 32 h + 31
-    const int r = 32 * (c & 3) + lane;    // weight row within the tile
-    uint32_t it = 0;
+    // Every converter thread takes part in every stage: weight row r = t % 256 (of chunk
+    // r / 128), K half h = t / 256 (values 32 h .. 32 h + 31 of the stage).
+    const int t = (warp - 4) * 32 + lane;
+    const int r = t & (kF4MaxN - 1), h = t >> 8;
+    const bool live = r < un;
+    const uint32_t rd = (uint32_t)(r >> 7) * kFp4ChunkBytes;  // this row's chunk in a stage
+    const uint32_t rr = (uint32_t)(r & 127);
+    RingPos uq{0, 0}, rq{0, 0}, cq{0, 0};
     bool ok = true;
     for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-      const Unit w = sched.unit(args, u);
-      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-        const int rs = it % kF4RawStages;
-        const int s = it % kF4Stages;
-        if (!wait_fast(raw_full(rs), (it / kF4RawStages) & 1u, abort_flag, args.status)) {
+      F4Desc w;
+      if (!get_unit(uq, w)) break;
+      release_unit(uq);
+      for (int kb = w.kb0; kb < w.kb1; ++kb, rq.next(kF4RawStages), cq.next(kF4CvtSlots)) {
+        if (!wait_fast(raw_full(rq.slot), rq.phase, abort_flag, args.status)) {
           ok = false;
           break;
         }
-        const uint8_t* chunk = raw_ptr + rs * kF4RawBytes;
-        const uint4 q = *reinterpret_cast<const uint4*>(chunk + h * 2048 + r * 16);
-        const uint32_t sc = *reinterpret_cast<const uint16_t*>(chunk + 4096 + r * 4 + 2 * h);
+        const uint32_t src = raw_base + rq.slot * kF4RawBytes + rd;
+        uint4 q = make_uint4(0u, 0u, 0u, 0u);
+        uint32_t scw = 0u;
+        if (live) {
+          q = lds128(src + h * 2048 + rr * 16);
+          scw = lds16(src + 4096 + rr * 4 + 2 * h);
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(raw_empty(rs));
-        // the scales of the half's two blocks as f16 pairs (exact)
-        __half2_raw s01 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)sc, __NV_E4M3);
-        __half2 sp;
-        memcpy(&sp, &s01, 4);
-        const __half2 sc0 = __low2half2(sp), sc1 = __high2half2(sp);
-        if (!wait_fast(stage_empty(s), ((it / kF4Stages) & 1u) ^ 1u, abort_flag, args.status)) {
+        if (lane == 0) mbar_arrive(raw_empty(rq.slot));
+        if (!wait_fast(cvt_empty(cq.slot), cq.phase ^ 1u, abort_flag, args.status)) {
           ok = false;
           break;
         }
-        const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-        const uint32_t row = w_stage(s) + r * 128;
+        if (live) {
+          uint32_t s0, s1;
+          e4m3x2_pairs(scw, s0, s1);        // the half's two blocks of 16 values
+          const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+          const uint32_t row = w_stage(cq.slot) + r * 128;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __half2 scl = i < 2 ? sc0 : sc1;
-          uint32_t o[4];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const uint32_t hv = e2m1x2_to_f16x2((words[i] >> (8 * b)) & 0xFFu);
-            __half2 v;
-            memcpy(&v, &hv, 4);
-            v = __hmul2(v, scl);
-            memcpy(&o[b], &v, 4);
+          for (int i = 0; i < 4; ++i) {     // values 8 i .. 8 i + 7 of the half
+            uint32_t o[4];
+            e2m1x8_scaled(words[i], i < 2 ? s0 : s1, o);
+            const uint32_t chunk16 = (uint32_t)((4 * h + i) ^ (r & 7));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + chunk16 * 16),
+                         "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                         : "memory");
           }
-          const uint32_t chunk16 = (uint32_t)((4 * h + i) ^ (r & 7));
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + chunk16 * 16),
-                       "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
-                       : "memory");
+          fence_proxy_async_smem();  // the MMA (async proxy) reads what these stores wrote
         }
-        fence_proxy_async_smem();  // the MMA (async proxy) reads what these stores wrote
         __syncwarp();
-        if (lane == 0) mbar_arrive(cvt_full(s));
+        if (lane == 0) mbar_arrive(cvt_full(cq.slot));
       }
     }
   } else if (warp >= 4 + kF4CvtWarps) {
     // ------------------------------------------------------------ epilogue
+    // D row m sits in TMEM lane m (M = 128) or, for M = 64, in lane 32 (m / 16) + m % 16:
+    // each lane quarter holds 16 rows in its first 16 lanes
     const int quarter = warp & 3;
-    const int r = 32 * quarter + lane;   // weight row within the tile
+    RingPos uq{0, 0};
     uint32_t uc = 0;
     for (int u = blockIdx.x; u < sched.units; u += gridDim.x, ++uc) {
-      const F4Unit w = f4_unit(args, sched, u);
+      F4Desc w;
+      if (!get_unit(uq, w)) break;
+      release_unit(uq);
       const GemmProblem& P = args.p[w.p];
-      const int e = f4_expert(P, w.mb, args.status);
-      const float alpha = __fdiv_rn(P.scale2 ? P.scale2[P.sorted_ids ? e : 0] : 1.f, P.gscale);
       const int buf = uc & 1;
       if (!wait_fast(tfull(buf), (uc >> 1) & 1u, abort_flag, args.status)) break;
       tc_fence_after();
-      const int m0 = w.mb * kFp4BS;
-      for (int c0 = 0; c0 < w.n; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * 128 + c0, v);
-        tmem_wait_ld(v);
-        // this lane's token column c0 + lane: its flat index (routed) or token
-        const int m = m0 + c0 + lane;
-        int f = -1;
-        if (c0 + lane < w.n) {
+      const bool m64 = w.rows <= 64;
+      const int rq0 = m64 ? 16 * quarter : 32 * quarter;  // the quarter's first row
+      if (rq0 < w.rows) {
+        // this lane's token row: its flat index (routed) or token, and its output row
+        const int m = m64 ? (lane < 16 ? rq0 + lane : kFp4BS) : rq0 + lane;
+        const int mr = w.mb * kFp4BS + m;
+        float* out = nullptr;
+        float scale = w.alpha;
+        if (m < w.rows) {
+          int f = -1;
           if (P.sorted_ids) {
-            const int x = P.sorted_ids[m];
+            const int x = P.sorted_ids[mr];
             if (x >= 0 && x < P.num_flat) f = x;
-          } else if (m < P.store_rows) {
-            f = m;
+          } else if (mr < P.store_rows) {
+            f = mr;
+          }
+          if (f >= 0) {
+            if (KIND == kGemmW13) {
+              out = P.part + (size_t)w.split * P.part_split_stride + (size_t)f * 2 * P.ldo;
+            } else {
+              int dest;
+              if (P.sorted_ids) {
+                dest = (f / P.top_k) * P.slots + (f % P.top_k);
+                if (P.row_weight) scale = w.alpha * P.row_weight[f];
+              } else {
+                dest = f * P.slots + P.slot_offset;
+              }
+              out = static_cast<float*>(P.out) + (size_t)w.split * P.out_split_stride +
+                    (size_t)dest * P.ldo;
+            }
+            out += (size_t)w.nt * un;
           }
         }
-        if (KIND == kGemmW13) {
-          float* dst = P.part + (size_t)w.split * P.part_split_stride + (size_t)w.nt * kF4M + r;
+        for (int c0 = 0; c0 < un; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * kF4MaxN + c0, v);
+          tmem_wait_ld(v);
+          if (out) {
+            float4* o4 = reinterpret_cast<float4*>(out + c0);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int fj = __shfl_sync(0xffffffffu, f, j);
-            if (fj >= 0) dst[(size_t)fj * 2 * P.ldo] = alpha * __uint_as_float(v[j]);
-          }
-        } else {
-          int dest = -1;
-          float wt = alpha;
-          if (f >= 0) {
-            if (P.sorted_ids) {
-              dest = (f / P.top_k) * P.slots + (f % P.top_k);
-              if (P.row_weight) wt = alpha * P.row_weight[f];
-            } else {
-              dest = f * P.slots + P.slot_offset;
-            }
-          }
-          float* outp = static_cast<float*>(P.out) + (size_t)w.split * P.out_split_stride +
-                        (size_t)w.nt * kF4M + r;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int dj = __shfl_sync(0xffffffffu, dest, j);
-            const float wj = __shfl_sync(0xffffffffu, wt, j);
-            if (dj >= 0) outp[(size_t)dj * P.ldo] = wj * __uint_as_float(v[j]);
+            for (int i = 0; i < 8; ++i)
+              o4[i] = make_float4(scale * __uint_as_float(v[4 * i]),
+                                  scale * __uint_as_float(v[4 * i + 1]),
+                                  scale * __uint_as_float(v[4 * i + 2]),
+                                  scale * __uint_as_float(v[4 * i + 3]));
           }
         }
       }
@@ -405,11 +556,17 @@ cudaError_t launch_gemm_fp4(int kind, const GemmLaunch& L, cudaStream_t stream) 
   if (kind != kGemmW13 && kind != kGemmW2) return cudaErrorInvalidValue;
   F4Maps maps;
   long units = 0;
+  int max_box = 0;  // widest token box any unit of the launch can take
+  // 256 weight rows per unit when every problem's weight rows split into 256s
+  maps.un = kF4MaxN;
+  for (int p = 0; p < L.num_problems; ++p)
+    if (L.p[p].b_rows_per_expert % kF4MaxN) maps.un = kF4TileRows;
   for (int p = 0; p < 2; ++p) {
     const GemmProblem& P = L.p[L.num_problems > p ? p : 0];
-    if (P.K % kF4BK || P.k_blocks != P.K / kF4BK || P.b_rows_per_expert % kF4M ||
-        P.n_tiles * kF4M != P.b_rows_per_expert || !P.B || !(P.gscale > 0.f) ||
-        (reinterpret_cast<uintptr_t>(P.B) & 15u) || (kind == kGemmW13 ? !P.part : !P.out))
+    if (P.K % kF4BK || P.k_blocks != P.K / kF4BK || P.b_rows_per_expert % maps.un ||
+        P.n_tiles * maps.un != P.b_rows_per_expert || !P.B || !(P.gscale > 0.f) ||
+        (reinterpret_cast<uintptr_t>(P.B) & 15u) || (kind == kGemmW13 ? !P.part : !P.out) ||
+        P.ldo % 4)
       return cudaErrorInvalidValue;
     for (int i = 0; i < kF4Boxes; ++i)
       if (!make_map_2d(&maps.x[p][i], P.A, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)P.K,
@@ -418,8 +575,21 @@ cudaError_t launch_gemm_fp4(int kind, const GemmLaunch& L, cudaStream_t stream) 
     if (p < L.num_problems) {
       if (splits_of(L, p) < 1 || P.k_blocks < splits_of(L, p)) return cudaErrorInvalidValue;
       units += (long)P.max_m_blocks * P.n_tiles * splits_of(L, p);
+      // an upper bound on the rows f4_desc gives a unit: routed blocks hold at most
+      // rows_bound real rows; identity rows up to a block
+      int rows = P.sorted_ids ? (P.rows_bound > 0 ? P.rows_bound : kFp4BS) : kFp4BS;
+      if (!P.sorted_ids && P.store_rows < rows) rows = P.store_rows;
+      rows = rows < 1 ? 1 : (rows > kFp4BS ? kFp4BS : rows);
+      const int n = (rows + 15) & ~15;
+      const int box = n <= 16 ? 0 : (n <= 32 ? 1 : (n <= 64 ? 2 : 3));
+      if (box > max_box) max_box = box;
     }
   }
+  // the token ring: slots of the widest box; the A read of the last slot (16 KB from its
+  // start) stays inside the ring's area
+  maps.tok_slot_bytes = (int)((16u << max_box) * 128);
+  maps.tok_stages = (int)((kF4TokArea - kF4ABytes) / (uint32_t)maps.tok_slot_bytes) + 1;
+  if (maps.tok_stages > kF4MaxTokStages) maps.tok_stages = kF4MaxTokStages;
   int grid = num_sms();
   if (units < grid) grid = (int)units;
   if (grid < 1) grid = 1;
