@@ -1,6 +1,6 @@
 """Seeded random layer configurations against the oracle (GPU): routing flavour, expert and
-group counts, top-k, shared expert, batch size (decode and prefill paths), bf16 or FP8
-weights. Routing must match bit for bit; the output stays within the layer's bound.
+group counts, top-k, shared expert, batch size (decode and prefill paths), bf16, FP8 or
+NVFP4 weights. Routing must match bit for bit; the output stays within the layer's bound.
 """
 from __future__ import annotations
 
@@ -83,3 +83,24 @@ def test_fuzz_layer(cuda_lib, seed, fp8):
     ids = layer.workspace[lay.topk_ids:lay.topk_ids + T * w.top_k * 4].view(torch.int32)
     assert np.array_equal(ids.cpu().numpy().reshape(T, w.top_k), parts["topk_ids"]), w
     check_close(y, y_ref, f"{w} T={T}")
+
+
+FP4_CASES = list(range(24))
+
+
+@pytest.mark.parametrize("seed", FP4_CASES, ids=[f"{s}-nvfp4" for s in FP4_CASES])
+def test_fuzz_layer_nvfp4(cuda_lib, seed):
+    """The NVFP4 layer on seeded random configurations: routing bit-exact, the act's
+    quantization decisions equal to the oracle's away from rounding midpoints, y within the
+    bound of the oracle's second GEMM and combine on the GPU's act (test_gpu_fp4)."""
+    from tests.test_gpu_fp4 import _check_layer, _fp4_layer
+    rng = np.random.default_rng(3000 + seed)
+    w = _random_workload(rng, True)
+    T = int(rng.choice([1, 2, 5, 16, 33, 150, 700]))
+    wts = inputs.make_fp4_weights(w, seed)
+    x, logits = tokens(w, T, wts["bias"], seed)
+    layer = _fp4_layer(w, wts, T)
+    y = layer(x.to(DEV), logits.to(DEV))
+    torch.cuda.synchronize()
+    assert layer.device_status() == binding.OK
+    _check_layer(w, wts, layer, x, logits, y, T)
