@@ -228,3 +228,46 @@ def test_workspace_size_nondecreasing_in_tokens(lib):
             sizes = [lib.moe_forward_workspace_size(ctypes.byref(cfg), T)
                      for T in list(range(0, 200)) + [256, 1000, 4096]]
             assert all(a <= b for a, b in zip(sizes, sizes[1:])), (w.name, quant)
+
+
+def test_nvfp4_validation(lib):
+    fp4 = dict(weight_quant="nvfp4")
+    sc = dict(w13_weight_scale_2=256, w2_weight_scale_2=256, input_scale=448.0, act_scale=100.0)
+    # the NVFP4 layer is the plain gated SiLU one
+    assert _fwd_ex(lib, _cfg(swiglu_limit=7.0, **fp4), **sc) == binding.ERR_UNSUPPORTED
+    assert _fwd_ex(lib, _cfg(gemm1_alpha=1.5, **fp4), **sc) == binding.ERR_UNSUPPORTED
+    assert _fwd_ex(lib, _cfg(is_act_and_mul=0, **fp4), **sc) == binding.ERR_UNSUPPORTED
+    assert _fwd_ex(lib, _cfg(apply_router_weight_on_input=True, **fp4),
+                   **sc) == binding.ERR_UNSUPPORTED
+    assert _fwd_ex(lib, _cfg(**fp4), w13_bias=256, **sc) == binding.ERR_UNSUPPORTED
+    # per-expert scales and positive finite per-tensor scales are required, and only here
+    for bad in (dict(w2_weight_scale_2=None), dict(input_scale=0.0), dict(act_scale=-1.0),
+                dict(act_scale=float("inf")), dict(input_scale=float("nan"))):
+        assert _fwd_ex(lib, _cfg(**fp4), **{**sc, **bad}) == binding.ERR_INVALID_ARG, bad
+    assert _fwd_ex(lib, _cfg(), w13_weight_scale_2=256) == binding.ERR_INVALID_ARG
+    assert _fwd_ex(lib, _cfg(**fp4), w13_scale=256, **sc) == binding.ERR_INVALID_ARG
+    # a shared expert needs its own scales
+    shared = _cfg(shared_intermediate_size=128, **fp4)
+    assert _fwd_ex(lib, shared, shared_w13=256, shared_w2=256, **sc) == binding.ERR_INVALID_ARG
+    ok = _cfg(**fp4)
+    need = lib.moe_forward_workspace_size(ctypes.byref(ok), 4)
+    assert need > 0 and _fwd_ex(lib, ok, workspace_bytes=need - 1, **sc) == binding.ERR_WORKSPACE
+    assert _fwd_ex(lib, ok, T=0, **sc) == binding.OK
+    # the first GEMM's fp32 partials are sized for every batch, prefill included
+    assert lib.moe_forward_workspace_size(ctypes.byref(ok), 4096) > \
+        lib.moe_forward_workspace_size(ctypes.byref(_cfg()), 4096)
+    # the standalone quant and the weight preparation
+    q = lib.moe_quant_nvfp4
+    P = ctypes.c_void_p
+    assert q(4, 40, P(256), 1.0, P(256), P(256), None) == binding.ERR_INVALID_ARG   # H % 16
+    assert q(4, 64, P(258), 1.0, P(256), P(256), None) == binding.ERR_INVALID_ARG   # x align
+    assert q(4, 64, P(256), 0.0, P(256), P(256), None) == binding.ERR_INVALID_ARG   # g
+    assert q(0, 64, None, 1.0, None, None, None) == binding.OK
+    assert binding.moe_nvfp4_prepared_bytes(256, 7168) == 256 * 7168 * 9 // 16
+    assert binding.moe_nvfp4_prepared_bytes(128, 64) == 4608
+    for rows, K in ((0, 64), (100, 64), (128, 96), (128, -64)):
+        assert binding.moe_nvfp4_prepared_bytes(rows, K) == 0
+    prep = lib.moe_nvfp4_prepare_weight
+    assert prep(100, 64, P(256), P(256), P(256), None) == binding.ERR_INVALID_ARG
+    assert prep(128, 64, P(264), P(256), P(256), None) == binding.ERR_INVALID_ARG
+    assert prep(128, 64, None, P(256), P(256), None) == binding.ERR_INVALID_ARG
