@@ -67,6 +67,12 @@ __device__ __forceinline__ void store_f32x32(float* dst, const uint32_t (&r)[32]
                        w * __uint_as_float(r[4 * v + 2]), w * __uint_as_float(r[4 * v + 3]));
 }
 
+#ifndef GBMOE_SHARED_PREFETCH
+#define GBMOE_SHARED_PREFETCH 1
+#endif
+constexpr bool kSharedPrefetch = GBMOE_SHARED_PREFETCH != 0;
+constexpr int kSharedPrefetchMaxRows = 4;
+
 template <int KIND, int BN, int AROWS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
@@ -122,6 +128,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   // launched only after the previous one got past its own wait, i.e. after the routing
   // finished. Every other thread waits here.
   constexpr bool kEarlyB = KIND == kGemmW2 && AROWS < kGemmBM;
+  // Decode w13 with a shared expert, T <= 4: the shared expert's weights do not depend on
+  // the routing, so while the routing runs (this kernel is waiting below) each CTA asks L2
+  // for its share of them, kept with an evict_last policy; the routed weights stream
+  // evict_first past them, and the shared units at the end of the launch find them in L2.
+  // (Measured: DeepSeek-V2 T = 1 82.6 -> 78.5 us, DeepSeek-V3 T = 1 157 -> 152 us; neutral
+  // at T = 4, slightly slower from T = 16, where the routing is short next to the GEMM.)
+  if (kSharedPrefetch && KIND != kGemmW2 && AROWS < kGemmBM && args.num_problems > 1 &&
+      args.p[1].store_rows <= kSharedPrefetchMaxRows && warp == 3 && lane == 0) {
+    const GemmProblem& Q = args.p[1];
+    const size_t bytes = (size_t)Q.b_rows * Q.K * 2;
+    const size_t per = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~(size_t)15;
+    const size_t off = per * blockIdx.x;
+    uint64_t keep;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+    for (size_t o = off; o < off + per && o < bytes; o += 65536) {
+      const size_t n = min((size_t)65536, min(off + per, bytes) - o);
+      asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(
+                       reinterpret_cast<uint64_t>(static_cast<const char*>(Q.B) + o)),
+                   "r"((uint32_t)(n & ~(size_t)15)), "l"(keep)
+                   : "memory");
+    }
+  }
   if (!kEarlyB || warp != 0) pdl_wait();  // the set-up above overlapped the previous kernel
   // the next kernel may launch once this one's inputs are complete (so that it, too, may
   // rely on everything before this kernel having finished). DEPENDENCE: the decode w2 GEMM
