@@ -251,10 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t sa = base + s * S::kStageBytes;
-          const uint32_t sb = sa + S::kARegion;
+          const uint64_t da = sdesc_sw128(sa), db = sdesc_sw128(sa + S::kARegion);
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk)
-            mma_bf16(d, sdesc_sw128(sa + kk * 32), sdesc_sw128(sb + kk * 32), idesc,
+            mma_bf16(d, sdesc_advance(da, kk * 32), sdesc_advance(db, kk * 32), idesc,
                      (kb > w.kb0 || kk != 0) ? 1u : 0u);
           mma_commit(empty_bar(s));
         }

@@ -188,11 +188,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           }
           tc_fence_after();
           const uint32_t sa = base + s * kF8StageBytes;
-          const uint32_t sb = sa + kGemmBM * kF8BK;
+          const uint64_t da = sdesc_sw128(sa), db = sdesc_sw128(sa + kGemmBM * kF8BK);
           const uint32_t d = tmem_base + buf * kF8BufStride;
 #pragma unroll
           for (int kk = 0; kk < kF8BK / 32; ++kk)
-            mma_e4m3(d, sdesc_sw128(sa + kk * 32), sdesc_sw128(sb + kk * 32), idesc,
+            mma_e4m3(d, sdesc_advance(da, kk * 32), sdesc_advance(db, kk * 32), idesc,
                      kk != 0 ? 1u : 0u);
           mma_commit(empty_bar(s));
           mma_commit(tfull_bar(buf));
@@ -534,14 +534,14 @@ __global__ void __launch_bounds__(kSwThreads, 1)
           }
           tc_fence_after();
           const uint32_t sw = base + s * kSwStageBytes;
-          const uint32_t sx = sw + 256 * kF8BK;
+          const uint64_t dw = sdesc_sw128(sw), dx = sdesc_sw128(sw + 256 * kF8BK);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint32_t d = tmem_base + buf * 64 + h * kSwN;
 #pragma unroll
             for (int kk = 0; kk < kF8BK / 32; ++kk)
-              mma_e4m3(d, sdesc_sw128(sw + h * 128 * kF8BK + kk * 32), sdesc_sw128(sx + kk * 32),
-                       idesc, kk != 0 ? 1u : 0u);
+              mma_e4m3(d, sdesc_advance(dw, h * 128 * kF8BK + kk * 32),
+                       sdesc_advance(dx, kk * 32), idesc, kk != 0 ? 1u : 0u);
           }
           mma_commit(empty_bar(s));
           mma_commit(tfull_bar(buf));

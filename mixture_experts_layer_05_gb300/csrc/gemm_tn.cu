@@ -344,10 +344,10 @@ __global__ void __launch_bounds__(kTnThreads, 1)
           }
           tc_fence_after();
           const uint32_t sw = base + s * kTnStageBytes;
-          const uint32_t sx = sw + kTnWRegion;
+          const uint64_t dw = sdesc_sw128(sw), dx = sdesc_sw128(sw + kTnWRegion);
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk)
-            mma_bf16_pair(d, sdesc_sw128(sw + kk * 32), sdesc_sw128(sx + kk * 32), idesc,
+            mma_bf16_pair(d, sdesc_advance(dw, kk * 32), sdesc_advance(dx, kk * 32), idesc,
                           (kb > 0 || kk != 0) ? 1u : 0u);
           mma_commit_pair(empty_bar(s));
         }

@@ -177,6 +177,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The descriptor of the operand `bytes` further on in shared memory: the start address
+// field counts 16-byte units and cannot carry out inside a CTA's shared memory, so the K
+// steps of a stage are plain adds (no per-MMA rebuild in the issuing thread's loop).
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t d, uint32_t bytes) {
+  return d + (bytes >> 4);
+}
+
 // Instruction descriptor of kind::f16: D fp32, A and B bf16, both K-major, N and M.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
