@@ -13,12 +13,12 @@
 // The weights arrive prepared (moe_nvfp4_prepare_weight): per tile of 128 rows and K stage
 // of 64 values one contiguous 4608-byte chunk, the packed codes of the stage's two K halves
 // (16 bytes per row each) then the rows' four scale bytes. A unit is a row block of up to
-// 128 token rows (the MMA's M side) against 256 weight rows (N; 128 when the weight rows do
-// not split into 256s) over a K range. Per 64-value K stage:
+// 128 token rows against 256 weight rows (128 when the weight rows do not split into 256s)
+// over a K range. Tokens-on-M mode (row blocks of more than 64 rows), per 64-value K stage:
 //
 //   warp 0       bulk copies of the stage's two prepared chunks into an 8-deep raw ring
-//   warp 1       TMEM (two 256-column accumulators) and the MMAs (M 128, or 64 for row
-//                blocks of at most 64 real rows; N 256; K 16)
+//   warp 1       TMEM (two 256-column accumulators) and the MMAs (tokens on M: 128, or 64
+//                for row blocks of at most 64 real rows; weights on N 256; K 16)
 //   warp 2       TMA of the token tile (16 / 32 / 64 / 128 rows) into a dense token ring
 //   warp 3       the unit scheduler: reads each unit's metadata from global memory ahead
 //                of time and publishes it in shared memory
@@ -27,12 +27,28 @@
 //                per pair) into the 128-byte-swizzled K-major f16 layout the MMA reads
 //   warps 20..23 epilogue: TMEM lane quarter warp & 3, one token row per thread
 //
-// Weights on N keep the tensor core at full width whatever the batch: an M = 128 MMA costs
-// about the same at N = 16 as at N = 256, so putting the few decode tokens on N (weights on
-// M) spent eight MMA issues per 16K weights where this layout spends four. The token ring
-// is dense: a 16-row tile takes 2 KB, and the MMA's 128-row A operand starting at a slot
-// reads the following slots as its (discarded) rows 16..127, so the ring's tail is padded
-// to keep that read inside the ring.
+// The token ring is dense: a 16-row tile takes 2 KB, and the MMA's 128-row A operand
+// starting at a slot reads the following slots as its (discarded) rows 16..127, so the
+// ring's tail is padded to keep that read inside the ring.
+//
+// Weights-in-TMEM mode (TS; launches whose row blocks hold at most 64 token rows, i.e. the
+// decode batches): the tensor core's time per MMA follows N, not M (M 128 x K 16 costs
+// about 45 cycles at N <= 64 and 128 at N = 256, the same for M = 64), so the few tokens go
+// on N and the expanded weights are the A operand, written by the converters straight into
+// tensor memory (tcgen05.st) instead of a shared-memory f16 tile that the MMA reads back:
+// shared memory then carries only the chunk copies and the token tiles. Roles:
+//
+//   warp 0       bulk copies into a 16-deep raw ring
+//   warp 2       the token tile of each stage into slot (stage mod S) of the token ring,
+//                completing on that stage's barrier (S = the A ring's stages)
+//   warps 1, 24  one MMA issuer per 128-row weight tile: M 128 (weights, A in TMEM) x N
+//                (the unit's token rows rounded to 16) x K 16, 4 per stage, one stage
+//                barrier wait and one commit per stage each
+//   warps 4..19  two groups of 8 on alternate stages: a thread expands one weight row's 64
+//                values of the stage (codes + four block scales) into the 32 TMEM columns
+//                of its tile in the stage's A slot (its warp's lane quarter)
+//   warps 20..23 epilogue: TMEM lane = output column, TMEM column = token row
+//
 // Every wait is bounded (kWaitTimeoutNs).
 #include "fp4.cuh"
 #include "tc.cuh"
@@ -49,7 +65,7 @@ constexpr uint32_t kF4RawBytes = 2 * kFp4ChunkBytes;  // the stage's prepared ch
 #define GBMOE_F4_RAW_STAGES 8
 #endif
 constexpr int kF4RawStages = GBMOE_F4_RAW_STAGES;
-constexpr int kF4MaxRawStages = 8;
+constexpr int kF4MaxRawStages = 16;
 constexpr int kF4CvtSlots = 3;                    // f16 weight stages
 constexpr uint32_t kF4WBytes = kF4MaxN * 128;     // f16 weights of a stage: 32 KB
 constexpr uint32_t kF4ABytes = kF4M * 128;        // the MMA's A operand: 128 rows, 16 KB
@@ -59,6 +75,7 @@ constexpr int kF4MaxTokStages = 16;
 constexpr int kF4CvtWarps = 16;
 constexpr int kF4EpiWarps = 4;
 constexpr int kF4Threads = 32 * (4 + kF4CvtWarps + kF4EpiWarps);
+constexpr int kF4TsThreads = kF4Threads + 32;     // TS: a second MMA-issuing warp (24)
 constexpr uint32_t kF4TmemCols = 512;             // two 256-column accumulators
 constexpr int kF4Boxes = 4;                       // token boxes of 16, 32, 64, 128 rows
 constexpr int kF4UnitRing = 8;                    // unit descriptors the scheduler runs ahead
@@ -69,6 +86,25 @@ constexpr uint32_t kF4BarBytes = 2048;
 constexpr size_t kF4Smem = 1024 + (size_t)kF4CvtSlots * kF4WBytes + kF4TokArea +
                            (size_t)kF4RawStages * kF4RawBytes + kF4BarBytes;
 static_assert(kF4Smem <= 232448, "shared memory per CTA exceeded");
+// Weights-in-TMEM mode (row blocks of at most 64 real rows): the expanded weights are the
+// MMA's A operand in tensor memory, so shared memory holds only the chunk ring (deeper) and
+// the token ring.
+constexpr int kF4TsRawStages = 16;
+constexpr int kF4TsMaxRows = 64;                  // token rows per unit (MMA N)
+constexpr int kF4TsMaxSlots = 8;                  // weight stages in TMEM (and token slots)
+constexpr size_t kF4TsSmem = 1024 + kF4TokArea + (size_t)kF4TsRawStages * kF4RawBytes +
+                             kF4BarBytes;
+static_assert(kF4TsSmem <= 232448, "shared memory per CTA exceeded");
+static_assert(kF4TsRawStages <= kF4MaxRawStages, "ring sizes");
+// TMEM in this mode: two accumulator buffers of two tiles (acc_stride columns each: the
+// launch's widest token box), then the A ring, 64 columns (two tiles x 64 f16 values) per
+// stage, as many stages as fit: 7 for 16-row boxes, 6 for 32, 4 for 64.
+__host__ __device__ constexpr int f4_ts_slots(int acc_stride) {
+  return (kF4TmemCols - 4 * acc_stride) / 64 < kF4TsMaxSlots ? (kF4TmemCols - 4 * acc_stride) / 64
+                                                              : kF4TsMaxSlots;
+}
+static_assert(f4_ts_slots(kF4TsMaxRows) >= 4 && f4_ts_slots(kF4TsMaxRows) * 8 * 1024 <= kF4TokArea,
+              "TS rings");
 static_assert(kF4RawBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
 static_assert(kF4RawStages <= kF4MaxRawStages && kF4TokArea >= kF4ABytes, "ring sizes");
 
@@ -77,6 +113,7 @@ struct F4Maps {
   int tok_stages;              // token ring stages (<= kF4MaxTokStages)
   int tok_slot_bytes;          // the widest token box of the launch (a multiple of 1024)
   int un;                      // weight rows per unit: 256, or 128
+  int acc_stride;              // TS: TMEM columns per accumulator tile (the widest box rows)
 };
 
 // Instruction descriptor of kind::f16 with f16 A and B (format code 0), fp32 D, K-major.
@@ -136,6 +173,33 @@ __device__ __forceinline__ void e2m1x8_scaled(uint32_t w, uint32_t sc, uint32_t 
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit TMEM columns from registers (this warp's lane quarter).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
+      "%10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, "
+      "%27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T, f16 inputs (A: lane = row, column c = values 2c, 2c + 1).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // Spin (bounded, ignoring the abort flag) until the phase of `bar` with parity `parity`
@@ -201,63 +265,70 @@ struct RingPos {
   }
 };
 
-template <int KIND>
-__global__ void __launch_bounds__(kF4Threads, 1)
+template <int KIND, bool TS>
+__global__ void __launch_bounds__(kF4TsThreads, 1)
     gemm_fp4_kernel(const __grid_constant__ F4Maps maps, const __grid_constant__ GemmLaunch args) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw0 = smem_addr(smem_raw);
   const uint32_t base = (raw0 + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw0);
-  // [f16 weight slots 3 x 32 KB] [token ring 48 KB] [raw ring] [barriers]
+  // [f16 weight slots 3 x 32 KB, not in TS mode] [token ring 48 KB] [raw ring] [barriers]
+  constexpr uint32_t kCvtArea = TS ? 0u : kF4CvtSlots * kF4WBytes;
+  constexpr int kRawStages = TS ? kF4TsRawStages : kF4RawStages;
+  // TS: the token ring is the A ring (one stage barrier for both)
+  const int kCvtSlots = TS ? f4_ts_slots(maps.acc_stride) : kF4CvtSlots;
+  const uint32_t acc_stride = TS ? (uint32_t)maps.acc_stride : 0u;
+  const uint32_t a_col = 4u * acc_stride;          // TS: first A ring column
   const int ts = maps.tok_stages;
   const uint32_t tsb = (uint32_t)maps.tok_slot_bytes;
   const int un = maps.un;
   const int chunks = un / kF4TileRows;             // prepared chunks per stage: 1 or 2
-  const uint32_t tok_base = base + kF4CvtSlots * kF4WBytes;
+  const uint32_t tok_base = base + kCvtArea;
   const uint32_t raw_base = tok_base + kF4TokArea;
-  uint8_t* raw_ptr = smem + kF4CvtSlots * kF4WBytes + kF4TokArea;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(raw_ptr + kF4RawStages * kF4RawBytes);
-  // bars: raw_full[8] raw_empty[8] cvt_full[4] cvt_empty[4] tfull[2] tempty[2]
+  uint8_t* raw_ptr = smem + kCvtArea + kF4TokArea;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw_ptr + kRawStages * kF4RawBytes);
+  // bars: raw_full[16] raw_empty[16] cvt_full[8] cvt_empty[8] tfull[2] tempty[2]
   //       unit_full[8] unit_empty[8] tok_full[16] tok_empty[16]; then the TMEM slot, the
   //       abort flag and (at byte 1024) the unit descriptors
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 44 + 2 * kF4MaxTokStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 68 + 2 * kF4MaxTokStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   F4Desc* descs = reinterpret_cast<F4Desc*>(reinterpret_cast<uint8_t*>(bars) + 1024);
   const uint32_t bar0 = smem_addr(bars);
   auto raw_full = [&](int s) { return bar0 + 8u * s; };
-  auto raw_empty = [&](int s) { return bar0 + 8u * (8 + s); };
-  auto cvt_full = [&](int s) { return bar0 + 8u * (16 + s); };
-  auto cvt_empty = [&](int s) { return bar0 + 8u * (20 + s); };
-  auto tfull = [&](int b) { return bar0 + 8u * (24 + b); };
-  auto tempty = [&](int b) { return bar0 + 8u * (26 + b); };
-  auto unit_full = [&](int i) { return bar0 + 8u * (28 + i); };
-  auto unit_empty = [&](int i) { return bar0 + 8u * (36 + i); };
-  auto tok_full = [&](int s) { return bar0 + 8u * (44 + s); };
-  auto tok_empty = [&](int s) { return bar0 + 8u * (44 + kF4MaxTokStages + s); };
+  auto raw_empty = [&](int s) { return bar0 + 8u * (16 + s); };
+  auto cvt_full = [&](int s) { return bar0 + 8u * (32 + s); };
+  auto cvt_empty = [&](int s) { return bar0 + 8u * (40 + s); };
+  auto tfull = [&](int b) { return bar0 + 8u * (48 + b); };
+  auto tempty = [&](int b) { return bar0 + 8u * (50 + b); };
+  auto unit_full = [&](int i) { return bar0 + 8u * (52 + i); };
+  auto unit_empty = [&](int i) { return bar0 + 8u * (60 + i); };
+  auto tok_full = [&](int s) { return bar0 + 8u * (68 + s); };
+  auto tok_empty = [&](int s) { return bar0 + 8u * (68 + kF4MaxTokStages + s); };
   auto w_stage = [&](int s) { return base + s * kF4WBytes; };
   auto x_stage = [&](int s) { return tok_base + s * tsb; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kF4RawStages; ++s) {
+    for (int s = 0; s < kRawStages; ++s) {
       mbar_init(raw_full(s), 1);
-      mbar_init(raw_empty(s), kF4CvtWarps);
+      mbar_init(raw_empty(s), TS ? kF4CvtWarps / 2 : kF4CvtWarps);
     }
-    for (int s = 0; s < kF4CvtSlots; ++s) {
-      mbar_init(cvt_full(s), kF4CvtWarps);
-      mbar_init(cvt_empty(s), 1);
+    for (int s = 0; s < kCvtSlots; ++s) {
+      // TS: the stage's converter group and the token tile's expect_tx arrival
+      mbar_init(cvt_full(s), TS ? kF4CvtWarps / 2 + 1 : kF4CvtWarps);
+      mbar_init(cvt_empty(s), TS ? chunks : 1);  // TS: one commit per tile's issuer
     }
     for (int s = 0; s < ts; ++s) {
       mbar_init(tok_full(s), 1);
-      mbar_init(tok_empty(s), 1);
+      mbar_init(tok_empty(s), TS ? chunks : 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(tfull(b), 1);
+      mbar_init(tfull(b), TS ? chunks : 1);
       mbar_init(tempty(b), kF4EpiWarps);
     }
     for (int i = 0; i < kF4UnitRing; ++i) {
       mbar_init(unit_full(i), 1);
-      mbar_init(unit_empty(i), kF4UnitReaders);
+      mbar_init(unit_empty(i), kF4UnitReaders + (TS ? 1 : 0));
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -309,7 +380,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                              ((size_t)w.tile * P.k_blocks + w.kb0) * (size_t)kFp4ChunkBytes;
         const size_t tile_bytes = (size_t)P.k_blocks * kFp4ChunkBytes;  // next tile's chunk
         for (int kb = w.kb0; kb < w.kb1;
-             ++kb, src += kFp4ChunkBytes, rq.next(kF4RawStages), ++issued) {
+             ++kb, src += kFp4ChunkBytes, rq.next(kRawStages), ++issued) {
           if (!wait_fast(raw_empty(rq.slot), rq.phase ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
@@ -322,8 +393,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         }
       }
       // the last copies of each slot land before the CTA can exit
-      for (uint32_t j = issued > (uint32_t)kF4RawStages ? issued - kF4RawStages : 0; j < issued; ++j)
-        drain_wait(raw_full(j % kF4RawStages), (j / kF4RawStages) & 1u);
+      for (uint32_t j = issued > (uint32_t)kRawStages ? issued - kRawStages : 0; j < issued; ++j)
+        drain_wait(raw_full(j % kRawStages), (j / kRawStages) & 1u);
     }
     __syncwarp();
   } else if (warp == 2) {
@@ -339,21 +410,42 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         uq.next(kF4UnitRing);
         const CUtensorMap* map = &maps.x[w.p][w.box];
         const uint32_t box_bytes = (uint32_t)(16 << w.box) * 128;
-        for (int kb = w.kb0; kb < w.kb1; ++kb, tq.next(ts), ++issued) {
-          if (!wait_fast(tok_empty(tq.slot), tq.phase ^ 1u, abort_flag, args.status)) {
-            ok = false;
-            break;
+        if constexpr (TS) {
+          // the token tile of stage j lands in slot j of the A ring and completes on that
+          // stage's barrier, so the MMA issuers wait once per stage
+          for (int kb = w.kb0; kb < w.kb1; ++kb, tq.next(kCvtSlots), ++issued) {
+            if (!wait_fast(cvt_empty(tq.slot), tq.phase ^ 1u, abort_flag, args.status)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(cvt_full(tq.slot), box_bytes);
+            tma_load_2d(x_stage(tq.slot), map, cvt_full(tq.slot), kb * kF4BK, w.mb * kFp4BS);
           }
-          mbar_expect_tx(tok_full(tq.slot), box_bytes);
-          tma_load_2d(x_stage(tq.slot), map, tok_full(tq.slot), kb * kF4BK, w.mb * kFp4BS);
+        } else {
+          for (int kb = w.kb0; kb < w.kb1; ++kb, tq.next(ts), ++issued) {
+            if (!wait_fast(tok_empty(tq.slot), tq.phase ^ 1u, abort_flag, args.status)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(tok_full(tq.slot), box_bytes);
+            tma_load_2d(x_stage(tq.slot), map, tok_full(tq.slot), kb * kF4BK, w.mb * kFp4BS);
+          }
         }
       }
-      for (uint32_t j = issued > (uint32_t)ts ? issued - ts : 0; j < issued; ++j)
-        drain_wait(tok_full(j % ts), (j / ts) & 1u);
+      if (TS) {
+        const uint32_t n = (uint32_t)kCvtSlots;
+        for (uint32_t j = issued > n ? issued - n : 0; j < issued; ++j)
+          drain_wait(cvt_full(j % n), (j / n) & 1u);
+      } else {
+        for (uint32_t j = issued > (uint32_t)ts ? issued - ts : 0; j < issued; ++j)
+          drain_wait(tok_full(j % ts), (j / ts) & 1u);
+      }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 || (TS && warp == 4 + kF4CvtWarps + kF4EpiWarps)) {
     // ------------------------------------------------------------ MMA issuer
+    // (TS: warp 1 issues tile 0's MMAs, warp 24 tile 1's, each with its own commits)
+    const int mt = warp == 1 ? 0 : 1;
     if (lane == 0) {
       RingPos uq{0, 0}, cq{0, 0}, tq{0, 0};
       uint32_t uc = 0;
@@ -364,22 +456,49 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         mbar_arrive(unit_empty(uq.slot));
         uq.next(kF4UnitRing);
         const int buf = uc & 1;
-        // row blocks of at most 64 real rows run M = 64 MMAs: half the tensor work
+        if constexpr (TS) {
+          // weights on M (128 rows per tile, A in TMEM), the unit's tokens on N
+          const uint32_t idesc = idesc_f16(kF4M, w.n);
+          if (!wait_fast(tempty(buf), ((uc >> 1) & 1u) ^ 1u, abort_flag, args.status)) break;
+          tc_fence_after();
+          if (mt >= chunks) continue;  // no second tile: this issuer only follows the units
+          const uint32_t d = tmem_base + (uint32_t)buf * 2u * acc_stride + (uint32_t)mt * acc_stride;
+          for (int kb = w.kb0; kb < w.kb1; ++kb, cq.next(kCvtSlots)) {
+            // the stage barrier: the group's weights in TMEM and the token tile in its slot
+            if (!wait_fast(cvt_full(cq.slot), cq.phase, abort_flag, args.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // K step kk: 32 bytes into the token rows' swizzled 128-byte atoms, 8 columns
+            // into the weights' TMEM stage
+            const uint64_t b0 = sdesc_sw128(x_stage(cq.slot));
+            const uint32_t a0 = tmem_base + a_col + (uint32_t)cq.slot * 64u + mt * 32u;
+            mma_f16_ts(d, a0, b0, idesc, kb == w.kb0 ? 0u : 1u);
+            mma_f16_ts(d, a0 + 8, sdesc_advance(b0, 32), idesc, 1u);
+            mma_f16_ts(d, a0 + 16, sdesc_advance(b0, 64), idesc, 1u);
+            mma_f16_ts(d, a0 + 24, sdesc_advance(b0, 96), idesc, 1u);
+            mma_commit(cvt_empty(cq.slot));
+          }
+          if (ok) mma_commit(tfull(buf));
+          continue;
+        }
+        // row blocks of at most 64 real rows run M = 64 MMAs (fewer discarded rows in TMEM)
         const uint32_t idesc = idesc_f16(w.rows <= 64 ? 64 : kF4M, un);
         if (!wait_fast(tempty(buf), ((uc >> 1) & 1u) ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + buf * kF4MaxN;
-        for (int kb = w.kb0; kb < w.kb1; ++kb, cq.next(kF4CvtSlots), tq.next(ts)) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb, cq.next(kCvtSlots), tq.next(ts)) {
           if (!wait_fast(tok_full(tq.slot), tq.phase, abort_flag, args.status) ||
               !wait_fast(cvt_full(cq.slot), cq.phase, abort_flag, args.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t xa = x_stage(tq.slot), wa = w_stage(cq.slot);
+          const uint64_t dx = sdesc_sw128(x_stage(tq.slot)), dw = sdesc_sw128(w_stage(cq.slot));
 #pragma unroll
           for (int kk = 0; kk < kF4BK / 16; ++kk)
-            mma_bf16(d, sdesc_sw128(xa + kk * 32), sdesc_sw128(wa + kk * 32), idesc,
+            mma_bf16(d, sdesc_advance(dx, kk * 32), sdesc_advance(dw, kk * 32), idesc,
                      (kb != w.kb0 || kk != 0) ? 1u : 0u);
           mma_commit(cvt_empty(cq.slot));
           mma_commit(tok_empty(tq.slot));
@@ -402,6 +521,149 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       }
     }
     __syncwarp();
+  } else if (TS && warp >= 4 && warp < 4 + kF4CvtWarps) {
+    // ------------------------------------------------------------ fp4 -> f16 into TMEM
+    // Two groups of 8 converter warps take alternate stages, so that one group's load ->
+    // convert -> TMEM store chain overlaps the other's. Warp c (0..15) of group c / 8
+    // writes TMEM lane quarter c % 4 (= warp % 4, the quarter a warp may access): weight
+    // row 32 (c % 4) + lane of tile (c / 4) % 2, all 64 values of the stage, i.e. the 32
+    // columns of that tile in the stage's A slot.
+    const int c = warp - 4;
+    const uint32_t grp = (uint32_t)(c >> 3);
+    const int tile = (c >> 2) & 1;
+    const uint32_t rr = (uint32_t)(32 * (c & 3) + lane);
+    const bool live = tile < chunks;  // warp-uniform
+    const uint32_t lanes = (uint32_t)(32 * (c & 3)) << 16;
+    const uint32_t col0 = a_col + (uint32_t)tile * 32u;
+    const uint32_t rd = (uint32_t)tile * kFp4ChunkBytes + rr * 16u;
+    const uint32_t sd = (uint32_t)tile * kFp4ChunkBytes + 4096u + rr * 4u;
+    RingPos uq{0, 0}, rq{0, 0}, cq{0, 0};
+    uint32_t jc = 0;  // stage counter of the CTA (both groups count every stage)
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+      F4Desc w;
+      if (!get_unit(uq, w)) break;
+      release_unit(uq);
+      for (int kb = w.kb0; kb < w.kb1;
+           ++kb, ++jc, rq.next(kRawStages), cq.next(kCvtSlots)) {
+        if ((jc & 1u) != grp) continue;
+        if (!wait_fast(raw_full(rq.slot), rq.phase, abort_flag, args.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t src = raw_base + rq.slot * kF4RawBytes;
+        uint4 q0 = make_uint4(0u, 0u, 0u, 0u), q1 = q0;
+        uint32_t scw = 0u;
+        if (live) {
+          q0 = lds128(src + rd);            // values 0..31 of the row's stage
+          q1 = lds128(src + rd + 2048u);    // values 32..63
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(scw) : "r"(src + sd));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(raw_empty(rq.slot));
+        if (!wait_fast(cvt_empty(cq.slot), cq.phase ^ 1u, abort_flag, args.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (live) {
+          uint32_t s0, s1, s2, s3;          // the four 16-value blocks' scales as f16 pairs
+          e4m3x2_pairs(scw & 0xFFFFu, s0, s1);
+          e4m3x2_pairs(scw >> 16, s2, s3);
+          uint32_t o[32];
+          const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+          const uint32_t scs[4] = {s0, s1, s2, s3};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint32_t o4[4];
+            e2m1x8_scaled(words[i], scs[i >> 1], o4);
+            o[4 * i] = o4[0];
+            o[4 * i + 1] = o4[1];
+            o[4 * i + 2] = o4[2];
+            o[4 * i + 3] = o4[3];
+          }
+          tmem_st32(tmem_base + lanes + col0 + (uint32_t)cq.slot * 64u, o);
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cvt_full(cq.slot));
+      }
+    }
+  } else if (TS && warp >= 4 + kF4CvtWarps && warp < 4 + kF4CvtWarps + kF4EpiWarps) {
+    // ------------------------------------------------------------ epilogue (TS)
+    // D of tile t: TMEM lane = weight row (this warp's quarter), column j = the unit's token
+    // row j. Lane j resolves token rows j and j + 32 to an output row and a scale; every
+    // column is then one coalesced 128-byte store per warp.
+    const int quarter = warp & 3;
+    RingPos uq{0, 0};
+    uint32_t uc = 0;
+    for (int u = blockIdx.x; u < sched.units; u += gridDim.x, ++uc) {
+      F4Desc w;
+      if (!get_unit(uq, w)) break;
+      release_unit(uq);
+      const GemmProblem& P = args.p[w.p];
+      const int buf = uc & 1;
+      float* rowp[2] = {nullptr, nullptr};
+      float rows_scale[2] = {0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int m = lane + 32 * i;
+        if (m >= w.rows) continue;
+        const int mr = w.mb * kFp4BS + m;
+        int f = -1;
+        if (P.sorted_ids) {
+          const int x = P.sorted_ids[mr];
+          if (x >= 0 && x < P.num_flat) f = x;
+        } else if (mr < P.store_rows) {
+          f = mr;
+        }
+        if (f < 0) continue;
+        float scale = w.alpha;
+        float* out;
+        if (KIND == kGemmW13) {
+          out = P.part + (size_t)w.split * P.part_split_stride + (size_t)f * 2 * P.ldo;
+        } else {
+          int dest;
+          if (P.sorted_ids) {
+            dest = (f / P.top_k) * P.slots + (f % P.top_k);
+            if (P.row_weight) scale = w.alpha * P.row_weight[f];
+          } else {
+            dest = f * P.slots + P.slot_offset;
+          }
+          out = static_cast<float*>(P.out) + (size_t)w.split * P.out_split_stride +
+                (size_t)dest * P.ldo;
+        }
+        rowp[i] = out + (size_t)w.nt * un;
+        rows_scale[i] = scale;
+      }
+      if (!wait_fast(tfull(buf), (uc >> 1) & 1u, abort_flag, args.status)) break;
+      tc_fence_after();
+      for (int t = 0; t < chunks; ++t) {
+        const int col = t * kF4TileRows + 32 * quarter + lane;  // this lane's output column
+        for (int c0 = 0; c0 < w.n; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                        (uint32_t)buf * 2u * acc_stride + (uint32_t)t * acc_stride + (uint32_t)c0,
+                    v);
+          tmem_wait_ld16(v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int j = c0 + i;  // token row of the unit (warp-uniform)
+            if (j >= w.rows) break;
+            const bool hi = j >= 32;
+            float* const op = reinterpret_cast<float*>(__shfl_sync(
+                0xffffffffu, reinterpret_cast<unsigned long long>(hi ? rowp[1] : rowp[0]),
+                j & 31));
+            const float sc = __shfl_sync(0xffffffffu, hi ? rows_scale[1] : rows_scale[0], j & 31);
+            if (op) op[col] = sc * __uint_as_float(v[i]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(buf));
+    }
   } else if (warp >= 4 && warp < 4 + kF4CvtWarps) {
     // ------------------------------------------------------------ fp4 -> f16 expansion
     // Every converter thread takes part in every stage: weight row r = t % 256 (of chunk
@@ -417,7 +679,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       F4Desc w;
       if (!get_unit(uq, w)) break;
       release_unit(uq);
-      for (int kb = w.kb0; kb < w.kb1; ++kb, rq.next(kF4RawStages), cq.next(kF4CvtSlots)) {
+      for (int kb = w.kb0; kb < w.kb1; ++kb, rq.next(kRawStages), cq.next(kCvtSlots)) {
         if (!wait_fast(raw_full(rq.slot), rq.phase, abort_flag, args.status)) {
           ok = false;
           break;
@@ -532,20 +794,22 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   }
 }
 
-template <int KIND>
+template <int KIND, bool TS>
 cudaError_t launch_fp4_typed(const F4Maps& maps, const GemmLaunch& args, int grid,
                              cudaStream_t stream) {
+  constexpr size_t smem = TS ? kF4TsSmem : kF4Smem;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_fp4_kernel<KIND>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_fp4_kernel<KIND, TS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kF4Smem);
+                                         (int)smem);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  return launch_kernel(gemm_fp4_kernel<KIND>, dim3(grid), dim3(kF4Threads), kF4Smem, stream,
+  return launch_kernel(gemm_fp4_kernel<KIND, TS>, dim3(grid), dim3(TS ? kF4TsThreads : kF4Threads),
+                       smem, stream,
                        maps, args);
 }
 
@@ -585,16 +849,23 @@ cudaError_t launch_gemm_fp4(int kind, const GemmLaunch& L, cudaStream_t stream) 
       if (box > max_box) max_box = box;
     }
   }
-  // the token ring: slots of the widest box; the A read of the last slot (16 KB from its
-  // start) stays inside the ring's area
+  // row blocks of at most 64 token rows: weights in TMEM on the MMA's M side, tokens on N
+  const bool ts_mode = (16 << max_box) <= kF4TsMaxRows;
+  // the token ring: slots of the widest box; in the tokens-on-M mode the A read of the last
+  // slot (16 KB from its start) stays inside the ring's area; in the TS mode it is the A ring
   maps.tok_slot_bytes = (int)((16u << max_box) * 128);
-  maps.tok_stages = (int)((kF4TokArea - kF4ABytes) / (uint32_t)maps.tok_slot_bytes) + 1;
+  maps.acc_stride = 16 << max_box;
+  maps.tok_stages = ts_mode ? f4_ts_slots(maps.acc_stride)
+                            : (int)((kF4TokArea - kF4ABytes) / (uint32_t)maps.tok_slot_bytes) + 1;
   if (maps.tok_stages > kF4MaxTokStages) maps.tok_stages = kF4MaxTokStages;
   int grid = num_sms();
   if (units < grid) grid = (int)units;
   if (grid < 1) grid = 1;
-  return kind == kGemmW13 ? launch_fp4_typed<kGemmW13>(maps, L, grid, stream)
-                          : launch_fp4_typed<kGemmW2>(maps, L, grid, stream);
+  if (ts_mode)
+    return kind == kGemmW13 ? launch_fp4_typed<kGemmW13, true>(maps, L, grid, stream)
+                            : launch_fp4_typed<kGemmW2, true>(maps, L, grid, stream);
+  return kind == kGemmW13 ? launch_fp4_typed<kGemmW13, false>(maps, L, grid, stream)
+                          : launch_fp4_typed<kGemmW2, false>(maps, L, grid, stream);
 }
 
 }  // namespace gbmoe
