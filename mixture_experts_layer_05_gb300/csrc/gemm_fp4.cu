@@ -89,21 +89,28 @@ static_assert(kF4Smem <= 232448, "shared memory per CTA exceeded");
 // Weights-in-TMEM mode (row blocks of at most 64 real rows): the expanded weights are the
 // MMA's A operand in tensor memory, so shared memory holds only the chunk ring (deeper) and
 // the token ring.
-constexpr int kF4TsRawStages = 16;
+// A TS stage is 128 K values: two prepared chunks per weight tile, copied as one 9216-byte
+// piece (a tile's chunks are consecutive along K), so one stage barrier covers 32K weights.
+constexpr int kF4TsStageK = 2 * kFp4StageK;
+constexpr uint32_t kF4TsRawBytes = 2 * kF4RawBytes;   // two tiles x two chunks
+constexpr int kF4TsRawStages = 8;
 constexpr int kF4TsMaxRows = 64;                  // token rows per unit (MMA N)
-constexpr int kF4TsMaxSlots = 8;                  // weight stages in TMEM (and token slots)
-constexpr size_t kF4TsSmem = 1024 + kF4TokArea + (size_t)kF4TsRawStages * kF4RawBytes +
+constexpr int kF4TsMaxSlots = 4;                  // weight stages in TMEM (and token slots)
+constexpr size_t kF4TsSmem = 1024 + kF4TokArea + (size_t)kF4TsRawStages * kF4TsRawBytes +
                              kF4BarBytes;
 static_assert(kF4TsSmem <= 232448, "shared memory per CTA exceeded");
 static_assert(kF4TsRawStages <= kF4MaxRawStages, "ring sizes");
 // TMEM in this mode: two accumulator buffers of two tiles (acc_stride columns each: the
-// launch's widest token box), then the A ring, 64 columns (two tiles x 64 f16 values) per
-// stage, as many stages as fit: 7 for 16-row boxes, 6 for 32, 4 for 64.
+// launch's widest token box), then the A ring, 128 columns (two tiles x 128 f16 values) per
+// stage, as many stages as fit: 3 for 16- and 32-row boxes, 2 for 64.
 __host__ __device__ constexpr int f4_ts_slots(int acc_stride) {
-  return (kF4TmemCols - 4 * acc_stride) / 64 < kF4TsMaxSlots ? (kF4TmemCols - 4 * acc_stride) / 64
-                                                              : kF4TsMaxSlots;
+  return (kF4TmemCols - 4 * acc_stride) / 128 < kF4TsMaxSlots
+             ? (kF4TmemCols - 4 * acc_stride) / 128
+             : kF4TsMaxSlots;
 }
-static_assert(f4_ts_slots(kF4TsMaxRows) >= 4 && f4_ts_slots(kF4TsMaxRows) * 8 * 1024 <= kF4TokArea,
+static_assert(f4_ts_slots(kF4TsMaxRows) >= 2 &&
+                  f4_ts_slots(16) * 2 * 16 * 128 <= (int)kF4TokArea &&
+                  f4_ts_slots(kF4TsMaxRows) * 2 * kF4TsMaxRows * 128 <= (int)kF4TokArea,
               "TS rings");
 static_assert(kF4RawBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
 static_assert(kF4RawStages <= kF4MaxRawStages && kF4TokArea >= kF4ABytes, "ring sizes");
@@ -275,6 +282,7 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
   // [f16 weight slots 3 x 32 KB, not in TS mode] [token ring 48 KB] [raw ring] [barriers]
   constexpr uint32_t kCvtArea = TS ? 0u : kF4CvtSlots * kF4WBytes;
   constexpr int kRawStages = TS ? kF4TsRawStages : kF4RawStages;
+  constexpr uint32_t kRawBytes = TS ? kF4TsRawBytes : kF4RawBytes;  // one raw ring stage
   // TS: the token ring is the A ring (one stage barrier for both)
   const int kCvtSlots = TS ? f4_ts_slots(maps.acc_stride) : kF4CvtSlots;
   const uint32_t acc_stride = TS ? (uint32_t)maps.acc_stride : 0u;
@@ -286,7 +294,7 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
   const uint32_t tok_base = base + kCvtArea;
   const uint32_t raw_base = tok_base + kF4TokArea;
   uint8_t* raw_ptr = smem + kCvtArea + kF4TokArea;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(raw_ptr + kRawStages * kF4RawBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw_ptr + kRawStages * kRawBytes);
   // bars: raw_full[16] raw_empty[16] cvt_full[8] cvt_empty[8] tfull[2] tempty[2]
   //       unit_full[8] unit_empty[8] tok_full[16] tok_empty[16]; then the TMEM slot, the
   //       abort flag and (at byte 1024) the unit descriptors
@@ -311,11 +319,11 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRawStages; ++s) {
       mbar_init(raw_full(s), 1);
-      mbar_init(raw_empty(s), TS ? kF4CvtWarps / 2 : kF4CvtWarps);
+      mbar_init(raw_empty(s), kF4CvtWarps);
     }
     for (int s = 0; s < kCvtSlots; ++s) {
-      // TS: the stage's converter group and the token tile's expect_tx arrival
-      mbar_init(cvt_full(s), TS ? kF4CvtWarps / 2 + 1 : kF4CvtWarps);
+      // TS: the converters and the token tile's expect_tx arrival
+      mbar_init(cvt_full(s), TS ? kF4CvtWarps + 1 : kF4CvtWarps);
       mbar_init(cvt_empty(s), TS ? chunks : 1);  // TS: one commit per tile's issuer
     }
     for (int s = 0; s < ts; ++s) {
@@ -376,20 +384,21 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
         mbar_arrive(unit_empty(uq.slot));
         uq.next(kF4UnitRing);
         const GemmProblem& P = args.p[w.p];
+        // chunks (64 K values of a 128-row tile) per stage and per tile; TS stages take two
+        constexpr int cps = TS ? 2 : 1;
+        constexpr uint32_t piece = cps * kFp4ChunkBytes;
         const uint8_t* src = static_cast<const uint8_t*>(P.B) +
-                             ((size_t)w.tile * P.k_blocks + w.kb0) * (size_t)kFp4ChunkBytes;
-        const size_t tile_bytes = (size_t)P.k_blocks * kFp4ChunkBytes;  // next tile's chunk
-        for (int kb = w.kb0; kb < w.kb1;
-             ++kb, src += kFp4ChunkBytes, rq.next(kRawStages), ++issued) {
+                             ((size_t)w.tile * P.k_blocks + w.kb0) * (size_t)piece;
+        const size_t tile_bytes = (size_t)P.k_blocks * piece;  // the next tile's chunks
+        for (int kb = w.kb0; kb < w.kb1; ++kb, src += piece, rq.next(kRawStages), ++issued) {
           if (!wait_fast(raw_empty(rq.slot), rq.phase ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(raw_full(rq.slot), chunks * kFp4ChunkBytes);
-          const uint32_t dst = raw_base + rq.slot * kF4RawBytes;
+          mbar_expect_tx(raw_full(rq.slot), chunks * piece);
+          const uint32_t dst = raw_base + rq.slot * kRawBytes;
           for (int c = 0; c < chunks; ++c)
-            bulk_load(dst + c * kFp4ChunkBytes, src + c * tile_bytes, kFp4ChunkBytes,
-                      raw_full(rq.slot), policy);
+            bulk_load(dst + c * piece, src + c * tile_bytes, piece, raw_full(rq.slot), policy);
         }
       }
       // the last copies of each slot land before the CTA can exit
@@ -413,13 +422,17 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
         if constexpr (TS) {
           // the token tile of stage j lands in slot j of the A ring and completes on that
           // stage's barrier, so the MMA issuers wait once per stage
+          // (two boxes of 64 K values per stage, the second acc_stride rows after the first)
           for (int kb = w.kb0; kb < w.kb1; ++kb, tq.next(kCvtSlots), ++issued) {
             if (!wait_fast(cvt_empty(tq.slot), tq.phase ^ 1u, abort_flag, args.status)) {
               ok = false;
               break;
             }
-            mbar_expect_tx(cvt_full(tq.slot), box_bytes);
-            tma_load_2d(x_stage(tq.slot), map, cvt_full(tq.slot), kb * kF4BK, w.mb * kFp4BS);
+            mbar_expect_tx(cvt_full(tq.slot), 2 * box_bytes);
+            tma_load_2d(x_stage(tq.slot), map, cvt_full(tq.slot), kb * kF4TsStageK,
+                        w.mb * kFp4BS);
+            tma_load_2d(x_stage(tq.slot) + acc_stride * 128u, map, cvt_full(tq.slot),
+                        kb * kF4TsStageK + kF4BK, w.mb * kFp4BS);
           }
         } else {
           for (int kb = w.kb0; kb < w.kb1; ++kb, tq.next(ts), ++issued) {
@@ -473,11 +486,16 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
             // K step kk: 32 bytes into the token rows' swizzled 128-byte atoms, 8 columns
             // into the weights' TMEM stage
             const uint64_t b0 = sdesc_sw128(x_stage(cq.slot));
-            const uint32_t a0 = tmem_base + a_col + (uint32_t)cq.slot * 64u + mt * 32u;
+            const uint64_t b1 = sdesc_advance(b0, acc_stride * 128u);  // the second 64 K values
+            const uint32_t a0 = tmem_base + a_col + (uint32_t)cq.slot * 128u + mt * 64u;
             mma_f16_ts(d, a0, b0, idesc, kb == w.kb0 ? 0u : 1u);
             mma_f16_ts(d, a0 + 8, sdesc_advance(b0, 32), idesc, 1u);
             mma_f16_ts(d, a0 + 16, sdesc_advance(b0, 64), idesc, 1u);
             mma_f16_ts(d, a0 + 24, sdesc_advance(b0, 96), idesc, 1u);
+            mma_f16_ts(d, a0 + 32, b1, idesc, 1u);
+            mma_f16_ts(d, a0 + 40, sdesc_advance(b1, 32), idesc, 1u);
+            mma_f16_ts(d, a0 + 48, sdesc_advance(b1, 64), idesc, 1u);
+            mma_f16_ts(d, a0 + 56, sdesc_advance(b1, 96), idesc, 1u);
             mma_commit(cvt_empty(cq.slot));
           }
           if (ok) mma_commit(tfull(buf));
@@ -523,39 +541,35 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
     __syncwarp();
   } else if (TS && warp >= 4 && warp < 4 + kF4CvtWarps) {
     // ------------------------------------------------------------ fp4 -> f16 into TMEM
-    // Two groups of 8 converter warps take alternate stages, so that one group's load ->
-    // convert -> TMEM store chain overlaps the other's. Warp c (0..15) of group c / 8
-    // writes TMEM lane quarter c % 4 (= warp % 4, the quarter a warp may access): weight
-    // row 32 (c % 4) + lane of tile (c / 4) % 2, all 64 values of the stage, i.e. the 32
-    // columns of that tile in the stage's A slot.
+    // Every converter warp takes part in every stage. Warp c (0..15) writes TMEM lane
+    // quarter c % 4 (= warp % 4, the quarter a warp may access): weight row 32 (c % 4) +
+    // lane of tile (c / 4) % 2, the 64 values of the stage's K chunk c / 8 (codes and four
+    // block scales), i.e. 32 columns of that tile in the stage's A slot.
     const int c = warp - 4;
-    const uint32_t grp = (uint32_t)(c >> 3);
-    const int tile = (c >> 2) & 1;
+    const int tile = (c >> 2) & 1, kc = c >> 3;
     const uint32_t rr = (uint32_t)(32 * (c & 3) + lane);
     const bool live = tile < chunks;  // warp-uniform
     const uint32_t lanes = (uint32_t)(32 * (c & 3)) << 16;
-    const uint32_t col0 = a_col + (uint32_t)tile * 32u;
-    const uint32_t rd = (uint32_t)tile * kFp4ChunkBytes + rr * 16u;
-    const uint32_t sd = (uint32_t)tile * kFp4ChunkBytes + 4096u + rr * 4u;
+    const uint32_t col0 = a_col + (uint32_t)tile * 64u + (uint32_t)kc * 32u;
+    const uint32_t chunk = (uint32_t)tile * 2u * kFp4ChunkBytes + (uint32_t)kc * kFp4ChunkBytes;
+    const uint32_t rd = chunk + rr * 16u;
+    const uint32_t sd = chunk + 4096u + rr * 4u;
     RingPos uq{0, 0}, rq{0, 0}, cq{0, 0};
-    uint32_t jc = 0;  // stage counter of the CTA (both groups count every stage)
     bool ok = true;
     for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
       F4Desc w;
       if (!get_unit(uq, w)) break;
       release_unit(uq);
-      for (int kb = w.kb0; kb < w.kb1;
-           ++kb, ++jc, rq.next(kRawStages), cq.next(kCvtSlots)) {
-        if ((jc & 1u) != grp) continue;
+      for (int kb = w.kb0; kb < w.kb1; ++kb, rq.next(kRawStages), cq.next(kCvtSlots)) {
         if (!wait_fast(raw_full(rq.slot), rq.phase, abort_flag, args.status)) {
           ok = false;
           break;
         }
-        const uint32_t src = raw_base + rq.slot * kF4RawBytes;
+        const uint32_t src = raw_base + rq.slot * kRawBytes;
         uint4 q0 = make_uint4(0u, 0u, 0u, 0u), q1 = q0;
         uint32_t scw = 0u;
         if (live) {
-          q0 = lds128(src + rd);            // values 0..31 of the row's stage
+          q0 = lds128(src + rd);            // values 0..31 of the row's chunk
           q1 = lds128(src + rd + 2048u);    // values 32..63
           asm volatile("ld.shared.b32 %0, [%1];" : "=r"(scw) : "r"(src + sd));
         }
@@ -582,7 +596,7 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
             o[4 * i + 2] = o4[2];
             o[4 * i + 3] = o4[3];
           }
-          tmem_st32(tmem_base + lanes + col0 + (uint32_t)cq.slot * 64u, o);
+          tmem_st32(tmem_base + lanes + col0 + (uint32_t)cq.slot * 128u, o);
           tmem_wait_st();
         }
         tc_fence_before();
@@ -849,12 +863,20 @@ cudaError_t launch_gemm_fp4(int kind, const GemmLaunch& L, cudaStream_t stream) 
       if (box > max_box) max_box = box;
     }
   }
-  // row blocks of at most 64 token rows: weights in TMEM on the MMA's M side, tokens on N
-  const bool ts_mode = (16 << max_box) <= kF4TsMaxRows;
+  // row blocks of at most 64 token rows (and K a multiple of the 128-value stage): weights
+  // in TMEM on the MMA's M side, tokens on N
+  GemmLaunch Lts = L;
+  bool ts_mode = (16 << max_box) <= kF4TsMaxRows;
+  for (int p = 0; ts_mode && p < L.num_problems; ++p) {
+    GemmProblem& P = Lts.p[p];
+    if (P.K % kF4TsStageK || P.K / kF4TsStageK < splits_of(L, p)) ts_mode = false;
+    P.k_blocks = P.K / kF4TsStageK;
+  }
   // the token ring: slots of the widest box; in the tokens-on-M mode the A read of the last
-  // slot (16 KB from its start) stays inside the ring's area; in the TS mode it is the A ring
-  maps.tok_slot_bytes = (int)((16u << max_box) * 128);
+  // slot (16 KB from its start) stays inside the ring's area; in the TS mode it is the A
+  // ring, a slot holding the stage's two boxes
   maps.acc_stride = 16 << max_box;
+  maps.tok_slot_bytes = (int)((16u << max_box) * 128) * (ts_mode ? 2 : 1);
   maps.tok_stages = ts_mode ? f4_ts_slots(maps.acc_stride)
                             : (int)((kF4TokArea - kF4ABytes) / (uint32_t)maps.tok_slot_bytes) + 1;
   if (maps.tok_stages > kF4MaxTokStages) maps.tok_stages = kF4MaxTokStages;
@@ -862,8 +884,8 @@ cudaError_t launch_gemm_fp4(int kind, const GemmLaunch& L, cudaStream_t stream) 
   if (units < grid) grid = (int)units;
   if (grid < 1) grid = 1;
   if (ts_mode)
-    return kind == kGemmW13 ? launch_fp4_typed<kGemmW13, true>(maps, L, grid, stream)
-                            : launch_fp4_typed<kGemmW2, true>(maps, L, grid, stream);
+    return kind == kGemmW13 ? launch_fp4_typed<kGemmW13, true>(maps, Lts, grid, stream)
+                            : launch_fp4_typed<kGemmW2, true>(maps, Lts, grid, stream);
   return kind == kGemmW13 ? launch_fp4_typed<kGemmW13, false>(maps, L, grid, stream)
                           : launch_fp4_typed<kGemmW2, false>(maps, L, grid, stream);
 }
