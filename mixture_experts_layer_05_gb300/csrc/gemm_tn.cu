@@ -55,6 +55,16 @@ namespace {
 
 constexpr int kTnBM = 256;                          // tokens per row block (= align block)
 constexpr int kTnStages = 6;
+#ifndef GBMOE_TN_GROUP
+#define GBMOE_TN_GROUP 2
+#endif
+// K blocks per barrier round trip: the producer fills kTnGroup consecutive stage buffers
+// under one full barrier and the MMA issuer releases them with one commit, so the issuing
+// thread's wait + commit (about 150 cycles, which a partial block's short MMAs do not
+// cover) is paid once per kTnGroup K blocks.
+constexpr int kTnGroup = GBMOE_TN_GROUP;
+constexpr int kTnSlots = kTnStages / kTnGroup;     // barrier pairs in use
+static_assert(kTnStages % kTnGroup == 0, "stage groups");
 constexpr int kTnEpiWarps = 8;
 constexpr int kTnThreads = 64 + 32 * kTnEpiWarps;
 constexpr uint32_t kTnTmemCols = 512;
@@ -290,27 +300,31 @@ __global__ void __launch_bounds__(kTnThreads, 1)
           tma_prefetch_l2_2d(tw, kb * kGemmBK, kGated ? w_row + P.up_offset : w_row);
           if (kGated) tma_prefetch_l2_2d(tw, kb * kGemmBK, w_row);
         }
-        for (int kb = 0; kb < P.k_blocks; ++kb, ++it) {
-          const int s = it % kTnStages;
-          const uint32_t ph = (it / kTnStages) & 1u;
-          if (!wait_bounded_cluster(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
+        for (int kb0 = 0; kb0 < P.k_blocks; kb0 += kTnGroup, ++it) {
+          const int q = it % kTnSlots;
+          const uint32_t ph = (it / kTnSlots) & 1u;
+          if (!wait_bounded_cluster(empty_bar(q), ph ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
           }
-          const uint32_t sw = base + s * kTnStageBytes;
-          const uint32_t sx = sw + kTnWRegion;
-          if (leader) mbar_expect_tx(full_bar(s), tx_bytes);
-          const uint32_t fb = leader_full0 + 8u * s;
-          if (kGated) {
-            tma_load_2d_pair(sw, tw, fb, kb * kGemmBK, w_row + P.up_offset);
-            tma_load_2d_pair(sw + 64 * 128, tw, fb, kb * kGemmBK, w_row);
-          } else {
-            tma_load_2d_pair(sw, tw, fb, kb * kGemmBK, w_row);
-          }
-          tma_load_2d_pair(sx, tx, fb, kb * kGemmBK, x_row);
-          if (pf > 0 && kb + pf < P.k_blocks) {
-            tma_prefetch_l2_2d(tw, (kb + pf) * kGemmBK, kGated ? w_row + P.up_offset : w_row);
-            if (kGated) tma_prefetch_l2_2d(tw, (kb + pf) * kGemmBK, w_row);
+          const int nst = P.k_blocks - kb0 < kTnGroup ? P.k_blocks - kb0 : kTnGroup;
+          if (leader) mbar_expect_tx(full_bar(q), (uint32_t)nst * tx_bytes);
+          const uint32_t fb = leader_full0 + 8u * q;
+          for (int j = 0; j < nst; ++j) {
+            const int kb = kb0 + j;
+            const uint32_t sw = base + (q * kTnGroup + j) * kTnStageBytes;
+            const uint32_t sx = sw + kTnWRegion;
+            if (kGated) {
+              tma_load_2d_pair(sw, tw, fb, kb * kGemmBK, w_row + P.up_offset);
+              tma_load_2d_pair(sw + 64 * 128, tw, fb, kb * kGemmBK, w_row);
+            } else {
+              tma_load_2d_pair(sw, tw, fb, kb * kGemmBK, w_row);
+            }
+            tma_load_2d_pair(sx, tx, fb, kb * kGemmBK, x_row);
+            if (pf > 0 && kb + pf < P.k_blocks) {
+              tma_prefetch_l2_2d(tw, (kb + pf) * kGemmBK, kGated ? w_row + P.up_offset : w_row);
+              if (kGated) tma_prefetch_l2_2d(tw, (kb + pf) * kGemmBK, w_row);
+            }
           }
         }
         w = wn;
@@ -335,21 +349,24 @@ __global__ void __launch_bounds__(kTnThreads, 1)
           break;
         tc_fence_after();
         const uint32_t d = tmem_base + acc * kTnAccStride;
-        for (int kb = 0; kb < k_blocks; ++kb, ++it) {
-          const int s = it % kTnStages;
-          const uint32_t ph = (it / kTnStages) & 1u;
-          if (!wait_bounded_cluster(full_bar(s), ph, abort_flag, args.status)) {
+        for (int kb0 = 0; kb0 < k_blocks; kb0 += kTnGroup, ++it) {
+          const int q = it % kTnSlots;
+          const uint32_t ph = (it / kTnSlots) & 1u;
+          if (!wait_bounded_cluster(full_bar(q), ph, abort_flag, args.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sw = base + s * kTnStageBytes;
-          const uint64_t dw = sdesc_sw128(sw), dx = sdesc_sw128(sw + kTnWRegion);
+          const int nst = k_blocks - kb0 < kTnGroup ? k_blocks - kb0 : kTnGroup;
+          for (int j = 0; j < nst; ++j) {
+            const uint32_t sw = base + (q * kTnGroup + j) * kTnStageBytes;
+            const uint64_t dw = sdesc_sw128(sw), dx = sdesc_sw128(sw + kTnWRegion);
 #pragma unroll
-          for (int kk = 0; kk < kGemmBK / 16; ++kk)
-            mma_bf16_pair(d, sdesc_advance(dw, kk * 32), sdesc_advance(dx, kk * 32), idesc,
-                          (kb > 0 || kk != 0) ? 1u : 0u);
-          mma_commit_pair(empty_bar(s));
+            for (int kk = 0; kk < kGemmBK / 16; ++kk)
+              mma_bf16_pair(d, sdesc_advance(dw, kk * 32), sdesc_advance(dx, kk * 32), idesc,
+                            (kb0 + j > 0 || kk != 0) ? 1u : 0u);
+          }
+          mma_commit_pair(empty_bar(q));
         }
         if (!ok) break;
         mma_commit_pair(tfull_bar(acc));
