@@ -14,40 +14,48 @@
 // of 64 values one contiguous 4608-byte chunk, the packed codes of the stage's two K halves
 // (16 bytes per row each) then the rows' four scale bytes. A unit is a row block of up to
 // 128 token rows against 256 weight rows (128 when the weight rows do not split into 256s)
-// over a K range. Tokens-on-M mode (row blocks of more than 64 rows), per 64-value K stage:
+// over a K range. Two modes:
+//
+// Weights-in-TMEM mode (TS; every launch whose K is a multiple of 128): the tensor core's
+// time per MMA follows N, not M (M 128 x K 16 costs about 45 cycles at N <= 64, 64 at 128
+// and 128 at N = 256, the same for M = 64), so the unit's tokens go on N and the expanded
+// weights are the A operand, written by the converters straight into tensor memory
+// (tcgen05.st) instead of a shared-memory f16 tile that the MMA reads back: shared memory
+// carries only the chunk copies and the token tiles. A stage is 128 K values. Roles:
+//
+//   warp 0       bulk copies (one 9216-byte piece per weight tile and stage) into an 8-deep
+//                raw ring
+//   warp 2       the stage's two token boxes into slot (stage mod S) of the token ring,
+//                completing on that stage's barrier (S = the TMEM A ring's stages)
+//   warps 1, 24  one MMA issuer per 128-row weight tile: M 128 (weights, A in TMEM) x N
+//                (the unit's token rows rounded to 16) x K 16, 8 per stage, one stage
+//                barrier wait and one commit per stage each
+//   warps 4..19  every stage, warp c expands weight row 32 (c % 4) + lane of tile
+//                (c / 4) % 2, K chunk c / 8 (64 values: codes and four block scales) into
+//                32 TMEM columns of the stage's A slot (its warp's lane quarter)
+//   warps 20..23 epilogue: TMEM lane = output column, TMEM column = token row
+//
+// TMEM holds two accumulator buffers (alternate units) when the launch's widest token box
+// is at most 64 rows; for 128-row boxes one buffer, so a unit's MMAs wait for the previous
+// unit's epilogue. (Releasing the buffer's two tiles one at a time, each to its own issuer,
+// measured 1-3 % slower.)
+//
+// Tokens-on-M mode (K not a multiple of 128), per 64-value K stage:
 //
 //   warp 0       bulk copies of the stage's two prepared chunks into an 8-deep raw ring
 //   warp 1       TMEM (two 256-column accumulators) and the MMAs (tokens on M: 128, or 64
 //                for row blocks of at most 64 real rows; weights on N 256; K 16)
 //   warp 2       TMA of the token tile (16 / 32 / 64 / 128 rows) into a dense token ring
-//   warp 3       the unit scheduler: reads each unit's metadata from global memory ahead
-//                of time and publishes it in shared memory
+//   warp 3       the unit scheduler (both modes): reads each unit's metadata from global
+//                memory ahead of time and publishes it in shared memory
 //   warps 4..19  converters: every stage, thread t expands weight row t % 256, K half
 //                t / 256 (hardware e2m1x2 and e4m3x2 conversions and one packed multiply
 //                per pair) into the 128-byte-swizzled K-major f16 layout the MMA reads
 //   warps 20..23 epilogue: TMEM lane quarter warp & 3, one token row per thread
 //
-// The token ring is dense: a 16-row tile takes 2 KB, and the MMA's 128-row A operand
-// starting at a slot reads the following slots as its (discarded) rows 16..127, so the
-// ring's tail is padded to keep that read inside the ring.
-//
-// Weights-in-TMEM mode (TS; launches whose row blocks hold at most 64 token rows, i.e. the
-// decode batches): the tensor core's time per MMA follows N, not M (M 128 x K 16 costs
-// about 45 cycles at N <= 64 and 128 at N = 256, the same for M = 64), so the few tokens go
-// on N and the expanded weights are the A operand, written by the converters straight into
-// tensor memory (tcgen05.st) instead of a shared-memory f16 tile that the MMA reads back:
-// shared memory then carries only the chunk copies and the token tiles. Roles:
-//
-//   warp 0       bulk copies into a 16-deep raw ring
-//   warp 2       the token tile of each stage into slot (stage mod S) of the token ring,
-//                completing on that stage's barrier (S = the A ring's stages)
-//   warps 1, 24  one MMA issuer per 128-row weight tile: M 128 (weights, A in TMEM) x N
-//                (the unit's token rows rounded to 16) x K 16, 4 per stage, one stage
-//                barrier wait and one commit per stage each
-//   warps 4..19  two groups of 8 on alternate stages: a thread expands one weight row's 64
-//                values of the stage (codes + four block scales) into the 32 TMEM columns
-//                of its tile in the stage's A slot (its warp's lane quarter)
-//   warps 20..23 epilogue: TMEM lane = output column, TMEM column = token row
+// The token ring of this mode is dense: a 16-row tile takes 2 KB, and the MMA's 128-row A
+// operand starting at a slot reads the following slots as its (discarded) rows 16..127, so
+// the ring's tail is padded to keep that read inside the ring.
 //
 // Every wait is bounded (kWaitTimeoutNs).
 #include "fp4.cuh"
@@ -94,23 +102,30 @@ static_assert(kF4Smem <= 232448, "shared memory per CTA exceeded");
 constexpr int kF4TsStageK = 2 * kFp4StageK;
 constexpr uint32_t kF4TsRawBytes = 2 * kF4RawBytes;   // two tiles x two chunks
 constexpr int kF4TsRawStages = 8;
-constexpr int kF4TsMaxRows = 64;                  // token rows per unit (MMA N)
+constexpr int kF4TsMaxRows = 128;                 // token rows per unit (MMA N)
 constexpr int kF4TsMaxSlots = 4;                  // weight stages in TMEM (and token slots)
-constexpr size_t kF4TsSmem = 1024 + kF4TokArea + (size_t)kF4TsRawStages * kF4TsRawBytes +
+constexpr uint32_t kF4TsTokArea = 64 * 1024;      // token ring: up to 2 stages of 2 x 16 KB
+constexpr size_t kF4TsSmem = 1024 + kF4TsTokArea + (size_t)kF4TsRawStages * kF4TsRawBytes +
                              kF4BarBytes;
 static_assert(kF4TsSmem <= 232448, "shared memory per CTA exceeded");
 static_assert(kF4TsRawStages <= kF4MaxRawStages, "ring sizes");
-// TMEM in this mode: two accumulator buffers of two tiles (acc_stride columns each: the
-// launch's widest token box), then the A ring, 128 columns (two tiles x 128 f16 values) per
-// stage, as many stages as fit: 3 for 16- and 32-row boxes, 2 for 64.
+// TMEM in this mode: the accumulators (two tiles of acc_stride columns each: the launch's
+// widest token box; two such buffers up to 64-row boxes, one for 128), then the A ring, 128
+// columns (two tiles x 128 f16 values) per stage, as many stages as fit: 3 for 16- and
+// 32-row boxes, 2 for 64 and 128.
+__host__ __device__ constexpr int f4_ts_bufs(int acc_stride) { return acc_stride >= 128 ? 1 : 2; }
+__host__ __device__ constexpr int f4_ts_acc_cols(int acc_stride) {
+  return 2 * f4_ts_bufs(acc_stride) * acc_stride;
+}
 __host__ __device__ constexpr int f4_ts_slots(int acc_stride) {
-  return (kF4TmemCols - 4 * acc_stride) / 128 < kF4TsMaxSlots
-             ? (kF4TmemCols - 4 * acc_stride) / 128
+  return ((int)kF4TmemCols - f4_ts_acc_cols(acc_stride)) / 128 < kF4TsMaxSlots
+             ? ((int)kF4TmemCols - f4_ts_acc_cols(acc_stride)) / 128
              : kF4TsMaxSlots;
 }
-static_assert(f4_ts_slots(kF4TsMaxRows) >= 2 &&
-                  f4_ts_slots(16) * 2 * 16 * 128 <= (int)kF4TokArea &&
-                  f4_ts_slots(kF4TsMaxRows) * 2 * kF4TsMaxRows * 128 <= (int)kF4TokArea,
+static_assert(f4_ts_slots(kF4TsMaxRows) >= 2 && f4_ts_slots(64) >= 2 &&
+                  f4_ts_slots(16) * 2 * 16 * 128 <= (int)kF4TsTokArea &&
+                  f4_ts_slots(64) * 2 * 64 * 128 <= (int)kF4TsTokArea &&
+                  f4_ts_slots(kF4TsMaxRows) * 2 * kF4TsMaxRows * 128 <= (int)kF4TsTokArea,
               "TS rings");
 static_assert(kF4RawBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
 static_assert(kF4RawStages <= kF4MaxRawStages && kF4TokArea >= kF4ABytes, "ring sizes");
@@ -286,14 +301,16 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
   // TS: the token ring is the A ring (one stage barrier for both)
   const int kCvtSlots = TS ? f4_ts_slots(maps.acc_stride) : kF4CvtSlots;
   const uint32_t acc_stride = TS ? (uint32_t)maps.acc_stride : 0u;
-  const uint32_t a_col = 4u * acc_stride;          // TS: first A ring column
+  const int nbuf = TS ? f4_ts_bufs(maps.acc_stride) : 2;          // accumulator buffers
+  const uint32_t a_col = TS ? (uint32_t)f4_ts_acc_cols(maps.acc_stride) : 0u;  // A ring
+  constexpr uint32_t kTokArea = TS ? kF4TsTokArea : kF4TokArea;
   const int ts = maps.tok_stages;
   const uint32_t tsb = (uint32_t)maps.tok_slot_bytes;
   const int un = maps.un;
   const int chunks = un / kF4TileRows;             // prepared chunks per stage: 1 or 2
   const uint32_t tok_base = base + kCvtArea;
-  const uint32_t raw_base = tok_base + kF4TokArea;
-  uint8_t* raw_ptr = smem + kCvtArea + kF4TokArea;
+  const uint32_t raw_base = tok_base + kTokArea;
+  uint8_t* raw_ptr = smem + kCvtArea + kTokArea;
   uint64_t* bars = reinterpret_cast<uint64_t*>(raw_ptr + kRawStages * kRawBytes);
   // bars: raw_full[16] raw_empty[16] cvt_full[8] cvt_empty[8] tfull[2] tempty[2]
   //       unit_full[8] unit_empty[8] tok_full[16] tok_empty[16]; then the TMEM slot, the
@@ -331,7 +348,7 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
       mbar_init(tok_empty(s), TS ? chunks : 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(tfull(b), TS ? chunks : 1);
+      mbar_init(tfull(b), TS ? chunks : 1);  // TS: both tiles' issuers commit
       mbar_init(tempty(b), kF4EpiWarps);
     }
     for (int i = 0; i < kF4UnitRing; ++i) {
@@ -470,12 +487,15 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
         uq.next(kF4UnitRing);
         const int buf = uc & 1;
         if constexpr (TS) {
-          // weights on M (128 rows per tile, A in TMEM), the unit's tokens on N
-          const uint32_t idesc = idesc_f16(kF4M, w.n);
-          if (!wait_fast(tempty(buf), ((uc >> 1) & 1u) ^ 1u, abort_flag, args.status)) break;
-          tc_fence_after();
+          // weights on M (128 rows per tile, A in TMEM), the unit's tokens on N; with one
+          // accumulator buffer every unit waits for the previous unit's epilogue
           if (mt >= chunks) continue;  // no second tile: this issuer only follows the units
-          const uint32_t d = tmem_base + (uint32_t)buf * 2u * acc_stride + (uint32_t)mt * acc_stride;
+          const uint32_t idesc = idesc_f16(kF4M, w.n);
+          const int tb = nbuf == 2 ? buf : 0;
+          const uint32_t tph = nbuf == 2 ? ((uc >> 1) & 1u) : (uc & 1u);
+          if (!wait_fast(tempty(tb), tph ^ 1u, abort_flag, args.status)) break;
+          tc_fence_after();
+          const uint32_t d = tmem_base + (uint32_t)tb * 2u * acc_stride + (uint32_t)mt * acc_stride;
           for (int kb = w.kb0; kb < w.kb1; ++kb, cq.next(kCvtSlots)) {
             // the stage barrier: the group's weights in TMEM and the token tile in its slot
             if (!wait_fast(cvt_full(cq.slot), cq.phase, abort_flag, args.status)) {
@@ -498,7 +518,7 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
             mma_f16_ts(d, a0 + 56, sdesc_advance(b1, 96), idesc, 1u);
             mma_commit(cvt_empty(cq.slot));
           }
-          if (ok) mma_commit(tfull(buf));
+          if (ok) mma_commit(tfull(tb));
           continue;
         }
         // row blocks of at most 64 real rows run M = 64 MMAs (fewer discarded rows in TMEM)
@@ -607,8 +627,8 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
   } else if (TS && warp >= 4 + kF4CvtWarps && warp < 4 + kF4CvtWarps + kF4EpiWarps) {
     // ------------------------------------------------------------ epilogue (TS)
     // D of tile t: TMEM lane = weight row (this warp's quarter), column j = the unit's token
-    // row j. Lane j resolves token rows j and j + 32 to an output row and a scale; every
-    // column is then one coalesced 128-byte store per warp.
+    // row j. Lane l resolves token rows l, l + 32, l + 64, l + 96 to an output row and a
+    // scale; every column is then one coalesced 128-byte store per warp.
     const int quarter = warp & 3;
     RingPos uq{0, 0};
     uint32_t uc = 0;
@@ -617,11 +637,12 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
       if (!get_unit(uq, w)) break;
       release_unit(uq);
       const GemmProblem& P = args.p[w.p];
-      const int buf = uc & 1;
-      float* rowp[2] = {nullptr, nullptr};
-      float rows_scale[2] = {0.f, 0.f};
+      const int tb = nbuf == 2 ? (int)(uc & 1u) : 0;   // accumulator buffer
+      const uint32_t tph = nbuf == 2 ? ((uc >> 1) & 1u) : (uc & 1u);
+      float* rowp[4] = {nullptr, nullptr, nullptr, nullptr};
+      float rows_scale[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const int m = lane + 32 * i;
         if (m >= w.rows) continue;
         const int mr = w.mb * kFp4BS + m;
@@ -651,32 +672,36 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
         rowp[i] = out + (size_t)w.nt * un;
         rows_scale[i] = scale;
       }
-      if (!wait_fast(tfull(buf), (uc >> 1) & 1u, abort_flag, args.status)) break;
+      if (!wait_fast(tfull(tb), tph, abort_flag, args.status)) break;
       tc_fence_after();
       for (int t = 0; t < chunks; ++t) {
         const int col = t * kF4TileRows + 32 * quarter + lane;  // this lane's output column
         for (int c0 = 0; c0 < w.n; c0 += 16) {
           uint32_t v[16];
           tmem_ld16(tmem_base + ((uint32_t)(quarter * 32) << 16) +
-                        (uint32_t)buf * 2u * acc_stride + (uint32_t)t * acc_stride + (uint32_t)c0,
+                        (uint32_t)tb * 2u * acc_stride + (uint32_t)t * acc_stride + (uint32_t)c0,
                     v);
           tmem_wait_ld16(v);
+          // the 32-row group of columns c0 .. c0 + 15 (warp-uniform)
+          const int g = c0 >> 5;
+          float* const gp = g == 0 ? rowp[0] : g == 1 ? rowp[1] : g == 2 ? rowp[2] : rowp[3];
+          const float gs = g == 0 ? rows_scale[0]
+                           : g == 1 ? rows_scale[1]
+                           : g == 2 ? rows_scale[2] : rows_scale[3];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int j = c0 + i;  // token row of the unit (warp-uniform)
             if (j >= w.rows) break;
-            const bool hi = j >= 32;
-            float* const op = reinterpret_cast<float*>(__shfl_sync(
-                0xffffffffu, reinterpret_cast<unsigned long long>(hi ? rowp[1] : rowp[0]),
-                j & 31));
-            const float sc = __shfl_sync(0xffffffffu, hi ? rows_scale[1] : rows_scale[0], j & 31);
+            float* const op = reinterpret_cast<float*>(
+                __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(gp), j & 31));
+            const float sc = __shfl_sync(0xffffffffu, gs, j & 31);
             if (op) op[col] = sc * __uint_as_float(v[i]);
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty(buf));
+      if (lane == 0) mbar_arrive(tempty(tb));
     }
   } else if (warp >= 4 && warp < 4 + kF4CvtWarps) {
     // ------------------------------------------------------------ fp4 -> f16 expansion
@@ -863,8 +888,8 @@ cudaError_t launch_gemm_fp4(int kind, const GemmLaunch& L, cudaStream_t stream) 
       if (box > max_box) max_box = box;
     }
   }
-  // row blocks of at most 64 token rows (and K a multiple of the 128-value stage): weights
-  // in TMEM on the MMA's M side, tokens on N
+  // K a multiple of the 128-value stage (and split-K ranges of whole stages): weights in
+  // TMEM on the MMA's M side, tokens on N
   GemmLaunch Lts = L;
   bool ts_mode = (16 << max_box) <= kF4TsMaxRows;
   for (int p = 0; ts_mode && p < L.num_problems; ++p) {
@@ -879,6 +904,8 @@ cudaError_t launch_gemm_fp4(int kind, const GemmLaunch& L, cudaStream_t stream) 
   maps.tok_slot_bytes = (int)((16u << max_box) * 128) * (ts_mode ? 2 : 1);
   maps.tok_stages = ts_mode ? f4_ts_slots(maps.acc_stride)
                             : (int)((kF4TokArea - kF4ABytes) / (uint32_t)maps.tok_slot_bytes) + 1;
+  if (ts_mode && maps.tok_stages * maps.tok_slot_bytes > (int)kF4TsTokArea)
+    return cudaErrorInvalidValue;
   if (maps.tok_stages > kF4MaxTokStages) maps.tok_stages = kF4MaxTokStages;
   int grid = num_sms();
   if (units < grid) grid = (int)units;
