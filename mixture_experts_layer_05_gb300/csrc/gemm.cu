@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sa, ta, full_bar(s), kb * kGemmBK, a_row);
             continue;
           }
-          if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
+          if (!wait_fast(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
           }
@@ -239,13 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit w = sched.unit(args, u);
         const int acc = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
-        if (!wait_bounded(tempty_bar(acc), (use & 1u) ^ 1u, abort_flag, args.status)) break;
+        if (!wait_fast(tempty_bar(acc), (use & 1u) ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + acc * kAccStride;
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
-          if (!wait_bounded(full_bar(s), ph, abort_flag, args.status)) {
+          if (!wait_fast(full_bar(s), ph, abort_flag, args.status)) {
             ok = false;
             break;
           }
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const GemmProblem& P = args.p[w.p];
       const int acc = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
-      if (!wait_bounded(tfull_bar(acc), use & 1u, abort_flag, args.status)) break;
+      if (!wait_fast(tfull_bar(acc), use & 1u, abort_flag, args.status)) break;
       tc_fence_after();
       const bool split = splits_of(args, w.p) > 1;
       const int m = w.mb * kGemmBM + row;
