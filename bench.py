@@ -516,9 +516,8 @@ def run_ours(args, w, T):
     # which w13 kernel the forward runs: the token-N CTA-pair GEMM when its blocks are 256
     tn = quant == "none" and binding.moe_forward_block_size(cfg, T) == 256
     kname = ("gemm_fp8_kernel<w13> (grouped e4m3 w13 GEMM + SiLU*mul + act quant)" if fp8
-             else ("gemm_fp4_kernel<w13> (grouped nvfp4 w13 GEMM, fp4 -> f16 into tensor "
-                   "memory, weights on M)" if T <= 64 else
-                   "gemm_fp4_kernel<w13> (grouped nvfp4 w13 GEMM, fp4 -> f16 in shared memory)")
+             else "gemm_fp4_kernel<w13> (grouped nvfp4 w13 GEMM, fp4 -> f16 into tensor memory, "
+                  "weights on M)"
              if quant == "nvfp4"
              else "gemm_tn_kernel<w13> (grouped w13 GEMM + SiLU*mul, tokens on N, CTA pairs)"
              if tn else "gemm_kernel<w13> (grouped w13 GEMM + SiLU*mul)")

@@ -14,50 +14,34 @@
 // of 64 values one contiguous 4608-byte chunk, the packed codes of the stage's two K halves
 // (16 bytes per row each) then the rows' four scale bytes. A unit is a row block of up to
 // 128 token rows against 256 weight rows (128 when the weight rows do not split into 256s)
-// over a K range. Two modes:
+// over a K range of whole 128-value stages.
 //
-// Weights-in-TMEM mode (TS; every launch whose K is a multiple of 128): the tensor core's
-// time per MMA follows N, not M (M 128 x K 16 costs about 45 cycles at N <= 64, 64 at 128
-// and 128 at N = 256, the same for M = 64), so the unit's tokens go on N and the expanded
-// weights are the A operand, written by the converters straight into tensor memory
-// (tcgen05.st) instead of a shared-memory f16 tile that the MMA reads back: shared memory
-// carries only the chunk copies and the token tiles. A stage is 128 K values. Roles:
+// The tensor core's time per MMA follows N, not M (M 128 x K 16 costs about 45 cycles at
+// N = 16 or 32, 48 at 64, 64 at 128 and 128 at N = 256, the same for M = 64), so the unit's tokens go on N
+// and the expanded weights are the A operand (M 128 per weight tile), written by the
+// converters straight into tensor memory (tcgen05.st): no f16 weight tile round-trips
+// through shared memory, which carries only the chunk copies and the token tiles. Roles:
 //
-//   warp 0       bulk copies (one 9216-byte piece per weight tile and stage) into an 8-deep
-//                raw ring
-//   warp 2       the stage's two token boxes into slot (stage mod S) of the token ring,
-//                completing on that stage's barrier (S = the TMEM A ring's stages)
+//   warp 0       bulk copies (one 9216-byte piece per weight tile and stage: the tile's two
+//                chunks are consecutive along K) into an 8-deep raw ring
+//   warp 2       the stage's two token boxes (16 / 32 / 64 / 128 rows x 64 values) into slot
+//                (stage mod S) of the token ring, completing on that stage's barrier (S =
+//                the TMEM A ring's stages)
+//   warp 3       the unit scheduler: reads each unit's metadata from global memory ahead
+//                of time and publishes it in shared memory
 //   warps 1, 24  one MMA issuer per 128-row weight tile: M 128 (weights, A in TMEM) x N
 //                (the unit's token rows rounded to 16) x K 16, 8 per stage, one stage
 //                barrier wait and one commit per stage each
 //   warps 4..19  every stage, warp c expands weight row 32 (c % 4) + lane of tile
-//                (c / 4) % 2, K chunk c / 8 (64 values: codes and four block scales) into
-//                32 TMEM columns of the stage's A slot (its warp's lane quarter)
+//                (c / 4) % 2, K chunk c / 8 (64 values: codes and four block scales, one
+//                hardware e2m1x2 conversion and one packed multiply per pair) into 32 TMEM
+//                columns of the stage's A slot (its warp's lane quarter)
 //   warps 20..23 epilogue: TMEM lane = output column, TMEM column = token row
 //
 // TMEM holds two accumulator buffers (alternate units) when the launch's widest token box
 // is at most 64 rows; for 128-row boxes one buffer, so a unit's MMAs wait for the previous
 // unit's epilogue. (Releasing the buffer's two tiles one at a time, each to its own issuer,
-// measured 1-3 % slower.)
-//
-// Tokens-on-M mode (K not a multiple of 128), per 64-value K stage:
-//
-//   warp 0       bulk copies of the stage's two prepared chunks into an 8-deep raw ring
-//   warp 1       TMEM (two 256-column accumulators) and the MMAs (tokens on M: 128, or 64
-//                for row blocks of at most 64 real rows; weights on N 256; K 16)
-//   warp 2       TMA of the token tile (16 / 32 / 64 / 128 rows) into a dense token ring
-//   warp 3       the unit scheduler (both modes): reads each unit's metadata from global
-//                memory ahead of time and publishes it in shared memory
-//   warps 4..19  converters: every stage, thread t expands weight row t % 256, K half
-//                t / 256 (hardware e2m1x2 and e4m3x2 conversions and one packed multiply
-//                per pair) into the 128-byte-swizzled K-major f16 layout the MMA reads
-//   warps 20..23 epilogue: TMEM lane quarter warp & 3, one token row per thread
-//
-// The token ring of this mode is dense: a 16-row tile takes 2 KB, and the MMA's 128-row A
-// operand starting at a slot reads the following slots as its (discarded) rows 16..127, so
-// the ring's tail is padded to keep that read inside the ring.
-//
-// Every wait is bounded (kWaitTimeoutNs).
+// measured 1-3 % slower.) Every wait is bounded (kWaitTimeoutNs).
 #include "fp4.cuh"
 #include "tc.cuh"
 
@@ -65,77 +49,55 @@ namespace gbmoe {
 namespace {
 
 constexpr int kF4TileRows = 128;                  // rows of a prepared tile
-constexpr int kF4MaxN = 256;                      // weight rows per unit (MMA N)
-constexpr int kF4M = 128;                         // token rows per unit (MMA M)
-constexpr int kF4BK = kFp4StageK;                 // K values per stage (one 128-byte atom)
-constexpr uint32_t kF4RawBytes = 2 * kFp4ChunkBytes;  // the stage's prepared chunks
-#ifndef GBMOE_F4_RAW_STAGES
-#define GBMOE_F4_RAW_STAGES 8
-#endif
-constexpr int kF4RawStages = GBMOE_F4_RAW_STAGES;
-constexpr int kF4MaxRawStages = 16;
-constexpr int kF4CvtSlots = 3;                    // f16 weight stages
-constexpr uint32_t kF4WBytes = kF4MaxN * 128;     // f16 weights of a stage: 32 KB
-constexpr uint32_t kF4ABytes = kF4M * 128;        // the MMA's A operand: 128 rows, 16 KB
-// token ring + the tail the last slot's 16 KB A read may cover
-constexpr uint32_t kF4TokArea = 48 * 1024;
-constexpr int kF4MaxTokStages = 16;
+constexpr int kF4MaxN = 256;                      // weight rows per unit
+constexpr int kF4M = 128;                         // weight rows per MMA (M)
+constexpr int kF4BK = kFp4StageK;                 // K values per prepared chunk and token box
+constexpr int kF4StageK = 2 * kFp4StageK;         // K values per stage
+constexpr uint32_t kF4Piece = 2 * kFp4ChunkBytes; // a tile's chunks of one stage
+constexpr uint32_t kF4RawBytes = 2 * kF4Piece;    // two tiles
+constexpr int kF4RawStages = 8;
+constexpr int kF4MaxRows = 128;                   // token rows per unit (MMA N)
+constexpr int kF4MaxSlots = 4;                    // weight stages in TMEM (and token slots)
+constexpr uint32_t kF4TokArea = 64 * 1024;        // token ring: up to 2 stages of 2 x 16 KB
 constexpr int kF4CvtWarps = 16;
 constexpr int kF4EpiWarps = 4;
-constexpr int kF4Threads = 32 * (4 + kF4CvtWarps + kF4EpiWarps);
-constexpr int kF4TsThreads = kF4Threads + 32;     // TS: a second MMA-issuing warp (24)
-constexpr uint32_t kF4TmemCols = 512;             // two 256-column accumulators
+constexpr int kF4Threads = 32 * (5 + kF4CvtWarps + kF4EpiWarps);  // + the second issuer
+constexpr int kF4Issuer2 = 4 + kF4CvtWarps + kF4EpiWarps;         // its warp (24)
+constexpr uint32_t kF4TmemCols = 512;
 constexpr int kF4Boxes = 4;                       // token boxes of 16, 32, 64, 128 rows
 constexpr int kF4UnitRing = 8;                    // unit descriptors the scheduler runs ahead
-// arrivals that free a descriptor: the two producers, the MMA issuer, every converter warp
-// and every epilogue warp
-constexpr int kF4UnitReaders = 3 + kF4CvtWarps + kF4EpiWarps;
+// arrivals that free a descriptor: the two producers, the two MMA issuers, every converter
+// warp and every epilogue warp
+constexpr int kF4UnitReaders = 4 + kF4CvtWarps + kF4EpiWarps;
 constexpr uint32_t kF4BarBytes = 2048;
-constexpr size_t kF4Smem = 1024 + (size_t)kF4CvtSlots * kF4WBytes + kF4TokArea +
-                           (size_t)kF4RawStages * kF4RawBytes + kF4BarBytes;
+constexpr size_t kF4Smem = 1024 + kF4TokArea + (size_t)kF4RawStages * kF4RawBytes + kF4BarBytes;
 static_assert(kF4Smem <= 232448, "shared memory per CTA exceeded");
-// Weights-in-TMEM mode (row blocks of at most 64 real rows): the expanded weights are the
-// MMA's A operand in tensor memory, so shared memory holds only the chunk ring (deeper) and
-// the token ring.
-// A TS stage is 128 K values: two prepared chunks per weight tile, copied as one 9216-byte
-// piece (a tile's chunks are consecutive along K), so one stage barrier covers 32K weights.
-constexpr int kF4TsStageK = 2 * kFp4StageK;
-constexpr uint32_t kF4TsRawBytes = 2 * kF4RawBytes;   // two tiles x two chunks
-constexpr int kF4TsRawStages = 8;
-constexpr int kF4TsMaxRows = 128;                 // token rows per unit (MMA N)
-constexpr int kF4TsMaxSlots = 4;                  // weight stages in TMEM (and token slots)
-constexpr uint32_t kF4TsTokArea = 64 * 1024;      // token ring: up to 2 stages of 2 x 16 KB
-constexpr size_t kF4TsSmem = 1024 + kF4TsTokArea + (size_t)kF4TsRawStages * kF4TsRawBytes +
-                             kF4BarBytes;
-static_assert(kF4TsSmem <= 232448, "shared memory per CTA exceeded");
-static_assert(kF4TsRawStages <= kF4MaxRawStages, "ring sizes");
-// TMEM in this mode: the accumulators (two tiles of acc_stride columns each: the launch's
-// widest token box; two such buffers up to 64-row boxes, one for 128), then the A ring, 128
-// columns (two tiles x 128 f16 values) per stage, as many stages as fit: 3 for 16- and
-// 32-row boxes, 2 for 64 and 128.
-__host__ __device__ constexpr int f4_ts_bufs(int acc_stride) { return acc_stride >= 128 ? 1 : 2; }
-__host__ __device__ constexpr int f4_ts_acc_cols(int acc_stride) {
-  return 2 * f4_ts_bufs(acc_stride) * acc_stride;
+static_assert(kF4Piece % 16 == 0, "bulk copies move multiples of 16 bytes");
+// TMEM: the accumulators (two tiles of acc_stride columns each: the launch's widest token
+// box; two such buffers up to 64-row boxes, one for 128), then the A ring, 128 columns (two
+// tiles x 128 f16 values) per stage, as many stages as fit: 3 for 16- and 32-row boxes, 2
+// for 64 and 128.
+__host__ __device__ constexpr int f4_bufs(int acc_stride) { return acc_stride >= 128 ? 1 : 2; }
+__host__ __device__ constexpr int f4_acc_cols(int acc_stride) {
+  return 2 * f4_bufs(acc_stride) * acc_stride;
 }
-__host__ __device__ constexpr int f4_ts_slots(int acc_stride) {
-  return ((int)kF4TmemCols - f4_ts_acc_cols(acc_stride)) / 128 < kF4TsMaxSlots
-             ? ((int)kF4TmemCols - f4_ts_acc_cols(acc_stride)) / 128
-             : kF4TsMaxSlots;
+__host__ __device__ constexpr int f4_slots(int acc_stride) {
+  return ((int)kF4TmemCols - f4_acc_cols(acc_stride)) / 128 < kF4MaxSlots
+             ? ((int)kF4TmemCols - f4_acc_cols(acc_stride)) / 128
+             : kF4MaxSlots;
 }
-static_assert(f4_ts_slots(kF4TsMaxRows) >= 2 && f4_ts_slots(64) >= 2 &&
-                  f4_ts_slots(16) * 2 * 16 * 128 <= (int)kF4TsTokArea &&
-                  f4_ts_slots(64) * 2 * 64 * 128 <= (int)kF4TsTokArea &&
-                  f4_ts_slots(kF4TsMaxRows) * 2 * kF4TsMaxRows * 128 <= (int)kF4TsTokArea,
-              "TS rings");
-static_assert(kF4RawBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
-static_assert(kF4RawStages <= kF4MaxRawStages && kF4TokArea >= kF4ABytes, "ring sizes");
+static_assert(f4_slots(kF4MaxRows) >= 2 && f4_slots(64) >= 2 &&
+                  f4_slots(16) * 2 * 16 * 128 <= (int)kF4TokArea &&
+                  f4_slots(64) * 2 * 64 * 128 <= (int)kF4TokArea &&
+                  f4_slots(kF4MaxRows) * 2 * kF4MaxRows * 128 <= (int)kF4TokArea,
+              "rings");
 
 struct F4Maps {
   CUtensorMap x[2][kF4Boxes];  // per problem: f16 token rows, box 64 values x (16 << i) rows
-  int tok_stages;              // token ring stages (<= kF4MaxTokStages)
-  int tok_slot_bytes;          // the widest token box of the launch (a multiple of 1024)
+  int slots;                   // stages of the TMEM A ring and of the token ring
+  int tok_slot_bytes;          // two boxes of the launch's widest box (a multiple of 2048)
   int un;                      // weight rows per unit: 256, or 128
-  int acc_stride;              // TS: TMEM columns per accumulator tile (the widest box rows)
+  int acc_stride;              // TMEM columns per accumulator tile (the widest box's rows)
 };
 
 // Instruction descriptor of kind::f16 with f16 A and B (format code 0), fp32 D, K-major.
@@ -159,9 +121,9 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
                : "r"(a));
   return v;
 }
-__device__ __forceinline__ uint32_t lds16(uint32_t a) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
 
@@ -191,10 +153,6 @@ __device__ __forceinline__ void e2m1x8_scaled(uint32_t w, uint32_t sc, uint32_t 
       "mul.rn.f16x2 %3, h3, %5;\n\t}"
       : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
       : "r"(w), "r"(sc));
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit TMEM columns from registers (this warp's lane quarter).
@@ -233,8 +191,8 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 // A unit as the scheduler warp publishes it in shared memory: the unit, its real token
-// rows, its MMA-side row count and token box, its expert's first weight tile, the output
-// scale.
+// rows, its MMA N (rows rounded up to 16) and token box, its expert's first weight tile, the
+// output scale.
 struct F4Desc {
   int p, split, mb, nt, kb0, kb1, rows, n, box, tile;
   float alpha;
@@ -287,73 +245,58 @@ struct RingPos {
   }
 };
 
-template <int KIND, bool TS>
-__global__ void __launch_bounds__(kF4TsThreads, 1)
+template <int KIND>
+__global__ void __launch_bounds__(kF4Threads, 1)
     gemm_fp4_kernel(const __grid_constant__ F4Maps maps, const __grid_constant__ GemmLaunch args) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw0 = smem_addr(smem_raw);
   const uint32_t base = (raw0 + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw0);
-  // [f16 weight slots 3 x 32 KB, not in TS mode] [token ring 48 KB] [raw ring] [barriers]
-  constexpr uint32_t kCvtArea = TS ? 0u : kF4CvtSlots * kF4WBytes;
-  constexpr int kRawStages = TS ? kF4TsRawStages : kF4RawStages;
-  constexpr uint32_t kRawBytes = TS ? kF4TsRawBytes : kF4RawBytes;  // one raw ring stage
-  // TS: the token ring is the A ring (one stage barrier for both)
-  const int kCvtSlots = TS ? f4_ts_slots(maps.acc_stride) : kF4CvtSlots;
-  const uint32_t acc_stride = TS ? (uint32_t)maps.acc_stride : 0u;
-  const int nbuf = TS ? f4_ts_bufs(maps.acc_stride) : 2;          // accumulator buffers
-  const uint32_t a_col = TS ? (uint32_t)f4_ts_acc_cols(maps.acc_stride) : 0u;  // A ring
-  constexpr uint32_t kTokArea = TS ? kF4TsTokArea : kF4TokArea;
-  const int ts = maps.tok_stages;
+  // [token ring 64 KB] [raw ring 8 x 18 KB] [barriers, TMEM slot, abort flag, descriptors]
+  const int nslots = maps.slots;
+  const uint32_t acc_stride = (uint32_t)maps.acc_stride;
+  const int nbuf = f4_bufs(maps.acc_stride);                  // accumulator buffers
+  const uint32_t a_col = (uint32_t)f4_acc_cols(maps.acc_stride);  // first A ring column
   const uint32_t tsb = (uint32_t)maps.tok_slot_bytes;
   const int un = maps.un;
-  const int chunks = un / kF4TileRows;             // prepared chunks per stage: 1 or 2
-  const uint32_t tok_base = base + kCvtArea;
-  const uint32_t raw_base = tok_base + kTokArea;
-  uint8_t* raw_ptr = smem + kCvtArea + kTokArea;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(raw_ptr + kRawStages * kRawBytes);
-  // bars: raw_full[16] raw_empty[16] cvt_full[8] cvt_empty[8] tfull[2] tempty[2]
-  //       unit_full[8] unit_empty[8] tok_full[16] tok_empty[16]; then the TMEM slot, the
-  //       abort flag and (at byte 1024) the unit descriptors
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 68 + 2 * kF4MaxTokStages);
+  const int chunks = un / kF4TileRows;             // weight tiles per unit: 1 or 2
+  const uint32_t tok_base = base;
+  const uint32_t raw_base = tok_base + kF4TokArea;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kF4TokArea + kF4RawStages * kF4RawBytes);
+  // bars: raw_full[8] raw_empty[8] stage_full[4] stage_empty[4] tfull[2] tempty[2]
+  //       unit_full[8] unit_empty[8]; then the TMEM slot, the abort flag and (at byte 1024)
+  //       the unit descriptors
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 44);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   F4Desc* descs = reinterpret_cast<F4Desc*>(reinterpret_cast<uint8_t*>(bars) + 1024);
   const uint32_t bar0 = smem_addr(bars);
   auto raw_full = [&](int s) { return bar0 + 8u * s; };
-  auto raw_empty = [&](int s) { return bar0 + 8u * (16 + s); };
-  auto cvt_full = [&](int s) { return bar0 + 8u * (32 + s); };
-  auto cvt_empty = [&](int s) { return bar0 + 8u * (40 + s); };
-  auto tfull = [&](int b) { return bar0 + 8u * (48 + b); };
-  auto tempty = [&](int b) { return bar0 + 8u * (50 + b); };
-  auto unit_full = [&](int i) { return bar0 + 8u * (52 + i); };
-  auto unit_empty = [&](int i) { return bar0 + 8u * (60 + i); };
-  auto tok_full = [&](int s) { return bar0 + 8u * (68 + s); };
-  auto tok_empty = [&](int s) { return bar0 + 8u * (68 + kF4MaxTokStages + s); };
-  auto w_stage = [&](int s) { return base + s * kF4WBytes; };
+  auto raw_empty = [&](int s) { return bar0 + 8u * (8 + s); };
+  auto stage_full = [&](int s) { return bar0 + 8u * (16 + s); };
+  auto stage_empty = [&](int s) { return bar0 + 8u * (20 + s); };
+  auto tfull = [&](int b) { return bar0 + 8u * (24 + b); };
+  auto tempty = [&](int b) { return bar0 + 8u * (26 + b); };
+  auto unit_full = [&](int i) { return bar0 + 8u * (28 + i); };
+  auto unit_empty = [&](int i) { return bar0 + 8u * (36 + i); };
   auto x_stage = [&](int s) { return tok_base + s * tsb; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kRawStages; ++s) {
+    for (int s = 0; s < kF4RawStages; ++s) {
       mbar_init(raw_full(s), 1);
       mbar_init(raw_empty(s), kF4CvtWarps);
     }
-    for (int s = 0; s < kCvtSlots; ++s) {
-      // TS: the converters and the token tile's expect_tx arrival
-      mbar_init(cvt_full(s), TS ? kF4CvtWarps + 1 : kF4CvtWarps);
-      mbar_init(cvt_empty(s), TS ? chunks : 1);  // TS: one commit per tile's issuer
-    }
-    for (int s = 0; s < ts; ++s) {
-      mbar_init(tok_full(s), 1);
-      mbar_init(tok_empty(s), TS ? chunks : 1);
+    for (int s = 0; s < nslots; ++s) {
+      mbar_init(stage_full(s), kF4CvtWarps + 1);  // the converters and the token expect_tx
+      mbar_init(stage_empty(s), chunks);          // one commit per tile's issuer
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(tfull(b), TS ? chunks : 1);  // TS: both tiles' issuers commit
+      mbar_init(tfull(b), chunks);                // both tiles' issuers commit
       mbar_init(tempty(b), kF4EpiWarps);
     }
     for (int i = 0; i < kF4UnitRing; ++i) {
       mbar_init(unit_full(i), 1);
-      mbar_init(unit_empty(i), kF4UnitReaders + (TS ? 1 : 0));
+      mbar_init(unit_empty(i), kF4UnitReaders);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -401,30 +344,33 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
         mbar_arrive(unit_empty(uq.slot));
         uq.next(kF4UnitRing);
         const GemmProblem& P = args.p[w.p];
-        // chunks (64 K values of a 128-row tile) per stage and per tile; TS stages take two
-        constexpr int cps = TS ? 2 : 1;
-        constexpr uint32_t piece = cps * kFp4ChunkBytes;
         const uint8_t* src = static_cast<const uint8_t*>(P.B) +
-                             ((size_t)w.tile * P.k_blocks + w.kb0) * (size_t)piece;
-        const size_t tile_bytes = (size_t)P.k_blocks * piece;  // the next tile's chunks
-        for (int kb = w.kb0; kb < w.kb1; ++kb, src += piece, rq.next(kRawStages), ++issued) {
+                             ((size_t)w.tile * P.k_blocks + w.kb0) * (size_t)kF4Piece;
+        const size_t tile_bytes = (size_t)P.k_blocks * kF4Piece;  // the next tile's chunks
+        for (int kb = w.kb0; kb < w.kb1;
+             ++kb, src += kF4Piece, rq.next(kF4RawStages), ++issued) {
           if (!wait_fast(raw_empty(rq.slot), rq.phase ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(raw_full(rq.slot), chunks * piece);
-          const uint32_t dst = raw_base + rq.slot * kRawBytes;
+          mbar_expect_tx(raw_full(rq.slot), chunks * kF4Piece);
+          const uint32_t dst = raw_base + rq.slot * kF4RawBytes;
           for (int c = 0; c < chunks; ++c)
-            bulk_load(dst + c * piece, src + c * tile_bytes, piece, raw_full(rq.slot), policy);
+            bulk_load(dst + c * kF4Piece, src + c * tile_bytes, kF4Piece, raw_full(rq.slot),
+                      policy);
         }
       }
       // the last copies of each slot land before the CTA can exit
-      for (uint32_t j = issued > (uint32_t)kRawStages ? issued - kRawStages : 0; j < issued; ++j)
-        drain_wait(raw_full(j % kRawStages), (j / kRawStages) & 1u);
+      for (uint32_t j = issued > (uint32_t)kF4RawStages ? issued - kF4RawStages : 0; j < issued;
+           ++j)
+        drain_wait(raw_full(j % kF4RawStages), (j / kF4RawStages) & 1u);
     }
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ token tiles
+    // The token tile of stage j lands in slot j of the token ring (two boxes of 64 values,
+    // the second acc_stride rows after the first) and completes on that stage's barrier, so
+    // the MMA issuers wait once per stage.
     if (lane == 0) {
       RingPos uq{0, 0}, tq{0, 0};
       uint32_t issued = 0;
@@ -436,48 +382,29 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
         uq.next(kF4UnitRing);
         const CUtensorMap* map = &maps.x[w.p][w.box];
         const uint32_t box_bytes = (uint32_t)(16 << w.box) * 128;
-        if constexpr (TS) {
-          // the token tile of stage j lands in slot j of the A ring and completes on that
-          // stage's barrier, so the MMA issuers wait once per stage
-          // (two boxes of 64 K values per stage, the second acc_stride rows after the first)
-          for (int kb = w.kb0; kb < w.kb1; ++kb, tq.next(kCvtSlots), ++issued) {
-            if (!wait_fast(cvt_empty(tq.slot), tq.phase ^ 1u, abort_flag, args.status)) {
-              ok = false;
-              break;
-            }
-            mbar_expect_tx(cvt_full(tq.slot), 2 * box_bytes);
-            tma_load_2d(x_stage(tq.slot), map, cvt_full(tq.slot), kb * kF4TsStageK,
-                        w.mb * kFp4BS);
-            tma_load_2d(x_stage(tq.slot) + acc_stride * 128u, map, cvt_full(tq.slot),
-                        kb * kF4TsStageK + kF4BK, w.mb * kFp4BS);
+        for (int kb = w.kb0; kb < w.kb1; ++kb, tq.next(nslots), ++issued) {
+          if (!wait_fast(stage_empty(tq.slot), tq.phase ^ 1u, abort_flag, args.status)) {
+            ok = false;
+            break;
           }
-        } else {
-          for (int kb = w.kb0; kb < w.kb1; ++kb, tq.next(ts), ++issued) {
-            if (!wait_fast(tok_empty(tq.slot), tq.phase ^ 1u, abort_flag, args.status)) {
-              ok = false;
-              break;
-            }
-            mbar_expect_tx(tok_full(tq.slot), box_bytes);
-            tma_load_2d(x_stage(tq.slot), map, tok_full(tq.slot), kb * kF4BK, w.mb * kFp4BS);
-          }
+          mbar_expect_tx(stage_full(tq.slot), 2 * box_bytes);
+          tma_load_2d(x_stage(tq.slot), map, stage_full(tq.slot), kb * kF4StageK,
+                      w.mb * kFp4BS);
+          tma_load_2d(x_stage(tq.slot) + acc_stride * 128u, map, stage_full(tq.slot),
+                      kb * kF4StageK + kF4BK, w.mb * kFp4BS);
         }
       }
-      if (TS) {
-        const uint32_t n = (uint32_t)kCvtSlots;
-        for (uint32_t j = issued > n ? issued - n : 0; j < issued; ++j)
-          drain_wait(cvt_full(j % n), (j / n) & 1u);
-      } else {
-        for (uint32_t j = issued > (uint32_t)ts ? issued - ts : 0; j < issued; ++j)
-          drain_wait(tok_full(j % ts), (j / ts) & 1u);
-      }
+      const uint32_t n = (uint32_t)nslots;
+      for (uint32_t j = issued > n ? issued - n : 0; j < issued; ++j)
+        drain_wait(stage_full(j % n), (j / n) & 1u);
     }
     __syncwarp();
-  } else if (warp == 1 || (TS && warp == 4 + kF4CvtWarps + kF4EpiWarps)) {
-    // ------------------------------------------------------------ MMA issuer
-    // (TS: warp 1 issues tile 0's MMAs, warp 24 tile 1's, each with its own commits)
+  } else if (warp == 1 || warp == kF4Issuer2) {
+    // ------------------------------------------------------------ MMA issuers
+    // warp 1 issues tile 0's MMAs, warp 24 tile 1's, each with its own commits
     const int mt = warp == 1 ? 0 : 1;
     if (lane == 0) {
-      RingPos uq{0, 0}, cq{0, 0}, tq{0, 0};
+      RingPos uq{0, 0}, cq{0, 0};
       uint32_t uc = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x, ++uc) {
@@ -485,63 +412,38 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
         if (!get_unit(uq, w)) break;
         mbar_arrive(unit_empty(uq.slot));
         uq.next(kF4UnitRing);
-        const int buf = uc & 1;
-        if constexpr (TS) {
-          // weights on M (128 rows per tile, A in TMEM), the unit's tokens on N; with one
-          // accumulator buffer every unit waits for the previous unit's epilogue
-          if (mt >= chunks) continue;  // no second tile: this issuer only follows the units
-          const uint32_t idesc = idesc_f16(kF4M, w.n);
-          const int tb = nbuf == 2 ? buf : 0;
-          const uint32_t tph = nbuf == 2 ? ((uc >> 1) & 1u) : (uc & 1u);
-          if (!wait_fast(tempty(tb), tph ^ 1u, abort_flag, args.status)) break;
-          tc_fence_after();
-          const uint32_t d = tmem_base + (uint32_t)tb * 2u * acc_stride + (uint32_t)mt * acc_stride;
-          for (int kb = w.kb0; kb < w.kb1; ++kb, cq.next(kCvtSlots)) {
-            // the stage barrier: the group's weights in TMEM and the token tile in its slot
-            if (!wait_fast(cvt_full(cq.slot), cq.phase, abort_flag, args.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            // K step kk: 32 bytes into the token rows' swizzled 128-byte atoms, 8 columns
-            // into the weights' TMEM stage
-            const uint64_t b0 = sdesc_sw128(x_stage(cq.slot));
-            const uint64_t b1 = sdesc_advance(b0, acc_stride * 128u);  // the second 64 K values
-            const uint32_t a0 = tmem_base + a_col + (uint32_t)cq.slot * 128u + mt * 64u;
-            mma_f16_ts(d, a0, b0, idesc, kb == w.kb0 ? 0u : 1u);
-            mma_f16_ts(d, a0 + 8, sdesc_advance(b0, 32), idesc, 1u);
-            mma_f16_ts(d, a0 + 16, sdesc_advance(b0, 64), idesc, 1u);
-            mma_f16_ts(d, a0 + 24, sdesc_advance(b0, 96), idesc, 1u);
-            mma_f16_ts(d, a0 + 32, b1, idesc, 1u);
-            mma_f16_ts(d, a0 + 40, sdesc_advance(b1, 32), idesc, 1u);
-            mma_f16_ts(d, a0 + 48, sdesc_advance(b1, 64), idesc, 1u);
-            mma_f16_ts(d, a0 + 56, sdesc_advance(b1, 96), idesc, 1u);
-            mma_commit(cvt_empty(cq.slot));
-          }
-          if (ok) mma_commit(tfull(tb));
-          continue;
-        }
-        // row blocks of at most 64 real rows run M = 64 MMAs (fewer discarded rows in TMEM)
-        const uint32_t idesc = idesc_f16(w.rows <= 64 ? 64 : kF4M, un);
-        if (!wait_fast(tempty(buf), ((uc >> 1) & 1u) ^ 1u, abort_flag, args.status)) break;
+        if (mt >= chunks) continue;  // no second tile: this issuer only follows the units
+        // weights on M (128 rows per tile, A in TMEM), the unit's tokens on N; with one
+        // accumulator buffer every unit waits for the previous unit's epilogue
+        const uint32_t idesc = idesc_f16(kF4M, w.n);
+        const int tb = nbuf == 2 ? (int)(uc & 1u) : 0;
+        const uint32_t tph = nbuf == 2 ? ((uc >> 1) & 1u) : (uc & 1u);
+        if (!wait_fast(tempty(tb), tph ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + buf * kF4MaxN;
-        for (int kb = w.kb0; kb < w.kb1; ++kb, cq.next(kCvtSlots), tq.next(ts)) {
-          if (!wait_fast(tok_full(tq.slot), tq.phase, abort_flag, args.status) ||
-              !wait_fast(cvt_full(cq.slot), cq.phase, abort_flag, args.status)) {
+        const uint32_t d = tmem_base + (uint32_t)tb * 2u * acc_stride + (uint32_t)mt * acc_stride;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, cq.next(nslots)) {
+          // the stage barrier: the weights in TMEM and the token tile in its slot
+          if (!wait_fast(stage_full(cq.slot), cq.phase, abort_flag, args.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t dx = sdesc_sw128(x_stage(tq.slot)), dw = sdesc_sw128(w_stage(cq.slot));
-#pragma unroll
-          for (int kk = 0; kk < kF4BK / 16; ++kk)
-            mma_bf16(d, sdesc_advance(dx, kk * 32), sdesc_advance(dw, kk * 32), idesc,
-                     (kb != w.kb0 || kk != 0) ? 1u : 0u);
-          mma_commit(cvt_empty(cq.slot));
-          mma_commit(tok_empty(tq.slot));
+          // K step kk: 32 bytes into the token rows' swizzled 128-byte atoms, 8 columns
+          // into the weights' TMEM stage
+          const uint64_t b0 = sdesc_sw128(x_stage(cq.slot));
+          const uint64_t b1 = sdesc_advance(b0, acc_stride * 128u);  // the second 64 K values
+          const uint32_t a0 = tmem_base + a_col + (uint32_t)cq.slot * 128u + mt * 64u;
+          mma_f16_ts(d, a0, b0, idesc, kb == w.kb0 ? 0u : 1u);
+          mma_f16_ts(d, a0 + 8, sdesc_advance(b0, 32), idesc, 1u);
+          mma_f16_ts(d, a0 + 16, sdesc_advance(b0, 64), idesc, 1u);
+          mma_f16_ts(d, a0 + 24, sdesc_advance(b0, 96), idesc, 1u);
+          mma_f16_ts(d, a0 + 32, b1, idesc, 1u);
+          mma_f16_ts(d, a0 + 40, sdesc_advance(b1, 32), idesc, 1u);
+          mma_f16_ts(d, a0 + 48, sdesc_advance(b1, 64), idesc, 1u);
+          mma_f16_ts(d, a0 + 56, sdesc_advance(b1, 96), idesc, 1u);
+          mma_commit(stage_empty(cq.slot));
         }
-        if (ok) mma_commit(tfull(buf));
+        if (ok) mma_commit(tfull(tb));
       }
     }
     __syncwarp();
@@ -559,7 +461,7 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
       }
     }
     __syncwarp();
-  } else if (TS && warp >= 4 && warp < 4 + kF4CvtWarps) {
+  } else if (warp >= 4 && warp < 4 + kF4CvtWarps) {
     // ------------------------------------------------------------ fp4 -> f16 into TMEM
     // Every converter warp takes part in every stage. Warp c (0..15) writes TMEM lane
     // quarter c % 4 (= warp % 4, the quarter a warp may access): weight row 32 (c % 4) +
@@ -571,7 +473,7 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
     const bool live = tile < chunks;  // warp-uniform
     const uint32_t lanes = (uint32_t)(32 * (c & 3)) << 16;
     const uint32_t col0 = a_col + (uint32_t)tile * 64u + (uint32_t)kc * 32u;
-    const uint32_t chunk = (uint32_t)tile * 2u * kFp4ChunkBytes + (uint32_t)kc * kFp4ChunkBytes;
+    const uint32_t chunk = (uint32_t)tile * kF4Piece + (uint32_t)kc * kFp4ChunkBytes;
     const uint32_t rd = chunk + rr * 16u;
     const uint32_t sd = chunk + 4096u + rr * 4u;
     RingPos uq{0, 0}, rq{0, 0}, cq{0, 0};
@@ -580,28 +482,28 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
       F4Desc w;
       if (!get_unit(uq, w)) break;
       release_unit(uq);
-      for (int kb = w.kb0; kb < w.kb1; ++kb, rq.next(kRawStages), cq.next(kCvtSlots)) {
+      for (int kb = w.kb0; kb < w.kb1; ++kb, rq.next(kF4RawStages), cq.next(nslots)) {
         if (!wait_fast(raw_full(rq.slot), rq.phase, abort_flag, args.status)) {
           ok = false;
           break;
         }
-        const uint32_t src = raw_base + rq.slot * kRawBytes;
+        const uint32_t src = raw_base + rq.slot * kF4RawBytes;
         uint4 q0 = make_uint4(0u, 0u, 0u, 0u), q1 = q0;
         uint32_t scw = 0u;
         if (live) {
           q0 = lds128(src + rd);            // values 0..31 of the row's chunk
           q1 = lds128(src + rd + 2048u);    // values 32..63
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(scw) : "r"(src + sd));
+          scw = lds32(src + sd);            // the four 16-value blocks' scales
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(raw_empty(rq.slot));
-        if (!wait_fast(cvt_empty(cq.slot), cq.phase ^ 1u, abort_flag, args.status)) {
+        if (!wait_fast(stage_empty(cq.slot), cq.phase ^ 1u, abort_flag, args.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
         if (live) {
-          uint32_t s0, s1, s2, s3;          // the four 16-value blocks' scales as f16 pairs
+          uint32_t s0, s1, s2, s3;          // the block scales as f16 pairs
           e4m3x2_pairs(scw & 0xFFFFu, s0, s1);
           e4m3x2_pairs(scw >> 16, s2, s3);
           uint32_t o[32];
@@ -621,11 +523,11 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(cvt_full(cq.slot));
+        if (lane == 0) mbar_arrive(stage_full(cq.slot));
       }
     }
-  } else if (TS && warp >= 4 + kF4CvtWarps && warp < 4 + kF4CvtWarps + kF4EpiWarps) {
-    // ------------------------------------------------------------ epilogue (TS)
+  } else if (warp >= 4 + kF4CvtWarps && warp < 4 + kF4CvtWarps + kF4EpiWarps) {
+    // ------------------------------------------------------------ epilogue
     // D of tile t: TMEM lane = weight row (this warp's quarter), column j = the unit's token
     // row j. Lane l resolves token rows l, l + 32, l + 64, l + 96 to an output row and a
     // scale; every column is then one coalesced 128-byte store per warp.
@@ -703,126 +605,6 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty(tb));
     }
-  } else if (warp >= 4 && warp < 4 + kF4CvtWarps) {
-    // ------------------------------------------------------------ fp4 -> f16 expansion
-    // Every converter thread takes part in every stage: weight row r = t % 256 (of chunk
-    // r / 128), K half h = t / 256 (values 32 h .. 32 h + 31 of the stage).
-    const int t = (warp - 4) * 32 + lane;
-    const int r = t & (kF4MaxN - 1), h = t >> 8;
-    const bool live = r < un;
-    const uint32_t rd = (uint32_t)(r >> 7) * kFp4ChunkBytes;  // this row's chunk in a stage
-    const uint32_t rr = (uint32_t)(r & 127);
-    RingPos uq{0, 0}, rq{0, 0}, cq{0, 0};
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-      F4Desc w;
-      if (!get_unit(uq, w)) break;
-      release_unit(uq);
-      for (int kb = w.kb0; kb < w.kb1; ++kb, rq.next(kRawStages), cq.next(kCvtSlots)) {
-        if (!wait_fast(raw_full(rq.slot), rq.phase, abort_flag, args.status)) {
-          ok = false;
-          break;
-        }
-        const uint32_t src = raw_base + rq.slot * kF4RawBytes + rd;
-        uint4 q = make_uint4(0u, 0u, 0u, 0u);
-        uint32_t scw = 0u;
-        if (live) {
-          q = lds128(src + h * 2048 + rr * 16);
-          scw = lds16(src + 4096 + rr * 4 + 2 * h);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(raw_empty(rq.slot));
-        if (!wait_fast(cvt_empty(cq.slot), cq.phase ^ 1u, abort_flag, args.status)) {
-          ok = false;
-          break;
-        }
-        if (live) {
-          uint32_t s0, s1;
-          e4m3x2_pairs(scw, s0, s1);        // the half's two blocks of 16 values
-          const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-          const uint32_t row = w_stage(cq.slot) + r * 128;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {     // values 8 i .. 8 i + 7 of the half
-            uint32_t o[4];
-            e2m1x8_scaled(words[i], i < 2 ? s0 : s1, o);
-            const uint32_t chunk16 = (uint32_t)((4 * h + i) ^ (r & 7));
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + chunk16 * 16),
-                         "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
-                         : "memory");
-          }
-          fence_proxy_async_smem();  // the MMA (async proxy) reads what these stores wrote
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(cvt_full(cq.slot));
-      }
-    }
-  } else if (warp >= 4 + kF4CvtWarps) {
-    // ------------------------------------------------------------ epilogue
-    // D row m sits in TMEM lane m (M = 128) or, for M = 64, in lane 32 (m / 16) + m % 16:
-    // each lane quarter holds 16 rows in its first 16 lanes
-    const int quarter = warp & 3;
-    RingPos uq{0, 0};
-    uint32_t uc = 0;
-    for (int u = blockIdx.x; u < sched.units; u += gridDim.x, ++uc) {
-      F4Desc w;
-      if (!get_unit(uq, w)) break;
-      release_unit(uq);
-      const GemmProblem& P = args.p[w.p];
-      const int buf = uc & 1;
-      if (!wait_fast(tfull(buf), (uc >> 1) & 1u, abort_flag, args.status)) break;
-      tc_fence_after();
-      const bool m64 = w.rows <= 64;
-      const int rq0 = m64 ? 16 * quarter : 32 * quarter;  // the quarter's first row
-      if (rq0 < w.rows) {
-        // this lane's token row: its flat index (routed) or token, and its output row
-        const int m = m64 ? (lane < 16 ? rq0 + lane : kFp4BS) : rq0 + lane;
-        const int mr = w.mb * kFp4BS + m;
-        float* out = nullptr;
-        float scale = w.alpha;
-        if (m < w.rows) {
-          int f = -1;
-          if (P.sorted_ids) {
-            const int x = P.sorted_ids[mr];
-            if (x >= 0 && x < P.num_flat) f = x;
-          } else if (mr < P.store_rows) {
-            f = mr;
-          }
-          if (f >= 0) {
-            if (KIND == kGemmW13) {
-              out = P.part + (size_t)w.split * P.part_split_stride + (size_t)f * 2 * P.ldo;
-            } else {
-              int dest;
-              if (P.sorted_ids) {
-                dest = (f / P.top_k) * P.slots + (f % P.top_k);
-                if (P.row_weight) scale = w.alpha * P.row_weight[f];
-              } else {
-                dest = f * P.slots + P.slot_offset;
-              }
-              out = static_cast<float*>(P.out) + (size_t)w.split * P.out_split_stride +
-                    (size_t)dest * P.ldo;
-            }
-            out += (size_t)w.nt * un;
-          }
-        }
-        for (int c0 = 0; c0 < un; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * kF4MaxN + c0, v);
-          tmem_wait_ld(v);
-          if (out) {
-            float4* o4 = reinterpret_cast<float4*>(out + c0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o4[i] = make_float4(scale * __uint_as_float(v[4 * i]),
-                                  scale * __uint_as_float(v[4 * i + 1]),
-                                  scale * __uint_as_float(v[4 * i + 2]),
-                                  scale * __uint_as_float(v[4 * i + 3]));
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty(buf));
-    }
   }
 
   tc_fence_before();
@@ -833,22 +615,20 @@ __global__ void __launch_bounds__(kF4TsThreads, 1)
   }
 }
 
-template <int KIND, bool TS>
+template <int KIND>
 cudaError_t launch_fp4_typed(const F4Maps& maps, const GemmLaunch& args, int grid,
                              cudaStream_t stream) {
-  constexpr size_t smem = TS ? kF4TsSmem : kF4Smem;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_fp4_kernel<KIND, TS>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_fp4_kernel<KIND>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+                                         (int)kF4Smem);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  return launch_kernel(gemm_fp4_kernel<KIND, TS>, dim3(grid), dim3(TS ? kF4TsThreads : kF4Threads),
-                       smem, stream,
+  return launch_kernel(gemm_fp4_kernel<KIND>, dim3(grid), dim3(kF4Threads), kF4Smem, stream,
                        maps, args);
 }
 
@@ -864,9 +644,11 @@ cudaError_t launch_gemm_fp4(int kind, const GemmLaunch& L, cudaStream_t stream) 
   maps.un = kF4MaxN;
   for (int p = 0; p < L.num_problems; ++p)
     if (L.p[p].b_rows_per_expert % kF4MaxN) maps.un = kF4TileRows;
+  // the caller counts K in 64-value chunks; the kernel's stages take two
+  GemmLaunch Ls = L;
   for (int p = 0; p < 2; ++p) {
     const GemmProblem& P = L.p[L.num_problems > p ? p : 0];
-    if (P.K % kF4BK || P.k_blocks != P.K / kF4BK || P.b_rows_per_expert % maps.un ||
+    if (P.K % kF4StageK || P.k_blocks != P.K / kF4BK || P.b_rows_per_expert % maps.un ||
         P.n_tiles * maps.un != P.b_rows_per_expert || !P.B || !(P.gscale > 0.f) ||
         (reinterpret_cast<uintptr_t>(P.B) & 15u) || (kind == kGemmW13 ? !P.part : !P.out) ||
         P.ldo % 4)
@@ -876,7 +658,8 @@ cudaError_t launch_gemm_fp4(int kind, const GemmLaunch& L, cudaStream_t stream) 
                        (uint64_t)P.a_rows, (uint32_t)(16 << i)))
         return cudaErrorInvalidValue;
     if (p < L.num_problems) {
-      if (splits_of(L, p) < 1 || P.k_blocks < splits_of(L, p)) return cudaErrorInvalidValue;
+      Ls.p[p].k_blocks = P.K / kF4StageK;
+      if (splits_of(L, p) < 1 || Ls.p[p].k_blocks < splits_of(L, p)) return cudaErrorInvalidValue;
       units += (long)P.max_m_blocks * P.n_tiles * splits_of(L, p);
       // an upper bound on the rows f4_desc gives a unit: routed blocks hold at most
       // rows_bound real rows; identity rows up to a block
@@ -888,33 +671,16 @@ cudaError_t launch_gemm_fp4(int kind, const GemmLaunch& L, cudaStream_t stream) 
       if (box > max_box) max_box = box;
     }
   }
-  // K a multiple of the 128-value stage (and split-K ranges of whole stages): weights in
-  // TMEM on the MMA's M side, tokens on N
-  GemmLaunch Lts = L;
-  bool ts_mode = (16 << max_box) <= kF4TsMaxRows;
-  for (int p = 0; ts_mode && p < L.num_problems; ++p) {
-    GemmProblem& P = Lts.p[p];
-    if (P.K % kF4TsStageK || P.K / kF4TsStageK < splits_of(L, p)) ts_mode = false;
-    P.k_blocks = P.K / kF4TsStageK;
-  }
-  // the token ring: slots of the widest box; in the tokens-on-M mode the A read of the last
-  // slot (16 KB from its start) stays inside the ring's area; in the TS mode it is the A
-  // ring, a slot holding the stage's two boxes
+  // the token ring: per stage two boxes of the widest box, as many stages as the TMEM A ring
   maps.acc_stride = 16 << max_box;
-  maps.tok_slot_bytes = (int)((16u << max_box) * 128) * (ts_mode ? 2 : 1);
-  maps.tok_stages = ts_mode ? f4_ts_slots(maps.acc_stride)
-                            : (int)((kF4TokArea - kF4ABytes) / (uint32_t)maps.tok_slot_bytes) + 1;
-  if (ts_mode && maps.tok_stages * maps.tok_slot_bytes > (int)kF4TsTokArea)
-    return cudaErrorInvalidValue;
-  if (maps.tok_stages > kF4MaxTokStages) maps.tok_stages = kF4MaxTokStages;
+  maps.tok_slot_bytes = 2 * maps.acc_stride * 128;
+  maps.slots = f4_slots(maps.acc_stride);
+  if (maps.slots * maps.tok_slot_bytes > (int)kF4TokArea) return cudaErrorInvalidValue;
   int grid = num_sms();
   if (units < grid) grid = (int)units;
   if (grid < 1) grid = 1;
-  if (ts_mode)
-    return kind == kGemmW13 ? launch_fp4_typed<kGemmW13, true>(maps, Lts, grid, stream)
-                            : launch_fp4_typed<kGemmW2, true>(maps, Lts, grid, stream);
-  return kind == kGemmW13 ? launch_fp4_typed<kGemmW13, false>(maps, L, grid, stream)
-                          : launch_fp4_typed<kGemmW2, false>(maps, L, grid, stream);
+  return kind == kGemmW13 ? launch_fp4_typed<kGemmW13>(maps, Ls, grid, stream)
+                          : launch_fp4_typed<kGemmW2>(maps, Ls, grid, stream);
 }
 
 }  // namespace gbmoe
