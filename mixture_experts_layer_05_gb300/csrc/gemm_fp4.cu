@@ -29,19 +29,23 @@
 //                the TMEM A ring's stages)
 //   warp 3       the unit scheduler: reads each unit's metadata from global memory ahead
 //                of time and publishes it in shared memory
-//   warps 1, 24  one MMA issuer per 128-row weight tile: M 128 (weights, A in TMEM) x N
-//                (the unit's token rows rounded to 16) x K 16, 8 per stage, one stage
-//                barrier wait and one commit per stage each
+//   warps 1,     four MMA issuers: M 128 (weights, A in TMEM) x N (the unit's token rows
+//   24..26       rounded to 16) x K 16, one stage barrier wait and one commit per stage
+//                each; issuer q takes weight tile q / 2 and the stage's K chunk q % 2 (4
+//                MMAs per stage into its own accumulator), or, for 128-row token boxes,
+//                issuers 0 and 1 take tile q (8 MMAs per stage). A thread's tcgen05.mma
+//                issue, not the tensor core, bounds this kernel's MMA side: one issuer for
+//                both tiles was 30 % slower than two, four are 10-15 % faster than two.
 //   warps 4..19  every stage, warp c expands weight row 32 (c % 4) + lane of tile
 //                (c / 4) % 2, K chunk c / 8 (64 values: codes and four block scales, one
 //                hardware e2m1x2 conversion and one packed multiply per pair) into 32 TMEM
 //                columns of the stage's A slot (its warp's lane quarter)
 //   warps 20..23 epilogue: TMEM lane = output column, TMEM column = token row
 //
-// TMEM holds two accumulator buffers (alternate units) when the launch's widest token box
-// is at most 64 rows; for 128-row boxes one buffer, so a unit's MMAs wait for the previous
-// unit's epilogue. (Releasing the buffer's two tiles one at a time, each to its own issuer,
-// measured 1-3 % slower.) Every wait is bounded (kWaitTimeoutNs).
+// TMEM holds the accumulators (four or two per buffer; two buffers, alternate units, for
+// 16-row boxes, else one, so a unit's MMAs wait for the previous unit's epilogue), then the
+// A ring. (Releasing a buffer's two tiles one at a time, each to its own issuer, measured
+// 1-3 % slower.) Every wait is bounded (kWaitTimeoutNs).
 #include "fp4.cuh"
 #include "tc.cuh"
 
@@ -61,33 +65,41 @@ constexpr int kF4MaxSlots = 4;                    // weight stages in TMEM (and 
 constexpr uint32_t kF4TokArea = 64 * 1024;        // token ring: up to 2 stages of 2 x 16 KB
 constexpr int kF4CvtWarps = 16;
 constexpr int kF4EpiWarps = 4;
-constexpr int kF4Threads = 32 * (5 + kF4CvtWarps + kF4EpiWarps);  // + the second issuer
-constexpr int kF4Issuer2 = 4 + kF4CvtWarps + kF4EpiWarps;         // its warp (24)
+constexpr int kF4Issuers = 4;                     // MMA-issuing warps: 1 and 24..26
+constexpr int kF4Threads = 32 * (3 + kF4Issuers + kF4CvtWarps + kF4EpiWarps);
+constexpr int kF4Issuer1 = 4 + kF4CvtWarps + kF4EpiWarps;         // warp of issuer 1 (24)
 constexpr uint32_t kF4TmemCols = 512;
 constexpr int kF4Boxes = 4;                       // token boxes of 16, 32, 64, 128 rows
 constexpr int kF4UnitRing = 8;                    // unit descriptors the scheduler runs ahead
-// arrivals that free a descriptor: the two producers, the two MMA issuers, every converter
-// warp and every epilogue warp
-constexpr int kF4UnitReaders = 4 + kF4CvtWarps + kF4EpiWarps;
+// arrivals that free a descriptor: the two producers, the MMA issuers, every converter warp
+// and every epilogue warp
+constexpr int kF4UnitReaders = 2 + kF4Issuers + kF4CvtWarps + kF4EpiWarps;
 constexpr uint32_t kF4BarBytes = 2048;
 constexpr size_t kF4Smem = 1024 + kF4TokArea + (size_t)kF4RawStages * kF4RawBytes + kF4BarBytes;
 static_assert(kF4Smem <= 232448, "shared memory per CTA exceeded");
 static_assert(kF4Piece % 16 == 0, "bulk copies move multiples of 16 bytes");
-// TMEM: the accumulators (two tiles of acc_stride columns each: the launch's widest token
-// box; two such buffers up to 64-row boxes, one for 128), then the A ring, 128 columns (two
-// tiles x 128 f16 values) per stage, as many stages as fit: 3 for 16- and 32-row boxes, 2
-// for 64 and 128.
-__host__ __device__ constexpr int f4_bufs(int acc_stride) { return acc_stride >= 128 ? 1 : 2; }
+// TMEM: the accumulators, then the A ring, 128 columns (two tiles x 128 f16 values) per
+// stage. An accumulator is acc_stride columns (the launch's widest token box). Boxes of up
+// to 64 rows: four accumulators per buffer, one per (weight tile, K chunk of the stage),
+// each written by its own MMA-issuing warp (the epilogue adds a tile's two in a fixed
+// order); 128-row boxes: two, one per tile. Two buffers (alternate units) when three A
+// stages still fit, else one.
+__host__ __device__ constexpr int f4_naccs(int acc_stride) { return acc_stride <= 64 ? 4 : 2; }
+__host__ __device__ constexpr int f4_bufs(int acc_stride) {
+  return 2 * f4_naccs(acc_stride) * acc_stride + 3 * 128 <= (int)kF4TmemCols ? 2 : 1;
+}
 __host__ __device__ constexpr int f4_acc_cols(int acc_stride) {
-  return 2 * f4_bufs(acc_stride) * acc_stride;
+  return f4_bufs(acc_stride) * f4_naccs(acc_stride) * acc_stride;
 }
 __host__ __device__ constexpr int f4_slots(int acc_stride) {
   return ((int)kF4TmemCols - f4_acc_cols(acc_stride)) / 128 < kF4MaxSlots
              ? ((int)kF4TmemCols - f4_acc_cols(acc_stride)) / 128
              : kF4MaxSlots;
 }
-static_assert(f4_slots(kF4MaxRows) >= 2 && f4_slots(64) >= 2 &&
+static_assert(f4_slots(16) == 3 && f4_slots(32) == 3 && f4_slots(64) == 2 &&
+                  f4_slots(kF4MaxRows) == 2 &&
                   f4_slots(16) * 2 * 16 * 128 <= (int)kF4TokArea &&
+                  f4_slots(32) * 2 * 32 * 128 <= (int)kF4TokArea &&
                   f4_slots(64) * 2 * 64 * 128 <= (int)kF4TokArea &&
                   f4_slots(kF4MaxRows) * 2 * kF4MaxRows * 128 <= (int)kF4TokArea,
               "rings");
@@ -256,6 +268,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   const int nslots = maps.slots;
   const uint32_t acc_stride = (uint32_t)maps.acc_stride;
   const int nbuf = f4_bufs(maps.acc_stride);                  // accumulator buffers
+  const int naccs = f4_naccs(maps.acc_stride);                // accumulators per buffer
   const uint32_t a_col = (uint32_t)f4_acc_cols(maps.acc_stride);  // first A ring column
   const uint32_t tsb = (uint32_t)maps.tok_slot_bytes;
   const int un = maps.un;
@@ -288,10 +301,10 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     }
     for (int s = 0; s < nslots; ++s) {
       mbar_init(stage_full(s), kF4CvtWarps + 1);  // the converters and the token expect_tx
-      mbar_init(stage_empty(s), chunks);          // one commit per tile's issuer
+      mbar_init(stage_empty(s), chunks * naccs / 2);  // one commit per active issuer
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(tfull(b), chunks);                // both tiles' issuers commit
+      mbar_init(tfull(b), chunks * naccs / 2);
       mbar_init(tempty(b), kF4EpiWarps);
     }
     for (int i = 0; i < kF4UnitRing; ++i) {
@@ -399,10 +412,15 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         drain_wait(stage_full(j % n), (j / n) & 1u);
     }
     __syncwarp();
-  } else if (warp == 1 || warp == kF4Issuer2) {
+  } else if (warp == 1 || (warp >= kF4Issuer1 && warp < kF4Issuer1 + kF4Issuers - 1)) {
     // ------------------------------------------------------------ MMA issuers
-    // warp 1 issues tile 0's MMAs, warp 24 tile 1's, each with its own commits
-    const int mt = warp == 1 ? 0 : 1;
+    // Issuer q (warp 1, then 24..26). Four accumulators: weight tile q / 2, the stage's K
+    // chunk q % 2, 4 MMAs per stage into accumulator q. Two: issuers 0 and 1 take tile q,
+    // 8 MMAs per stage; 2 and 3 idle. One thread issues into each accumulator, so its
+    // summation order is fixed.
+    const int q = warp == 1 ? 0 : warp - kF4Issuer1 + 1;
+    const int mt = naccs == 4 ? q >> 1 : q;   // weight tile
+    const int kc = q & 1;                     // K chunk (four accumulators)
     if (lane == 0) {
       RingPos uq{0, 0}, cq{0, 0};
       uint32_t uc = 0;
@@ -412,7 +430,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         if (!get_unit(uq, w)) break;
         mbar_arrive(unit_empty(uq.slot));
         uq.next(kF4UnitRing);
-        if (mt >= chunks) continue;  // no second tile: this issuer only follows the units
+        if (mt >= chunks || (naccs == 2 && q >= 2)) continue;  // this issuer follows only
         // weights on M (128 rows per tile, A in TMEM), the unit's tokens on N; with one
         // accumulator buffer every unit waits for the previous unit's epilogue
         const uint32_t idesc = idesc_f16(kF4M, w.n);
@@ -420,7 +438,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         const uint32_t tph = nbuf == 2 ? ((uc >> 1) & 1u) : (uc & 1u);
         if (!wait_fast(tempty(tb), tph ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)tb * 2u * acc_stride + (uint32_t)mt * acc_stride;
+        const uint32_t d =
+            tmem_base + ((uint32_t)tb * (uint32_t)naccs + (uint32_t)q) * acc_stride;
         for (int kb = w.kb0; kb < w.kb1; ++kb, cq.next(nslots)) {
           // the stage barrier: the weights in TMEM and the token tile in its slot
           if (!wait_fast(stage_full(cq.slot), cq.phase, abort_flag, args.status)) {
@@ -429,18 +448,29 @@ __global__ void __launch_bounds__(kF4Threads, 1)
           }
           tc_fence_after();
           // K step kk: 32 bytes into the token rows' swizzled 128-byte atoms, 8 columns
-          // into the weights' TMEM stage
+          // into the weights' TMEM stage; the stage's second 64 K values sit in the token
+          // slot's second box and in the tile's columns 32..63
           const uint64_t b0 = sdesc_sw128(x_stage(cq.slot));
-          const uint64_t b1 = sdesc_advance(b0, acc_stride * 128u);  // the second 64 K values
           const uint32_t a0 = tmem_base + a_col + (uint32_t)cq.slot * 128u + mt * 64u;
-          mma_f16_ts(d, a0, b0, idesc, kb == w.kb0 ? 0u : 1u);
-          mma_f16_ts(d, a0 + 8, sdesc_advance(b0, 32), idesc, 1u);
-          mma_f16_ts(d, a0 + 16, sdesc_advance(b0, 64), idesc, 1u);
-          mma_f16_ts(d, a0 + 24, sdesc_advance(b0, 96), idesc, 1u);
-          mma_f16_ts(d, a0 + 32, b1, idesc, 1u);
-          mma_f16_ts(d, a0 + 40, sdesc_advance(b1, 32), idesc, 1u);
-          mma_f16_ts(d, a0 + 48, sdesc_advance(b1, 64), idesc, 1u);
-          mma_f16_ts(d, a0 + 56, sdesc_advance(b1, 96), idesc, 1u);
+          const uint32_t first = kb == w.kb0 ? 0u : 1u;
+          if (naccs == 4) {
+            const uint64_t bk = sdesc_advance(b0, (uint32_t)kc * acc_stride * 128u);
+            const uint32_t ak = a0 + (uint32_t)kc * 32u;
+            mma_f16_ts(d, ak, bk, idesc, first);
+            mma_f16_ts(d, ak + 8, sdesc_advance(bk, 32), idesc, 1u);
+            mma_f16_ts(d, ak + 16, sdesc_advance(bk, 64), idesc, 1u);
+            mma_f16_ts(d, ak + 24, sdesc_advance(bk, 96), idesc, 1u);
+          } else {
+            const uint64_t b1 = sdesc_advance(b0, acc_stride * 128u);
+            mma_f16_ts(d, a0, b0, idesc, first);
+            mma_f16_ts(d, a0 + 8, sdesc_advance(b0, 32), idesc, 1u);
+            mma_f16_ts(d, a0 + 16, sdesc_advance(b0, 64), idesc, 1u);
+            mma_f16_ts(d, a0 + 24, sdesc_advance(b0, 96), idesc, 1u);
+            mma_f16_ts(d, a0 + 32, b1, idesc, 1u);
+            mma_f16_ts(d, a0 + 40, sdesc_advance(b1, 32), idesc, 1u);
+            mma_f16_ts(d, a0 + 48, sdesc_advance(b1, 64), idesc, 1u);
+            mma_f16_ts(d, a0 + 56, sdesc_advance(b1, 96), idesc, 1u);
+          }
           mma_commit(stage_empty(cq.slot));
         }
         if (ok) mma_commit(tfull(tb));
@@ -579,11 +609,22 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       for (int t = 0; t < chunks; ++t) {
         const int col = t * kF4TileRows + 32 * quarter + lane;  // this lane's output column
         for (int c0 = 0; c0 < w.n; c0 += 16) {
+          // tile t's accumulator(s) in buffer tb: one, or the two K chunks' (added in order)
+          const uint32_t acc0 = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                ((uint32_t)tb * (uint32_t)naccs +
+                                 (uint32_t)(naccs == 4 ? 2 * t : t)) * acc_stride +
+                                (uint32_t)c0;
           uint32_t v[16];
-          tmem_ld16(tmem_base + ((uint32_t)(quarter * 32) << 16) +
-                        (uint32_t)tb * 2u * acc_stride + (uint32_t)t * acc_stride + (uint32_t)c0,
-                    v);
+          tmem_ld16(acc0, v);
           tmem_wait_ld16(v);
+          if (naccs == 4) {
+            uint32_t v2[16];
+            tmem_ld16(acc0 + acc_stride, v2);
+            tmem_wait_ld16(v2);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(v2[i]));
+          }
           // the 32-row group of columns c0 .. c0 + 15 (warp-uniform)
           const int g = c0 >> 5;
           float* const gp = g == 0 ? rowp[0] : g == 1 ? rowp[1] : g == 2 ? rowp[2] : rowp[3];
