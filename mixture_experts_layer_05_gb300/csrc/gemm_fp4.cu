@@ -17,10 +17,11 @@
 // over a K range of whole 128-value stages.
 //
 // The tensor core's time per MMA follows N, not M (M 128 x K 16 costs about 45 cycles at
-// N = 16 or 32, 48 at 64, 64 at 128 and 128 at N = 256, the same for M = 64), so the unit's tokens go on N
-// and the expanded weights are the A operand (M 128 per weight tile), written by the
-// converters straight into tensor memory (tcgen05.st): no f16 weight tile round-trips
-// through shared memory, which carries only the chunk copies and the token tiles. Roles:
+// N = 16 or 32, 48 at 64, 64 at 128 and 128 at N = 256, the same for M = 64), so the unit's
+// tokens go on N and the expanded weights are the A operand (M 128 per weight tile), written
+// by the converters straight into tensor memory (tcgen05.st): no f16 weight tile
+// round-trips through shared memory, which carries only the chunk copies and the token
+// tiles. Roles:
 //
 //   warp 0       bulk copies (one 9216-byte piece per weight tile and stage: the tile's two
 //                chunks are consecutive along K) into an 8-deep raw ring
@@ -79,21 +80,22 @@ constexpr size_t kF4Smem = 1024 + kF4TokArea + (size_t)kF4RawStages * kF4RawByte
 static_assert(kF4Smem <= 232448, "shared memory per CTA exceeded");
 static_assert(kF4Piece % 16 == 0, "bulk copies move multiples of 16 bytes");
 // TMEM: the accumulators, then the A ring, 128 columns (two tiles x 128 f16 values) per
-// stage. An accumulator is acc_stride columns (the launch's widest token box). Boxes of up
-// to 64 rows: four accumulators per buffer, one per (weight tile, K chunk of the stage),
-// each written by its own MMA-issuing warp (the epilogue adds a tile's two in a fixed
-// order); 128-row boxes: two, one per tile. Two buffers (alternate units) when three A
+// stage. Four accumulators per buffer, one per MMA-issuing warp, acc columns each (the
+// launch's widest token box, at most 64): for a unit of at most 64 token rows accumulator q
+// holds weight tile q / 2 and the stage's K chunk q % 2 (the epilogue adds a tile's two in
+// a fixed order); for a wider unit accumulators 2 t and 2 t + 1 hold tile t's token rows
+// 0..63 and 64..127, one 128-column accumulator. Two buffers (alternate units) when three A
 // stages still fit, else one.
-__host__ __device__ constexpr int f4_naccs(int acc_stride) { return acc_stride <= 64 ? 4 : 2; }
-__host__ __device__ constexpr int f4_bufs(int acc_stride) {
-  return 2 * f4_naccs(acc_stride) * acc_stride + 3 * 128 <= (int)kF4TmemCols ? 2 : 1;
+__host__ __device__ constexpr int f4_acc(int box_rows) { return box_rows < 64 ? box_rows : 64; }
+__host__ __device__ constexpr int f4_bufs(int box_rows) {
+  return 2 * 4 * f4_acc(box_rows) + 3 * 128 <= (int)kF4TmemCols ? 2 : 1;
 }
-__host__ __device__ constexpr int f4_acc_cols(int acc_stride) {
-  return f4_bufs(acc_stride) * f4_naccs(acc_stride) * acc_stride;
+__host__ __device__ constexpr int f4_acc_cols(int box_rows) {
+  return f4_bufs(box_rows) * 4 * f4_acc(box_rows);
 }
-__host__ __device__ constexpr int f4_slots(int acc_stride) {
-  return ((int)kF4TmemCols - f4_acc_cols(acc_stride)) / 128 < kF4MaxSlots
-             ? ((int)kF4TmemCols - f4_acc_cols(acc_stride)) / 128
+__host__ __device__ constexpr int f4_slots(int box_rows) {
+  return ((int)kF4TmemCols - f4_acc_cols(box_rows)) / 128 < kF4MaxSlots
+             ? ((int)kF4TmemCols - f4_acc_cols(box_rows)) / 128
              : kF4MaxSlots;
 }
 static_assert(f4_slots(16) == 3 && f4_slots(32) == 3 && f4_slots(64) == 2 &&
@@ -108,8 +110,9 @@ struct F4Maps {
   CUtensorMap x[2][kF4Boxes];  // per problem: f16 token rows, box 64 values x (16 << i) rows
   int slots;                   // stages of the TMEM A ring and of the token ring
   int tok_slot_bytes;          // two boxes of the launch's widest box (a multiple of 2048)
+  int box_rows;                // the launch's widest token box (16, 32, 64 or 128 rows)
   int un;                      // weight rows per unit: 256, or 128
-  int acc_stride;              // TMEM columns per accumulator tile (the widest box's rows)
+  int acc_stride;              // TMEM columns per accumulator (box rows, at most 64)
 };
 
 // Instruction descriptor of kind::f16 with f16 A and B (format code 0), fp32 D, K-major.
@@ -202,6 +205,24 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > 10000000ull) return;
 }
 
+// wait_bounded for a thread that only keeps pace (an idle MMA issuer): it sleeps between
+// polls so that its spinning does not take issue slots from the warps doing the work.
+__device__ __noinline__ bool wait_sleepy(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(256);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      *abort_flag = 1;
+      record_status(status, GBMOE_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // A unit as the scheduler warp publishes it in shared memory: the unit, its real token
 // rows, its MMA N (rows rounded up to 16) and token box, its expert's first weight tile, the
 // output scale.
@@ -267,9 +288,9 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   // [token ring 64 KB] [raw ring 8 x 18 KB] [barriers, TMEM slot, abort flag, descriptors]
   const int nslots = maps.slots;
   const uint32_t acc_stride = (uint32_t)maps.acc_stride;
-  const int nbuf = f4_bufs(maps.acc_stride);                  // accumulator buffers
-  const int naccs = f4_naccs(maps.acc_stride);                // accumulators per buffer
-  const uint32_t a_col = (uint32_t)f4_acc_cols(maps.acc_stride);  // first A ring column
+  const uint32_t box_rows = (uint32_t)maps.box_rows;
+  const int nbuf = f4_bufs(maps.box_rows);                    // accumulator buffers
+  const uint32_t a_col = (uint32_t)f4_acc_cols(maps.box_rows);  // first A ring column
   const uint32_t tsb = (uint32_t)maps.tok_slot_bytes;
   const int un = maps.un;
   const int chunks = un / kF4TileRows;             // weight tiles per unit: 1 or 2
@@ -301,10 +322,10 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     }
     for (int s = 0; s < nslots; ++s) {
       mbar_init(stage_full(s), kF4CvtWarps + 1);  // the converters and the token expect_tx
-      mbar_init(stage_empty(s), chunks * naccs / 2);  // one commit per active issuer
+      mbar_init(stage_empty(s), 2 * chunks);      // one commit per active issuer
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(tfull(b), chunks * naccs / 2);
+      mbar_init(tfull(b), 2 * chunks);
       mbar_init(tempty(b), kF4EpiWarps);
     }
     for (int i = 0; i < kF4UnitRing; ++i) {
@@ -382,7 +403,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   } else if (warp == 2) {
     // ------------------------------------------------------------ token tiles
     // The token tile of stage j lands in slot j of the token ring (two boxes of 64 values,
-    // the second acc_stride rows after the first) and completes on that stage's barrier, so
+    // the second box_rows rows after the first) and completes on that stage's barrier, so
     // the MMA issuers wait once per stage.
     if (lane == 0) {
       RingPos uq{0, 0}, tq{0, 0};
@@ -403,7 +424,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
           mbar_expect_tx(stage_full(tq.slot), 2 * box_bytes);
           tma_load_2d(x_stage(tq.slot), map, stage_full(tq.slot), kb * kF4StageK,
                       w.mb * kFp4BS);
-          tma_load_2d(x_stage(tq.slot) + acc_stride * 128u, map, stage_full(tq.slot),
+          tma_load_2d(x_stage(tq.slot) + box_rows * 128u, map, stage_full(tq.slot),
                       kb * kF4StageK + kF4BK, w.mb * kFp4BS);
         }
       }
@@ -414,13 +435,19 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     __syncwarp();
   } else if (warp == 1 || (warp >= kF4Issuer1 && warp < kF4Issuer1 + kF4Issuers - 1)) {
     // ------------------------------------------------------------ MMA issuers
-    // Issuer q (warp 1, then 24..26). Four accumulators: weight tile q / 2, the stage's K
-    // chunk q % 2, 4 MMAs per stage into accumulator q. Two: issuers 0 and 1 take tile q,
-    // 8 MMAs per stage; 2 and 3 idle. One thread issues into each accumulator, so its
-    // summation order is fixed.
-    const int q = warp == 1 ? 0 : warp - kF4Issuer1 + 1;
-    const int mt = naccs == 4 ? q >> 1 : q;   // weight tile
-    const int kc = q & 1;                     // K chunk (four accumulators)
+    // Issuer q (warps 1, 25, 24, 26 for q = 0..3) takes weight tile q / 2. A unit of at
+    // most 64 token rows: the stage's K chunk q % 2, 4 MMAs per stage into its own
+    // accumulator q (the epilogue adds a tile's two). A wider unit: issuer 2 t takes all of
+    // tile t, 8 MMAs of N = the unit's rows per stage into accumulators 2 t and 2 t + 1 side
+    // by side (128 columns); its partner issues no MMAs but keeps the same protocol (every
+    // wait, one arrival per stage and per unit), so every stage barrier gets its arrivals
+    // from the same issuers in every unit and no issuer runs ahead of the stage ring. (A
+    // partner that skipped the unit's stages instead could see a stage barrier two phases
+    // on as complete, by parity, and over-arrive on it: that faulted the GPU.) One thread
+    // issues into each accumulator, so its summation order is fixed. Issuers 0 and 2, a
+    // wide unit's two, sit on different SM sub-partitions (warps 1 and 24).
+    const int q = warp == 1 ? 0 : warp == kF4Issuer1 ? 2 : warp == kF4Issuer1 + 1 ? 1 : 3;
+    const int mt = q >> 1, sub = q & 1;   // weight tile; K chunk
     if (lane == 0) {
       RingPos uq{0, 0}, cq{0, 0};
       uint32_t uc = 0;
@@ -430,7 +457,9 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         if (!get_unit(uq, w)) break;
         mbar_arrive(unit_empty(uq.slot));
         uq.next(kF4UnitRing);
-        if (mt >= chunks || (naccs == 2 && q >= 2)) continue;  // this issuer follows only
+        if (mt >= chunks) continue;  // no second tile: this issuer only follows the units
+        const bool wide = w.n > 64;
+        const bool idle = wide && sub == 1;   // the partner issues this unit's MMAs
         // weights on M (128 rows per tile, A in TMEM), the unit's tokens on N; with one
         // accumulator buffer every unit waits for the previous unit's epilogue
         const uint32_t idesc = idesc_f16(kF4M, w.n);
@@ -438,42 +467,62 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         const uint32_t tph = nbuf == 2 ? ((uc >> 1) & 1u) : (uc & 1u);
         if (!wait_fast(tempty(tb), tph ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
-        const uint32_t d =
-            tmem_base + ((uint32_t)tb * (uint32_t)naccs + (uint32_t)q) * acc_stride;
-        for (int kb = w.kb0; kb < w.kb1; ++kb, cq.next(nslots)) {
-          // the stage barrier: the weights in TMEM and the token tile in its slot
-          if (!wait_fast(stage_full(cq.slot), cq.phase, abort_flag, args.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // K step kk: 32 bytes into the token rows' swizzled 128-byte atoms, 8 columns
-          // into the weights' TMEM stage; the stage's second 64 K values sit in the token
-          // slot's second box and in the tile's columns 32..63
-          const uint64_t b0 = sdesc_sw128(x_stage(cq.slot));
-          const uint32_t a0 = tmem_base + a_col + (uint32_t)cq.slot * 128u + mt * 64u;
-          const uint32_t first = kb == w.kb0 ? 0u : 1u;
-          if (naccs == 4) {
-            const uint64_t bk = sdesc_advance(b0, (uint32_t)kc * acc_stride * 128u);
-            const uint32_t ak = a0 + (uint32_t)kc * 32u;
-            mma_f16_ts(d, ak, bk, idesc, first);
+        const uint32_t d = tmem_base + ((uint32_t)tb * 4u + (uint32_t)q) * acc_stride;
+        // K step kk: 32 bytes into the token rows' swizzled 128-byte atoms, 8 columns into
+        // the weights' TMEM stage; the stage's second 64 K values sit in the token slot's
+        // second box and in the tile's columns 32..63
+        if (!wide) {
+          const uint32_t boff = (uint32_t)sub * box_rows * 128u, aoff = (uint32_t)sub * 32u;
+          for (int kb = w.kb0; kb < w.kb1; ++kb, cq.next(nslots)) {
+            // the stage barrier: the weights in TMEM and the token tile in its slot
+            if (!wait_fast(stage_full(cq.slot), cq.phase, abort_flag, args.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t bk = sdesc_advance(sdesc_sw128(x_stage(cq.slot)), boff);
+            const uint32_t ak = tmem_base + a_col + (uint32_t)cq.slot * 128u + mt * 64u + aoff;
+            mma_f16_ts(d, ak, bk, idesc, kb == w.kb0 ? 0u : 1u);
             mma_f16_ts(d, ak + 8, sdesc_advance(bk, 32), idesc, 1u);
             mma_f16_ts(d, ak + 16, sdesc_advance(bk, 64), idesc, 1u);
             mma_f16_ts(d, ak + 24, sdesc_advance(bk, 96), idesc, 1u);
-          } else {
-            const uint64_t b1 = sdesc_advance(b0, acc_stride * 128u);
-            mma_f16_ts(d, a0, b0, idesc, first);
-            mma_f16_ts(d, a0 + 8, sdesc_advance(b0, 32), idesc, 1u);
-            mma_f16_ts(d, a0 + 16, sdesc_advance(b0, 64), idesc, 1u);
-            mma_f16_ts(d, a0 + 24, sdesc_advance(b0, 96), idesc, 1u);
-            mma_f16_ts(d, a0 + 32, b1, idesc, 1u);
-            mma_f16_ts(d, a0 + 40, sdesc_advance(b1, 32), idesc, 1u);
-            mma_f16_ts(d, a0 + 48, sdesc_advance(b1, 64), idesc, 1u);
-            mma_f16_ts(d, a0 + 56, sdesc_advance(b1, 96), idesc, 1u);
+            mma_commit(stage_empty(cq.slot));
           }
-          mma_commit(stage_empty(cq.slot));
+          if (ok) mma_commit(tfull(tb));
+        } else {
+          for (int kb = w.kb0; kb < w.kb1; ++kb, cq.next(nslots)) {
+            if (!(idle ? wait_sleepy(stage_full(cq.slot), cq.phase, abort_flag, args.status)
+                       : wait_fast(stage_full(cq.slot), cq.phase, abort_flag, args.status))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (!idle) {
+              const uint64_t b0 = sdesc_sw128(x_stage(cq.slot));
+              const uint64_t b1 = sdesc_advance(b0, box_rows * 128u);
+              const uint32_t a0 = tmem_base + a_col + (uint32_t)cq.slot * 128u + mt * 64u;
+              mma_f16_ts(d, a0, b0, idesc, kb == w.kb0 ? 0u : 1u);
+              mma_f16_ts(d, a0 + 8, sdesc_advance(b0, 32), idesc, 1u);
+              mma_f16_ts(d, a0 + 16, sdesc_advance(b0, 64), idesc, 1u);
+              mma_f16_ts(d, a0 + 24, sdesc_advance(b0, 96), idesc, 1u);
+              mma_f16_ts(d, a0 + 32, b1, idesc, 1u);
+              mma_f16_ts(d, a0 + 40, sdesc_advance(b1, 32), idesc, 1u);
+              mma_f16_ts(d, a0 + 48, sdesc_advance(b1, 64), idesc, 1u);
+              mma_f16_ts(d, a0 + 56, sdesc_advance(b1, 96), idesc, 1u);
+              mma_commit(stage_empty(cq.slot));
+            } else {
+              // nothing of this unit to track (its earlier MMAs completed before this
+              // unit's accumulator barrier): a plain arrival, no tcgen05 instruction
+              mbar_arrive(stage_empty(cq.slot));
+            }
+          }
+          if (ok) {
+            if (idle)
+              mbar_arrive(tfull(tb));
+            else
+              mma_commit(tfull(tb));
+          }
         }
-        if (ok) mma_commit(tfull(tb));
       }
     }
     __syncwarp();
@@ -609,15 +658,18 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       for (int t = 0; t < chunks; ++t) {
         const int col = t * kF4TileRows + 32 * quarter + lane;  // this lane's output column
         for (int c0 = 0; c0 < w.n; c0 += 16) {
-          // tile t's accumulator(s) in buffer tb: one, or the two K chunks' (added in order)
+          // tile t's accumulators in buffer tb: the two K chunks' (added in order), or,
+          // for a unit of more than 64 rows, the one 128-column accumulator (its row half
+          // holding columns c0 .. c0 + 15)
+          const bool halves = w.n > 64;
+          const int h = halves && c0 >= 64 ? 1 : 0;
           const uint32_t acc0 = tmem_base + ((uint32_t)(quarter * 32) << 16) +
-                                ((uint32_t)tb * (uint32_t)naccs +
-                                 (uint32_t)(naccs == 4 ? 2 * t : t)) * acc_stride +
-                                (uint32_t)c0;
+                                ((uint32_t)tb * 4u + (uint32_t)(2 * t + h)) * acc_stride +
+                                (uint32_t)(c0 - 64 * h);
           uint32_t v[16];
           tmem_ld16(acc0, v);
           tmem_wait_ld16(v);
-          if (naccs == 4) {
+          if (!halves) {
             uint32_t v2[16];
             tmem_ld16(acc0 + acc_stride, v2);
             tmem_wait_ld16(v2);
@@ -713,9 +765,10 @@ cudaError_t launch_gemm_fp4(int kind, const GemmLaunch& L, cudaStream_t stream) 
     }
   }
   // the token ring: per stage two boxes of the widest box, as many stages as the TMEM A ring
-  maps.acc_stride = 16 << max_box;
-  maps.tok_slot_bytes = 2 * maps.acc_stride * 128;
-  maps.slots = f4_slots(maps.acc_stride);
+  maps.box_rows = 16 << max_box;
+  maps.acc_stride = f4_acc(maps.box_rows);
+  maps.tok_slot_bytes = 2 * maps.box_rows * 128;
+  maps.slots = f4_slots(maps.box_rows);
   if (maps.slots * maps.tok_slot_bytes > (int)kF4TokArea) return cudaErrorInvalidValue;
   int grid = num_sms();
   if (units < grid) grid = (int)units;
