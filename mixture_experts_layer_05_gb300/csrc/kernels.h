@@ -237,7 +237,8 @@ cudaError_t launch_silu_reduce_fp8(const GemmLaunch& L, const int* npp, int max_
 constexpr int kFp4BS = 128;             // align block size of the NVFP4 forward (max MMA N)
 constexpr int kFp4ChunkBytes = 4608;    // prepared weights: 128 rows x 64 K (4096 B of codes
                                         // + 512 B of block scales) per chunk
-constexpr int kFp4StageK = 64;          // K per NVFP4 GEMM stage (GemmProblem.k_blocks = K / it)
+constexpr int kFp4StageK = 64;          // K per prepared chunk (GemmProblem.k_blocks = K / it;
+                                        // the GEMM's stages take two chunks)
 // weight rows per NVFP4 GEMM unit (GemmProblem.n_tiles = weight rows / it): 256 when every
 // problem of the launch has a multiple of 256 weight rows per expert, else 128
 inline int fp4_unit_rows(int rows0, int rows1) {
@@ -253,9 +254,10 @@ cudaError_t launch_quant_fp4(const void* x, int rows, int H, float g, uint8_t* q
 cudaError_t launch_quant_gather_fp4(const void* x, int H, const int* inv, int n, int k, int T,
                                     int max_rows, float g, void* x_perm, void* x_tok,
                                     float g_tok, cudaStream_t stream);
-// NVFP4 grouped GEMMs (the row block's tokens on M, 256 or 128 weight rows on N): kGemmW13
-// writes alpha-scaled fp32 partials [split][row][2 ldo] (gate | up), kGemmW2 weighted fp32
-// slot outputs.
+// NVFP4 grouped GEMMs (256 or 128 weight rows per unit, expanded into tensor memory as the
+// MMA's M side; the row block's tokens on N; K a multiple of 128): kGemmW13 writes
+// alpha-scaled fp32 partials [split][row][2 ldo] (gate | up), kGemmW2 weighted fp32 slot
+// outputs.
 cudaError_t launch_gemm_fp4(int kind, const GemmLaunch& L, cudaStream_t stream);
 // act = silu(sum gate) * sum up of an NVFP4 first-GEMM launch, block-quantized with g_act
 // (routed) / g_act_shared, written as f16 q * sf to out (routed rows through flat_row).
